@@ -1,0 +1,270 @@
+"""CPU oracle for the CSA2 hot path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` leg of
+``bench.py`` may import this package. The CUDA library never calls it and
+shares no code with it. The arithmetic lives in ``csa2_oracle.c`` (plain C,
+double accumulation); this module compiles it with gcc on first use and
+exposes numpy-facing wrappers.
+
+Sources cited in the C file:
+  [R]  "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+       (technical-report digest)
+  [B]  "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression"
+       (mer.dev reading notes)
+  [V4] "DeepSeek-V4: Towards Highly Efficient Million-Token Context
+       Intelligence" (paperglide summary)
+
+Parity pins: every function here is pinned by ``tests/test_oracle_*.py``
+against closed forms, library routines, brute force or the pages' numbers.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "csa2_oracle.c")
+_HDR = os.path.join(_HERE, "csa2_oracle.h")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+IDX_HEADS = 32
+IDX_DIM = 128
+KV_DIM = 512
+
+
+def build(force: bool = False) -> str:
+    """Compile csa2_oracle.c into liboracle.so (gcc, OpenMP). Returns the path."""
+    stale = (not os.path.exists(_LIB)) or any(
+        os.path.getmtime(p) > os.path.getmtime(_LIB) for p in (_SRC, _HDR))
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fopenmp", "-fPIC", "-shared",
+               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            d, i64, i32, u8p, f32p, f64p, i32p = (
+                ctypes.c_double, ctypes.c_int64, ctypes.c_int,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p)
+            L.orc_e2m1_value.restype = d
+            L.orc_e2m1_value.argtypes = [ctypes.c_uint]
+            L.orc_e4m3_value.restype = d
+            L.orc_e4m3_value.argtypes = [ctypes.c_uint]
+            L.orc_e8m0_value.restype = d
+            L.orc_e8m0_value.argtypes = [ctypes.c_uint]
+            L.orc_e2m1_encode.restype = ctypes.c_uint
+            L.orc_e2m1_encode.argtypes = [ctypes.c_float]
+            L.orc_e4m3_encode.restype = ctypes.c_uint
+            L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            L.orc_quant_mxfp4.argtypes = [f32p, i64, i32, u8p, u8p]
+            L.orc_dequant_mxfp4.argtypes = [u8p, u8p, i64, i32, f64p]
+            L.orc_pack_kv_fp4.argtypes = [f32p, i64, u8p, u8p]
+            L.orc_unpack_kv_fp4.argtypes = [u8p, u8p, i64, f64p]
+            L.orc_pack_fp8.argtypes = [f32p, i64, u8p]
+            L.orc_unpack_fp8.argtypes = [u8p, i64, f64p]
+            L.orc_main_kv_entry_bytes.restype = i32
+            L.orc_indexer_k_entry_bytes.restype = i32
+            L.orc_index_score.restype = ctypes.c_uint64
+            L.orc_index_score.argtypes = [u8p, u8p, f32p, u8p, u8p, i32p, i64, f32p, f64p]
+            L.orc_topk.restype = i32
+            L.orc_topk.argtypes = [f32p, i32p, i64, i32, i32p]
+            L.orc_block_pool.restype = i32
+            L.orc_block_pool.argtypes = [f32p, i64, i32, i32, i32p]
+            L.orc_sparse_attn.argtypes = [f32p, i32, i32, u8p, u8p, i32p, i32, u8p, i32, d, f64p, f64p]
+            L.orc_decode_batch.restype = ctypes.c_uint64
+            L.orc_decode_batch.argtypes = [i32, i64, i32p, u8p, u8p, f32p, u8p, u8p, u8p, u8p,
+                                           i32, i32, f32p, i32, i32, u8p, i32, d, i32p, f64p, i32]
+            L.orc_max_threads.restype = i32
+            _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- element formats --------------------------------------------------------
+
+def e2m1_value(code: int) -> float:
+    return lib().orc_e2m1_value(code)
+
+
+def e4m3_value(code: int) -> float:
+    return lib().orc_e4m3_value(code)
+
+
+def e8m0_value(code: int) -> float:
+    return lib().orc_e8m0_value(code)
+
+
+def e2m1_encode(x: float) -> int:
+    return lib().orc_e2m1_encode(x)
+
+
+def e4m3_encode(x: float) -> int:
+    return lib().orc_e4m3_encode(x)
+
+
+# ---- codecs -----------------------------------------------------------------
+
+def quant_mxfp4(x):
+    """x: float32 [rows, cols] (cols % 32 == 0) -> (data u8 [rows, cols/2], e8m0 u8 [rows, cols/32])."""
+    x = _c(x, np.float32)
+    rows, cols = x.shape
+    assert cols % 32 == 0
+    data = np.zeros((rows, cols // 2), np.uint8)
+    sc = np.zeros((rows, cols // 32), np.uint8)
+    lib().orc_quant_mxfp4(_p(x), rows, cols, _p(data), _p(sc))
+    return data, sc
+
+
+def dequant_mxfp4(data, e8m0):
+    data = _c(data, np.uint8)
+    e8m0 = _c(e8m0, np.uint8)
+    rows = data.shape[0]
+    cols = data.shape[1] * 2
+    out = np.zeros((rows, cols), np.float64)
+    lib().orc_dequant_mxfp4(_p(data), _p(e8m0), rows, cols, _p(out))
+    return out
+
+
+def pack_kv_fp4(x):
+    """x: float32 [n, 512] -> (kv_data u8 [n, 256], kv_scale u8 [n, 32])."""
+    x = _c(x, np.float32)
+    n = x.shape[0]
+    assert x.shape[1] == KV_DIM
+    data = np.zeros((n, KV_DIM // 2), np.uint8)
+    sc = np.zeros((n, KV_DIM // 16), np.uint8)
+    lib().orc_pack_kv_fp4(_p(x), n, _p(data), _p(sc))
+    return data, sc
+
+
+def unpack_kv_fp4(kv_data, kv_scale):
+    kv_data = _c(kv_data, np.uint8)
+    kv_scale = _c(kv_scale, np.uint8)
+    n = kv_data.shape[0]
+    out = np.zeros((n, KV_DIM), np.float64)
+    lib().orc_unpack_kv_fp4(_p(kv_data), _p(kv_scale), n, _p(out))
+    return out
+
+
+def pack_fp8(x):
+    x = _c(x, np.float32)
+    out = np.zeros(x.shape, np.uint8)
+    lib().orc_pack_fp8(_p(x), x.size, _p(out))
+    return out
+
+
+def unpack_fp8(b):
+    b = _c(b, np.uint8)
+    out = np.zeros(b.shape, np.float64)
+    lib().orc_unpack_fp8(_p(b), b.size, _p(out))
+    return out
+
+
+def main_kv_entry_bytes() -> int:
+    return lib().orc_main_kv_entry_bytes()
+
+
+def indexer_k_entry_bytes() -> int:
+    return lib().orc_indexer_k_entry_bytes()
+
+
+# ---- indexer -----------------------------------------------------------------
+
+def index_score(q_data, q_e8m0, w, ik_data, ik_scale, n=None, positions=None):
+    """Scores of one query. q_data [32,64], q_e8m0 [32,4], w [32];
+    ik planes [cap,64] / [cap,4]. Scores positions 0..n-1, or `positions`.
+    Returns (fp32 scores, float64 scores, multiply-accumulate count)."""
+    q_data = _c(q_data, np.uint8)
+    q_e8m0 = _c(q_e8m0, np.uint8)
+    w = _c(w, np.float32)
+    ik_data = _c(ik_data, np.uint8)
+    ik_scale = _c(ik_scale, np.uint8)
+    if positions is not None:
+        positions = _c(positions, np.int32)
+        n = positions.size
+    elif n is None:
+        n = ik_data.shape[0]
+    out32 = np.zeros(n, np.float32)
+    out64 = np.zeros(n, np.float64)
+    macs = lib().orc_index_score(_p(q_data), _p(q_e8m0), _p(w), _p(ik_data), _p(ik_scale),
+                                 _p(positions), n, _p(out32), _p(out64))
+    return out32, out64, int(macs)
+
+
+def topk(scores, k, positions=None):
+    scores = _c(scores, np.float32)
+    if positions is not None:
+        positions = _c(positions, np.int32)
+    idx = np.zeros(k, np.int32)
+    nv = lib().orc_topk(_p(scores), _p(positions), scores.size, k, _p(idx))
+    return idx, int(nv)
+
+
+def block_pool(scores, block=8, n_blocks=2048):
+    scores = _c(scores, np.float32)
+    pool = np.zeros(block * n_blocks, np.int32)
+    kept = lib().orc_block_pool(_p(scores), scores.size, block, n_blocks, _p(pool))
+    return pool, int(kept)
+
+
+def sparse_attn(q, kv_data, kv_scale, idx, swa, sm_scale=1.0):
+    """q float32 [H, D] (bf16-exact values); kv planes of one sequence;
+    idx int32 [k]; swa u8 [n_swa, D]. Returns (out float64 [H, D], lse [H])."""
+    q = _c(q, np.float32)
+    H, D = q.shape
+    kv_data = _c(kv_data, np.uint8)
+    kv_scale = _c(kv_scale, np.uint8)
+    idx = _c(idx, np.int32)
+    swa = _c(swa, np.uint8).reshape(-1, D) if swa is not None else np.zeros((0, D), np.uint8)
+    out = np.zeros((H, D), np.float64)
+    lse = np.zeros(H, np.float64)
+    lib().orc_sparse_attn(_p(q), H, D, _p(kv_data), _p(kv_scale), _p(idx), idx.size,
+                          _p(swa) if swa.size else None, swa.shape[0], float(sm_scale),
+                          _p(out), _p(lse))
+    return out, lse
+
+
+def decode_batch(n_visible, q_data, q_e8m0, w, ik_data, ik_scale, kv_data, kv_scale,
+                 Q, swa, k=512, sm_scale=1.0, n_threads=0):
+    """Whole decode step for B sequences (score -> Top-k -> attention for the L
+    layers sharing the indices). Returns (idx [B, k], out [B, L, H, D], macs)."""
+    n_visible = _c(n_visible, np.int32)
+    B = n_visible.size
+    cap = ik_data.shape[1]
+    Q = _c(Q, np.float32)
+    _, L, H, D = Q.shape
+    swa = _c(swa, np.uint8)
+    n_swa = swa.shape[2]
+    arrs = [_c(a, np.uint8) for a in (q_data, q_e8m0, ik_data, ik_scale, kv_data, kv_scale)]
+    w = _c(w, np.float32)
+    idx = np.zeros((B, k), np.int32)
+    out = np.zeros((B, L, H, D), np.float64)
+    macs = lib().orc_decode_batch(B, cap, _p(n_visible), _p(arrs[0]), _p(arrs[1]), _p(w),
+                                  _p(arrs[2]), _p(arrs[3]), _p(arrs[4]), _p(arrs[5]), k, L,
+                                  _p(Q), H, D, _p(swa), n_swa, float(sm_scale), _p(idx),
+                                  _p(out), int(n_threads))
+    return idx, out, int(macs)
+
+
+def max_threads() -> int:
+    return lib().orc_max_threads()
