@@ -1,0 +1,437 @@
+"""Benchmark of the CSA2 decode hot path on GB300.
+
+One step = one decode pass of the whole index-and-attend path for a batch of
+sequences of the Full-layer decode workload (32 sequences x 65,536 visible
+entries; 32 x 128 MXFP4 indexer, Top-512, 64 x 512 attention over the 512
+selected FP4 latents + 128 FP8 SWA rows):
+
+    csa2_quant_mxfp4 (indexer q)  ->  csa2_index_score  ->  csa2_topk
+      ->  csa2_sparse_attn_decode
+
+with the KV cache resident in HBM. The timed region holds exactly --steps
+steps, each bracketed by CUDA events on the launching stream, with an L2
+flush (a 512 MiB write) between steps outside the events.
+
+Prints one JSON line. `value` is queries/s over all ranks; `e2e` is the same
+metric with each step's inputs copied from pinned host memory and its
+outputs copied back inside the timed region; `roofline` reports the indexer
+scan kernel (68 algorithmic bytes per scored entry) against the measured HBM
+copy bandwidth; `cpu_baseline` is the CPU oracle on a bounded sample.
+
+--impl reference runs the CPU oracle instead (the reference arm).
+Multi-GPU: launched with torch.distributed.run, every rank runs its own
+batch of sequences (weak scaling, no data-path collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD_ID = 1
+METRIC = "CSA2 decode queries/s at 64K-1M ctx; indexer-scan HBM GB/s vs GB300 peak"
+IK_BYTES_PER_ENTRY = 68        # 64 B E2M1 + 4 B E8M0 per indexer key
+KV_BYTES_PER_ENTRY = 288       # 256 B E2M1 + 32 B E4M3 per main-KV latent
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------- host logic
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_sequences(rank: int, B: int) -> list[int]:
+    """Sequence ids this rank owns: each rank runs its own batch of B."""
+    return list(range(rank * B, (rank + 1) * B))
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (barrier semantics come from the collective)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+def build_inputs(csa2, torch, B, N, seqs, device):
+    """Synthetic resident caches and per-step inputs, packed with the library's
+    own packers on the device (indexer K: MXFP4; main KV: E2M1 + E4M3/16;
+    SWA: E4M3)."""
+    from fp4_kv_cache_02_gb300.inputs import CAP_ALIGN, device_normal, device_uniform, round_up, seed_for
+    cap = round_up(N, CAP_ALIGN)
+    ik_data = torch.empty(B, cap, 64, dtype=torch.uint8, device=device)
+    ik_scale = torch.empty(B, cap, 4, dtype=torch.uint8, device=device)
+    kv_data = torch.empty(B, cap, 256, dtype=torch.uint8, device=device)
+    kv_scale = torch.empty(B, cap, 32, dtype=torch.uint8, device=device)
+    q_idx = torch.empty(B, 32, 128, dtype=torch.bfloat16, device=device)
+    w = torch.empty(B, 32, dtype=torch.float32, device=device)
+    Q = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=device)
+    swa = torch.empty(B, 1, 128, 512, dtype=torch.uint8, device=device)
+    for b, s in enumerate(seqs):
+        seed = seed_for(WORKLOAD_ID, s)
+        ik = device_normal((cap, 128), 4 * seed + 1, device)
+        csa2.csa2_quant_mxfp4(ik, ik_data[b], ik_scale[b])
+        kv = device_normal((cap, 512), 4 * seed + 2, device)
+        csa2.csa2_pack_kv_fp4(kv, kv_data[b], kv_scale[b])
+        q_idx[b] = device_normal((32, 128), 4 * seed + 3, device)
+        w[b] = device_uniform((32,), 4 * seed + 3, device)
+        Q[b] = device_normal((1, 64, 512), 4 * seed + 4, device, scale=1.0 / math.sqrt(512))
+        csa2.csa2_pack_fp8_e4m3(device_normal((1, 128, 512), 4 * seed + 5, device), swa[b])
+    n_visible = torch.full((B,), N, dtype=torch.int32, device=device)
+    torch.cuda.synchronize()
+    return dict(cap=cap, ik_data=ik_data, ik_scale=ik_scale, kv_data=kv_data, kv_scale=kv_scale, q_idx=q_idx, w=w,
+                Q=Q, swa=swa, n_visible=n_visible)
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    from fp4_kv_cache_02_gb300 import csa2
+    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
+
+    wl = WORKLOADS[WORKLOAD_ID]
+    B, N, K, W = wl.B, wl.N, 512, 128
+    seqs = rank_sequences(rank, B)
+    inp = build_inputs(csa2, torch, B, N, seqs, device)
+    cap = inp["cap"]
+    stream = torch.cuda.current_stream(device)
+
+    q_data = torch.empty(B, 32, 64, dtype=torch.uint8, device=device)
+    q_sc = torch.empty(B, 32, 4, dtype=torch.uint8, device=device)
+    scores = torch.empty(B, cap, dtype=torch.float32, device=device)
+    idx = torch.empty(B, K, dtype=torch.int32, device=device)
+    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=device)
+    tws = csa2.topk_workspace(B, cap, K, device=device)
+    aws = csa2.attn_workspace(B, K, W, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        csa2.csa2_index_score(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], scores,
+                              stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        csa2.csa2_topk(scores, K, idx, tws, n_valid=inp["n_visible"], stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        csa2.csa2_sparse_attn_decode(inp["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], idx, inp["swa"],
+                                     out, aws, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(1)                 # L2 flush between timed steps, outside the events
+            step(evs[i])
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    stage = [0.0] * 4
+    total = 0.0
+    for e in evs:
+        for j in range(4):
+            stage[j] += e[j].elapsed_time(e[j + 1])
+        total += e[0].elapsed_time(e[4])
+    ms = total / args.steps
+    stage_ms = [s / args.steps for s in stage]
+    ms_max = reduce_max(ms, world, device)
+
+    # ---- end to end: per-step inputs from pinned host memory, outputs back ----
+    h_q = inp["q_idx"].cpu().pin_memory()
+    h_w = inp["w"].cpu().pin_memory()
+    h_Q = inp["Q"].cpu().pin_memory()
+    h_swa = inp["swa"].cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_w, h_Q, h_swa))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out, h_idx))
+
+    def e2e_step():
+        inp["q_idx"].copy_(h_q, non_blocking=True)
+        inp["w"].copy_(h_w, non_blocking=True)
+        inp["Q"].copy_(h_Q, non_blocking=True)
+        inp["swa"].copy_(h_swa, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_idx.copy_(idx, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b_.record(stream)
+        b_.synchronize()
+        e2e_ms += a.elapsed_time(b_)
+    e2e_ms = reduce_max(e2e_ms / args.steps, world, device)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    hbm_peak, peak_kind = peaks()
+    scan_bytes = B * N * IK_BYTES_PER_ENTRY
+    scan_gbs = scan_bytes / (stage_ms[1] * 1e-3) / 1e9
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    if os.path.exists(tp):
+        try:
+            traffic = json.load(open(tp)).get("dram_bytes_per_launch")
+        except (ValueError, OSError):
+            traffic = None
+    qps = world * B / (ms_max * 1e-3)
+    n_attn_launches = 2 * math.ceil(B / 256)
+    line = {
+        "metric": METRIC,
+        "value": round(qps, 1),
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1/e4m3/e8m0 storage; fp32 scores; bf16 attention with fp32 accumulate",
+        "data": "synthetic N(0,1) caches drawn on the device, packed by the library",
+        "config": {"workload": "full_decode_b32_n65536", "sequences_per_gpu": B, "visible_entries": N,
+                   "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
+                   "l2": "flushed between steps (512 MiB write)", "parallelism": f"dp{world} (sequences)"},
+        "stages_ms": {"quant_q": round(stage_ms[0], 5), "index_score": round(stage_ms[1], 5),
+                      "topk": round(stage_ms[2], 5), "sparse_attn": round(stage_ms[3], 5)},
+        "entries_scored_per_s": round(world * B * N / (ms_max * 1e-3), 1),
+        "indexer_scan_gbs": round(scan_gbs, 1),
+        "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": round(scan_gbs, 1),
+                     "peak": hbm_peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
+                     "frac": round(scan_gbs / hbm_peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": scan_bytes},
+        "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": args.steps * (1 + 1 + 2 + n_attn_launches),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(n_seq: int, N: int):
+    """Host caches of `n_seq` sequences of the workload, quantised by the oracle."""
+    import numpy as np
+
+    import oracle
+    from fp4_kv_cache_02_gb300.inputs import decode_sequence
+    try:
+        import torch
+        gen_dev = "cuda" if torch.cuda.is_available() else None
+    except ImportError:
+        gen_dev = None
+    qd = np.zeros((n_seq, 32, 64), np.uint8)
+    qs = np.zeros((n_seq, 32, 4), np.uint8)
+    w = np.zeros((n_seq, 32), np.float32)
+    ikd = np.zeros((n_seq, N, 64), np.uint8)
+    iks = np.zeros((n_seq, N, 4), np.uint8)
+    kvd = np.zeros((n_seq, N, 256), np.uint8)
+    kvs = np.zeros((n_seq, N, 32), np.uint8)
+    Q = np.zeros((n_seq, 1, 64, 512), np.float32)
+    swa = np.zeros((n_seq, 1, 128, 512), np.uint8)
+    for b in range(n_seq):
+        d = decode_sequence(WORKLOAD_ID, b, N, device=gen_dev)
+        qd[b], qs[b] = oracle.quant_mxfp4(d["q_idx"])
+        w[b] = d["w"]
+        ikd[b], iks[b] = oracle.quant_mxfp4(d["ik"])
+        kvd[b], kvs[b] = oracle.pack_kv_fp4(d["kv"])
+        Q[b] = d["Q"]
+        swa[b] = oracle.pack_fp8(d["swa"].reshape(-1)).reshape(1, 128, 512)
+    return dict(n_visible=np.full(n_seq, N, np.int32), qd=qd, qs=qs, w=w, ikd=ikd, iks=iks, kvd=kvd, kvs=kvs, Q=Q,
+                swa=swa)
+
+
+def oracle_time(sample, threads: int, reps: int = 1) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode_batch(sample["n_visible"], sample["qd"], sample["qs"], sample["w"], sample["ikd"],
+                            sample["iks"], sample["kvd"], sample["kvs"], sample["Q"], sample["swa"], k=512,
+                            n_threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(budget_s: float = 20.0):
+    import oracle
+    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
+    N = WORKLOADS[WORKLOAD_ID].N
+    cores = oracle.max_threads()
+    n_seq = max(1, cores)
+    sample = oracle_sample(n_seq, N)
+    t = oracle_time(sample, cores)
+    reps = max(1, int(budget_s / max(t, 1e-3)) - 1)
+    t = oracle_time(sample, cores, reps) / reps
+    return {"value": round(n_seq / t, 3), "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_seq} sequences x {N} entries of the Full-layer decode workload "
+                      f"(score + Top-512 + attention), {reps} repetitions, OpenMP over sequences"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, timed on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
+    oracle.build()
+    N = WORKLOADS[WORKLOAD_ID].N
+    cores = oracle.max_threads()
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    probe = oracle_sample(1, N)
+    t1 = oracle_time(probe, cores)
+    n_seq = int(max(1, min(cores, per_step / max(t1, 1e-3))))
+    sample = oracle_sample(n_seq, N) if n_seq > 1 else probe
+    for _ in range(args.warmup):
+        oracle_time(sample, cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_time(sample, cores)
+    ms = (time.perf_counter() - t0) / args.steps * 1e3
+    qps = n_seq / (ms * 1e-3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(qps, 3), "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (oracle)", "data": "synthetic",
+        "config": {"workload": "full_decode_b32_n65536", "visible_entries": N, "topk": 512},
+        "cpu_baseline": {"value": round(qps, 3), "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_seq} sequence(s) x {N} entries per step"},
+        "e2e": {"value": round(qps, 3), "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

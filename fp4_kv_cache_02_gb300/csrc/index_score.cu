@@ -1,0 +1,151 @@
+// index_score.cu -- lightning-indexer scores over the MXFP4 indexer-K planes.
+//
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", section
+// 2.3 (indexer scores main-KV entries with indexer Q and indexer K), 2.3.1
+// (Full and Reindex layers run the indexer) and 2.3.2 (Reindex layers score
+// only the candidate pool); mer.dev notes section 4.4 (32 x 128 multiply-adds
+// per query-entry pair, ReLU-weighted sum over heads).
+//
+//   s[b][i] = sum_h w[b][h] * ReLU( qhat[b][h] . khat[b][p_i] )
+//
+// This file holds the CUDA-core scan used for positions lists, prefill and
+// small problems; the tensor-core scan lives in index_score_tc.cu.
+#include "common.cuh"
+
+namespace csa2 {
+
+__device__ int g_index_error = 0;
+
+// Dequantise one query's MXFP4 q into shared memory [32][128] fp32.
+__device__ __forceinline__ void load_qhat(const uint8_t* __restrict__ q_data,
+                                          const uint8_t* __restrict__ q_e8m0, float* qs) {
+  for (int i = threadIdx.x; i < kIdxHeads * kIdxDim; i += blockDim.x) {
+    int h = i / kIdxDim, c = i % kIdxDim;
+    uint32_t byte = q_data[h * kIkBytes + c / 2];
+    uint32_t code = (c & 1) ? (byte >> 4) : (byte & 0xF);
+    qs[i] = e2m1_to_f32(code) * e8m0_to_f32(q_e8m0[h * kIkScales + c / 32]);
+  }
+}
+
+// Score of one key row against the shared qhat: per 32-channel block the key
+// values are decoded into registers and folded into 32 per-head partial dots.
+__device__ __forceinline__ float score_row(const uint8_t* __restrict__ kd,
+                                           const uint8_t* __restrict__ ksc,
+                                           const float* qs, const float* ws) {
+  float dot[kIdxHeads];
+#pragma unroll
+  for (int h = 0; h < kIdxHeads; ++h) dot[h] = 0.0f;
+  uint32_t scales = *reinterpret_cast<const uint32_t*>(ksc);
+#pragma unroll 1
+  for (int kb = 0; kb < 4; ++kb) {
+    uint4 v = *reinterpret_cast<const uint4*>(kd + kb * 16);
+    float s = e8m0_to_f32((scales >> (8 * kb)) & 0xFF);
+    uint32_t words[4] = {v.x, v.y, v.z, v.w};
+    float kv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) kv[i] = e2m1_to_f32((words[i / 8] >> (4 * (i % 8))) & 0xF) * s;
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; ++h) {
+      const float* qrow = qs + h * kIdxDim + kb * 32;
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc = fmaf(qrow[i], kv[i], acc);
+      dot[h] += acc;
+    }
+  }
+  float s = 0.0f;
+#pragma unroll
+  for (int h = 0; h < kIdxHeads; ++h) s = fmaf(ws[h], fmaxf(dot[h], 0.0f), s);
+  return s;
+}
+
+// grid (ceil(n_pos / blockDim), B); one thread per scored row.
+__global__ void __launch_bounds__(128) index_score_simple_kernel(
+    const uint8_t* __restrict__ q_data, const uint8_t* __restrict__ q_e8m0,
+    const float* __restrict__ w, const uint8_t* __restrict__ ik_data,
+    const uint8_t* __restrict__ ik_scale, int64_t cap, const int32_t* __restrict__ n_visible,
+    const int32_t* __restrict__ positions, int64_t n_pos, float* __restrict__ scores) {
+  __shared__ float qs[kIdxHeads * kIdxDim];
+  __shared__ float ws[kIdxHeads];
+  const int b = blockIdx.y;
+  load_qhat(q_data + (int64_t)b * kIdxHeads * kIkBytes, q_e8m0 + (int64_t)b * kIdxHeads * kIkScales, qs);
+  if (threadIdx.x < kIdxHeads) ws[threadIdx.x] = w[b * kIdxHeads + threadIdx.x];
+  __syncthreads();
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_pos) return;
+  int64_t p = positions ? (int64_t)positions[(int64_t)b * n_pos + i] : i;
+  int64_t nv = n_visible[b];
+  float out = -INFINITY;
+  if (p >= 0 && p < nv && p < cap) {
+    const uint8_t* kd = ik_data + ((int64_t)b * cap + p) * kIkBytes;
+    const uint8_t* ks = ik_scale + ((int64_t)b * cap + p) * kIkScales;
+    out = score_row(kd, ks, qs, ws);
+  }
+  scores[(int64_t)b * n_pos + i] = out;
+}
+
+// Prefill: grid (ceil(n_entries / blockDim), T); query t sees 0..p0+t.
+__global__ void __launch_bounds__(128) prefill_score_simple_kernel(
+    const uint8_t* __restrict__ q_data, const uint8_t* __restrict__ q_e8m0,
+    const float* __restrict__ w, const uint8_t* __restrict__ ik_data,
+    const uint8_t* __restrict__ ik_scale, int64_t n_entries, int64_t p0,
+    float* __restrict__ scores) {
+  __shared__ float qs[kIdxHeads * kIdxDim];
+  __shared__ float ws[kIdxHeads];
+  const int t = blockIdx.y;
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x;
+  const int64_t last_visible = p0 + t;
+  int64_t i = first + threadIdx.x;
+  if (first > last_visible) {  // whole block masked
+    if (i < n_entries) scores[(int64_t)t * n_entries + i] = -INFINITY;
+    return;
+  }
+  load_qhat(q_data + (int64_t)t * kIdxHeads * kIkBytes, q_e8m0 + (int64_t)t * kIdxHeads * kIkScales, qs);
+  if (threadIdx.x < kIdxHeads) ws[threadIdx.x] = w[t * kIdxHeads + threadIdx.x];
+  __syncthreads();
+  if (i >= n_entries) return;
+  float out = -INFINITY;
+  if (i <= last_visible) out = score_row(ik_data + i * kIkBytes, ik_scale + i * kIkScales, qs, ws);
+  scores[(int64_t)t * n_entries + i] = out;
+}
+
+}  // namespace csa2
+
+using namespace csa2;
+
+int csa2_read_and_clear_index_error(cudaStream_t s) {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_index_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_index_error, &z, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CSA2_ERR_CUDA;
+  return v;
+}
+
+// Launch helpers shared with the fused path in capi.cu.
+int csa2_launch_index_score_simple(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
+                                   const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
+                                   const int32_t* n_visible, const int32_t* positions, int64_t n_pos,
+                                   float* scores, cudaStream_t stream) {
+  if (n_pos == 0 || B == 0) return CSA2_OK;
+  dim3 grid((unsigned)((n_pos + 127) / 128), (unsigned)B);
+  index_score_simple_kernel<<<grid, 128, 0, stream>>>(q_data, q_e8m0, w, ik_data, ik_scale, cap, n_visible,
+                                                      positions, n_pos, scores);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}
+
+extern "C" int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w,
+                                        int32_t T, const uint8_t* ik_data, const uint8_t* ik_scale,
+                                        int64_t n_entries, int64_t p0, float* scores, csa2_stream_t stream) {
+  if (!q_data || !q_e8m0 || !w || !ik_data || !ik_scale || !scores) return CSA2_ERR_INVALID_ARG;
+  if (T < 0 || n_entries < 0 || p0 < 0 || p0 + T > n_entries) return CSA2_ERR_INVALID_ARG;
+  if (!csa2_aligned(ik_data, 16) || !csa2_aligned(ik_scale, 4)) return CSA2_ERR_ALIGNMENT;
+  if (T == 0 || n_entries == 0) return CSA2_OK;
+  dim3 grid((unsigned)((n_entries + 127) / 128), (unsigned)T);
+  prefill_score_simple_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(q_data, q_e8m0, w, ik_data, ik_scale,
+                                                                       n_entries, p0, scores);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}

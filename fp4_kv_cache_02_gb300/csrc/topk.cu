@@ -1,0 +1,476 @@
+// topk.cu -- Top-K selection and the hierarchical block pool.
+//
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", section
+// 2.3 (the indexer selects the Top-K entries for each query) and section 2.3.2
+// with Figure 5 (each block of positions takes the maximum index score among
+// its positions; the highest-scoring blocks form the candidate pool).
+//
+// Radix/threshold select on order-preserving 32-bit keys of the fp32 scores:
+//   1. histogram of the top 12 key bits per row (shared-memory histogram per
+//      CTA, flushed to a per-row global histogram);
+//   2. every CTA finds the threshold bin t of its row (the bin in which the
+//      running count from the top reaches k), then streams its slice: keys
+//      above bin t are selected outright, keys inside bin t become candidates;
+//   3. the last CTA of the row (ticket counter, no waiting) resolves bin t
+//      exactly on the remaining 20 key bits, breaks exact ties by smaller
+//      position, sorts the k positions ascending and writes them.
+// The result does not depend on the order in which CTAs run.
+#include "common.cuh"
+
+namespace csa2 {
+
+__device__ int g_topk_error = 0;
+
+constexpr int kHistBits = 12;
+constexpr int kHistBins = 1 << kHistBits;  // 4096
+constexpr int kSelThreads = 256;
+
+struct RowCounters {
+  uint32_t n_sel;   // positions appended to sel
+  uint32_t n_cand;  // (key, position) pairs appended to cand
+  uint32_t done;    // CTAs of the row that finished streaming
+  uint32_t pad;
+};
+
+struct TopkWs {
+  uint32_t* hist;       // [B][4096]
+  RowCounters* cnt;     // [B]
+  int32_t* sel;         // [B][k]
+  uint2* cand;          // [B][n]  (key, position)
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline size_t topk_ws_layout(int32_t B, int64_t n, int32_t k, TopkWs* ws, char* base) {
+  size_t off = 0;
+  size_t hist = off; off = align_up(off + (size_t)B * kHistBins * 4, 256);
+  size_t cnt = off;  off = align_up(off + (size_t)B * sizeof(RowCounters), 256);
+  size_t sel = off;  off = align_up(off + (size_t)B * k * 4, 256);
+  size_t cand = off; off = align_up(off + (size_t)B * (size_t)(n > 0 ? n : 1) * 8, 256);
+  if (ws) {
+    ws->hist = (uint32_t*)(base + hist);
+    ws->cnt = (RowCounters*)(base + cnt);
+    ws->sel = (int32_t*)(base + sel);
+    ws->cand = (uint2*)(base + cand);
+  }
+  return off;
+}
+
+__host__ __device__ inline size_t topk_ws_zero_bytes(int32_t B) {
+  return align_up(align_up((size_t)B * kHistBins * 4, 256) + (size_t)B * sizeof(RowCounters), 256);
+}
+
+__device__ __forceinline__ bool load_candidate(const float* __restrict__ scores, const int32_t* __restrict__ positions,
+                                               int64_t row_off, int64_t i, int64_t nv, uint32_t* key, int32_t* pos) {
+  if (i >= nv) return false;
+  float s = scores[row_off + i];
+  int32_t p = positions ? positions[row_off + i] : (int32_t)i;
+  if (p < 0 || !score_is_candidate(s)) return false;
+  *key = score_key(s);
+  *pos = p;
+  return true;
+}
+
+// ---- pass 1: histogram of the top 12 key bits --------------------------------
+__global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
+    const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
+    const int32_t* __restrict__ positions, int64_t chunk, TopkWs ws) {
+  __shared__ uint32_t sh[kHistBins];
+  const int b = blockIdx.y;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  const int64_t row_off = (int64_t)b * n;
+  int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
+  int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    uint32_t key;
+    int32_t p;
+    if (load_candidate(scores, positions, row_off, i, nv, &key, &p)) atomicAdd(&sh[key >> (32 - kHistBits)], 1u);
+  }
+  __syncthreads();
+  uint32_t* gh = ws.hist + (size_t)b * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+}
+
+// Block-wide search, from the top bin down, for the first bin at which the
+// running count reaches `need`. Returns the bin (-1 if the total is below
+// `need`) and the count strictly above it. `h` has `nbins` entries in shared
+// memory; nbins is a multiple of blockDim.x.
+__device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
+                                  uint32_t* scratch /* blockDim.x + 2 */) {
+  const int per = nbins / blockDim.x;
+  // thread j owns bins [nbins - (j+1)*per, nbins - j*per) (descending order)
+  const int top = nbins - threadIdx.x * per;
+  uint32_t local = 0;
+  for (int i = 1; i <= per; ++i) local += h[top - i];
+  scratch[threadIdx.x] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t run = 0;
+    int found = -1;
+    uint32_t above = 0;
+    for (int j = 0; j < (int)blockDim.x && found < 0; ++j) {
+      if (run + scratch[j] >= need) {
+        // resolve within thread j's bins
+        int tj = nbins - j * per;
+        for (int i = 1; i <= per; ++i) {
+          uint32_t c = h[tj - i];
+          if (run + c >= need) { found = tj - i; above = run; break; }
+          run += c;
+        }
+      } else {
+        run += scratch[j];
+      }
+    }
+    scratch[blockDim.x] = (uint32_t)found;
+    scratch[blockDim.x + 1] = found < 0 ? run : above;
+  }
+  __syncthreads();
+  int bin = (int)scratch[blockDim.x];
+  *above_out = scratch[blockDim.x + 1];
+  __syncthreads();
+  return bin;
+}
+
+// Exact r-th largest among `count` 32-bit keys (in global memory, key field of
+// uint2 or the `x` values of an int array transform), restricted to those whose
+// top `fixed_bits` equal `prefix`. Radix passes over the remaining bits with
+// `bits_per_pass` bits each. Returns the full threshold key; *r_left is how
+// many keys equal to the threshold are still needed.
+template <typename KeyFn>
+__device__ uint32_t radix_select_desc(int count, uint32_t need, int fixed_bits, uint32_t prefix,
+                                      KeyFn keyfn, uint32_t* hist /*1024*/, uint32_t* scratch,
+                                      uint32_t* r_left) {
+  int done_bits = fixed_bits;
+  while (done_bits < 32) {
+    int pass_bits = min(10, 32 - done_bits);
+    int nb = 1 << pass_bits;
+    int nbins = nb < (int)blockDim.x ? (int)blockDim.x : nb;  // pad to a multiple of blockDim
+    for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    int shift = 32 - done_bits - pass_bits;
+    for (int i = threadIdx.x; i < count; i += blockDim.x) {
+      uint32_t key = keyfn(i);
+      bool match = done_bits == 0 ? true : ((key >> (32 - done_bits)) == (prefix >> (32 - done_bits)));
+      if (match) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    uint32_t above;
+    int bin = find_threshold_bin(hist, nbins, need, &above, scratch);
+    // bin >= 0 always: callers guarantee at least `need` matching keys
+    prefix |= ((uint32_t)bin) << shift;
+    need -= above;
+    done_bits += pass_bits;
+  }
+  *r_left = need;
+  return prefix;
+}
+
+__device__ void bitonic_sort_asc(int32_t* a, int n_pow2) {
+  for (int size = 2; size <= n_pow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        int j = i ^ stride;
+        if (j > i) {
+          bool up = (i & size) == 0;
+          int32_t x = a[i], y = a[j];
+          if ((x > y) == up) { a[i] = y; a[j] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// ---- pass 2: stream, select above the threshold bin, finalize in the last CTA --
+__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
+    const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
+    const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws,
+    int32_t* __restrict__ idx) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* h = smem;                           // kHistBins
+  uint32_t* scratch = smem + kHistBins;         // kSelThreads + 8
+  __shared__ int s_is_last;
+  const int b = blockIdx.y;
+  const uint32_t* gh = ws.hist + (size_t)b * kHistBins;
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = __ldcg(gh + i);
+  __syncthreads();
+  uint32_t above;
+  const int t = find_threshold_bin(h, kHistBins, (uint32_t)k, &above, scratch);
+  const uint32_t c_t = t >= 0 ? h[t] : 0u;
+
+  const int64_t row_off = (int64_t)b * n;
+  int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
+  int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
+  RowCounters* cnt = ws.cnt + b;
+  int32_t* sel = ws.sel + (size_t)b * k;
+  uint2* cand = ws.cand + (size_t)b * n;
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = lo; base < hi; base += blockDim.x) {
+    int64_t i = base + threadIdx.x;
+    uint32_t key = 0;
+    int32_t p = 0;
+    bool ok = i < hi && load_candidate(scores, positions, row_off, i, nv, &key, &p);
+    int digit = ok ? (int)(key >> (32 - kHistBits)) : -2;
+    bool take = ok && digit > t;
+    bool keep = ok && digit == t;
+    uint32_t mt = __ballot_sync(0xffffffffu, take);
+    uint32_t mk = __ballot_sync(0xffffffffu, keep);
+    uint32_t bt = 0, bk = 0;
+    if (lane == 0) {
+      if (mt) bt = atomicAdd(&cnt->n_sel, __popc(mt));
+      if (mk) bk = atomicAdd(&cnt->n_cand, __popc(mk));
+    }
+    bt = __shfl_sync(0xffffffffu, bt, 0);
+    bk = __shfl_sync(0xffffffffu, bk, 0);
+    uint32_t lower = (1u << lane) - 1u;
+    if (take) {
+      uint32_t slot = bt + __popc(mt & lower);
+      if (slot < (uint32_t)k) sel[slot] = p;
+      else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+    }
+    if (keep) {
+      uint32_t slot = bk + __popc(mk & lower);
+      if (slot < (uint32_t)n) cand[slot] = make_uint2(key, (uint32_t)p);
+      else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t ticket = atomicAdd(&cnt->done, 1u);
+    s_is_last = ticket == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_is_last) return;
+  __threadfence();
+
+  // ---- finalize row b ----
+  int32_t* out = (int32_t*)(smem + kHistBins + kSelThreads + 8);  // room for CSA2_MAX_TOPK
+  __shared__ uint32_t s_nout;
+  const uint32_t n_sel = min(__ldcg(&cnt->n_sel), (uint32_t)k);
+  const uint32_t n_cand = min(__ldcg(&cnt->n_cand), (uint32_t)n);
+  if (threadIdx.x == 0) s_nout = 0;
+  for (uint32_t i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = __ldcg(sel + i);
+  __syncthreads();
+  if (threadIdx.x == 0) s_nout = n_sel;
+  __syncthreads();
+  if (t >= 0) {
+    uint32_t r = (uint32_t)k - above;  // still needed from bin t (1 <= r <= c_t)
+    if (r >= n_cand || r >= c_t) {
+      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+        uint32_t slot = atomicAdd(&s_nout, 1u);
+        if (slot < (uint32_t)k) out[slot] = (int32_t)__ldcg(&cand[i].y);
+      }
+    } else {
+      uint32_t r2;
+      uint32_t T = radix_select_desc(
+          (int)n_cand, r, kHistBits, ((uint32_t)t) << (32 - kHistBits),
+          [&](int i) { return __ldcg(&cand[i].x); }, h, scratch, &r2);
+      // keys above T are all taken; among keys equal to T the r2 smallest
+      // positions are taken (select on ~position, largest first)
+      uint32_t n_eq = 0;
+      {
+        // count keys == T
+        __shared__ uint32_t s_eq;
+        if (threadIdx.x == 0) s_eq = 0;
+        __syncthreads();
+        uint32_t local = 0;
+        for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) local += (__ldcg(&cand[i].x) == T);
+        atomicAdd(&s_eq, local);
+        __syncthreads();
+        n_eq = s_eq;
+        __syncthreads();
+      }
+      uint32_t P = 0xFFFFFFFFu, r3 = 0;
+      bool all_eq = r2 >= n_eq;
+      if (!all_eq) {
+        // positions are >= 0, so ~position has bit 31 set: select the r2
+        // largest ~position among keys == T
+        P = radix_select_desc(
+            (int)n_cand, r2, 0, 0u,
+            [&](int i) {
+              uint2 c = __ldcg(&cand[i]);
+              return c.x == T ? ~c.y : 0u;
+            },
+            h, scratch, &r3);
+      }
+      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
+        uint2 c = __ldcg(&cand[i]);
+        bool take = c.x > T || (c.x == T && (all_eq || (~c.y) > P));
+        if (take) {
+          uint32_t slot = atomicAdd(&s_nout, 1u);
+          if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
+        }
+      }
+      __syncthreads();
+      // exactly r3 further ties sit at ~position == P (distinct positions: r3 <= 1)
+      if (!all_eq && threadIdx.x == 0) {
+        for (uint32_t i = 0; i < n_cand && r3 > 0; ++i) {
+          uint2 c = __ldcg(&cand[i]);
+          if (c.x == T && ~c.y == P) {
+            uint32_t slot = s_nout++;
+            if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
+            --r3;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  uint32_t nout = min(s_nout, (uint32_t)k);
+  int n2 = 1;
+  while (n2 < k) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    if (i >= (int)nout) out[i] = 0x7FFFFFFF;
+  __syncthreads();
+  bitonic_sort_asc(out, n2);
+  int32_t* dst = idx + (size_t)b * k;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) dst[i] = i < (int)nout ? out[i] : -1;
+}
+
+// ---- block pool ---------------------------------------------------------------
+// bmax[b][j] = max of scores[b][block*j .. block*j+block) within [0, n_visible[b]).
+__global__ void block_max_kernel(const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_visible,
+                                 int32_t block, int64_t nb, float* __restrict__ bmax) {
+  const int b = blockIdx.y;
+  int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= nb) return;
+  int64_t nv = n_visible ? min((int64_t)n_visible[b], n) : n;
+  float m = -INFINITY;
+  for (int r = 0; r < block; ++r) {
+    int64_t p = j * block + r;
+    if (p < nv) {
+      float s = scores[(int64_t)b * n + p];
+      if (!isnan(s)) m = fmaxf(m, s);
+    }
+  }
+  bmax[(int64_t)b * nb + j] = m;
+}
+
+__global__ void pool_expand_kernel(const int32_t* __restrict__ blocks, int32_t n_blocks, int32_t block,
+                                   const int32_t* __restrict__ n_visible, int64_t n, int32_t* __restrict__ pool) {
+  const int b = blockIdx.y;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)n_blocks * block) return;
+  int64_t nv = n_visible ? min((int64_t)n_visible[b], n) : n;
+  int32_t blk = blocks[(int64_t)b * n_blocks + i / block];
+  int64_t p = blk >= 0 ? (int64_t)blk * block + i % block : -1;
+  pool[(int64_t)b * n_blocks * block + i] = (p >= 0 && p < nv) ? (int32_t)p : -1;
+}
+
+}  // namespace csa2
+
+using namespace csa2;
+
+int csa2_read_and_clear_topk_error(cudaStream_t s) {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_topk_error, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaMemcpyToSymbolAsync(g_topk_error, &z, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CSA2_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CSA2_ERR_CUDA;
+  return v;
+}
+
+static int64_t topk_chunk(int32_t B, int64_t n) {
+  // aim for a few CTAs per SM across the whole batch
+  int64_t target_ctas = 152 * 4;
+  int64_t per_row = (target_ctas + B - 1) / B;
+  int64_t chunk = (n + per_row - 1) / per_row;
+  chunk = (chunk + 1023) / 1024 * 1024;
+  if (chunk < 2048) chunk = 2048;
+  return chunk;
+}
+
+static size_t topk_select_smem(int32_t k) {
+  int n2 = 1;
+  while (n2 < k) n2 <<= 1;
+  return (size_t)(kHistBins + kSelThreads + 8) * 4 + (size_t)n2 * 4;
+}
+
+extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
+  if (B <= 0 || n < 0 || k <= 0) return 0;
+  return topk_ws_layout(B, n, k, nullptr, nullptr);
+}
+
+int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
+                     int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (B == 0) return CSA2_OK;
+  size_t need = topk_ws_layout(B, n, k, nullptr, nullptr);
+  if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
+  TopkWs ws;
+  topk_ws_layout(B, n, k, &ws, (char*)workspace);
+  if (cudaMemsetAsync(workspace, 0, topk_ws_zero_bytes(B), stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  int64_t chunk = topk_chunk(B, n);
+  int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
+  dim3 grid((unsigned)chunks, (unsigned)B);
+  topk_hist_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, ws);
+  CSA2_CHECK_LAUNCH();
+  size_t smem = topk_select_smem(k);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)topk_select_smem(CSA2_MAX_TOPK));
+    attr_set = true;
+  }
+  topk_select_kernel<<<grid, kSelThreads, smem, stream>>>(scores, n, n_valid, positions, chunk, k, ws, idx);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}
+
+extern "C" int csa2_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid,
+                         const int32_t* positions, int32_t k, int32_t* idx, void* workspace,
+                         size_t workspace_bytes, csa2_stream_t stream) {
+  if (!scores || !idx || B < 0 || n < 0) return CSA2_ERR_INVALID_ARG;
+  if (k <= 0 || k > CSA2_MAX_TOPK) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (n > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  return csa2_launch_topk(scores, B, n, n_valid, positions, k, idx, workspace, workspace_bytes,
+                          (cudaStream_t)stream);
+}
+
+extern "C" size_t csa2_block_pool_workspace_size(int32_t B, int64_t n, int32_t block, int32_t n_blocks) {
+  if (B <= 0 || n < 0 || block <= 0 || n_blocks <= 0) return 0;
+  int64_t nb = (n + block - 1) / block;
+  size_t off = align_up((size_t)B * (size_t)(nb > 0 ? nb : 1) * 4, 256);
+  off += align_up((size_t)B * n_blocks * 4, 256);
+  off += topk_ws_layout(B, nb, n_blocks, nullptr, nullptr);
+  return off;
+}
+
+int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
+                           int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  if (B == 0) return CSA2_OK;
+  size_t need = csa2_block_pool_workspace_size(B, n, block, n_blocks);
+  if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
+  int64_t nb = (n + block - 1) / block;
+  char* base = (char*)workspace;
+  float* bmax = (float*)base;
+  size_t off = align_up((size_t)B * (size_t)(nb > 0 ? nb : 1) * 4, 256);
+  int32_t* blocks = (int32_t*)(base + off);
+  off += align_up((size_t)B * n_blocks * 4, 256);
+  if (nb > 0) {
+    dim3 g1((unsigned)((nb + 255) / 256), (unsigned)B);
+    block_max_kernel<<<g1, 256, 0, stream>>>(scores, n, n_visible, block, nb, bmax);
+    CSA2_CHECK_LAUNCH();
+  }
+  int rc = csa2_launch_topk(bmax, B, nb, nullptr, nullptr, n_blocks, blocks, base + off, workspace_bytes - off,
+                            stream);
+  if (rc) return rc;
+  int64_t total = (int64_t)n_blocks * block;
+  dim3 g2((unsigned)((total + 255) / 256), (unsigned)B);
+  pool_expand_kernel<<<g2, 256, 0, stream>>>(blocks, n_blocks, block, n_visible, n, pool);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}
+
+extern "C" int csa2_block_pool(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
+                               int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
+                               csa2_stream_t stream) {
+  if (!scores || !pool || B < 0 || n < 0 || block <= 0 || n_blocks <= 0) return CSA2_ERR_INVALID_ARG;
+  if (n_blocks > CSA2_MAX_TOPK || n > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  return csa2_launch_block_pool(scores, B, n, n_visible, block, n_blocks, pool, workspace, workspace_bytes,
+                                (cudaStream_t)stream);
+}

@@ -85,20 +85,32 @@ def _normal(rng: np.random.Generator, shape) -> np.ndarray:
     return rng.standard_normal(shape, dtype=np.float32)
 
 
+def _big_normal(rng: np.random.Generator, shape, seed: int, device) -> np.ndarray:
+    """N(0,1) float32 on the host; drawn with torch's seeded generator on
+    `device` when given (fast for the 1M-entry workloads), else with numpy."""
+    if device is None:
+        return _normal(rng, shape)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32).cpu().numpy()
+
+
 def decode_sequence(workload: int, seq: int, N: int, L: int = 1,
                     reindex: bool = False, planted_blocks: int = 0,
-                    n_swa: int = SWA_W) -> dict:
+                    n_swa: int = SWA_W, device=None) -> dict:
     """Host (numpy float32, bf16-exact) inputs of one decode sequence.
 
     Keys: q_idx [32,128], w [32], ik [N,128], kv [N,512], Q [L,64,512],
     swa [L,n_swa,512]; for reindex also q_re [32,128], w_re [32], and
-    planted (the planted block ids, sorted)."""
-    rng = np.random.default_rng(seed_for(workload, seq))
+    planted (the planted block ids, sorted). With `device`, the two large
+    planes (ik, kv) are drawn by torch's generator on that device."""
+    seed = seed_for(workload, seq)
+    rng = np.random.default_rng(seed)
     out = {}
     out["q_idx"] = bf16_round(_normal(rng, (IDX_HEADS, IDX_DIM)))
     out["w"] = rng.uniform(0.0, 1.0, IDX_HEADS).astype(np.float32)
-    ik = _normal(rng, (N, IDX_DIM))
-    out["kv"] = bf16_round(_normal(rng, (N, HEAD_DIM)))
+    ik = _big_normal(rng, (N, IDX_DIM), 4 * seed + 1, device)
+    out["kv"] = bf16_round(_big_normal(rng, (N, HEAD_DIM), 4 * seed + 2, device))
     out["Q"] = bf16_round(_normal(rng, (L, HEADS, HEAD_DIM)) / np.float32(math.sqrt(HEAD_DIM)))
     out["swa"] = bf16_round(_normal(rng, (L, n_swa, HEAD_DIM)))
     if reindex:
@@ -118,19 +130,21 @@ def decode_sequence(workload: int, seq: int, N: int, L: int = 1,
     return out
 
 
-def prefill_chunk(workload: int, T: int, N0: int, n_swa: int = SWA_W) -> dict:
+def prefill_chunk(workload: int, T: int, N0: int, n_swa: int = SWA_W, device=None) -> dict:
     """Host inputs of a prefill chunk: T queries at positions N0..N0+T-1 over
     N0+T entries. Keys: q_idx [T,32,128], w [T,32], ik [N0+T,128],
     kv [N0+T,512], Q [T,64,512], swa [T+n_swa-1,512] (row r is position
-    N0-(n_swa-1)+r)."""
-    rng = np.random.default_rng(seed_for(workload, 0))
+    N0-(n_swa-1)+r). With `device`, the large arrays are drawn there."""
+    seed = seed_for(workload, 0)
+    rng = np.random.default_rng(seed)
     N = N0 + T
     return {
-        "q_idx": bf16_round(_normal(rng, (T, IDX_HEADS, IDX_DIM))),
+        "q_idx": bf16_round(_big_normal(rng, (T, IDX_HEADS, IDX_DIM), 4 * seed + 1, device)),
         "w": rng.uniform(0.0, 1.0, (T, IDX_HEADS)).astype(np.float32),
-        "ik": bf16_round(_normal(rng, (N, IDX_DIM))),
-        "kv": bf16_round(_normal(rng, (N, HEAD_DIM))),
-        "Q": bf16_round(_normal(rng, (T, HEADS, HEAD_DIM)) / np.float32(math.sqrt(HEAD_DIM))),
+        "ik": bf16_round(_big_normal(rng, (N, IDX_DIM), 4 * seed + 2, device)),
+        "kv": bf16_round(_big_normal(rng, (N, HEAD_DIM), 4 * seed + 3, device)),
+        "Q": bf16_round(_big_normal(rng, (T, HEADS, HEAD_DIM), 4 * seed + 4, device)
+                        / np.float32(math.sqrt(HEAD_DIM))),
         "swa": bf16_round(_normal(rng, (T + n_swa - 1, HEAD_DIM))),
     }
 

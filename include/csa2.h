@@ -1,0 +1,294 @@
+/*
+ * csa2.h -- C ABI of the CSA2 sparse-attention hot path over an FP4 global
+ * KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation follows the CSA2 layer of "DeepSeek-V4.1-Flash: Pushing the
+ * Limits of KV Cache Compression" (technical report, sections 2.3, 2.3.1,
+ * 2.3.2 and 2.4.4), with the sizes given in the mer.dev notes on the same
+ * report (section 1 setup, section 2 byte layout, section 4):
+ *   - lightning-indexer score of every visible entry,
+ *       s[j] = sum_h w[h] * ReLU(q_h . k_j)   (32 heads x 128, MXFP4 q and k)
+ *   - optional hierarchical candidate pool (top 2,048 blocks of 8 positions
+ *     by block-max score) that restricts later Reindex layers;
+ *   - Top-512 selection;
+ *   - 64-head, head-dim-512 attention in which the selected 512-channel
+ *     latents (E2M1 + one E4M3 scale per 16 channels) serve as both K and V,
+ *     in one softmax with the 128-row FP8 sliding window of the layer.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer is a caller-owned DEVICE pointer unless stated otherwise.
+ *     No entry point allocates device memory. Scratch space is sized by the
+ *     matching *_workspace_size function and passed in by the caller.
+ *   - Every call is asynchronous and ordered on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream). A return of CSA2_OK means the work
+ *     was enqueued; errors found by the kernels themselves (an index out of
+ *     range, a bounded wait that ran out) are recorded in a sticky device
+ *     word that csa2_get_last_error() reads and clears.
+ *   - Host-side argument checks return a negative status and enqueue nothing.
+ *   - bf16 arrays are passed as `const void*` holding IEEE bfloat16 values.
+ *   - Packed FP4: element 2i of a row is the low nibble of byte i, element
+ *     2i+1 the high nibble.
+ *   - Cache planes are struct-of-arrays, one plane per field, sequences
+ *     `cap` entries apart:
+ *         ik_data  [B][cap][64]  E2M1 indexer key       (64 B / entry)
+ *         ik_scale [B][cap][4]   E8M0, one per 32       ( 4 B / entry)
+ *         kv_data  [B][cap][256] E2M1 main-KV latent    (256 B / entry)
+ *         kv_scale [B][cap][32]  E4M3, one per 16       ( 32 B / entry)
+ *     which is 68 + 288 = 356 bytes per entry as in the notes' section 2.
+ *     `cap` must be a multiple of CSA2_CAP_ALIGN and plane base pointers
+ *     16-byte aligned; entries at positions >= n_visible[b] may hold any
+ *     bytes and are never selected.
+ *   - Rounding of the encoders: round-to-nearest-even, saturating at the
+ *     largest finite value; inputs must be finite.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/** A cudaStream_t. */
+typedef struct CUstream_st* csa2_stream_t;
+
+/* status codes */
+#define CSA2_OK 0
+#define CSA2_ERR_INVALID_ARG (-1)      /* null pointer, negative size, bad value   */
+#define CSA2_ERR_UNSUPPORTED_SHAPE (-2) /* a size outside what the kernels support  */
+#define CSA2_ERR_ALIGNMENT (-3)        /* pointer or capacity not aligned          */
+#define CSA2_ERR_CUDA (-4)             /* a CUDA runtime call or launch failed     */
+#define CSA2_ERR_TIMEOUT (-5)          /* a bounded device-side wait ran out       */
+#define CSA2_ERR_WORKSPACE (-6)        /* workspace too small or misaligned        */
+#define CSA2_ERR_DEVICE (-7)           /* a kernel rejected an input (e.g. index)  */
+
+/* sizes fixed by the method (notes section 1 setup) */
+#define CSA2_IDX_HEADS 32
+#define CSA2_IDX_DIM 128
+#define CSA2_HEADS 64
+#define CSA2_HEAD_DIM 512
+#define CSA2_TOPK 512
+#define CSA2_SWA 128
+#define CSA2_POOL_BLOCK 8
+#define CSA2_POOL_BLOCKS 2048
+#define CSA2_CAP_ALIGN 128
+#define CSA2_MAX_TOPK 4096
+
+/** Library version, major*10000 + minor*100 + patch. */
+int csa2_version(void);
+
+/** A static string naming a status code. */
+const char* csa2_status_string(int status);
+
+/**
+ * Waits for `stream`, then reads and clears the sticky device error words of
+ * all kernels. *device_status receives CSA2_OK or the first negative status a
+ * kernel recorded. Returns CSA2_ERR_CUDA if the synchronisation failed.
+ */
+int csa2_get_last_error(csa2_stream_t stream, int* device_status);
+
+/* ======================================================================== */
+/* FP4 / FP8 codecs                                                          */
+/* ======================================================================== */
+
+/**
+ * MXFP4 quantisation (report section 2.4.4: OCP-standard MXFP4 for indexer
+ * queries and keys; notes section 2: one E8M0 scale per 32 elements).
+ * x [rows][cols] bf16 -> data [rows][cols/2] packed E2M1, e8m0 [rows][cols/32].
+ * Per 32-element block: X = floor(log2(amax)) - 2 clamped to [-127, 127]
+ * (X = -127 for an all-zero block), scale byte X + 127, element
+ * RNE_E2M1(x * 2^-X) saturating at +-6. cols must be a positive multiple of
+ * 32. Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA.
+ */
+int csa2_quant_mxfp4(const void* x_bf16, int64_t rows, int32_t cols,
+                     uint8_t* data, uint8_t* e8m0, csa2_stream_t stream);
+
+/** Inverse of csa2_quant_mxfp4: out [rows][cols] fp32 = e2m1 * 2^(e - 127). */
+int csa2_dequant_mxfp4(const uint8_t* data, const uint8_t* e8m0, int64_t rows,
+                       int32_t cols, float* out, csa2_stream_t stream);
+
+/**
+ * Main-KV packing (report section 2.4.4: E2M1 with one E4M3 scale per 16
+ * channels, NVFP4 without its second-level global scale).
+ * x [n][512] bf16 -> kv_data [n][256], kv_scale [n][32].
+ * Per 16-channel block: s = RNE_E4M3(amax / 6) with the quotient in IEEE
+ * fp32; element RNE_E2M1(x / s) in fp32 saturating at +-6; s == 0 gives an
+ * all-zero block. Errors: INVALID_ARG, CUDA.
+ */
+int csa2_pack_kv_fp4(const void* x_bf16, int64_t n, uint8_t* kv_data,
+                     uint8_t* kv_scale, csa2_stream_t stream);
+
+/** Inverse of csa2_pack_kv_fp4: out [n][512] bf16 = e2m1 * e4m3 (exact). */
+int csa2_unpack_kv_fp4(const uint8_t* kv_data, const uint8_t* kv_scale,
+                       int64_t n, void* out_bf16, csa2_stream_t stream);
+
+/**
+ * SWA KV in FP8 (report section 2.4.4, last paragraph: SWA KV stays FP8).
+ * x [n] bf16 -> out [n] E4M3 bytes, RNE saturating at +-448, no scale.
+ */
+int csa2_pack_fp8_e4m3(const void* x_bf16, int64_t n, uint8_t* out,
+                       csa2_stream_t stream);
+
+/** Inverse of csa2_pack_fp8_e4m3: out [n] bf16 (exact). */
+int csa2_unpack_fp8_e4m3(const uint8_t* in, int64_t n, void* out_bf16,
+                         csa2_stream_t stream);
+
+/* ======================================================================== */
+/* Lightning indexer, pool and Top-K                                         */
+/* ======================================================================== */
+
+/**
+ * Indexer scores (report sections 2.3 and 2.3.2; notes section 4.1 and 4.4:
+ * 32 x 128 multiply-adds per query-entry pair).
+ *   s[b][i] = sum_h w[b][h] * ReLU( sum_c qhat[b][h][c] * khat[b][p][c] )
+ * with p = i (positions == NULL) or p = positions[b][i] (a Reindex layer
+ * scoring its candidate pool). qhat, khat are the MXFP4 values.
+ *   q_data [B][32][64], q_e8m0 [B][32][4]  (from csa2_quant_mxfp4)
+ *   w [B][32] fp32 head weights
+ *   ik planes with capacity `cap`, n_visible [B] int32 (0 <= n_visible <= cap)
+ *   positions [B][n_pos] int32 or NULL
+ *   scores [B][n_pos] fp32 out; -inf where p < 0 or p >= n_visible[b].
+ * Errors: INVALID_ARG, ALIGNMENT (cap or plane pointers), CUDA.
+ */
+int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
+                     const float* w, int32_t B, const uint8_t* ik_data,
+                     const uint8_t* ik_scale, int64_t cap,
+                     const int32_t* n_visible, const int32_t* positions,
+                     int64_t n_pos, float* scores, csa2_stream_t stream);
+
+/**
+ * Bytes of workspace csa2_topk needs for B rows of n scores and a given k.
+ */
+size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k);
+
+/**
+ * Top-K per row (report section 2.3: the indexer selects the Top-K entries
+ * for each query; K = 512 in the notes' setup).
+ *   scores [B][n] fp32; an element is a candidate when its score is neither
+ *   NaN nor -inf, its column is < n_valid[b] (n_valid may be NULL) and its
+ *   position is >= 0. position = positions[b][i] (or i when NULL).
+ *   idx [B][k] int32 out: the positions of the k largest candidates, ties
+ *   broken by smaller position, written in ascending position order and
+ *   padded with -1 at the end when fewer than k candidates exist.
+ * 1 <= k <= CSA2_MAX_TOPK. The result is deterministic.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE, CUDA.
+ */
+int csa2_topk(const float* scores, int32_t B, int64_t n,
+              const int32_t* n_valid, const int32_t* positions, int32_t k,
+              int32_t* idx, void* workspace, size_t workspace_bytes,
+              csa2_stream_t stream);
+
+/** Bytes of workspace csa2_block_pool needs. */
+size_t csa2_block_pool_workspace_size(int32_t B, int64_t n, int32_t block,
+                                      int32_t n_blocks);
+
+/**
+ * Hierarchical candidate pool (report section 2.3.2 and Figure 5: each block
+ * takes the maximum index score among its positions; the best blocks form
+ * the pool, e.g. 2,048 blocks of 8 = 16,384 positions).
+ *   scores [B][n] fp32 from the Full layer's scan; block b covers positions
+ *   [block*b, block*b + block) within [0, n_visible[b]).
+ *   pool [B][n_blocks * block] int32 out: the positions of the n_blocks
+ *   blocks with the largest block maxima (ties: smaller block id), blocks in
+ *   ascending order, -1 past n_visible and in unused slots.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, WORKSPACE, CUDA.
+ */
+int csa2_block_pool(const float* scores, int32_t B, int64_t n,
+                    const int32_t* n_visible, int32_t block, int32_t n_blocks,
+                    int32_t* pool, void* workspace, size_t workspace_bytes,
+                    csa2_stream_t stream);
+
+/** Bytes of workspace csa2_index_topk needs (pool_blocks 0 = no pool). */
+size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_pos, int32_t k,
+                                      int32_t pool_blocks);
+
+/**
+ * Fused indexer scan + Top-K (+ pool): the Full-layer and Reindex-layer
+ * index path of report section 2.3.1 in one call. Arguments as in
+ * csa2_index_score and csa2_topk; if pool != NULL and pool_blocks > 0 the
+ * call also builds the block pool [B][pool_blocks * CSA2_POOL_BLOCK] from the
+ * same scores (only meaningful when positions == NULL).
+ * Errors: as csa2_index_score and csa2_topk.
+ */
+int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0,
+                    const float* w, int32_t B, const uint8_t* ik_data,
+                    const uint8_t* ik_scale, int64_t cap,
+                    const int32_t* n_visible, const int32_t* positions,
+                    int64_t n_pos, int32_t k, int32_t* idx,
+                    int32_t pool_blocks, int32_t* pool, void* workspace,
+                    size_t workspace_bytes, csa2_stream_t stream);
+
+/**
+ * Prefill indexer scores with causal masking (report section 2.3; the
+ * encoder-side prefill indexer cost in notes section 4.4 item 4).
+ * T queries at positions p0 .. p0+T-1 of one sequence; query t sees entries
+ * 0 .. p0+t (itself included).
+ *   q_data [T][32][64], q_e8m0 [T][32][4], w [T][32]
+ *   ik planes of the sequence with n_entries >= p0 + T entries
+ *   scores [T][n_entries] fp32 out, -inf beyond each query's prefix.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
+                             const float* w, int32_t T,
+                             const uint8_t* ik_data, const uint8_t* ik_scale,
+                             int64_t n_entries, int64_t p0, float* scores,
+                             csa2_stream_t stream);
+
+/* ======================================================================== */
+/* Sparse attention                                                          */
+/* ======================================================================== */
+
+/** Bytes of workspace the attention entry points need for n_queries
+ *  (query-layers in decode, queries in prefill). */
+size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k,
+                                       int32_t n_swa);
+
+/**
+ * Sparse decode attention (report section 2.3: each query attends to the
+ * selected entries together with the layer-local SWA KV; section 2.3.1:
+ * Reuse layers use the Top-K of the preceding indexing layer with their own
+ * query and SWA KV; notes section 1: 64 heads of dim 512, the 512-dim latent
+ * shared as K and V).
+ *   q [B][L][64][512] bf16: the L layers of sequence b share idx[b]
+ *     (L = 1 for one layer, 4 for 1 Full + 3 Reuse).
+ *   kv planes with capacity cap; n_visible [B]; idx [B][k] int32 positions
+ *     (-1 entries are skipped; a position >= n_visible[b] is a device error).
+ *   swa [B][L][n_swa][512] E4M3 bytes (0 <= n_swa <= 512).
+ *   S = sm_scale * q . row over the k selected rows and the n_swa SWA rows,
+ *   one softmax, out = P . rows.
+ *   out [B][L][64][512] bf16; out_f32 (nullable) the same before the bf16
+ *   rounding; lse (nullable) [B][L][64] natural-log sum of exp(S), -inf for
+ *   a query with no rows (its output is 0).
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ */
+int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
+                            const uint8_t* kv_data, const uint8_t* kv_scale,
+                            int64_t cap, const int32_t* n_visible,
+                            const int32_t* idx, int32_t k, const uint8_t* swa,
+                            int32_t n_swa, float sm_scale, void* out_bf16,
+                            float* out_f32, float* lse, void* workspace,
+                            size_t workspace_bytes, csa2_stream_t stream);
+
+/**
+ * Sparse prefill attention: T queries of one sequence, each with its own
+ * Top-K and its own causal SWA window.
+ *   q [T][64][512] bf16; kv planes of the sequence with n_entries entries;
+ *   idx [T][k]; swa [T + n_swa - 1][512] E4M3 where query t uses rows
+ *   t .. t + n_swa - 1 (the last one is the query's own position).
+ *   out/out_f32/lse as in csa2_sparse_attn_decode with [T] leading.
+ * Errors: as csa2_sparse_attn_decode.
+ */
+int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T,
+                             const uint8_t* kv_data, const uint8_t* kv_scale,
+                             int64_t n_entries, const int32_t* idx, int32_t k,
+                             const uint8_t* swa, int32_t n_swa, float sm_scale,
+                             void* out_bf16, float* out_f32, float* lse,
+                             void* workspace, size_t workspace_bytes,
+                             csa2_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

@@ -139,6 +139,10 @@ void orc_quant_mxfp4(const float* x, int64_t rows, int cols, uint8_t* data,
                      uint8_t* e8m0) {
   int64_t r;
   int nb = cols / ORC_MX_BLOCK;
+  /* rows are independent; OpenMP only spreads them over cores */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) if (rows > 4096)
+#endif
   for (r = 0; r < rows; ++r) {
     const float* xr = x + r * cols;
     uint8_t* dr = data + r * (cols / 2);
@@ -175,6 +179,9 @@ void orc_pack_kv_fp4(const float* x, int64_t n, uint8_t* kv_data,
                      uint8_t* kv_scale) {
   int64_t t;
   const int nb = ORC_KV_DIM / ORC_KV_BLOCK;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) if (n > 4096)
+#endif
   for (t = 0; t < n; ++t) {
     const float* xr = x + t * ORC_KV_DIM;
     uint8_t* dr = kv_data + t * (ORC_KV_DIM / 2);
@@ -215,6 +222,9 @@ void orc_unpack_kv_fp4(const uint8_t* kv_data, const uint8_t* kv_scale,
 /* SWA KV stays FP8 E4M3 ([R] 2.4.4 last paragraph); no scale is described. */
 void orc_pack_fp8(const float* x, int64_t n, uint8_t* out) {
   int64_t i;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) if (n > 65536)
+#endif
   for (i = 0; i < n; ++i) out[i] = (uint8_t)orc_e4m3_encode(x[i]);
 }
 
@@ -239,14 +249,18 @@ uint64_t orc_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
                          const float* w, const uint8_t* ik_data,
                          const uint8_t* ik_scale, const int32_t* positions,
                          int64_t n, float* out32, double* out64) {
-  double q[ORC_IDX_HEADS][ORC_IDX_DIM], k[ORC_IDX_DIM];
+  double q[ORC_IDX_HEADS][ORC_IDX_DIM];
   uint64_t macs = 0;
   int64_t i;
-  int h, c;
   orc_dequant_mxfp4(q_data, q_e8m0, ORC_IDX_HEADS, ORC_IDX_DIM, &q[0][0]);
+  /* entries are independent; OpenMP only spreads them over cores */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) reduction(+ : macs) if (n > 8192)
+#endif
   for (i = 0; i < n; ++i) {
     int64_t p = positions ? (int64_t)positions[i] : i;
-    double s = 0.0;
+    double s = 0.0, k[ORC_IDX_DIM];
+    int h, c;
     if (p < 0) {
       out32[i] = -INFINITY;
       if (out64) out64[i] = -INFINITY;

@@ -1,0 +1,115 @@
+"""GPU parity of the sparse attention entry points against the oracle, given
+the oracle's index set, plus the closed-form special cases."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp4_kv_cache_02_gb300.inputs import bf16_round, prefill_chunk
+
+from helpers import ATTN_ROW_TOL, DecodeCase, attn_row_error, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa2():
+    from fp4_kv_cache_02_gb300 import csa2 as m
+    return m
+
+
+def _run_decode(csa2, g, idx, k, n_swa, B, L):
+    out = torch.empty(B, L, 64, 512, dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty(B, L, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, L, 64, dtype=torch.float32, device="cuda")
+    ws = csa2.attn_workspace(B * L, k, n_swa)
+    csa2.csa2_sparse_attn_decode(g["Q"], g["kv_data"], g["kv_scale"], g["n_visible"], idx,
+                                 g["swa"] if n_swa else None, out, ws, out_f32=out32, lse=lse)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    return out, out32, lse
+
+
+def test_decode_attention_matches_oracle(csa2):
+    case = DecodeCase(workload=94, Ns=[3000, 700], L=2)
+    g = case.to_device()
+    k = 512
+    rng = np.random.default_rng(1)
+    idx = np.stack([rng.permutation(n)[:k] if n >= k else np.concatenate([rng.permutation(n), -np.ones(k - n)])
+                    for n in case.Ns]).astype(np.int32)
+    idx[0, 10:20] = -1
+    out, out32, lse = _run_decode(csa2, g, dev(idx), k, 128, case.B, case.L)
+    o32 = out32.cpu().numpy()
+    assert torch.equal(out, out32.to(torch.bfloat16))  # bf16 output is the RNE of the fp32 one
+    for b in range(case.B):
+        for l in range(case.L):
+            ref, ref_lse = case.oracle_attention(b, l, idx[b])
+            assert attn_row_error(o32[b, l], ref) <= ATTN_ROW_TOL
+            np.testing.assert_allclose(lse.cpu().numpy()[b, l], ref_lse, rtol=1e-5, atol=1e-5)
+            assert attn_row_error(out.float().cpu().numpy()[b, l], ref) <= ATTN_ROW_TOL + 2.0 ** -8
+
+
+def test_decode_attention_special_cases(csa2):
+    case = DecodeCase(workload=95, Ns=[300], n_swa=0)
+    g = case.to_device()
+    # one selected entry, no SWA rows: the output is that latent, exactly
+    idx = np.full((1, 8), -1, np.int32)
+    idx[0, 3] = 123
+    out, out32, lse = _run_decode(csa2, g, dev(idx), 8, 0, 1, 1)
+    row = oracle.unpack_kv_fp4(case.kv_data[0, 123:124], case.kv_scale[0, 123:124])[0]
+    np.testing.assert_array_equal(out32.cpu().numpy()[0, 0], np.tile(row, (64, 1)).astype(np.float32))
+    # no rows at all: zero output and -inf lse
+    idx[0, 3] = -1
+    out, out32, lse = _run_decode(csa2, g, dev(idx), 8, 0, 1, 1)
+    assert torch.all(out32 == 0) and torch.all(lse == -float("inf"))
+    # zero query: the mean of the rows
+    g["Q"].zero_()
+    idx = np.arange(64, dtype=np.int32)[None, :] * 3
+    out, out32, lse = _run_decode(csa2, g, dev(idx), 64, 0, 1, 1)
+    rows = oracle.unpack_kv_fp4(case.kv_data[0, idx[0]], case.kv_scale[0, idx[0]])
+    np.testing.assert_allclose(out32.cpu().numpy()[0, 0], np.tile(rows.mean(0), (64, 1)), rtol=1e-5, atol=1e-5)
+
+
+def test_decode_attention_rejects_out_of_range_index(csa2):
+    case = DecodeCase(workload=96, Ns=[200])
+    g = case.to_device()
+    idx = np.arange(8, dtype=np.int32)[None, :]
+    idx[0, 2] = 250   # >= n_visible: a device error, the row is skipped
+    _ = csa2.csa2_get_last_error()
+    out = torch.empty(1, 1, 64, 512, dtype=torch.bfloat16, device="cuda")
+    csa2.csa2_sparse_attn_decode(g["Q"], g["kv_data"], g["kv_scale"], g["n_visible"], dev(idx), g["swa"], out,
+                                 csa2.attn_workspace(1, 8, 128))
+    assert csa2.csa2_get_last_error() == -7
+    assert csa2.csa2_get_last_error() == 0  # the error word is cleared
+
+
+def test_decode_attention_is_deterministic(csa2):
+    case = DecodeCase(workload=97, Ns=[2000, 2000])
+    g = case.to_device()
+    rng = np.random.default_rng(2)
+    idx = dev(np.stack([rng.permutation(2000)[:512] for _ in range(2)]).astype(np.int32))
+    a, _, _ = _run_decode(csa2, g, idx, 512, 128, 2, 1)
+    b, _, _ = _run_decode(csa2, g, idx, 512, 128, 2, 1)
+    assert torch.equal(a, b)
+
+
+def test_prefill_attention_matches_oracle(csa2):
+    T, N0, k, W = 5, 1000, 64, 128
+    d = prefill_chunk(98, T, N0)
+    N = N0 + T
+    kvd, kvs = oracle.pack_kv_fp4(d["kv"])
+    swa = oracle.pack_fp8(d["swa"].reshape(-1)).reshape(T + W - 1, 512)
+    rng = np.random.default_rng(4)
+    idx = np.stack([rng.permutation(N0 + t + 1)[:k] for t in range(T)]).astype(np.int32)
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty(T, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(T, 64, dtype=torch.float32, device="cuda")
+    csa2.csa2_sparse_attn_prefill(dev(d["Q"]).to(torch.bfloat16), dev(kvd), dev(kvs), dev(idx), dev(swa), W, out,
+                                  csa2.attn_workspace(T, k, W), out_f32=out32, lse=lse)
+    torch.cuda.synchronize()
+    o = out32.cpu().numpy()
+    for t in range(T):
+        ref, ref_lse = oracle.sparse_attn(d["Q"][t], kvd, kvs, idx[t], swa[t:t + W])
+        assert attn_row_error(o[t], ref) <= ATTN_ROW_TOL
+        np.testing.assert_allclose(lse.cpu().numpy()[t], ref_lse, rtol=1e-5, atol=1e-5)
