@@ -179,7 +179,7 @@ def run_gpu(args):
     from fp4_kv_cache_02_gb300.inputs import WORKLOADS
 
     wl = WORKLOADS[WORKLOAD_ID]
-    B, N, K, W = wl.B, wl.N, 512, 128
+    B, N, K, W = args.batch or wl.B, wl.N, 512, 128
     seqs = rank_sequences(rank, B)
     inp = build_inputs(csa2, torch, B, N, seqs, device)
     cap = inp["cap"]
@@ -223,9 +223,11 @@ def run_gpu(args):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed_steps")   # lets ncu filter to the timed region
         for i in range(args.steps):
             flush.fill_(1)                 # L2 flush between timed steps, outside the events
             step(evs[i])
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
@@ -302,7 +304,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e2m1/e4m3/e8m0 storage; fp32 scores; bf16 attention with fp32 accumulate",
         "data": "synthetic N(0,1) caches drawn on the device, packed by the library",
-        "config": {"workload": "full_decode_b32_n65536", "sequences_per_gpu": B, "visible_entries": N,
+        "config": {"workload": f"full_decode_b{B}_n{N}", "sequences_per_gpu": B, "visible_entries": N,
                    "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
                    "l2": "flushed between steps (512 MiB write)", "parallelism": f"dp{world} (sequences)"},
         "stages_ms": {"quant_q": round(stage_ms[0], 5), "index_score": round(stage_ms[1], 5),
@@ -426,6 +428,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's 32)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
