@@ -32,7 +32,9 @@ CAP_ALIGN = 128
 MAX_TOPK = 4096
 
 STATUS = {0: "ok", -1: "invalid argument", -2: "unsupported shape", -3: "misaligned",
-          -4: "CUDA error", -5: "device wait timed out", -6: "workspace", -7: "device rejected input"}
+          -4: "CUDA error", -5: "device wait timed out", -6: "workspace", -7: "device rejected input",
+          -8: "needs more than the static scratch buffer"}
+TOPK_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class Csa2Error(RuntimeError):
@@ -61,6 +63,7 @@ def _load():
         "csa2_index_score": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32]),
         "csa2_topk": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp, sz, vp]),
+        "csa2_topk_static": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp]),
         "csa2_block_pool_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_block_pool": (ctypes.c_int, [vp, i32, i64, vp, i32, i32, vp, vp, sz, vp]),
         "csa2_index_topk_workspace_size": (sz, [i32, i64, i32, i32]),
@@ -192,6 +195,17 @@ def csa2_topk(scores, k, idx, workspace, n_valid=None, positions=None, stream=No
     B, n = scores.shape
     _call("csa2_topk", _p(scores), B, n, _p(n_valid), _p(positions), k, _p(idx), _p(workspace),
           workspace.numel(), _s(stream))
+
+
+def csa2_topk_static(scores, k, idx, n_valid=None, positions=None, stream=None):
+    """csa2_topk without a workspace: for callers that cannot allocate device
+    memory. Its scratch is a fixed 32 MiB buffer inside the library, shared by
+    all calls (order calls on one stream; overlapping calls race). The first
+    call on a device looks the buffer up; make it before any stream capture."""
+    _req(scores, torch.float32, "scores"); _req(idx, torch.int32, "idx")
+    _req(n_valid, torch.int32, "n_valid", allow_none=True); _req(positions, torch.int32, "positions", allow_none=True)
+    B, n = scores.shape
+    _call("csa2_topk_static", _p(scores), B, n, _p(n_valid), _p(positions), k, _p(idx), _s(stream))
 
 
 def csa2_block_pool(scores, n_visible, pool, workspace, block=POOL_BLOCK, n_blocks=POOL_BLOCKS, stream=None):

@@ -28,6 +28,7 @@ extern "C" const char* csa2_status_string(int status) {
     case CSA2_ERR_TIMEOUT: return "bounded device wait ran out";
     case CSA2_ERR_WORKSPACE: return "workspace too small or misaligned";
     case CSA2_ERR_DEVICE: return "a kernel rejected an input";
+    case CSA2_ERR_SCRATCH_LIMIT: return "problem needs more than the static scratch buffer";
     default: return "unknown status";
   }
 }

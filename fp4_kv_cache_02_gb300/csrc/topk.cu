@@ -17,6 +17,8 @@
 // The result does not depend on the order in which CTAs run.
 #include "common.cuh"
 
+#include <mutex>
+
 namespace csa2 {
 
 __device__ int g_topk_error = 0;
@@ -473,4 +475,43 @@ extern "C" int csa2_block_pool(const float* scores, int32_t B, int64_t n, const 
   if (n_blocks > CSA2_MAX_TOPK || n > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
   return csa2_launch_block_pool(scores, B, n, n_visible, block, n_blocks, pool, workspace, workspace_bytes,
                                 (cudaStream_t)stream);
+}
+
+// ---- Top-K without allocation: scratch in a fixed device buffer ---------------
+// The buffer is a file-scope device array; host code must not pass its name to
+// a kernel (on the host it is only a stand-in symbol), so the device address is
+// looked up once per device with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_topk_static_scratch[CSA2_TOPK_STATIC_SCRATCH_BYTES];
+
+static int topk_static_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static void* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_topk_static_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return CSA2_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return CSA2_OK;
+}
+
+extern "C" int csa2_topk_static(const float* scores, int32_t B, int64_t n, const int32_t* n_valid,
+                                const int32_t* positions, int32_t k, int32_t* idx, csa2_stream_t stream) {
+  if (!scores || !idx || B < 0 || n < 0) return CSA2_ERR_INVALID_ARG;
+  if (k <= 0 || k > CSA2_MAX_TOPK) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (n > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (B == 0) return CSA2_OK;
+  if (topk_ws_layout(B, n, k, nullptr, nullptr) > (size_t)CSA2_TOPK_STATIC_SCRATCH_BYTES) return CSA2_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  int rc = topk_static_scratch_address(&ws);
+  if (rc) return rc;
+  return csa2_launch_topk(scores, B, n, n_valid, positions, k, idx, ws, CSA2_TOPK_STATIC_SCRATCH_BYTES,
+                          (cudaStream_t)stream);
 }

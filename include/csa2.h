@@ -63,6 +63,7 @@ typedef struct CUstream_st* csa2_stream_t;
 #define CSA2_ERR_TIMEOUT (-5)          /* a bounded device-side wait ran out       */
 #define CSA2_ERR_WORKSPACE (-6)        /* workspace too small or misaligned        */
 #define CSA2_ERR_DEVICE (-7)           /* a kernel rejected an input (e.g. index)  */
+#define CSA2_ERR_SCRATCH_LIMIT (-8)    /* problem needs more than the static scratch */
 
 /* sizes fixed by the method (notes section 1 setup) */
 #define CSA2_IDX_HEADS 32
@@ -179,6 +180,33 @@ int csa2_topk(const float* scores, int32_t B, int64_t n,
               const int32_t* n_valid, const int32_t* positions, int32_t k,
               int32_t* idx, void* workspace, size_t workspace_bytes,
               csa2_stream_t stream);
+
+/**
+ * Top-K that allocates nothing and takes no workspace: the same selection as
+ * csa2_topk (same arguments, same result), with its scratch held in a fixed
+ * device buffer of CSA2_TOPK_STATIC_SCRATCH_BYTES that lives inside this
+ * library. The report has no counterpart of this entry point; it exists for
+ * callers that may not allocate device memory at all -- for example a plugin
+ * whose host engine owns every device allocation and hands it only input and
+ * output buffers, or a serving loop that must not pay cudaMalloc's implicit
+ * device synchronisation on its request path.
+ *   - Every GPU that loads the library holds the buffer until the process
+ *     exits.
+ *   - The first call on a device looks up the buffer's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one buffer and it keeps the last call's contents;
+ *     the call clears what must start at zero. Calls that overlap on the GPU
+ *     (different streams, or different host threads) race on the buffer:
+ *     order them on one stream.
+ *   - Returns CSA2_ERR_SCRATCH_LIMIT when csa2_topk_workspace_size(B, n, k)
+ *     exceeds CSA2_TOPK_STATIC_SCRATCH_BYTES (32 MiB: e.g. 32 rows of 65,536
+ *     scores at k = 512 fit), and otherwise the errors of csa2_topk.
+ */
+#define CSA2_TOPK_STATIC_SCRATCH_BYTES (32u << 20)
+int csa2_topk_static(const float* scores, int32_t B, int64_t n,
+                     const int32_t* n_valid, const int32_t* positions,
+                     int32_t k, int32_t* idx, csa2_stream_t stream);
 
 /** Bytes of workspace csa2_block_pool needs. */
 size_t csa2_block_pool_workspace_size(int32_t B, int64_t n, int32_t block,
