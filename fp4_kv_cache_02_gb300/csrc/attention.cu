@@ -9,19 +9,17 @@
 // SWA KV); mer.dev notes section 1 (64 heads of dim 512; the 512-dim KV latent
 // is shared as K and V).
 //
-// Work split: one CTA per (query, chunk of kRows rows) computes an
-// unnormalised partial (m, l, O) of its rows; a second kernel merges the
-// chunks of a query in fixed chunk order, so results are deterministic.
+// Work split: one CTA per (query, chunk of 128 rows) computes an
+// unnormalised partial (m, l, O) of its rows on the tensor cores
+// (attention_tc.cuh); a second kernel merges the chunks of a query in fixed
+// chunk order, so results are deterministic.
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace csa2 {
 
 __device__ int g_attn_error = 0;
-
-constexpr int kRows = 64;                 // rows (selected entries or SWA rows) per CTA
-constexpr int kThreads = 256;
-constexpr int kQStride = kHeadDim + 8;    // bf16 elements per smem row (padded)
-constexpr int kSStride = kRows + 1;
 
 struct AttnArgs {
   const uint16_t* q;        // query rows, [n_q][64][512] bf16
@@ -43,227 +41,52 @@ struct AttnArgs {
   int32_t q0;               // first query of this launch
 };
 
-__device__ __forceinline__ void dequant_kv_block16(const uint8_t* d8, uint8_t s8, uint16_t* dst) {
-  uint2 v = *reinterpret_cast<const uint2*>(d8);
-  float s = e4m3_to_f32(s8);
-  uint32_t w[2] = {v.x, v.y};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 2; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint32_t b = (w[i] >> (8 * j)) & 0xFFu;
-      __nv_bfloat162 p = __floats2bfloat162_rn(e2m1_to_f32(b & 0xF) * s, e2m1_to_f32(b >> 4) * s);
-      o[4 * i + j] = *reinterpret_cast<uint32_t*>(&p);
-    }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void dequant_swa16(const uint8_t* src, uint16_t* dst) {
-  uint4 v = *reinterpret_cast<const uint4*>(src);
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint32_t b = w[i] >> (16 * j);
-      __nv_bfloat162 p = __floats2bfloat162_rn(e4m3_to_f32(b & 0xFF), e4m3_to_f32((b >> 8) & 0xFF));
-      o[2 * i + j] = *reinterpret_cast<uint32_t*>(&p);
-    }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-  d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-}
-
-__device__ __forceinline__ void bf16x8_to_f32(uint4 v, float* f) {
-  uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// grid (n_split, n_q_in_launch), block kThreads
-__global__ void __launch_bounds__(kThreads) attn_partial_kernel(AttnArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);                    // [64][kQStride]
-  uint16_t* KVs = Qs + kHeads * kQStride;                             // [kRows][kQStride]
-  float* Ss = reinterpret_cast<float*>(KVs + kRows * kQStride);        // [64][kSStride]
-  __shared__ int row_valid[kRows];
-  __shared__ float m_s[kHeads], l_s[kHeads];
-
-  const int qi = a.q0 + blockIdx.y;            // global query index
-  const int seq = qi / a.L;
-  const int split = blockIdx.x;
-  const int tid = threadIdx.x;
-
-  // ---- load Q (64 x 512 bf16) ----
-  const uint16_t* qg = a.q + (int64_t)qi * kHeads * kHeadDim;
-  for (int i = tid; i < kHeads * kHeadDim / 8; i += kThreads) {
-    int h = i / (kHeadDim / 8), c8 = i % (kHeadDim / 8);
-    *reinterpret_cast<uint4*>(Qs + h * kQStride + c8 * 8) =
-        *reinterpret_cast<const uint4*>(qg + h * kHeadDim + c8 * 8);
-  }
-  // ---- gather + dequantise the chunk's rows ----
-  const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
-  const int32_t* idx_row = a.idx + (int64_t)seq * a.k;
-  if (tid < kRows) {
-    int t = split * kRows + tid;
-    int valid = 0;
-    if (t < a.k) {
-      int32_t p = idx_row[t];
-      if (p >= 0) {
-        if (p < nv) valid = 1;
-        else record_error(&g_attn_error, CSA2_ERR_DEVICE);
-      }
-    } else if (t < a.k + a.n_swa) {
-      valid = 1;
-    }
-    row_valid[tid] = valid;
-  }
-  __syncthreads();
-  for (int i = tid; i < kRows * (kHeadDim / 16); i += kThreads) {
-    int r = i / (kHeadDim / 16), blk = i % (kHeadDim / 16);
-    int t = split * kRows + r;
-    uint16_t* dst = KVs + r * kQStride + blk * 16;
-    if (!row_valid[r]) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(dst + 8) = make_uint4(0, 0, 0, 0);
-    } else if (t < a.k) {
-      int64_t p = (int64_t)seq * a.kv_seq_stride + idx_row[t];
-      dequant_kv_block16(a.kv_data + p * kKvBytes + blk * 8, a.kv_scale[p * kKvScales + blk], dst);
-    } else {
-      const uint8_t* src = a.swa + (int64_t)qi * a.swa_q_stride + (int64_t)(t - a.k) * kHeadDim + blk * 16;
-      dequant_swa16(src, dst);
-    }
-  }
-  __syncthreads();
-
-  // ---- S = sm_scale * Q . KV^T over the chunk: thread owns 4 heads x 4 rows ----
-  {
-    const int h0 = (tid >> 4) * 4, r0 = (tid & 15) * 4;
-    float acc[4][4] = {};
-    for (int c = 0; c < kHeadDim; c += 8) {
-      float qf[4][8], kf[4][8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) bf16x8_to_f32(*reinterpret_cast<const uint4*>(Qs + (h0 + i) * kQStride + c), qf[i]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bf16x8_to_f32(*reinterpret_cast<const uint4*>(KVs + (r0 + j) * kQStride + c), kf[j]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[i][j] = fmaf(qf[i][e], kf[j][e], acc[i][j]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        Ss[(h0 + i) * kSStride + r0 + j] = row_valid[r0 + j] ? acc[i][j] * a.sm_scale : -INFINITY;
-  }
-  __syncthreads();
-
-  // ---- per-head max / exp / sum over the chunk: one warp per 8 heads ----
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int h = warp * 8; h < warp * 8 + 8; ++h) {
-      float s0 = Ss[h * kSStride + lane], s1 = Ss[h * kSStride + lane + 32];
-      float m = fmaxf(s0, s1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float p0 = (s0 == -INFINITY) ? 0.0f : expf(s0 - m);
-      float p1 = (s1 == -INFINITY) ? 0.0f : expf(s1 - m);
-      float l = p0 + p1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-      Ss[h * kSStride + lane] = p0;
-      Ss[h * kSStride + lane + 32] = p1;
-      if (lane == 0) { m_s[h] = m; l_s[h] = l; }
-    }
-  }
-  __syncthreads();
-
-  // ---- O_partial = P . KV: warp owns 4 heads, lane owns 16 channels; 2 passes ----
-  const int lq = blockIdx.y;                  // query within this launch
-  float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    const int c0 = lane * 16;
-    for (int pass = 0; pass < 2; ++pass) {
-      const int h0 = pass * 32 + warp * 4;
-      float acc[4][16] = {};
-      for (int r = 0; r < kRows; ++r) {
-        float kf[16];
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(KVs + r * kQStride + c0), kf);
-        bf16x8_to_f32(*reinterpret_cast<const uint4*>(KVs + r * kQStride + c0 + 8), kf + 8);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float p = Ss[(h0 + i) * kSStride + r];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) acc[i][e] = fmaf(p, kf[e], acc[i][e]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float4* d = reinterpret_cast<float4*>(po + (h0 + i) * kHeadDim + c0);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) d[e] = make_float4(acc[i][4 * e], acc[i][4 * e + 1], acc[i][4 * e + 2], acc[i][4 * e + 3]);
-      }
-    }
-  }
-  if (tid < kHeads) {
-    float* ml = a.part_ml + (((int64_t)lq * a.n_split + split) * kHeads + tid) * 2;
-    ml[0] = m_s[tid];
-    ml[1] = l_s[tid];
-  }
-}
-
-// grid (n_q_in_launch), block 256: merge the splits of each (query, head) in
-// fixed split order.
+// grid (n_q_in_launch, 8), block 256: merge the splits of 8 heads of one
+// query, in fixed split order.
 __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part_o,
                                                            const float* __restrict__ part_ml, int32_t n_split,
                                                            int32_t q0, uint16_t* __restrict__ out,
                                                            float* __restrict__ out_f32, float* __restrict__ lse) {
-  __shared__ float scale_s[kHeads][16];
-  __shared__ float inv_l[kHeads];
+  constexpr int kHeadsPerCta = 8;
+  __shared__ float scale_s[kHeadsPerCta][16];
+  __shared__ float inv_l[kHeadsPerCta];
   const int lq = blockIdx.x;
   const int qi = q0 + lq;
+  const int h0 = blockIdx.y * kHeadsPerCta;
   const int tid = threadIdx.x;
-  if (tid < kHeads) {
+  if (tid < kHeadsPerCta) {
+    const int h = h0 + tid;
     float M = -INFINITY;
     for (int s = 0; s < n_split; ++s) {
-      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + tid) * 2;
+      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + h) * 2;
       if (ml[1] > 0.0f) M = fmaxf(M, ml[0]);
     }
     float Lsum = 0.0f;
     for (int s = 0; s < n_split; ++s) {
-      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + tid) * 2;
-      float f = (ml[1] > 0.0f) ? expf(ml[0] - M) : 0.0f;
+      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + h) * 2;
+      const float f = (ml[1] > 0.0f) ? expf(ml[0] - M) : 0.0f;
       scale_s[tid][s] = f;
       Lsum += ml[1] * f;
     }
     inv_l[tid] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-    if (lse) lse[(int64_t)qi * kHeads + tid] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
+    if (lse) lse[(int64_t)qi * kHeads + h] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
   }
   __syncthreads();
-  for (int i = tid; i < kHeads * kHeadDim / 4; i += blockDim.x) {
-    int h = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+  for (int i = tid; i < kHeadsPerCta * kHeadDim / 4; i += blockDim.x) {
+    const int hl = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
+    const int h = h0 + hl;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < n_split; ++s) {
-      float f = scale_s[h][s];
+      const float f = scale_s[hl][s];
       if (f == 0.0f) continue;
-      float4 v = *reinterpret_cast<const float4*>(part_o + (((int64_t)lq * n_split + s) * kHeads + h) * kHeadDim + c4 * 4);
+      const float4 v =
+          *reinterpret_cast<const float4*>(part_o + (((int64_t)lq * n_split + s) * kHeads + h) * kHeadDim + c4 * 4);
       acc.x = fmaf(v.x, f, acc.x); acc.y = fmaf(v.y, f, acc.y);
       acc.z = fmaf(v.z, f, acc.z); acc.w = fmaf(v.w, f, acc.w);
     }
-    float il = inv_l[h];
+    const float il = inv_l[hl];
     acc.x *= il; acc.y *= il; acc.z *= il; acc.w *= il;
-    int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4 * 4;
+    const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4 * 4;
     if (out_f32) *reinterpret_cast<float4*>(out_f32 + o) = acc;
     __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
     *reinterpret_cast<uint2*>(out + o) = make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
@@ -272,7 +95,22 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
 
 }  // namespace csa2
 
+#include "attention_tc.cuh"
+
 using namespace csa2;
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
 
 static constexpr int kMaxSplit = 16;  // k + n_swa <= 1024 rows per query
 static constexpr int kQueriesPerLaunch = 256;
@@ -287,10 +125,8 @@ int csa2_read_and_clear_attn_error(cudaStream_t s) {
   return v;
 }
 
-static inline int attn_splits(int32_t k, int32_t n_swa) { return (k + n_swa + kRows - 1) / kRows; }
-
-static inline size_t attn_smem_bytes() {
-  return (size_t)(kHeads + kRows) * kQStride * 2 + (size_t)kHeads * kSStride * 4;
+static inline int attn_splits(int32_t k, int32_t n_swa) {
+  return (k + n_swa + attn_tc::kRowsTc - 1) / attn_tc::kRowsTc;
 }
 
 extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, int32_t n_swa) {
@@ -316,19 +152,34 @@ static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, f
   o_bytes = (o_bytes + 255) / 256 * 256;
   a.part_o = (float*)ws;
   a.part_ml = (float*)((char*)ws + o_bytes);
-  size_t smem = attn_smem_bytes();
   static bool attr = false;
   if (!attr) {
-    if (cudaFuncSetAttribute(attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_tc::attn_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_tc::kSmemBytes) != cudaSuccess)
       return CSA2_ERR_CUDA;
     attr = true;
   }
+  // Q rows of all queries as a 2-D bf16 tensor [n_q * 64][512], loaded in
+  // [64 heads][64 channels] boxes with the 128-byte swizzle the MMA reads.
+  auto encode = tensor_map_encoder();
+  if (!encode) return CSA2_ERR_CUDA;
+  CUtensorMap qmap;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_q * kHeads};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kHeads};
+  cuuint32_t estr[2] = {1, 1};
+  if (encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)a.q, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CSA2_ERR_CUDA;
   for (int32_t q0 = 0; q0 < n_q; q0 += kQueriesPerLaunch) {
     int32_t nq = n_q - q0 < kQueriesPerLaunch ? n_q - q0 : kQueriesPerLaunch;
     a.q0 = q0;
-    attn_partial_kernel<<<dim3((unsigned)a.n_split, (unsigned)nq), kThreads, smem, stream>>>(a);
+    attn_tc::attn_partial_tc_kernel<<<dim3((unsigned)a.n_split, (unsigned)nq), attn_tc::kThreads,
+                                       attn_tc::kSmemBytes, stream>>>(qmap, a);
     CSA2_CHECK_LAUNCH();
-    attn_combine_kernel<<<(unsigned)nq, 256, 0, stream>>>(a.part_o, a.part_ml, a.n_split, q0, out, out_f32, lse);
+    attn_combine_kernel<<<dim3((unsigned)nq, kHeads / 8), 256, 0, stream>>>(a.part_o, a.part_ml, a.n_split, q0, out,
+                                                                         out_f32, lse);
     CSA2_CHECK_LAUNCH();
   }
   return CSA2_OK;

@@ -63,6 +63,8 @@ static int check_index_args(const uint8_t* q_data, const uint8_t* q_e8m0, const 
 static int launch_scores(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                          const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap, const int32_t* n_visible,
                          const int32_t* positions, int64_t n_pos, float* scores, cudaStream_t s) {
+  if (positions == nullptr)  // contiguous scan: tensor cores, TMA-fed
+    return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos, scores, s);
   return csa2_launch_index_score_simple(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos,
                                         scores, s);
 }

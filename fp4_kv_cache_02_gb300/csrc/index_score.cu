@@ -16,6 +16,12 @@ namespace csa2 {
 
 __device__ int g_index_error = 0;
 
+}  // namespace csa2
+
+#include "index_score_tc.cuh"
+
+namespace csa2 {
+
 // Dequantise one query's MXFP4 q into shared memory [32][128] fp32.
 __device__ __forceinline__ void load_qhat(const uint8_t* __restrict__ q_data,
                                           const uint8_t* __restrict__ q_e8m0, float* qs) {
@@ -121,6 +127,70 @@ int csa2_read_and_clear_index_error(cudaStream_t s) {
     return CSA2_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return CSA2_ERR_CUDA;
   return v;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static int device_sm_count() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = v > 0 ? v : 148;
+  }
+  return sms[dev];
+}
+
+// Tensor-core scan of positions 0..n_pos-1 of every sequence.
+int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
+                               const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
+                               const int32_t* n_visible, int64_t n_pos, float* scores, cudaStream_t stream) {
+  if (n_pos == 0 || B == 0) return CSA2_OK;
+  if (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)) return CSA2_ERR_ALIGNMENT;
+  auto encode = tensor_map_encoder();
+  if (!encode) return CSA2_ERR_CUDA;
+  CUtensorMap map;
+  cuuint64_t dims[3] = {(cuuint64_t)kIkBytes, (cuuint64_t)cap, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)kIkBytes, (cuuint64_t)cap * kIkBytes};
+  cuuint32_t box[3] = {(cuuint32_t)kIkBytes, (cuuint32_t)scan_tc::kTileRows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)ik_data, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CSA2_ERR_CUDA;
+  // one wave of 3 CTAs per SM, each on a contiguous run of tiles of one sequence
+  const int64_t tiles = (n_pos + scan_tc::kTileRows - 1) / scan_tc::kTileRows;
+  const int64_t target = 3LL * device_sm_count();
+  int64_t chunks = target / B;
+  if (chunks < 1) chunks = 1;
+  if (chunks > tiles) chunks = tiles;
+  const int64_t per = (tiles + chunks - 1) / chunks;
+  chunks = (tiles + per - 1) / per;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(scan_tc::index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             scan_tc::kSmemBytes) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    attr = true;
+  }
+  scan_tc::Params prm{q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per};
+  scan_tc::index_score_tc_kernel<<<dim3((unsigned)chunks, (unsigned)B), scan_tc::kThreads, scan_tc::kSmemBytes,
+                                   stream>>>(map, prm);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
 }
 
 // Launch helpers shared with the fused path in capi.cu.

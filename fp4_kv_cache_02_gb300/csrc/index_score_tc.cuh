@@ -1,0 +1,233 @@
+// index_score_tc.cuh -- tensor-core lightning-indexer scan (included by
+// index_score.cu, which owns the error word g_index_error).
+//
+// "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression" section
+// 2.3 / 2.4.4 and mer.dev notes section 4.4: every visible entry is scored as
+// s = sum_h w_h ReLU(q_h . k) with 32 heads x 128 channels, q and k both
+// MXFP4 (E2M1 values, one E8M0 scale per 32).
+//
+// One CTA scans a contiguous run of 128-key tiles of one sequence:
+//   warp 4       TMA producer: 128 x 64 B E2M1 tile (3-D tensor map, 64-byte
+//                swizzle) + the tile's 512 B of E8M0 scales (bulk copy) per
+//                pipeline stage;
+//   warp 5       MMA issuer: rearranges the tile's scales for tcgen05.cp into
+//                tensor memory, then issues two block-scaled MXF4 MMAs
+//                (M = 128 keys, N = 32 heads, K = 64 each) into one of two
+//                tensor-memory accumulators;
+//   warps 0..3   epilogue: tcgen05.ld of each key's 32 head dots, ReLU, the
+//                w-weighted fp32 sum, masking past n_visible, coalesced store.
+// The scan is HBM-bound at 68 bytes per key; the tensor cores do the 4,096
+// multiply-adds per key that CUDA cores could not sustain at that rate.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "tc_common.cuh"
+
+namespace csa2 {
+namespace scan_tc {
+
+constexpr int kStages = 6;
+constexpr int kTileRows = 128;
+constexpr int kTileBytes = kTileRows * kIkBytes;    // 8192
+constexpr int kSfBytes = kTileRows * kIkScales;     // 512
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 128;
+__host__ __device__ constexpr uint32_t acc_col(int a) { return 32u * (uint32_t)a; }      // 2 x 32 fp32 columns
+__host__ __device__ constexpr uint32_t sfa_col(int a) { return 64u + 8u * (uint32_t)a; }  // 2 x 4 scale columns
+constexpr uint32_t kSfbCol = 80;
+
+// shared-memory layout (offsets from a 1024-byte-aligned base)
+constexpr int kOffA = 0;
+constexpr int kOffSfRaw = kOffA + kStages * kTileBytes;
+constexpr int kOffSfT = kOffSfRaw + kStages * kSfBytes;
+constexpr int kOffQ = kOffSfT + kStages * kSfBytes;   // 1024-aligned: kStages * 9216 is
+constexpr int kOffSfb = kOffQ + kIdxHeads * kIkBytes; // 2048 bytes of q
+constexpr int kOffBars = kOffSfb + 512;
+constexpr int kNumBars = 2 * kStages + 4;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + alignment slack
+static_assert(kOffQ % 1024 == 0, "q operand must be 1024-byte aligned");
+
+struct Params {
+  const uint8_t* q_data;
+  const uint8_t* q_e8m0;
+  const float* w;
+  const uint8_t* ik_scale;
+  int64_t cap;
+  const int32_t* n_visible;
+  int64_t n_pos;
+  float* scores;
+  int32_t tiles_per_cta;
+};
+
+__global__ void __launch_bounds__(kThreads, 3)
+    index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap_ik, Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = tc::smem_u32(smem_raw);
+  uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
+  uint8_t* sA = sm + kOffA;
+  uint8_t* sSfRaw = sm + kOffSfRaw;
+  uint8_t* sSfT = sm + kOffSfT;
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sSfb = sm + kOffSfb;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBars);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int64_t n_tiles_all = (p.n_pos + kTileRows - 1) / kTileRows;
+  int64_t nv = (int64_t)p.n_visible[b];
+  nv = nv < 0 ? 0 : (nv > p.n_pos ? p.n_pos : nv);
+  const int64_t t_begin = (int64_t)blockIdx.x * p.tiles_per_cta;
+  int64_t t_end_all = t_begin + p.tiles_per_cta;
+  if (t_end_all > n_tiles_all) t_end_all = n_tiles_all;
+  int64_t t_end = (nv + kTileRows - 1) / kTileRows;
+  if (t_end > t_end_all) t_end = t_end_all;
+  const int n_tiles = t_end > t_begin ? (int)(t_end - t_begin) : 0;
+
+  // ---- set-up: barriers, the q operand (B) and its scales, tensor memory ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], 128);
+    }
+    *s_abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (threadIdx.x < 128) {
+    // q: 32 rows x 64 B, K-major with the 64-byte swizzle
+    const int r = threadIdx.x >> 2, c = threadIdx.x & 3;
+    uint4 v = *reinterpret_cast<const uint4*>(p.q_data + ((int64_t)b * kIdxHeads + r) * kIkBytes + c * 16);
+    *reinterpret_cast<uint4*>(sQ + tc::sw64_offset(r, c)) = v;
+  } else if (threadIdx.x < 160) {
+    // scales of q for tcgen05.cp: row i holds the four E8M0 bytes of head i
+    // (bytes for rows i+32, i+64, i+96 do not exist for N = 32 and are 2^0)
+    const int i = threadIdx.x - 128;
+    uint32_t s = *reinterpret_cast<const uint32_t*>(p.q_e8m0 + ((int64_t)b * kIdxHeads + i) * kIkScales);
+    *reinterpret_cast<uint4*>(sSfb + i * 16) = make_uint4(s, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  }
+  tc::fence_proxy_async_smem();
+  if (warp == kMmaWarp) tc::tmem_alloc(s_tmem, kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == kProducerWarp) {
+    // ---- TMA producer ----
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, &g_index_error)) break;
+        const int64_t row0 = (t_begin + i) * kTileRows;
+        tc::mbar_arrive_expect_tx(&full[s], kTileBytes + kSfBytes);
+        tc::tma_load_3d(sA + s * kTileBytes, &tmap_ik, 0, (int32_t)row0, b, &full[s]);
+        tc::bulk_load(sSfRaw + s * kSfBytes, p.ik_scale + ((int64_t)b * p.cap + row0) * kIkScales, kSfBytes,
+                      &full[s]);
+        ++issued;
+      }
+      if (*s_abort) {
+        // let copies already in flight land before the CTA's memory goes away
+        for (int i = issued - kStages; i < issued; ++i)
+          if (i >= 0) tc::mbar_wait_bounded(&full[i % kStages], (uint32_t)(i / kStages) & 1u, s_abort,
+                                            &g_index_error, 100000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issuer ----
+    const uint32_t q_addr = tc::smem_u32(sQ);
+    const uint64_t bdesc0 = tc::smem_desc(q_addr, 0, 512, tc::kSwizzle64B);
+    const uint64_t bdesc1 = tc::smem_desc(q_addr + 32, 0, 512, tc::kSwizzle64B);
+    constexpr uint32_t idesc0 = tc::idesc_mxf4(128, 32, 0, 0);
+    constexpr uint32_t idesc1 = tc::idesc_mxf4(128, 32, 2, 2);
+    if (lane == 0 && n_tiles > 0)
+      tc::tmem_cp_32x128_x4(tmem + kSfbCol, tc::smem_desc(tc::smem_u32(sSfb), 0, 128, tc::kSwizzleNone));
+    __syncwarp();
+    int last = -1;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const int a = i & 1;
+      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      bool ok = tc::mbar_wait_bounded(&acc_empty[a], aph ^ 1u, s_abort, &g_index_error) &&
+                tc::mbar_wait_bounded(&full[s], ph, s_abort, &g_index_error);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      // scales of keys lane, lane+32, lane+64, lane+96 -> one 16-byte row
+      const uint32_t* raw = reinterpret_cast<const uint32_t*>(sSfRaw + s * kSfBytes);
+      uint4 v = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
+      *reinterpret_cast<uint4*>(sSfT + s * kSfBytes + lane * 16) = v;
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sfa = tmem + sfa_col(a);
+        const uint32_t d = tmem + acc_col(a);
+        tc::tmem_cp_32x128_x4(sfa, tc::smem_desc(tc::smem_u32(sSfT + s * kSfBytes), 0, 128, tc::kSwizzleNone));
+        const uint32_t a_addr = tc::smem_u32(sA + s * kTileBytes);
+        tc::mma_mxf4(d, tc::smem_desc(a_addr, 0, 512, tc::kSwizzle64B), bdesc0, idesc0, sfa, tmem + kSfbCol, 0);
+        tc::mma_mxf4(d, tc::smem_desc(a_addr + 32, 0, 512, tc::kSwizzle64B), bdesc1, idesc1, sfa,
+                     tmem + kSfbCol, 1);
+        tc::mma_commit(&empty[s]);
+        tc::mma_commit(&acc_full[a]);
+      }
+      last = i;
+      __syncwarp();
+    }
+    if (*s_abort && last >= 0 && lane == 0)  // MMAs must finish before tensor memory is freed
+      tc::mbar_wait_bounded(&acc_full[last & 1], (uint32_t)(last >> 1) & 1u, s_abort, &g_index_error,
+                            100000000ull);
+    __syncwarp();
+  } else {
+    // ---- epilogue: warps 0..3, one key row per thread ----
+    float wr[kIdxHeads];
+#pragma unroll
+    for (int h = 0; h < kIdxHeads; ++h) wr[h] = p.w[(int64_t)b * kIdxHeads + h];
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float* out = p.scores + (int64_t)b * p.n_pos;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int a = i & 1;
+      const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+      if (!tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error)) break;
+      tc::tc_fence_after();
+      uint32_t r[32];
+      tc::tmem_ld_32x32b_x32(tmem + lane_base + acc_col(a), r);
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acc_empty[a]);
+      float sc = 0.0f;
+#pragma unroll
+      for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);
+      const int64_t pos = (t_begin + i) * kTileRows + row;
+      if (pos < p.n_pos) out[pos] = pos < nv ? sc : -INFINITY;
+    }
+    // positions of this CTA's range past the visible entries
+    const int64_t lo = (t_begin > t_end ? t_begin : t_end) * kTileRows;
+    int64_t hi = t_end_all * kTileRows;
+    if (hi > p.n_pos) hi = p.n_pos;
+    for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace scan_tc
+}  // namespace csa2

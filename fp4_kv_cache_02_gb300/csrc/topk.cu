@@ -28,10 +28,13 @@ constexpr int kHistBins = 1 << kHistBits;  // 4096
 constexpr int kSelThreads = 256;
 
 struct RowCounters {
-  uint32_t n_sel;   // positions appended to sel
-  uint32_t n_cand;  // (key, position) pairs appended to cand
-  uint32_t done;    // CTAs of the row that finished streaming
-  uint32_t pad;
+  uint32_t n_sel;      // positions appended to sel
+  uint32_t n_cand;     // (key, position) pairs appended to cand
+  uint32_t done;       // select CTAs of the row that finished streaming
+  uint32_t hist_done;  // histogram CTAs of the row that flushed their counts
+  int32_t t;           // threshold bin (-1: fewer candidates than k)
+  uint32_t above;      // candidates in bins above t
+  uint32_t pad[2];
 };
 
 struct TopkWs {
@@ -73,10 +76,13 @@ __device__ __forceinline__ bool load_candidate(const float* __restrict__ scores,
   return true;
 }
 
+__device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
+                                  uint32_t* scratch);
+
 // ---- pass 1: histogram of the top 12 key bits --------------------------------
 __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
-    const int32_t* __restrict__ positions, int64_t chunk, TopkWs ws) {
+    const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws) {
   __shared__ uint32_t sh[kHistBins];
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
@@ -93,43 +99,76 @@ __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
   uint32_t* gh = ws.hist + (size_t)b * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
     if (sh[i]) atomicAdd(&gh[i], sh[i]);
+  // the last CTA of the row turns the row's histogram into its threshold bin
+  __shared__ int s_last;
+  __shared__ uint32_t scratch[kSelThreads + 8];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&ws.cnt[b].hist_done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = __ldcg(gh + i);
+  __syncthreads();
+  uint32_t above;
+  const int t = find_threshold_bin(sh, kHistBins, (uint32_t)k, &above, scratch);
+  if (threadIdx.x == 0) {
+    ws.cnt[b].t = t;
+    ws.cnt[b].above = above;
+  }
 }
 
 // Block-wide search, from the top bin down, for the first bin at which the
 // running count reaches `need`. Returns the bin (-1 if the total is below
 // `need`) and the count strictly above it. `h` has `nbins` entries in shared
-// memory; nbins is a multiple of blockDim.x.
+// memory, nbins a multiple of blockDim.x (a multiple of 32); `scratch` holds
+// blockDim.x + 2 words. Thread j owns bins [nbins-(j+1)*per, nbins-j*per); a
+// warp-shuffle scan over the threads finds the owner of the crossing.
 __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
-                                  uint32_t* scratch /* blockDim.x + 2 */) {
+                                  uint32_t* scratch) {
   const int per = nbins / blockDim.x;
-  // thread j owns bins [nbins - (j+1)*per, nbins - j*per) (descending order)
-  const int top = nbins - threadIdx.x * per;
+  const int j = threadIdx.x, lane = j & 31, warp = j >> 5, nwarps = blockDim.x >> 5;
+  const int top = nbins - j * per;
   uint32_t local = 0;
-  for (int i = 1; i <= per; ++i) local += h[top - i];
-  scratch[threadIdx.x] = local;
+  for (int i = 0; i < per; ++i) local += h[top - 1 - ((i + j) % per)];  // rotated: no bank conflicts
+  uint32_t incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) scratch[warp] = incl;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t run = 0;
-    int found = -1;
-    uint32_t above = 0;
-    for (int j = 0; j < (int)blockDim.x && found < 0; ++j) {
-      if (run + scratch[j] >= need) {
-        // resolve within thread j's bins
-        int tj = nbins - j * per;
-        for (int i = 1; i <= per; ++i) {
-          uint32_t c = h[tj - i];
-          if (run + c >= need) { found = tj - i; above = run; break; }
-          run += c;
-        }
-      } else {
-        run += scratch[j];
-      }
+  if (warp == 0) {
+    uint32_t wt = lane < nwarps ? scratch[lane] : 0u, wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += v;
     }
-    scratch[blockDim.x] = (uint32_t)found;
-    scratch[blockDim.x + 1] = found < 0 ? run : above;
+    __syncwarp();
+    if (lane < nwarps) scratch[lane] = wi - wt;  // exclusive prefix of warp totals
   }
   __syncthreads();
-  int bin = (int)scratch[blockDim.x];
+  const uint32_t excl = scratch[warp] + incl - local;
+  __syncthreads();
+  if (excl < need && excl + local >= need) {
+    uint32_t run = excl;
+    for (int i = 1; i <= per; ++i) {
+      const uint32_t c = h[top - i];
+      if (run + c >= need) {
+        scratch[blockDim.x] = (uint32_t)(top - i);
+        scratch[blockDim.x + 1] = run;
+        break;
+      }
+      run += c;
+    }
+  } else if (j == (int)blockDim.x - 1 && excl + local < need) {
+    scratch[blockDim.x] = 0xFFFFFFFFu;       // total below need
+    scratch[blockDim.x + 1] = excl + local;  // = total
+  }
+  __syncthreads();
+  const int bin = (int)scratch[blockDim.x];
   *above_out = scratch[blockDim.x + 1];
   __syncthreads();
   return bin;
@@ -195,12 +234,9 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   uint32_t* scratch = smem + kHistBins;         // kSelThreads + 8
   __shared__ int s_is_last;
   const int b = blockIdx.y;
-  const uint32_t* gh = ws.hist + (size_t)b * kHistBins;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = __ldcg(gh + i);
-  __syncthreads();
-  uint32_t above;
-  const int t = find_threshold_bin(h, kHistBins, (uint32_t)k, &above, scratch);
-  const uint32_t c_t = t >= 0 ? h[t] : 0u;
+  const int t = __ldcg(&ws.cnt[b].t);
+  const uint32_t above = __ldcg(&ws.cnt[b].above);
+  const uint32_t c_t = t >= 0 ? __ldcg(ws.hist + (size_t)b * kHistBins + t) : 0u;
 
   const int64_t row_off = (int64_t)b * n;
   int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
@@ -408,7 +444,7 @@ int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n
   int64_t chunk = topk_chunk(B, n);
   int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
   dim3 grid((unsigned)chunks, (unsigned)B);
-  topk_hist_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, ws);
+  topk_hist_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, k, ws);
   CSA2_CHECK_LAUNCH();
   size_t smem = topk_select_smem(k);
   static bool attr_set = false;

@@ -188,3 +188,32 @@ def test_prefill_index_score(csa2):
                                  n=N0 + t + 1)[0]
         _scores_close(s[t, :N0 + t + 1], ref)
         assert np.all(s[t, N0 + t + 1:] == -np.inf)
+
+
+def test_index_score_block_scales_land_on_their_own_rows_and_blocks(csa2):
+    """Keys and queries whose 32-channel blocks carry very different power-of-two
+    magnitudes: a scale applied to the wrong key row, head or channel block
+    changes the score by orders of magnitude."""
+    rng = np.random.default_rng(55)
+    B, N = 2, 1000
+    cap = 1024
+    ik = rng.standard_normal((B, N, 128)) * 2.0 ** rng.integers(-12, 12, (B, N, 4)).repeat(32, axis=2)
+    q = rng.standard_normal((B, 32, 128)) * 2.0 ** rng.integers(-6, 6, (B, 32, 4)).repeat(32, axis=2)
+    from fp4_kv_cache_02_gb300.inputs import bf16_round
+    ik, q = bf16_round(ik.astype(np.float32)), bf16_round(q.astype(np.float32))
+    w = rng.uniform(0, 1, (B, 32)).astype(np.float32)
+    ikd = np.zeros((B, cap, 64), np.uint8)
+    iks = np.zeros((B, cap, 4), np.uint8)
+    qd = np.zeros((B, 32, 64), np.uint8)
+    qs = np.zeros((B, 32, 4), np.uint8)
+    for b in range(B):
+        ikd[b, :N], iks[b, :N] = oracle.quant_mxfp4(ik[b])
+        qd[b], qs[b] = oracle.quant_mxfp4(q[b])
+    nv = np.array([N, N - 77], np.int32)
+    scores = torch.empty(B, cap, dtype=torch.float32, device="cuda")
+    csa2.csa2_index_score(dev(qd), dev(qs), dev(w), dev(ikd), dev(iks), dev(nv), scores)
+    s = scores.cpu().numpy()
+    for b in range(B):
+        ref = oracle.index_score(qd[b], qs[b], w[b], ikd[b], iks[b], n=int(nv[b]))[0]
+        _scores_close(s[b, :nv[b]], ref)
+        assert np.all(s[b, nv[b]:] == -np.inf)
