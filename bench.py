@@ -5,7 +5,7 @@ sequences of the Full-layer decode workload (32 sequences x 65,536 visible
 entries; 32 x 128 MXFP4 indexer, Top-512, 64 x 512 attention over the 512
 selected FP4 latents + 128 FP8 SWA rows):
 
-    csa2_quant_mxfp4 (indexer q)  ->  csa2_index_score  ->  csa2_topk
+    csa2_quant_mxfp4 (indexer q)  ->  csa2_index_topk (scan + Top-512)
       ->  csa2_sparse_attn_decode
 
 with the KV cache resident in HBM. The timed region holds exactly --steps
@@ -18,7 +18,10 @@ Prints one JSON line. `value` is queries/s over all ranks; `e2e` is the same
 metric with each step's inputs copied from pinned host memory and its
 outputs copied back inside the timed region; `roofline` reports the indexer
 scan kernel (68 algorithmic bytes per scored entry) against the measured HBM
-copy bandwidth; `cpu_baseline` is the CPU oracle on a bounded sample.
+copy bandwidth, timed in a second loop of csa2_index_score on the same
+inputs (the same kernel; inside csa2_index_topk it also builds the Top-K
+histogram in its epilogue); `cpu_baseline` is the CPU oracle on a bounded
+sample.
 
 --impl reference runs the CPU oracle instead (the reference arm).
 Multi-GPU: launched with torch.distributed.run, every rank runs its own
@@ -192,7 +195,7 @@ def run_gpu(args):
     scores = torch.empty(B, cap, dtype=torch.float32, device=device)
     idx = torch.empty(B, K, dtype=torch.int32, device=device)
     out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=device)
-    tws = csa2.topk_workspace(B, cap, K, device=device)
+    iws = csa2.index_topk_workspace(B, cap, K, device=device)
     aws = csa2.attn_workspace(B, K, W, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
@@ -207,17 +210,14 @@ def run_gpu(args):
         csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc, stream)
         if ev is not None:
             ev[1].record(stream)
-        csa2.csa2_index_score(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], scores,
-                              stream=stream)
+        csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
+                             iws, stream=stream)
         if ev is not None:
             ev[2].record(stream)
-        csa2.csa2_topk(scores, K, idx, tws, n_valid=inp["n_visible"], stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
         csa2.csa2_sparse_attn_decode(inp["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], idx, inp["swa"],
                                      out, aws, stream=stream)
         if ev is not None:
-            ev[4].record(stream)
+            ev[3].record(stream)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -225,7 +225,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert csa2.csa2_get_last_error() == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         if world > 1:
             torch.distributed.barrier()
@@ -238,15 +238,28 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    stage = [0.0] * 4
+    stage = [0.0] * 3
     total = 0.0
     for e in evs:
-        for j in range(4):
+        for j in range(3):
             stage[j] += e[j].elapsed_time(e[j + 1])
-        total += e[0].elapsed_time(e[4])
+        total += e[0].elapsed_time(e[3])
     ms = total / args.steps
     stage_ms = [s / args.steps for s in stage]
     ms_max = reduce_max(ms, world, device)
+
+    # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed) ----
+    scan_ms = 0.0
+    for _ in range(args.steps):
+        flush_l2()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        csa2.csa2_index_score(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], scores,
+                              stream=stream)
+        b_.record(stream)
+        b_.synchronize()
+        scan_ms += a.elapsed_time(b_)
+    scan_ms /= args.steps
 
     # ---- end to end: per-step inputs from pinned host memory, outputs back ----
     h_q = inp["q_idx"].cpu().pin_memory()
@@ -288,7 +301,7 @@ def run_gpu(args):
 
     hbm_peak, peak_kind = peaks()
     scan_bytes = B * N * IK_BYTES_PER_ENTRY
-    scan_gbs = scan_bytes / (stage_ms[1] * 1e-3) / 1e9
+    scan_gbs = scan_bytes / (scan_ms * 1e-3) / 1e9
     traffic = None
     tp = os.path.join(ROOT, "profiles", "index_score_traffic.json")
     if os.path.exists(tp):
@@ -314,8 +327,8 @@ def run_gpu(args):
         "config": {"workload": f"full_decode_b{B}_n{N}", "sequences_per_gpu": B, "visible_entries": N,
                    "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)", "parallelism": f"dp{world} (sequences)"},
-        "stages_ms": {"quant_q": round(stage_ms[0], 5), "index_score": round(stage_ms[1], 5),
-                      "topk": round(stage_ms[2], 5), "sparse_attn": round(stage_ms[3], 5)},
+        "stages_ms": {"quant_q": round(stage_ms[0], 5), "index_topk": round(stage_ms[1], 5),
+                      "sparse_attn": round(stage_ms[2], 5), "index_score_alone": round(scan_ms, 5)},
         "entries_scored_per_s": round(world * B * N / (ms_max * 1e-3), 1),
         "indexer_scan_gbs": round(scan_gbs, 1),
         "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": round(scan_gbs, 1),
@@ -324,6 +337,7 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": scan_bytes},
         "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        # per step: quant, scan, Top-K select + finalize, attention partial + combine
         "gpu_launches": args.steps * (1 + 1 + 2 + n_attn_launches),
         "clocks": clk.summary(),
     }

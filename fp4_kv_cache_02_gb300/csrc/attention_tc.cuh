@@ -141,15 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // ---- gather + dequantise R: [128 t][512 c] bf16 as 8 blocks [128 t][128 B] ----
   // warp w owns rows 16w..16w+15; pass j covers 8 rows x one 64-channel block,
-  // 4 lanes per row, each lane 16 channels (two 16-byte chunks). All loads of a
-  // half (8 passes) are issued before any is used.
+  // 4 lanes per row, each lane 16 channels (two 16-byte chunks). All 16 loads
+  // of a thread are issued before any is used.
+  {
+    constexpr int kPasses = 16;
+    uint4 raw[kPasses];
+    uint32_t sc[kPasses];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    uint4 raw[8];
-    uint32_t sc[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = half * 8 + jj;
+    for (int jj = 0; jj < kPasses; ++jj) {
+      const int j = jj;
       const int r = warp * 16 + (j & 1) * 8 + (lane >> 2);
       const int blk = (j >> 1) * 4 + (lane & 3);
       const int kind = row_valid[r];
@@ -166,8 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = half * 8 + jj;
+    for (int jj = 0; jj < kPasses; ++jj) {
+      const int j = jj;
       const int r = warp * 16 + (j & 1) * 8 + (lane >> 2);
       const int blk = (j >> 1) * 4 + (lane & 3);
       const int kind = row_valid[r];

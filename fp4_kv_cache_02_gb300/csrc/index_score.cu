@@ -157,7 +157,8 @@ static int device_sm_count() {
 // Tensor-core scan of positions 0..n_pos-1 of every sequence.
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                               const int32_t* n_visible, int64_t n_pos, float* scores, cudaStream_t stream) {
+                               const int32_t* n_visible, int64_t n_pos, float* scores, uint32_t* hist,
+                               cudaStream_t stream) {
   if (n_pos == 0 || B == 0) return CSA2_OK;
   if (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)) return CSA2_ERR_ALIGNMENT;
   auto encode = tensor_map_encoder();
@@ -186,7 +187,7 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
       return CSA2_ERR_CUDA;
     attr = true;
   }
-  scan_tc::Params prm{q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per};
+  scan_tc::Params prm{q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per, hist};
   scan_tc::index_score_tc_kernel<<<dim3((unsigned)chunks, (unsigned)B), scan_tc::kThreads, scan_tc::kSmemBytes,
                                    stream>>>(map, prm);
   CSA2_CHECK_LAUNCH();

@@ -48,7 +48,8 @@ constexpr int kOffSfb = kOffQ + kIdxHeads * kIkBytes; // 2048 bytes of q
 constexpr int kOffBars = kOffSfb + 512;
 constexpr int kNumBars = 2 * kStages + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + alignment slack
+constexpr int kOffHist = kOffMisc + 16;               // Top-K histogram of this CTA's scores
+constexpr int kSmemBytes = kOffHist + kTopkHistBins * 4 + 1024;  // + alignment slack
 static_assert(kOffQ % 1024 == 0, "q operand must be 1024-byte aligned");
 
 struct Params {
@@ -61,6 +62,7 @@ struct Params {
   int64_t n_pos;
   float* scores;
   int32_t tiles_per_cta;
+  uint32_t* hist;  // optional [B][kTopkHistBins] Top-K histogram (zeroed by the caller)
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -79,6 +81,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint64_t* acc_empty = acc_full + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
+  uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + kOffHist);
+  const bool with_hist = p.hist != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
@@ -117,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     uint32_t s = *reinterpret_cast<const uint32_t*>(p.q_e8m0 + ((int64_t)b * kIdxHeads + i) * kIkScales);
     *reinterpret_cast<uint4*>(sSfb + i * 16) = make_uint4(s, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
   }
+  if (with_hist)
+    for (int i = threadIdx.x; i < kTopkHistBins; i += kThreads) s_hist[i] = 0u;
   tc::fence_proxy_async_smem();
   if (warp == kMmaWarp) tc::tmem_alloc(s_tmem, kTmemCols);
   tc::tc_fence_before();
@@ -214,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);
       const int64_t pos = (t_begin + i) * kTileRows + row;
       if (pos < p.n_pos) out[pos] = pos < nv ? sc : -INFINITY;
+      if (with_hist && pos < nv && score_is_candidate(sc))
+        atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
     }
     // positions of this CTA's range past the visible entries
     const int64_t lo = (t_begin > t_end ? t_begin : t_end) * kTileRows;
@@ -226,6 +234,11 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (warp == kMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (with_hist) {
+    uint32_t* gh = p.hist + (int64_t)b * kTopkHistBins;
+    for (int i = threadIdx.x; i < kTopkHistBins; i += kThreads)
+      if (s_hist[i]) atomicAdd(&gh[i], s_hist[i]);
   }
 }
 

@@ -6,14 +6,15 @@
 // its positions; the highest-scoring blocks form the candidate pool).
 //
 // Radix/threshold select on order-preserving 32-bit keys of the fp32 scores:
-//   1. histogram of the top 12 key bits per row (shared-memory histogram per
-//      CTA, flushed to a per-row global histogram);
+//   1. histogram of the top 11 key bits per row (shared-memory histogram per
+//      CTA, flushed to a per-row global histogram; the decode scan can build
+//      it in its epilogue);
 //   2. every CTA finds the threshold bin t of its row (the bin in which the
 //      running count from the top reaches k), then streams its slice: keys
 //      above bin t are selected outright, keys inside bin t become candidates;
-//   3. the last CTA of the row (ticket counter, no waiting) resolves bin t
-//      exactly on the remaining 20 key bits, breaks exact ties by smaller
-//      position, sorts the k positions ascending and writes them.
+//   3. one CTA per row resolves bin t exactly on the remaining 21 key bits,
+//      breaks exact ties by smaller position, sorts the k positions ascending
+//      and writes them.
 // The result does not depend on the order in which CTAs run.
 #include "common.cuh"
 
@@ -23,8 +24,8 @@ namespace csa2 {
 
 __device__ int g_topk_error = 0;
 
-constexpr int kHistBits = 12;
-constexpr int kHistBins = 1 << kHistBits;  // 4096
+constexpr int kHistBits = kTopkHistBits;  // 11
+constexpr int kHistBins = kTopkHistBins;  // 2048
 constexpr int kSelThreads = 256;
 
 struct RowCounters {
@@ -79,7 +80,7 @@ __device__ __forceinline__ bool load_candidate(const float* __restrict__ scores,
 __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
                                   uint32_t* scratch);
 
-// ---- pass 1: histogram of the top 12 key bits --------------------------------
+// ---- pass 1: histogram of the top kHistBits key bits --------------------------
 __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
     const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws) {
@@ -90,32 +91,23 @@ __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
   const int64_t row_off = (int64_t)b * n;
   int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
   int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
-  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
-    uint32_t key;
-    int32_t p;
-    if (load_candidate(scores, positions, row_off, i, nv, &key, &p)) atomicAdd(&sh[key >> (32 - kHistBits)], 1u);
+  for (int64_t sub = lo; sub < hi; sub += (int64_t)kSelThreads * 16) {
+    uint32_t key[16];
+    uint32_t ok = 0;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {  // all loads of the sub-chunk in flight first
+      const int64_t i = sub + (int64_t)e * kSelThreads + threadIdx.x;
+      int32_t p;
+      ok |= (uint32_t)(i < hi && load_candidate(scores, positions, row_off, i, nv, &key[e], &p)) << e;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (ok & (1u << e)) atomicAdd(&sh[key[e] >> (32 - kHistBits)], 1u);
   }
   __syncthreads();
   uint32_t* gh = ws.hist + (size_t)b * kHistBins;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x)
     if (sh[i]) atomicAdd(&gh[i], sh[i]);
-  // the last CTA of the row turns the row's histogram into its threshold bin
-  __shared__ int s_last;
-  __shared__ uint32_t scratch[kSelThreads + 8];
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&ws.cnt[b].hist_done, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = __ldcg(gh + i);
-  __syncthreads();
-  uint32_t above;
-  const int t = find_threshold_bin(sh, kHistBins, (uint32_t)k, &above, scratch);
-  if (threadIdx.x == 0) {
-    ws.cnt[b].t = t;
-    ws.cnt[b].above = above;
-  }
 }
 
 // Block-wide search, from the top bin down, for the first bin at which the
@@ -181,11 +173,11 @@ __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, u
 // many keys equal to the threshold are still needed.
 template <typename KeyFn>
 __device__ uint32_t radix_select_desc(int count, uint32_t need, int fixed_bits, uint32_t prefix,
-                                      KeyFn keyfn, uint32_t* hist /*1024*/, uint32_t* scratch,
+                                      KeyFn keyfn, uint32_t* hist /*kHistBins*/, uint32_t* scratch,
                                       uint32_t* r_left) {
   int done_bits = fixed_bits;
   while (done_bits < 32) {
-    int pass_bits = min(10, 32 - done_bits);
+    int pass_bits = min(kHistBits, 32 - done_bits);
     int nb = 1 << pass_bits;
     int nbins = nb < (int)blockDim.x ? (int)blockDim.x : nb;  // pad to a multiple of blockDim
     for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
@@ -208,104 +200,193 @@ __device__ uint32_t radix_select_desc(int count, uint32_t need, int fixed_bits, 
   return prefix;
 }
 
-__device__ void bitonic_sort_asc(int32_t* a, int n_pow2) {
-  for (int size = 2; size <= n_pow2; size <<= 1) {
+// Ascending bitonic sort of a[0..n2) in shared memory, n2 = E * blockDim.x
+// (blockDim.x a multiple of 32, E a power of two <= 16). Thread (warp w, lane
+// l) keeps the E elements w*32E + r*32 + l in registers: partners less than 32
+// apart are exchanged with shuffles, those within a warp's run in registers,
+// and only strides of 32E and more go through shared memory.
+template <int E>
+__device__ void block_sort_asc_e(int32_t* a) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n2 = E * (int)blockDim.x;
+  const int base = warp * 32 * E + lane;
+  int32_t v[E];
+#pragma unroll
+  for (int r = 0; r < E; ++r) v[r] = a[base + r * 32];
+  for (int size = 2; size <= n2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
-        int j = i ^ stride;
-        if (j > i) {
-          bool up = (i & size) == 0;
-          int32_t x = a[i], y = a[j];
-          if ((x > y) == up) { a[i] = y; a[j] = x; }
+      if (stride >= 32 * E) {
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < E; ++r) a[base + r * 32] = v[r];
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int e = base + r * 32;
+          const int32_t y = a[e ^ stride];
+          const bool keep_min = ((e & stride) == 0) == ((e & size) == 0);
+          v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+        }
+      } else if (stride >= 32) {
+        // partners are registers r and r ^ (stride / 32); unrolled over the
+        // possible strides so every register index is a compile-time constant
+#pragma unroll
+        for (int rs = 1; rs < E; rs <<= 1) {
+          if (rs == (stride >> 5)) {
+            int32_t w[E];
+#pragma unroll
+            for (int r = 0; r < E; ++r) {
+              const int e = base + r * 32;
+              const bool keep_min = ((r & rs) == 0) == ((e & size) == 0);
+              w[r] = keep_min ? min(v[r], v[r ^ rs]) : max(v[r], v[r ^ rs]);
+            }
+#pragma unroll
+            for (int r = 0; r < E; ++r) v[r] = w[r];
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < E; ++r) {
+          const int e = base + r * 32;
+          const int32_t y = __shfl_xor_sync(0xffffffffu, v[r], stride);
+          const bool keep_min = ((lane & stride) == 0) == ((e & size) == 0);
+          v[r] = keep_min ? min(v[r], y) : max(v[r], y);
         }
       }
-      __syncthreads();
     }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < E; ++r) a[base + r * 32] = v[r];
+  __syncthreads();
+}
+
+// n2 a power of two, blockDim.x <= n2 <= 16 * blockDim.x.
+__device__ void block_sort_asc(int32_t* a, int n2) {
+  switch (n2 / (int)blockDim.x) {
+    case 1: block_sort_asc_e<1>(a); break;
+    case 2: block_sort_asc_e<2>(a); break;
+    case 4: block_sort_asc_e<4>(a); break;
+    case 8: block_sort_asc_e<8>(a); break;
+    default: block_sort_asc_e<16>(a); break;
   }
 }
 
+// Exclusive prefix sum of v over the block (blockDim.x a multiple of 32,
+// <= 1024); *total receives the block sum. `sh` holds 33 words.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total, uint32_t* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t wt = lane < nwarps ? sh[lane] : 0u;
+    uint32_t wi = wt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += x;
+    }
+    if (lane < nwarps) sh[lane] = wi - wt;
+    if (lane == 31) sh[32] = wi;
+  }
+  __syncthreads();
+  const uint32_t r = sh[warp] + incl - v;
+  *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
 // ---- pass 2: stream, select above the threshold bin, finalize in the last CTA --
+// Each sub-chunk of kSelThreads x kPerThread scores is classified in registers;
+// one block scan and one reservation atomic per output list place the
+// selected positions (key above bin t) and the bin-t candidates.
+constexpr int kPerThread = 16;
+constexpr int kSmemCand = 4096;  // bin-t candidates finalized in shared memory up to this count
+
 __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
-    const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws,
-    int32_t* __restrict__ idx) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* h = smem;                           // kHistBins
-  uint32_t* scratch = smem + kHistBins;         // kSelThreads + 8
-  __shared__ int s_is_last;
+    const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws) {
+  __shared__ uint32_t h[kHistBins];
+  __shared__ uint32_t scratch[kSelThreads + 8];
+  __shared__ uint32_t s_base[2];
   const int b = blockIdx.y;
-  const int t = __ldcg(&ws.cnt[b].t);
-  const uint32_t above = __ldcg(&ws.cnt[b].above);
-  const uint32_t c_t = t >= 0 ? __ldcg(ws.hist + (size_t)b * kHistBins + t) : 0u;
-
+  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = __ldcg(ws.hist + (size_t)b * kHistBins + i);
+  __syncthreads();
+  uint32_t above;
+  const int t = find_threshold_bin(h, kHistBins, (uint32_t)k, &above, scratch);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    ws.cnt[b].t = t;
+    ws.cnt[b].above = above;
+  }
   const int64_t row_off = (int64_t)b * n;
   int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
   int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
   RowCounters* cnt = ws.cnt + b;
   int32_t* sel = ws.sel + (size_t)b * k;
   uint2* cand = ws.cand + (size_t)b * n;
-  const int lane = threadIdx.x & 31;
-  for (int64_t base = lo; base < hi; base += blockDim.x) {
-    int64_t i = base + threadIdx.x;
-    uint32_t key = 0;
-    int32_t p = 0;
-    bool ok = i < hi && load_candidate(scores, positions, row_off, i, nv, &key, &p);
-    int digit = ok ? (int)(key >> (32 - kHistBits)) : -2;
-    bool take = ok && digit > t;
-    bool keep = ok && digit == t;
-    uint32_t mt = __ballot_sync(0xffffffffu, take);
-    uint32_t mk = __ballot_sync(0xffffffffu, keep);
-    uint32_t bt = 0, bk = 0;
-    if (lane == 0) {
-      if (mt) bt = atomicAdd(&cnt->n_sel, __popc(mt));
-      if (mk) bk = atomicAdd(&cnt->n_cand, __popc(mk));
+  for (int64_t sub = lo; sub < hi; sub += (int64_t)kSelThreads * kPerThread) {
+    uint32_t key[kPerThread];
+    int32_t pos[kPerThread];
+    uint32_t take = 0, keep = 0;
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      const int64_t i = sub + (int64_t)e * kSelThreads + threadIdx.x;
+      const bool ok = i < hi && load_candidate(scores, positions, row_off, i, nv, &key[e], &pos[e]);
+      const int digit = ok ? (int)(key[e] >> (32 - kHistBits)) : -2;
+      take |= (uint32_t)(ok && digit > t) << e;
+      keep |= (uint32_t)(ok && digit == t) << e;
     }
-    bt = __shfl_sync(0xffffffffu, bt, 0);
-    bk = __shfl_sync(0xffffffffu, bk, 0);
-    uint32_t lower = (1u << lane) - 1u;
-    if (take) {
-      uint32_t slot = bt + __popc(mt & lower);
-      if (slot < (uint32_t)k) sel[slot] = p;
-      else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan(__popc(take) | ((uint32_t)__popc(keep) << 16), &total, scratch);
+    if (threadIdx.x == 0) {
+      s_base[0] = (total & 0xFFFFu) ? atomicAdd(&cnt->n_sel, total & 0xFFFFu) : 0u;
+      s_base[1] = (total >> 16) ? atomicAdd(&cnt->n_cand, total >> 16) : 0u;
     }
-    if (keep) {
-      uint32_t slot = bk + __popc(mk & lower);
-      if (slot < (uint32_t)n) cand[slot] = make_uint2(key, (uint32_t)p);
-      else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+    __syncthreads();
+    uint32_t st = s_base[0] + (excl & 0xFFFFu), sk = s_base[1] + (excl >> 16);
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      if (take & (1u << e)) {
+        if (st < (uint32_t)k) sel[st] = pos[e];
+        else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+        ++st;
+      }
+      if (keep & (1u << e)) {
+        if (sk < (uint32_t)n) cand[sk] = make_uint2(key[e], (uint32_t)pos[e]);
+        else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+        ++sk;
+      }
     }
+    __syncthreads();  // s_base is rewritten by the next sub-chunk
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t ticket = atomicAdd(&cnt->done, 1u);
-    s_is_last = ticket == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!s_is_last) return;
-  __threadfence();
+}
 
-  // ---- finalize row b ----
-  int32_t* out = (int32_t*)(smem + kHistBins + kSelThreads + 8);  // room for CSA2_MAX_TOPK
-  __shared__ uint32_t s_nout;
-  const uint32_t n_sel = min(__ldcg(&cnt->n_sel), (uint32_t)k);
-  const uint32_t n_cand = min(__ldcg(&cnt->n_cand), (uint32_t)n);
-  if (threadIdx.x == 0) s_nout = 0;
-  for (uint32_t i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = __ldcg(sel + i);
-  __syncthreads();
-  if (threadIdx.x == 0) s_nout = n_sel;
-  __syncthreads();
+// Resolves bin t exactly and writes one row: out[0..s_nout) already holds the
+// positions whose key lies above bin t; the n_cand bin-t candidates are read
+// through `ld`. Keys above the exact threshold key are taken; among keys equal
+// to it, the smallest positions. The k positions are sorted ascending into dst
+// (-1 padding). h has kHistBins words, scratch blockDim.x + 8.
+template <typename LoadFn>
+__device__ void finalize_row(int t, uint32_t above, uint32_t c_t, uint32_t n_cand, int32_t k, LoadFn ld,
+                             int32_t* out, uint32_t& s_nout, uint32_t* h, uint32_t* scratch, int32_t* dst) {
   if (t >= 0) {
     uint32_t r = (uint32_t)k - above;  // still needed from bin t (1 <= r <= c_t)
     if (r >= n_cand || r >= c_t) {
       for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
         uint32_t slot = atomicAdd(&s_nout, 1u);
-        if (slot < (uint32_t)k) out[slot] = (int32_t)__ldcg(&cand[i].y);
+        if (slot < (uint32_t)k) out[slot] = (int32_t)ld(i).y;
       }
     } else {
       uint32_t r2;
       uint32_t T = radix_select_desc(
           (int)n_cand, r, kHistBits, ((uint32_t)t) << (32 - kHistBits),
-          [&](int i) { return __ldcg(&cand[i].x); }, h, scratch, &r2);
+          [&](int i) { return ld((uint32_t)i).x; }, h, scratch, &r2);
       // keys above T are all taken; among keys equal to T the r2 smallest
       // positions are taken (select on ~position, largest first)
       uint32_t n_eq = 0;
@@ -315,7 +396,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
         if (threadIdx.x == 0) s_eq = 0;
         __syncthreads();
         uint32_t local = 0;
-        for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) local += (__ldcg(&cand[i].x) == T);
+        for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) local += (ld(i).x == T);
         atomicAdd(&s_eq, local);
         __syncthreads();
         n_eq = s_eq;
@@ -329,13 +410,13 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
         P = radix_select_desc(
             (int)n_cand, r2, 0, 0u,
             [&](int i) {
-              uint2 c = __ldcg(&cand[i]);
+              const uint2 c = ld((uint32_t)i);
               return c.x == T ? ~c.y : 0u;
             },
             h, scratch, &r3);
       }
       for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        uint2 c = __ldcg(&cand[i]);
+        const uint2 c = ld(i);
         bool take = c.x > T || (c.x == T && (all_eq || (~c.y) > P));
         if (take) {
           uint32_t slot = atomicAdd(&s_nout, 1u);
@@ -346,7 +427,7 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
       // exactly r3 further ties sit at ~position == P (distinct positions: r3 <= 1)
       if (!all_eq && threadIdx.x == 0) {
         for (uint32_t i = 0; i < n_cand && r3 > 0; ++i) {
-          uint2 c = __ldcg(&cand[i]);
+          const uint2 c = ld(i);
           if (c.x == T && ~c.y == P) {
             uint32_t slot = s_nout++;
             if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
@@ -358,14 +439,41 @@ __global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
   }
   __syncthreads();
   uint32_t nout = min(s_nout, (uint32_t)k);
-  int n2 = 1;
+  int n2 = (int)blockDim.x;
   while (n2 < k) n2 <<= 1;
   for (int i = threadIdx.x; i < n2; i += blockDim.x)
     if (i >= (int)nout) out[i] = 0x7FFFFFFF;
   __syncthreads();
-  bitonic_sort_asc(out, n2);
-  int32_t* dst = idx + (size_t)b * k;
+  block_sort_asc(out, n2);
   for (int i = threadIdx.x; i < k; i += blockDim.x) dst[i] = i < (int)nout ? out[i] : -1;
+}
+
+// ---- pass 3: one CTA per row resolves bin t exactly and writes the row ------
+__global__ void __launch_bounds__(kSelThreads) topk_finalize_kernel(int64_t n, int32_t k, TopkWs ws,
+                                                                    int32_t* __restrict__ idx) {
+  extern __shared__ uint32_t smem[];
+  uint32_t* h = smem;                    // kHistBins
+  uint32_t* scratch = smem + kHistBins;  // kSelThreads + 8
+  int32_t* out = (int32_t*)(smem + kHistBins + kSelThreads + 8);                 // CSA2_MAX_TOPK
+  uint2* cand_s = (uint2*)(smem + kHistBins + kSelThreads + 8 + CSA2_MAX_TOPK);  // kSmemCand
+  __shared__ uint32_t s_nout;
+  const int b = blockIdx.x;
+  RowCounters* cnt = ws.cnt + b;
+  const int32_t* sel = ws.sel + (size_t)b * k;
+  const uint2* cand = ws.cand + (size_t)b * n;
+  const int t = cnt->t;
+  const uint32_t above = cnt->above;
+  const uint32_t c_t = t >= 0 ? ws.hist[(size_t)b * kHistBins + t] : 0u;
+  const uint32_t n_sel = min(cnt->n_sel, (uint32_t)k);
+  const uint32_t n_cand = min(cnt->n_cand, (uint32_t)n);
+  const bool in_smem = n_cand <= (uint32_t)kSmemCand;
+  if (in_smem)
+    for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) cand_s[i] = cand[i];
+  for (uint32_t i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = sel[i];
+  if (threadIdx.x == 0) s_nout = n_sel;
+  __syncthreads();
+  finalize_row(t, above, c_t, n_cand, k, [&](uint32_t i) -> uint2 { return in_smem ? cand_s[i] : cand[i]; }, out,
+               s_nout, h, scratch, idx + (size_t)b * k);
 }
 
 // ---- block pool ---------------------------------------------------------------
@@ -422,10 +530,9 @@ static int64_t topk_chunk(int32_t B, int64_t n) {
   return chunk;
 }
 
-static size_t topk_select_smem(int32_t k) {
-  int n2 = 1;
-  while (n2 < k) n2 <<= 1;
-  return (size_t)(kHistBins + kSelThreads + 8) * 4 + (size_t)n2 * 4;
+static size_t topk_finalize_smem() {
+  // histogram / radix scratch, the output list (up to CSA2_MAX_TOPK), kSmemCand candidates
+  return (size_t)(kHistBins + kSelThreads + 8 + CSA2_MAX_TOPK) * 4 + (size_t)kSmemCand * 8;
 }
 
 extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
@@ -433,29 +540,56 @@ extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
   return topk_ws_layout(B, n, k, nullptr, nullptr);
 }
 
-int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
-                     int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  if (B == 0) return CSA2_OK;
+// Clears the histogram and counters of a Top-K workspace (enqueued on
+// `stream`) and returns the per-row histogram [B][kTopkHistBins] that a
+// producer of the scores may fill (the decode scan does it in its epilogue).
+int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream, uint32_t** hist) {
   size_t need = topk_ws_layout(B, n, k, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
   TopkWs ws;
   topk_ws_layout(B, n, k, &ws, (char*)workspace);
   if (cudaMemsetAsync(workspace, 0, topk_ws_zero_bytes(B), stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (hist) *hist = ws.hist;
+  return CSA2_OK;
+}
+
+// Select + finalize over scores whose histogram is complete in the workspace.
+int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
+                        int32_t k, int32_t* idx, void* workspace, cudaStream_t stream) {
+  TopkWs ws;
+  topk_ws_layout(B, n, k, &ws, (char*)workspace);
+  int64_t chunk = topk_chunk(B, n);
+  int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
+  dim3 grid((unsigned)chunks, (unsigned)B);
+  topk_select_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, k, ws);
+  CSA2_CHECK_LAUNCH();
+  const size_t smem = topk_finalize_smem();
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return CSA2_ERR_CUDA;
+    attr_set = true;
+  }
+  topk_finalize_kernel<<<(unsigned)B, kSelThreads, smem, stream>>>(n, k, ws, idx);
+  CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}
+
+int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
+                     int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (B == 0) return CSA2_OK;
+  int rc = csa2_topk_prepare(B, n, k, workspace, workspace_bytes, stream, nullptr);
+  if (rc) return rc;
+  TopkWs ws;
+  topk_ws_layout(B, n, k, &ws, (char*)workspace);
   int64_t chunk = topk_chunk(B, n);
   int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
   dim3 grid((unsigned)chunks, (unsigned)B);
   topk_hist_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, k, ws);
   CSA2_CHECK_LAUNCH();
-  size_t smem = topk_select_smem(k);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(topk_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)topk_select_smem(CSA2_MAX_TOPK));
-    attr_set = true;
-  }
-  topk_select_kernel<<<grid, kSelThreads, smem, stream>>>(scores, n, n_valid, positions, chunk, k, ws, idx);
-  CSA2_CHECK_LAUNCH();
-  return CSA2_OK;
+  return csa2_topk_from_hist(scores, B, n, n_valid, positions, k, idx, workspace, stream);
 }
 
 extern "C" int csa2_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid,
