@@ -141,7 +141,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- GPU arm
 
-def build_inputs(csa2, torch, B, N, seqs, device):
+def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device):
     """Synthetic resident caches and per-step inputs, packed with the library's
     own packers on the device (indexer K: MXFP4; main KV: E2M1 + E4M3/16;
     SWA: E4M3)."""
@@ -153,22 +153,27 @@ def build_inputs(csa2, torch, B, N, seqs, device):
     kv_scale = torch.empty(B, cap, 32, dtype=torch.uint8, device=device)
     q_idx = torch.empty(B, 32, 128, dtype=torch.bfloat16, device=device)
     w = torch.empty(B, 32, dtype=torch.float32, device=device)
-    Q = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=device)
-    swa = torch.empty(B, 1, 128, 512, dtype=torch.uint8, device=device)
+    Q = torch.empty(B, L, 64, 512, dtype=torch.bfloat16, device=device)
+    swa = torch.empty(B, L, 128, 512, dtype=torch.uint8, device=device)
+    q_re = torch.empty(B, 32, 128, dtype=torch.bfloat16, device=device) if reindex else None
+    w_re = torch.empty(B, 32, dtype=torch.float32, device=device) if reindex else None
     for b, s in enumerate(seqs):
-        seed = seed_for(WORKLOAD_ID, s)
+        seed = seed_for(wid, s)
         ik = device_normal((cap, 128), 4 * seed + 1, device)
         csa2.csa2_quant_mxfp4(ik, ik_data[b], ik_scale[b])
         kv = device_normal((cap, 512), 4 * seed + 2, device)
         csa2.csa2_pack_kv_fp4(kv, kv_data[b], kv_scale[b])
         q_idx[b] = device_normal((32, 128), 4 * seed + 3, device)
         w[b] = device_uniform((32,), 4 * seed + 3, device)
-        Q[b] = device_normal((1, 64, 512), 4 * seed + 4, device, scale=1.0 / math.sqrt(512))
-        csa2.csa2_pack_fp8_e4m3(device_normal((1, 128, 512), 4 * seed + 5, device), swa[b])
+        Q[b] = device_normal((L, 64, 512), 4 * seed + 4, device, scale=1.0 / math.sqrt(512))
+        csa2.csa2_pack_fp8_e4m3(device_normal((L, 128, 512), 4 * seed + 5, device), swa[b])
+        if reindex:
+            q_re[b] = device_normal((32, 128), 4 * seed + 6, device)
+            w_re[b] = device_uniform((32,), 4 * seed + 6, device)
     n_visible = torch.full((B,), N, dtype=torch.int32, device=device)
     torch.cuda.synchronize()
     return dict(cap=cap, ik_data=ik_data, ik_scale=ik_scale, kv_data=kv_data, kv_scale=kv_scale, q_idx=q_idx, w=w,
-                Q=Q, swa=swa, n_visible=n_visible)
+                Q=Q, swa=swa, n_visible=n_visible, q_re=q_re, w_re=w_re)
 
 
 def run_gpu(args):
@@ -183,10 +188,14 @@ def run_gpu(args):
     from fp4_kv_cache_02_gb300 import csa2
     from fp4_kv_cache_02_gb300.inputs import WORKLOADS
 
-    wl = WORKLOADS[WORKLOAD_ID]
-    B, N, K, W = args.batch or wl.B, wl.N, 512, 128
+    wid = args.workload
+    wl = WORKLOADS[wid]
+    if wl.kind == "prefill":
+        raise SystemExit("the prefill workload is measured by the parity tests, not by this bench")
+    reindex = wl.kind == "reindex"
+    B, N, L, K, W = args.batch or wl.B, wl.N, wl.L, 512, 128
     seqs = rank_sequences(rank, B)
-    inp = build_inputs(csa2, torch, B, N, seqs, device)
+    inp = build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device)
     cap = inp["cap"]
     stream = torch.cuda.current_stream(device)
 
@@ -194,9 +203,16 @@ def run_gpu(args):
     q_sc = torch.empty(B, 32, 4, dtype=torch.uint8, device=device)
     scores = torch.empty(B, cap, dtype=torch.float32, device=device)
     idx = torch.empty(B, K, dtype=torch.int32, device=device)
-    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device=device)
-    iws = csa2.index_topk_workspace(B, cap, K, device=device)
-    aws = csa2.attn_workspace(B, K, W, device=device)
+    out = torch.empty(B, L, 64, 512, dtype=torch.bfloat16, device=device)
+    NBLK = 2048
+    iws = csa2.index_topk_workspace(B, cap, K, NBLK if reindex else 0, device=device)
+    aws = csa2.attn_workspace(B * L, K, W, device=device)
+    if reindex:
+        pool = torch.empty(B, NBLK * 8, dtype=torch.int32, device=device)
+        idx_full = torch.empty(B, K, dtype=torch.int32, device=device)
+        qr_data = torch.empty(B, 32, 64, dtype=torch.uint8, device=device)
+        qr_sc = torch.empty(B, 32, 4, dtype=torch.uint8, device=device)
+        rws = csa2.index_topk_workspace(B, NBLK * 8, K, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
 
@@ -204,20 +220,42 @@ def run_gpu(args):
         flush.fill_(1)
         flush_rd.max()
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    # the step as named stages (each a sequence of public C-ABI calls)
+    def st_quant():
         csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
-                             iws, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def st_index():
+        if reindex:
+            csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx_full,
+                                 iws, pool_blocks=NBLK, pool=pool, stream=stream)
+        else:
+            csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
+                                 iws, stream=stream)
+
+    def st_reindex():
+        csa2.csa2_quant_mxfp4(inp["q_re"], qr_data, qr_sc, stream)
+        csa2.csa2_index_topk(qr_data, qr_sc, inp["w_re"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
+                             rws, positions=pool, stream=stream)
+
+    def st_attn():
         csa2.csa2_sparse_attn_decode(inp["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], idx, inp["swa"],
                                      out, aws, stream=stream)
+
+    stages = [("quant_q", st_quant), ("index_topk_pool" if reindex else "index_topk", st_index)]
+    if reindex:
+        stages.append(("reindex_topk", st_reindex))
+    stages.append(("sparse_attn", st_attn))
+    # our kernels per step: quant 1; fused scan + select + finalize 3; pool: block max, histogram, select,
+    # finalize, expand 5; reindex: quant, scan, histogram, select, finalize 5; attention partial + combine
+    n_launches = 1 + 3 + (5 + 5 if reindex else 0) + 2 * math.ceil(B * L / 256)
+
+    def step(ev=None):
+        for j, (_, fn) in enumerate(stages):
+            if ev is not None:
+                ev[j].record(stream)
+            fn()
         if ev is not None:
-            ev[3].record(stream)
+            ev[len(stages)].record(stream)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -225,7 +263,8 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert csa2.csa2_get_last_error() == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    nst = len(stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         if world > 1:
             torch.distributed.barrier()
@@ -238,12 +277,12 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    stage = [0.0] * 3
+    stage = [0.0] * nst
     total = 0.0
     for e in evs:
-        for j in range(3):
+        for j in range(nst):
             stage[j] += e[j].elapsed_time(e[j + 1])
-        total += e[0].elapsed_time(e[3])
+        total += e[0].elapsed_time(e[nst])
     ms = total / args.steps
     stage_ms = [s / args.steps for s in stage]
     ms_max = reduce_max(ms, world, device)
@@ -262,20 +301,16 @@ def run_gpu(args):
     scan_ms /= args.steps
 
     # ---- end to end: per-step inputs from pinned host memory, outputs back ----
-    h_q = inp["q_idx"].cpu().pin_memory()
-    h_w = inp["w"].cpu().pin_memory()
-    h_Q = inp["Q"].cpu().pin_memory()
-    h_swa = inp["swa"].cpu().pin_memory()
+    per_step_in = [inp[k_] for k_ in ("q_idx", "w", "Q", "swa", "q_re", "w_re") if inp.get(k_) is not None]
+    host_in = [t.cpu().pin_memory() for t in per_step_in]
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_idx = torch.empty(idx.shape, dtype=idx.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_w, h_Q, h_swa))
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in (h_out, h_idx))
 
     def e2e_step():
-        inp["q_idx"].copy_(h_q, non_blocking=True)
-        inp["w"].copy_(h_w, non_blocking=True)
-        inp["Q"].copy_(h_Q, non_blocking=True)
-        inp["swa"].copy_(h_swa, non_blocking=True)
+        for d_, h_ in zip(per_step_in, host_in):
+            d_.copy_(h_, non_blocking=True)
         step()
         h_out.copy_(out, non_blocking=True)
         h_idx.copy_(idx, non_blocking=True)
@@ -310,7 +345,6 @@ def run_gpu(args):
         except (ValueError, OSError):
             traffic = None
     qps = world * B / (ms_max * 1e-3)
-    n_attn_launches = 2 * math.ceil(B / 256)   # partial + combine per 256 query-layers
     line = {
         "metric": METRIC,
         "value": round(qps, 1),
@@ -324,12 +358,13 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e2m1/e4m3/e8m0 storage; fp32 scores; bf16 attention with fp32 accumulate",
         "data": "synthetic N(0,1) caches drawn on the device, packed by the library",
-        "config": {"workload": f"full_decode_b{B}_n{N}", "sequences_per_gpu": B, "visible_entries": N,
+        "config": {"workload": wl.name if B == wl.B else f"{wl.name}_batch{B}", "sequences_per_gpu": B,
+                   "visible_entries": N, "layers_sharing_topk": L,
                    "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)", "parallelism": f"dp{world} (sequences)"},
-        "stages_ms": {"quant_q": round(stage_ms[0], 5), "index_topk": round(stage_ms[1], 5),
-                      "sparse_attn": round(stage_ms[2], 5), "index_score_alone": round(scan_ms, 5)},
-        "entries_scored_per_s": round(world * B * N / (ms_max * 1e-3), 1),
+        "stages_ms": dict([(nm, round(v, 5)) for (nm, _), v in zip(stages, stage_ms)] +
+                          [("index_score_alone", round(scan_ms, 5))]),
+        "entries_scored_per_s": round(world * B * (N + (NBLK * 8 if reindex else 0)) / (ms_max * 1e-3), 1),
         "indexer_scan_gbs": round(scan_gbs, 1),
         "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": round(scan_gbs, 1),
                      "peak": hbm_peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
@@ -337,11 +372,10 @@ def run_gpu(args):
                      "algorithmic_bytes_per_launch": scan_bytes},
         "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        # per step: quant, scan, Top-K select + finalize, attention partial + combine
-        "gpu_launches": args.steps * (1 + 1 + 2 + n_attn_launches),
+        "gpu_launches": args.steps * n_launches,
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and wid == WORKLOAD_ID:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -449,7 +483,9 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
-    ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's 32)")
+    ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 4],
+                    help="decode workload id (default 1: 32 sequences x 65,536 entries)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)

@@ -415,24 +415,18 @@ __device__ void finalize_row(int t, uint32_t above, uint32_t c_t, uint32_t n_can
             },
             h, scratch, &r3);
       }
+      // keys above T, ties at T with ~position above P, and r3 of the ties
+      // sitting exactly at ~position == P (a ticket; they share one position)
+      __shared__ uint32_t s_r3;
+      if (threadIdx.x == 0) s_r3 = 0;
+      __syncthreads();
       for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
         const uint2 c = ld(i);
         bool take = c.x > T || (c.x == T && (all_eq || (~c.y) > P));
+        if (!take && !all_eq && c.x == T && ~c.y == P) take = atomicAdd(&s_r3, 1u) < r3;
         if (take) {
           uint32_t slot = atomicAdd(&s_nout, 1u);
           if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
-        }
-      }
-      __syncthreads();
-      // exactly r3 further ties sit at ~position == P (distinct positions: r3 <= 1)
-      if (!all_eq && threadIdx.x == 0) {
-        for (uint32_t i = 0; i < n_cand && r3 > 0; ++i) {
-          const uint2 c = ld(i);
-          if (c.x == T && ~c.y == P) {
-            uint32_t slot = s_nout++;
-            if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
-            --r3;
-          }
         }
       }
     }
