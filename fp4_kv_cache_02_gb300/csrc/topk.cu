@@ -7,15 +7,26 @@
 //
 // Radix/threshold select on order-preserving 32-bit keys of the fp32 scores:
 //   1. histogram of the top 11 key bits per row (shared-memory histogram per
-//      CTA, flushed to a per-row global histogram; the decode scan can build
-//      it in its epilogue);
-//   2. every CTA finds the threshold bin t of its row (the bin in which the
-//      running count from the top reaches k), then streams its slice: keys
-//      above bin t are selected outright, keys inside bin t become candidates;
-//   3. one CTA per row resolves bin t exactly on the remaining 21 key bits,
-//      breaks exact ties by smaller position, sorts the k positions ascending
-//      and writes them.
-// The result does not depend on the order in which CTAs run.
+//      CTA, flushed to a per-row global histogram; the decode scan builds it
+//      in its epilogue);
+//   2. select: the row is cut into regions of 4096 scores (more for very long
+//      rows), one CTA each. While the region's loads are in flight the CTA
+//      finds the threshold bin t of the row (the bin in which the running
+//      count from the top reaches k). Every key in bin t or above is written,
+//      in position order, to the region's own slice of the candidate buffer
+//      (no global atomics), and the keys inside bin t are counted in a
+//      second-level histogram of the next 11 key bits;
+//   3. finalize, one CTA per row: the second-level threshold bin t2 splits the
+//      candidates into taken ones and the few inside t2, which are ranked
+//      exactly (key, then smaller position). The taken keys are compacted in
+//      list order, which is ascending position when the row is dense, so the
+//      ascending output needs no sort: the few exact-rank winners are merged
+//      in by binary search. Rows given through a positions map are sorted at
+//      the end unless already ascending.
+// Indexer scores crowd into a narrow band of values, so one 11-bit level
+// leaves thousands of candidates in bin t at a million entries; the second
+// level cuts that to a handful. The result does not depend on the order in
+// which CTAs run.
 #include "common.cuh"
 
 #include <mutex>
@@ -27,43 +38,65 @@ __device__ int g_topk_error = 0;
 constexpr int kHistBits = kTopkHistBits;  // 11
 constexpr int kHistBins = kTopkHistBins;  // 2048
 constexpr int kSelThreads = 256;
+constexpr int kPerThread = 16;                      // consecutive scores per select thread
+constexpr int kSelTile = kSelThreads * kPerThread;  // 4096 scores
+constexpr int kMaxRegions = 8192;                   // regions per row (their offsets live in shared memory)
+constexpr int kFinThreads = 512;
+constexpr int kFinPerThread = 8;
+constexpr int kTieCap = 1024;                       // second-level ties ranked in shared memory
+constexpr int kHist2Shift = 32 - 2 * kHistBits;     // 10: second-level digit is key bits [20, 10]
 
 struct RowCounters {
-  uint32_t n_sel;      // positions appended to sel
-  uint32_t n_cand;     // (key, position) pairs appended to cand
-  uint32_t done;       // select CTAs of the row that finished streaming
-  uint32_t hist_done;  // histogram CTAs of the row that flushed their counts
-  int32_t t;           // threshold bin (-1: fewer candidates than k)
-  uint32_t above;      // candidates in bins above t
-  uint32_t pad[2];
+  int32_t t;       // threshold bin (-1: fewer candidates than k)
+  uint32_t above;  // candidates in bins above t
+  uint32_t pad[6];
 };
 
 struct TopkWs {
-  uint32_t* hist;       // [B][4096]
-  RowCounters* cnt;     // [B]
-  int32_t* sel;         // [B][k]
-  uint2* cand;          // [B][n]  (key, position)
+  uint32_t* hist;     // [B][kHistBins]  top 11 key bits
+  uint32_t* hist2;    // [B][kHistBins]  next 11 key bits of the keys in bin t
+  RowCounters* cnt;   // [B]
+  uint32_t* rcount;   // [B][n_regions]  keys each region wrote
+  uint2* cand;        // [B][n]  (key, position); region r owns [r*region, r*region + its scores)
+  int64_t region;     // scores per region (a multiple of kSelTile)
+  int32_t n_regions;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+__host__ __device__ inline void topk_regions(int64_t n, int64_t* region, int32_t* n_regions) {
+  const int64_t tiles = n > 0 ? (n + kSelTile - 1) / kSelTile : 1;
+  const int64_t m = (tiles + kMaxRegions - 1) / kMaxRegions;
+  *region = m * kSelTile;
+  *n_regions = (int32_t)((tiles + m - 1) / m);
+}
+
 __host__ __device__ inline size_t topk_ws_layout(int32_t B, int64_t n, int32_t k, TopkWs* ws, char* base) {
+  (void)k;
+  int64_t region;
+  int32_t nr;
+  topk_regions(n, &region, &nr);
   size_t off = 0;
-  size_t hist = off; off = align_up(off + (size_t)B * kHistBins * 4, 256);
-  size_t cnt = off;  off = align_up(off + (size_t)B * sizeof(RowCounters), 256);
-  size_t sel = off;  off = align_up(off + (size_t)B * k * 4, 256);
-  size_t cand = off; off = align_up(off + (size_t)B * (size_t)(n > 0 ? n : 1) * 8, 256);
+  size_t hist = off;   off = align_up(off + (size_t)B * kHistBins * 4, 256);
+  size_t hist2 = off;  off = align_up(off + (size_t)B * kHistBins * 4, 256);
+  size_t cnt = off;    off = align_up(off + (size_t)B * sizeof(RowCounters), 256);
+  size_t rcount = off; off = align_up(off + (size_t)B * nr * 4, 256);
+  size_t cand = off;   off = align_up(off + (size_t)B * (size_t)(n > 0 ? n : 1) * 8, 256);
   if (ws) {
     ws->hist = (uint32_t*)(base + hist);
+    ws->hist2 = (uint32_t*)(base + hist2);
     ws->cnt = (RowCounters*)(base + cnt);
-    ws->sel = (int32_t*)(base + sel);
+    ws->rcount = (uint32_t*)(base + rcount);
     ws->cand = (uint2*)(base + cand);
+    ws->region = region;
+    ws->n_regions = nr;
   }
   return off;
 }
 
+// The histograms and counters (the leading part of the layout) start at zero.
 __host__ __device__ inline size_t topk_ws_zero_bytes(int32_t B) {
-  return align_up(align_up((size_t)B * kHistBins * 4, 256) + (size_t)B * sizeof(RowCounters), 256);
+  return align_up(2 * align_up((size_t)B * kHistBins * 4, 256) + (size_t)B * sizeof(RowCounters), 256);
 }
 
 __device__ __forceinline__ bool load_candidate(const float* __restrict__ scores, const int32_t* __restrict__ positions,
@@ -163,6 +196,60 @@ __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, u
   const int bin = (int)scratch[blockDim.x];
   *above_out = scratch[blockDim.x + 1];
   __syncthreads();
+  return bin;
+}
+
+// One warp finds, in a global histogram of kHistBins counts, the first bin
+// from the top at which the running count reaches `need` (-1 if the total is
+// below it) and the count strictly above that bin. Lane l owns bins
+// [kHistBins - 64(l+1), kHistBins - 64 l); a warp scan over the lanes finds the
+// owning lane, then the lanes split that lane's 64 bins two apiece. The row
+// must be 256-byte aligned; counts are read through L2 (__ldcg) because other
+// CTAs of an earlier kernel wrote them with atomics.
+__device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need, uint32_t* above_out) {
+  static_assert(kHistBins == 32 * 64, "one warp covers the histogram 64 bins a lane");
+  const int lane = threadIdx.x & 31;
+  const uint4* p = reinterpret_cast<const uint4*>(gh + kHistBins - 64 * (lane + 1));
+  uint32_t s = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint4 v = __ldcg(p + i);
+    s += v.x + v.y + v.z + v.w;
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total < need) {
+    *above_out = total;
+    return -1;
+  }
+  const int c = __ffs(__ballot_sync(0xffffffffu, incl >= need)) - 1;
+  const uint32_t excl_c = __shfl_sync(0xffffffffu, incl - s, c);
+  const int top_c = kHistBins - 64 * c;
+  // lane l: bins top_c-1-2l (.y) and top_c-2-2l (.x)
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(gh + top_c - 2 - 2 * lane));
+  const uint32_t ps = v.x + v.y;
+  uint32_t incl2 = ps;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) incl2 += x;
+  }
+  const int c2 = __ffs(__ballot_sync(0xffffffffu, excl_c + incl2 >= need)) - 1;
+  uint32_t base = excl_c + __shfl_sync(0xffffffffu, incl2 - ps, c2);
+  const uint32_t hy = __shfl_sync(0xffffffffu, v.y, c2);
+  int bin;
+  if (base + hy >= need) {
+    bin = top_c - 1 - 2 * c2;
+  } else {
+    bin = top_c - 2 - 2 * c2;
+    base += hy;
+  }
+  *above_out = base;
   return bin;
 }
 
@@ -302,172 +389,459 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   return r;
 }
 
-// ---- pass 2: stream, select above the threshold bin, finalize in the last CTA --
-// Each sub-chunk of kSelThreads x kPerThread scores is classified in registers;
-// one block scan and one reservation atomic per output list place the
-// selected positions (key above bin t) and the bin-t candidates.
-constexpr int kPerThread = 16;
-constexpr int kSmemCand = 4096;  // bin-t candidates finalized in shared memory up to this count
-
-__global__ void __launch_bounds__(kSelThreads) topk_select_kernel(
-    const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
-    const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws) {
-  __shared__ uint32_t h[kHistBins];
-  __shared__ uint32_t scratch[kSelThreads + 8];
-  __shared__ uint32_t s_base[2];
-  const int b = blockIdx.y;
-  for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) h[i] = __ldcg(ws.hist + (size_t)b * kHistBins + i);
-  __syncthreads();
-  uint32_t above;
-  const int t = find_threshold_bin(h, kHistBins, (uint32_t)k, &above, scratch);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    ws.cnt[b].t = t;
-    ws.cnt[b].above = above;
-  }
-  const int64_t row_off = (int64_t)b * n;
-  int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
-  int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
-  RowCounters* cnt = ws.cnt + b;
-  int32_t* sel = ws.sel + (size_t)b * k;
-  uint2* cand = ws.cand + (size_t)b * n;
-  for (int64_t sub = lo; sub < hi; sub += (int64_t)kSelThreads * kPerThread) {
-    uint32_t key[kPerThread];
-    int32_t pos[kPerThread];
-    uint32_t take = 0, keep = 0;
+// ---- pass 2: every key in bin t or above, written per region in order ------
+// Loads the kPerThread consecutive scores [i0, i0 + kPerThread) of a row (16-byte
+// vectors when the row allows) and returns the mask of candidates.
+template <bool kPositions>
+__device__ __forceinline__ uint32_t load_run(const float* __restrict__ scores, const int32_t* __restrict__ positions,
+                                             int64_t row_off, int64_t i0, int64_t nv, bool vec, uint32_t* key,
+                                             int32_t* pos) {
+  float s[kPerThread];
+  int32_t p[kPerThread];
+  if (vec && i0 + kPerThread <= nv) {
+    const float4* sp = reinterpret_cast<const float4*>(scores + row_off + i0);
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-      const int64_t i = sub + (int64_t)e * kSelThreads + threadIdx.x;
-      const bool ok = i < hi && load_candidate(scores, positions, row_off, i, nv, &key[e], &pos[e]);
-      const int digit = ok ? (int)(key[e] >> (32 - kHistBits)) : -2;
-      take |= (uint32_t)(ok && digit > t) << e;
-      keep |= (uint32_t)(ok && digit == t) << e;
+    for (int q = 0; q < kPerThread / 4; ++q) {
+      const float4 v = sp[q];
+      s[4 * q] = v.x; s[4 * q + 1] = v.y; s[4 * q + 2] = v.z; s[4 * q + 3] = v.w;
     }
-    uint32_t total;
-    const uint32_t excl = block_exclusive_scan(__popc(take) | ((uint32_t)__popc(keep) << 16), &total, scratch);
-    if (threadIdx.x == 0) {
-      s_base[0] = (total & 0xFFFFu) ? atomicAdd(&cnt->n_sel, total & 0xFFFFu) : 0u;
-      s_base[1] = (total >> 16) ? atomicAdd(&cnt->n_cand, total >> 16) : 0u;
-    }
-    __syncthreads();
-    uint32_t st = s_base[0] + (excl & 0xFFFFu), sk = s_base[1] + (excl >> 16);
+    if (kPositions) {
+      const int4* pp = reinterpret_cast<const int4*>(positions + row_off + i0);
 #pragma unroll
-    for (int e = 0; e < kPerThread; ++e) {
-      if (take & (1u << e)) {
-        if (st < (uint32_t)k) sel[st] = pos[e];
-        else record_error(&g_topk_error, CSA2_ERR_DEVICE);
-        ++st;
-      }
-      if (keep & (1u << e)) {
-        if (sk < (uint32_t)n) cand[sk] = make_uint2(key[e], (uint32_t)pos[e]);
-        else record_error(&g_topk_error, CSA2_ERR_DEVICE);
-        ++sk;
+      for (int q = 0; q < kPerThread / 4; ++q) {
+        const int4 v = pp[q];
+        p[4 * q] = v.x; p[4 * q + 1] = v.y; p[4 * q + 2] = v.z; p[4 * q + 3] = v.w;
       }
     }
-    __syncthreads();  // s_base is rewritten by the next sub-chunk
+  } else {
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      const bool in = i0 + e < nv;
+      s[e] = in ? scores[row_off + i0 + e] : __uint_as_float(0x7fc00000u);
+      if (kPositions) p[e] = in ? positions[row_off + i0 + e] : -1;
+    }
   }
+  uint32_t ok = 0;
+#pragma unroll
+  for (int e = 0; e < kPerThread; ++e) {
+    const int32_t pe = kPositions ? p[e] : (int32_t)(i0 + e);
+    ok |= (uint32_t)(i0 + e < nv && pe >= 0 && score_is_candidate(s[e])) << e;
+    key[e] = score_key(s[e]);
+    if (kPositions) pos[e] = pe;
+  }
+  return ok;
 }
 
-// Resolves bin t exactly and writes one row: out[0..s_nout) already holds the
-// positions whose key lies above bin t; the n_cand bin-t candidates are read
-// through `ld`. Keys above the exact threshold key are taken; among keys equal
-// to it, the smallest positions. The k positions are sorted ascending into dst
-// (-1 padding). h has kHistBins words, scratch blockDim.x + 8.
-template <typename LoadFn>
-__device__ void finalize_row(int t, uint32_t above, uint32_t c_t, uint32_t n_cand, int32_t k, LoadFn ld,
-                             int32_t* out, uint32_t& s_nout, uint32_t* h, uint32_t* scratch, int32_t* dst) {
-  if (t >= 0) {
-    uint32_t r = (uint32_t)k - above;  // still needed from bin t (1 <= r <= c_t)
-    if (r >= n_cand || r >= c_t) {
-      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        uint32_t slot = atomicAdd(&s_nout, 1u);
-        if (slot < (uint32_t)k) out[slot] = (int32_t)ld(i).y;
+template <bool kPositions>
+__global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
+    const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
+    const int32_t* __restrict__ positions, int32_t k, TopkWs ws) {
+  __shared__ uint32_t h2[kHistBins];
+  __shared__ uint32_t s_wsum[kSelThreads / 32];
+  __shared__ uint32_t s_wex[kSelThreads / 32];
+  __shared__ uint32_t s_scan[33];
+  __shared__ int s_t;
+  const int b = blockIdx.y;
+  const int r = blockIdx.x;
+  const int64_t row_off = (int64_t)b * n;
+  const int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
+  const int64_t lo_r = (int64_t)r * ws.region;
+  uint32_t* rcount = ws.rcount + (size_t)b * ws.n_regions;
+  if (lo_r >= nv && r != 0) {  // region 0 always runs: it records t
+    if (threadIdx.x == 0) rcount[r] = 0u;
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool vec = (((uintptr_t)(scores + row_off)) & 15) == 0 &&
+                   (!kPositions || (((uintptr_t)(positions + row_off)) & 15) == 0);
+  // this thread's loads go out first; the threshold search overlaps them
+  uint32_t key[kPerThread];
+  int32_t pos[kPositions ? kPerThread : 1];
+  int64_t lo = lo_r;
+  uint32_t ok = lo < nv ? load_run<kPositions>(scores, positions, row_off, lo + (int64_t)threadIdx.x * kPerThread,
+                                               nv, vec, key, pos)
+                        : 0u;
+  // threshold bin t of the row: thread j sums the 8 bins [2040 - 8j, 2048 - 8j),
+  // a block scan from the top finds the thread whose bins reach k
+  static_assert(kHistBins == 8 * kSelThreads, "8 histogram bins per select thread");
+  const uint4* hp =
+      reinterpret_cast<const uint4*>(ws.hist + (size_t)b * kHistBins + kHistBins - 8 * (threadIdx.x + 1));
+  const uint4 hlo = __ldcg(hp), hhi = __ldcg(hp + 1);  // bins base+0..3, base+4..7
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0u;
+  const uint32_t hs = hlo.x + hlo.y + hlo.z + hlo.w + hhi.x + hhi.y + hhi.z + hhi.w;
+  uint32_t hin = hs;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, hin, o);
+    if (lane >= o) hin += x;
+  }
+  if (lane == 31) s_wsum[warp] = hin;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int kWarps = kSelThreads / 32;
+    const uint32_t wv = lane < kWarps ? s_wsum[lane] : 0u;
+    uint32_t wi = wv;
+#pragma unroll
+    for (int o = 1; o < kWarps; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += x;
+    }
+    if (lane < kWarps) s_wex[lane] = wi - wv;
+    if (lane == kWarps - 1 && wi < (uint32_t)k) {  // fewer candidates than k
+      s_t = -1;
+      if (r == 0) {
+        ws.cnt[b].t = -1;
+        ws.cnt[b].above = wi;
       }
-    } else {
-      uint32_t r2;
-      uint32_t T = radix_select_desc(
-          (int)n_cand, r, kHistBits, ((uint32_t)t) << (32 - kHistBits),
-          [&](int i) { return ld((uint32_t)i).x; }, h, scratch, &r2);
-      // keys above T are all taken; among keys equal to T the r2 smallest
-      // positions are taken (select on ~position, largest first)
-      uint32_t n_eq = 0;
-      {
-        // count keys == T
-        __shared__ uint32_t s_eq;
-        if (threadIdx.x == 0) s_eq = 0;
-        __syncthreads();
-        uint32_t local = 0;
-        for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) local += (ld(i).x == T);
-        atomicAdd(&s_eq, local);
-        __syncthreads();
-        n_eq = s_eq;
-        __syncthreads();
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t hex = s_wex[warp] + hin - hs;  // count in the bins above this thread's
+    if (hex < (uint32_t)k && hex + hs >= (uint32_t)k) {
+      const uint32_t v[8] = {hhi.w, hhi.z, hhi.y, hhi.x, hlo.w, hlo.z, hlo.y, hlo.x};  // top bin first
+      uint32_t run = hex;
+      int bin = kHistBins - 8 * (int)threadIdx.x - 1;
+#pragma unroll
+      for (int i = 0; i < 7; ++i) {
+        if (run + v[i] >= (uint32_t)k) break;
+        run += v[i];
+        --bin;
       }
-      uint32_t P = 0xFFFFFFFFu, r3 = 0;
-      bool all_eq = r2 >= n_eq;
-      if (!all_eq) {
-        // positions are >= 0, so ~position has bit 31 set: select the r2
-        // largest ~position among keys == T
-        P = radix_select_desc(
-            (int)n_cand, r2, 0, 0u,
-            [&](int i) {
-              const uint2 c = ld((uint32_t)i);
-              return c.x == T ? ~c.y : 0u;
-            },
-            h, scratch, &r3);
+      s_t = bin;
+      if (r == 0) {
+        ws.cnt[b].t = bin;
+        ws.cnt[b].above = run;
       }
-      // keys above T, ties at T with ~position above P, and r3 of the ties
-      // sitting exactly at ~position == P (a ticket; they share one position)
-      __shared__ uint32_t s_r3;
-      if (threadIdx.x == 0) s_r3 = 0;
-      __syncthreads();
-      for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) {
-        const uint2 c = ld(i);
-        bool take = c.x > T || (c.x == T && (all_eq || (~c.y) > P));
-        if (!take && !all_eq && c.x == T && ~c.y == P) take = atomicAdd(&s_r3, 1u) < r3;
-        if (take) {
-          uint32_t slot = atomicAdd(&s_nout, 1u);
-          if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
+    }
+  }
+  __syncthreads();
+  const int t = s_t;
+  const int64_t hi_r = min(lo_r + ws.region, nv);
+  uint2* cand = ws.cand + row_off;
+  uint32_t written = 0;  // keys this region wrote so far (same in every thread)
+  bool any_t = false;
+  for (;;) {
+    uint32_t flag = 0;
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      const int digit = (int)(key[e] >> (32 - kHistBits));
+      const bool f = ((ok >> e) & 1u) && digit >= t;
+      flag |= (uint32_t)f << e;
+      if (f && digit == t) {
+        atomicAdd(&h2[(key[e] >> kHist2Shift) & (kHistBins - 1)], 1u);
+        any_t = true;
+      }
+    }
+    uint32_t total;
+    const uint32_t excl = block_exclusive_scan((uint32_t)__popc(flag), &total, s_scan);
+    if (flag) {
+      int64_t o = lo_r + written + excl;
+#pragma unroll
+      for (int e = 0; e < kPerThread; ++e) {
+        if ((flag >> e) & 1u) {
+          const int32_t p = kPositions ? pos[kPositions ? e : 0] : (int32_t)(lo + (int64_t)threadIdx.x * kPerThread + e);
+          if (o < hi_r) cand[o] = make_uint2(key[e], (uint32_t)p);
+          else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+          ++o;
         }
       }
     }
+    written += total;
+    lo += kSelTile;
+    if (lo >= hi_r) break;
+    ok = load_run<kPositions>(scores, positions, row_off, lo + (int64_t)threadIdx.x * kPerThread, nv, vec, key, pos);
   }
-  __syncthreads();
-  uint32_t nout = min(s_nout, (uint32_t)k);
-  int n2 = (int)blockDim.x;
-  while (n2 < k) n2 <<= 1;
-  for (int i = threadIdx.x; i < n2; i += blockDim.x)
-    if (i >= (int)nout) out[i] = 0x7FFFFFFF;
-  __syncthreads();
-  block_sort_asc(out, n2);
-  for (int i = threadIdx.x; i < k; i += blockDim.x) dst[i] = i < (int)nout ? out[i] : -1;
+  if (threadIdx.x == 0) rcount[r] = written;
+  if (__syncthreads_or(any_t)) {
+    uint32_t* gh2 = ws.hist2 + (size_t)b * kHistBins;
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+      if (h2[i]) atomicAdd(&gh2[i], h2[i]);
+  }
 }
 
-// ---- pass 3: one CTA per row resolves bin t exactly and writes the row ------
-__global__ void __launch_bounds__(kSelThreads) topk_finalize_kernel(int64_t n, int32_t k, TopkWs ws,
-                                                                    int32_t* __restrict__ idx) {
-  extern __shared__ uint32_t smem[];
-  uint32_t* h = smem;                    // kHistBins
-  uint32_t* scratch = smem + kHistBins;  // kSelThreads + 8
-  int32_t* out = (int32_t*)(smem + kHistBins + kSelThreads + 8);                 // CSA2_MAX_TOPK
-  uint2* cand_s = (uint2*)(smem + kHistBins + kSelThreads + 8 + CSA2_MAX_TOPK);  // kSmemCand
-  __shared__ uint32_t s_nout;
-  const int b = blockIdx.x;
-  RowCounters* cnt = ws.cnt + b;
-  const int32_t* sel = ws.sel + (size_t)b * k;
-  const uint2* cand = ws.cand + (size_t)b * n;
-  const int t = cnt->t;
-  const uint32_t above = cnt->above;
-  const uint32_t c_t = t >= 0 ? ws.hist[(size_t)b * kHistBins + t] : 0u;
-  const uint32_t n_sel = min(cnt->n_sel, (uint32_t)k);
-  const uint32_t n_cand = min(cnt->n_cand, (uint32_t)n);
-  const bool in_smem = n_cand <= (uint32_t)kSmemCand;
-  if (in_smem)
-    for (uint32_t i = threadIdx.x; i < n_cand; i += blockDim.x) cand_s[i] = cand[i];
-  for (uint32_t i = threadIdx.x; i < n_sel; i += blockDim.x) out[i] = sel[i];
-  if (threadIdx.x == 0) s_nout = n_sel;
+// Appends every entry [0, count) of `ld` to out (through the s_nout ticket).
+template <typename LoadFn>
+__device__ void take_all(uint32_t count, LoadFn ld, int32_t k, int32_t* out, uint32_t& s_nout) {
+  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
+    const uint32_t slot = atomicAdd(&s_nout, 1u);
+    if (slot < (uint32_t)k) out[slot] = (int32_t)ld(i).y;
+  }
+}
+
+// Takes the `need` largest of `count` (key, position) entries read through
+// `ld`, every key's top `fixed_bits` equal to those of `prefix`: keys above the
+// exact threshold key T are taken, and among keys equal to T the smallest
+// positions. h has kHistBins words (or blockDim.x if more), scratch
+// blockDim.x + 8.
+template <typename LoadFn>
+__device__ void resolve_exact(uint32_t count, uint32_t need, int fixed_bits, uint32_t prefix, LoadFn ld, int32_t k,
+                              int32_t* out, uint32_t& s_nout, uint32_t* h, uint32_t* scratch) {
+  if (need >= count) {
+    take_all(count, ld, k, out, s_nout);
+    return;
+  }
+  uint32_t r2;
+  const uint32_t T = radix_select_desc(
+      (int)count, need, fixed_bits, prefix, [&](int i) { return ld((uint32_t)i).x; }, h, scratch, &r2);
+  __shared__ uint32_t s_eq, s_r3;
+  if (threadIdx.x == 0) {
+    s_eq = 0;
+    s_r3 = 0;
+  }
   __syncthreads();
-  finalize_row(t, above, c_t, n_cand, k, [&](uint32_t i) -> uint2 { return in_smem ? cand_s[i] : cand[i]; }, out,
-               s_nout, h, scratch, idx + (size_t)b * k);
+  uint32_t local = 0;
+  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) local += (ld(i).x == T);
+  atomicAdd(&s_eq, local);
+  __syncthreads();
+  const uint32_t n_eq = s_eq;
+  const bool all_eq = r2 >= n_eq;
+  uint32_t P = 0xFFFFFFFFu, r3 = 0;
+  if (!all_eq) {
+    // positions are >= 0, so ~position has bit 31 set: select the r2 largest
+    // ~position among keys == T
+    P = radix_select_desc(
+        (int)count, r2, 0, 0u,
+        [&](int i) {
+          const uint2 c = ld((uint32_t)i);
+          return c.x == T ? ~c.y : 0u;
+        },
+        h, scratch, &r3);
+  }
+  // keys above T, ties at T with ~position above P, and r3 of the ties sitting
+  // exactly at ~position == P (a ticket: they share one position)
+  for (uint32_t i = threadIdx.x; i < count; i += blockDim.x) {
+    const uint2 c = ld(i);
+    bool tk = c.x > T || (c.x == T && (all_eq || (~c.y) > P));
+    if (!tk && !all_eq && c.x == T && ~c.y == P) tk = atomicAdd(&s_r3, 1u) < r3;
+    if (tk) {
+      const uint32_t slot = atomicAdd(&s_nout, 1u);
+      if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
+    }
+  }
+}
+
+// Region holding flat list index g: the largest j in [0, R) with prefix[j] <= g.
+__device__ __forceinline__ int region_of(const uint32_t* prefix, int R, uint32_t g) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= g) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Number of entries of the ascending array a[0..len) that are below v.
+__device__ __forceinline__ uint32_t count_below(const int32_t* a, uint32_t len, int32_t v) {
+  uint32_t lo = 0, hi = len;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (a[mid] < v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// ---- pass 3: one CTA per row resolves bin t and writes the row -------------
+// Shared memory (dynamic): ties (uint2) [kTieCap], prefix [kMaxRegions + 1],
+// out [CSA2_MAX_TOPK], h [kHistBins], scratch [kFinThreads + 8], tsel [kTieCap].
+static constexpr size_t kFinSmem =
+    (size_t)kTieCap * 8 + (size_t)(kMaxRegions + 1 + CSA2_MAX_TOPK + kHistBins + kFinThreads + 8 + kTieCap) * 4;
+
+__global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n, int32_t k, TopkWs ws,
+                                                                       int32_t* __restrict__ idx, int dense) {
+  extern __shared__ __align__(16) unsigned char fsm[];
+  uint2* ties = reinterpret_cast<uint2*>(fsm);
+  uint32_t* prefix = reinterpret_cast<uint32_t*>(fsm + (size_t)kTieCap * 8);
+  int32_t* out = reinterpret_cast<int32_t*>(prefix + kMaxRegions + 1);
+  uint32_t* h = reinterpret_cast<uint32_t*>(out + CSA2_MAX_TOPK);
+  uint32_t* scratch = h + kHistBins;
+  int32_t* tsel = reinterpret_cast<int32_t*>(scratch + kFinThreads + 8);
+  __shared__ uint32_t s_nout, s_ntie, s_nsel, s_above2;
+  __shared__ int s_t2;
+  const int b = blockIdx.x;
+  const int R = ws.n_regions;
+  const int64_t row_off = (int64_t)b * n;
+  const uint2* cand = ws.cand + row_off;
+  int32_t* dst = idx + (size_t)b * k;
+  const int t = __ldcg(&ws.cnt[b].t);
+  const uint32_t above = __ldcg(&ws.cnt[b].above);
+  const uint32_t c_t = t >= 0 ? __ldcg(ws.hist + (size_t)b * kHistBins + t) : 0u;
+  const uint32_t r = t >= 0 ? (uint32_t)k - above : 0u;  // still needed from bin t
+  const bool need_res = t >= 0 && r < c_t;
+  // region sizes -> offsets (the loads are in flight while warp 0 finds t2)
+  const uint32_t* rc = ws.rcount + (size_t)b * R;
+  const int per = (R + kFinThreads - 1) / kFinThreads;
+  const int j0 = (int)threadIdx.x * per, j1 = min(j0 + per, R);
+  uint32_t local = 0;
+  for (int j = j0; j < j1; ++j) local += __ldcg(rc + j);
+  if (need_res && threadIdx.x < 32) {
+    uint32_t above2;
+    const int t2 = warp_threshold_bin(ws.hist2 + (size_t)b * kHistBins, r, &above2);
+    if (threadIdx.x == 0) {
+      s_t2 = t2;
+      s_above2 = above2;
+    }
+  }
+  if (threadIdx.x == 0) {
+    s_nout = 0;
+    s_ntie = 0;
+    s_nsel = 0;
+  }
+  uint32_t total_m;
+  uint32_t run = block_exclusive_scan(local, &total_m, scratch);
+  for (int j = j0; j < j1; ++j) {
+    prefix[j] = run;
+    run += __ldcg(rc + j);
+  }
+  if (threadIdx.x == 0) prefix[R] = total_m;
+  __syncthreads();
+  const uint32_t M = total_m;
+  int t2 = -1;
+  uint32_t c_t2 = 0, r2 = 0;
+  bool res_ties = false;
+  if (need_res) {
+    t2 = s_t2;
+    if (t2 >= 0) {
+      c_t2 = __ldcg(ws.hist2 + (size_t)b * kHistBins + t2);
+      r2 = r - s_above2;
+      res_ties = r2 < c_t2;
+    }
+  }
+  const auto ld_flat = [&](uint32_t g) -> uint2 {
+    const int j = region_of(prefix, R, g);
+    return __ldcg(cand + (int64_t)j * ws.region + (g - prefix[j]));
+  };
+  bool sort_out = !dense;
+  if (!need_res || (t2 >= 0 && c_t2 <= (uint32_t)kTieCap)) {
+    // one ordered pass: keys above (t, t2) are compacted in list order; the
+    // keys at (t, t2) are collected when only some of them are taken
+    for (uint32_t base = 0; base < M; base += (uint32_t)kFinThreads * kFinPerThread) {
+      const uint32_t g0 = base + threadIdx.x * kFinPerThread;
+      uint2 c[kFinPerThread];
+      uint32_t valid = 0;
+      if (g0 < M) {
+        int j = region_of(prefix, R, g0);
+#pragma unroll
+        for (int e = 0; e < kFinPerThread; ++e) {
+          const uint32_t g = g0 + e;
+          if (g < M) {
+            while (j + 1 < R && prefix[j + 1] <= g) ++j;
+            c[e] = __ldcg(cand + (int64_t)j * ws.region + (g - prefix[j]));
+            valid |= 1u << e;
+          }
+        }
+      }
+      uint32_t def = 0;
+#pragma unroll
+      for (int e = 0; e < kFinPerThread; ++e) {
+        if (!((valid >> e) & 1u)) continue;
+        const int digit = (int)(c[e].x >> (32 - kHistBits));
+        const int d2 = (int)((c[e].x >> kHist2Shift) & (kHistBins - 1));
+        const bool at_t = need_res && digit == t;
+        const bool taken = !at_t || d2 > t2 || (d2 == t2 && !res_ties);
+        def |= (uint32_t)taken << e;
+        if (at_t && d2 == t2 && res_ties) {
+          const uint32_t slot = atomicAdd(&s_ntie, 1u);
+          if (slot < (uint32_t)kTieCap) ties[slot] = c[e];
+        }
+      }
+      uint32_t tot;
+      const uint32_t ex = block_exclusive_scan((uint32_t)__popc(def), &tot, scratch);
+      uint32_t o = s_nout + ex;
+#pragma unroll
+      for (int e = 0; e < kFinPerThread; ++e) {
+        if ((def >> e) & 1u) {
+          if (o < (uint32_t)k) out[o] = (int32_t)c[e].y;
+          else record_error(&g_topk_error, CSA2_ERR_DEVICE);
+          ++o;
+        }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) s_nout += tot;
+      __syncthreads();
+    }
+    const uint32_t n_def = min(s_nout, (uint32_t)k);
+    if (res_ties) {
+      // exact rank of each tie: larger key first, then smaller position, then list slot
+      const uint32_t nt = min(s_ntie, (uint32_t)kTieCap);
+      for (uint32_t i = threadIdx.x; i < nt; i += kFinThreads) {
+        const uint2 ci = ties[i];
+        uint32_t rank = 0;
+        for (uint32_t j = 0; j < nt; ++j) {
+          const uint2 cj = ties[j];
+          rank += (cj.x > ci.x) || (cj.x == ci.x && ((int32_t)cj.y < (int32_t)ci.y || (cj.y == ci.y && j < i)));
+        }
+        if (rank < r2) tsel[atomicAdd(&s_nsel, 1u)] = (int32_t)ci.y;
+      }
+      __syncthreads();
+      const uint32_t nsel = s_nsel;
+      if (dense) {
+        // positions are distinct: sort the few winners by rank, then merge the
+        // two ascending lists straight into the output row
+        int32_t* tsorted = reinterpret_cast<int32_t*>(ties);
+        for (uint32_t i = threadIdx.x; i < nsel; i += kFinThreads) {
+          const int32_t v = tsel[i];
+          uint32_t rank = 0;
+          for (uint32_t j = 0; j < nsel; ++j) rank += tsel[j] < v;
+          tsorted[rank] = v;
+        }
+        __syncthreads();
+        for (uint32_t i = threadIdx.x; i < n_def; i += kFinThreads) {
+          const int32_t q = out[i];
+          const uint32_t d = i + count_below(tsorted, nsel, q);
+          if (d < (uint32_t)k) dst[d] = q;
+        }
+        for (uint32_t j = threadIdx.x; j < nsel; j += kFinThreads) {
+          const int32_t pj = tsorted[j];
+          const uint32_t d = j + count_below(out, n_def, pj);
+          if (d < (uint32_t)k) dst[d] = pj;
+        }
+        for (uint32_t i = n_def + nsel + threadIdx.x; i < (uint32_t)k; i += kFinThreads) dst[i] = -1;
+        return;
+      }
+      for (uint32_t i = threadIdx.x; i < nsel; i += kFinThreads)
+        if (n_def + i < (uint32_t)k) out[n_def + i] = tsel[i];
+      if (threadIdx.x == 0) s_nout = min(n_def + nsel, (uint32_t)k);
+      sort_out = true;
+    } else if (dense) {
+      for (uint32_t i = threadIdx.x; i < (uint32_t)k; i += kFinThreads) dst[i] = i < n_def ? out[i] : -1;
+      return;
+    }
+  } else {
+    // heavy exact ties at (t, t2): keys above bin t are taken and bin t is
+    // resolved exactly over the whole list (keys outside bin t read as 0,
+    // below every candidate key)
+    for (uint32_t g = threadIdx.x; g < M; g += kFinThreads) {
+      const uint2 c = ld_flat(g);
+      if ((int)(c.x >> (32 - kHistBits)) > t) {
+        const uint32_t slot = atomicAdd(&s_nout, 1u);
+        if (slot < (uint32_t)k) out[slot] = (int32_t)c.y;
+      }
+    }
+    const auto ld_bin = [&](uint32_t g) -> uint2 {
+      uint2 c = ld_flat(g);
+      if ((int)(c.x >> (32 - kHistBits)) != t) c.x = 0u;
+      return c;
+    };
+    __syncthreads();
+    resolve_exact(M, r, kHistBits, (uint32_t)t << (32 - kHistBits), ld_bin, k, out, s_nout, h, scratch);
+    sort_out = true;
+  }
+  __syncthreads();
+  const uint32_t nout = min(s_nout, (uint32_t)k);
+  bool inverted = false;
+  for (uint32_t i = threadIdx.x; i + 1 < nout; i += kFinThreads) inverted |= out[i] > out[i + 1];
+  if (__syncthreads_or(sort_out && inverted)) {
+    int n2 = (int)blockDim.x;
+    while (n2 < k) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += blockDim.x)
+      if (i >= (int)nout) out[i] = 0x7FFFFFFF;
+    __syncthreads();
+    block_sort_asc(out, n2);
+  }
+  for (uint32_t i = threadIdx.x; i < (uint32_t)k; i += kFinThreads) dst[i] = i < nout ? out[i] : -1;
 }
 
 // ---- block pool ---------------------------------------------------------------
@@ -524,9 +898,21 @@ static int64_t topk_chunk(int32_t B, int64_t n) {
   return chunk;
 }
 
-static size_t topk_finalize_smem() {
-  // histogram / radix scratch, the output list (up to CSA2_MAX_TOPK), kSmemCand candidates
-  return (size_t)(kHistBins + kSelThreads + 8 + CSA2_MAX_TOPK) * 4 + (size_t)kSmemCand * 8;
+// Opts the finalize kernel into its dynamic shared memory, once per device.
+static int topk_finalize_attr() {
+  constexpr int kMaxDevices = 64;
+  static bool done[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinSmem) !=
+        cudaSuccess)
+      return CSA2_ERR_CUDA;
+    done[dev] = true;
+  }
+  return CSA2_OK;
 }
 
 extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
@@ -553,20 +939,15 @@ int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t
                         int32_t k, int32_t* idx, void* workspace, cudaStream_t stream) {
   TopkWs ws;
   topk_ws_layout(B, n, k, &ws, (char*)workspace);
-  int64_t chunk = topk_chunk(B, n);
-  int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
-  dim3 grid((unsigned)chunks, (unsigned)B);
-  topk_select_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, k, ws);
+  dim3 grid((unsigned)ws.n_regions, (unsigned)B);
+  if (positions)
+    topk_select_kernel<true><<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, k, ws);
+  else
+    topk_select_kernel<false><<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, nullptr, k, ws);
   CSA2_CHECK_LAUNCH();
-  const size_t smem = topk_finalize_smem();
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return CSA2_ERR_CUDA;
-    attr_set = true;
-  }
-  topk_finalize_kernel<<<(unsigned)B, kSelThreads, smem, stream>>>(n, k, ws, idx);
+  int rc = topk_finalize_attr();
+  if (rc) return rc;
+  topk_finalize_kernel<<<(unsigned)B, kFinThreads, kFinSmem, stream>>>(n, k, ws, idx, positions == nullptr);
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
 }
