@@ -3,14 +3,10 @@
 #include "common.cuh"
 
 // launchers defined in the kernel units
-int csa2_launch_index_score_simple(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
-                                   const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                                   const int32_t* n_visible, const int32_t* positions, int64_t n_pos,
-                                   float* scores, cudaStream_t stream);
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                               const int32_t* n_visible, int64_t n_pos, float* scores, uint32_t* hist,
-                               cudaStream_t stream);
+                               const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
+                               uint32_t* hist, cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -65,16 +61,6 @@ static int check_index_args(const uint8_t* q_data, const uint8_t* q_e8m0, const 
   return CSA2_OK;
 }
 
-static int launch_scores(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
-                         const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap, const int32_t* n_visible,
-                         const int32_t* positions, int64_t n_pos, float* scores, cudaStream_t s) {
-  if (positions == nullptr)  // contiguous scan: tensor cores, TMA-fed
-    return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos, scores,
-                                      nullptr, s);
-  return csa2_launch_index_score_simple(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos,
-                                        scores, s);
-}
-
 extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                 const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                 const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
@@ -83,8 +69,9 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (rc) return rc;
   if (!scores) return CSA2_ERR_INVALID_ARG;
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
-  return launch_scores(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                       (cudaStream_t)stream);
+  if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
+  return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
+                                    nullptr, (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -112,6 +99,7 @@ extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, con
     return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (pool_blocks > 0 && (!pool || positions)) return CSA2_ERR_INVALID_ARG;
+  if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   size_t need = csa2_index_topk_workspace_size(B, n_pos, k, pool_blocks);
   if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
   if (B == 0) return CSA2_OK;
@@ -120,19 +108,14 @@ extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, con
   size_t off = al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
   char* rest = (char*)workspace + off;
   size_t rest_bytes = workspace_bytes - off;
-  if (positions == nullptr) {
-    // decode scan: the scan's epilogue builds the Top-K histogram
-    uint32_t* hist = nullptr;
-    rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist);
-    if (rc) return rc;
-    rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos, scores, hist, s);
-    if (rc) return rc;
-    rc = csa2_topk_from_hist(scores, B, n_pos, n_visible, nullptr, k, idx, rest, s);
-  } else {
-    rc = launch_scores(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores, s);
-    if (rc) return rc;
-    rc = csa2_launch_topk(scores, B, n_pos, nullptr, positions, k, idx, rest, rest_bytes, s);
-  }
+  // the scan's epilogue builds the Top-K histogram
+  uint32_t* hist = nullptr;
+  rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist);
+  if (rc) return rc;
+  rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
+                                  hist, s);
+  if (rc) return rc;
+  rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);
   if (rc) return rc;
   if (pool_blocks > 0)
     rc = csa2_launch_block_pool(scores, B, n_pos, n_visible, CSA2_POOL_BLOCK, pool_blocks, pool, rest, rest_bytes, s);

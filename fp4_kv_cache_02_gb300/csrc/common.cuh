@@ -24,7 +24,7 @@ constexpr int kIkScales = kIdxDim / 32;    // 4
 constexpr int kKvBytes = kHeadDim / 2;     // 256
 constexpr int kKvScales = kHeadDim / 16;   // 32
 // Top-K histogram: bins are the top kTopkHistBits bits of score_key()
-constexpr int kTopkHistBits = 11;
+constexpr int kTopkHistBits = 12;
 constexpr int kTopkHistBins = 1 << kTopkHistBits;
 
 // ---- sticky device error word --------------------------------------------

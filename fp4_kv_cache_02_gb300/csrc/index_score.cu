@@ -8,8 +8,9 @@
 //
 //   s[b][i] = sum_h w[b][h] * ReLU( qhat[b][h] . khat[b][p_i] )
 //
-// This file holds the CUDA-core scan used for positions lists, prefill and
-// small problems; the tensor-core scan lives in index_score_tc.cu.
+// The decode scan (contiguous entries, or a positions list for Reindex
+// layers) runs on the tensor cores (index_score_tc.cuh); the CUDA-core
+// kernel here serves the prefill scan.
 #include "common.cuh"
 
 namespace csa2 {
@@ -63,31 +64,6 @@ __device__ __forceinline__ float score_row(const uint8_t* __restrict__ kd,
 #pragma unroll
   for (int h = 0; h < kIdxHeads; ++h) s = fmaf(ws[h], fmaxf(dot[h], 0.0f), s);
   return s;
-}
-
-// grid (ceil(n_pos / blockDim), B); one thread per scored row.
-__global__ void __launch_bounds__(128) index_score_simple_kernel(
-    const uint8_t* __restrict__ q_data, const uint8_t* __restrict__ q_e8m0,
-    const float* __restrict__ w, const uint8_t* __restrict__ ik_data,
-    const uint8_t* __restrict__ ik_scale, int64_t cap, const int32_t* __restrict__ n_visible,
-    const int32_t* __restrict__ positions, int64_t n_pos, float* __restrict__ scores) {
-  __shared__ float qs[kIdxHeads * kIdxDim];
-  __shared__ float ws[kIdxHeads];
-  const int b = blockIdx.y;
-  load_qhat(q_data + (int64_t)b * kIdxHeads * kIkBytes, q_e8m0 + (int64_t)b * kIdxHeads * kIkScales, qs);
-  if (threadIdx.x < kIdxHeads) ws[threadIdx.x] = w[b * kIdxHeads + threadIdx.x];
-  __syncthreads();
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n_pos) return;
-  int64_t p = positions ? (int64_t)positions[(int64_t)b * n_pos + i] : i;
-  int64_t nv = n_visible[b];
-  float out = -INFINITY;
-  if (p >= 0 && p < nv && p < cap) {
-    const uint8_t* kd = ik_data + ((int64_t)b * cap + p) * kIkBytes;
-    const uint8_t* ks = ik_scale + ((int64_t)b * cap + p) * kIkScales;
-    out = score_row(kd, ks, qs, ws);
-  }
-  scores[(int64_t)b * n_pos + i] = out;
 }
 
 // Prefill: grid (ceil(n_entries / blockDim), T); query t sees 0..p0+t.
@@ -154,11 +130,13 @@ static int device_sm_count() {
   return sms[dev];
 }
 
-// Tensor-core scan of positions 0..n_pos-1 of every sequence.
+// Tensor-core scan of list entries 0..n_pos-1 of every sequence: cache
+// positions 0..n_pos-1 (TMA tiles) or, with a positions list, the listed ones
+// (gathered row by row).
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                               const int32_t* n_visible, int64_t n_pos, float* scores, uint32_t* hist,
-                               cudaStream_t stream) {
+                               const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
+                               uint32_t* hist, cudaStream_t stream) {
   if (n_pos == 0 || B == 0) return CSA2_OK;
   if (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)) return CSA2_ERR_ALIGNMENT;
   auto encode = tensor_map_encoder();
@@ -187,22 +165,10 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
       return CSA2_ERR_CUDA;
     attr = true;
   }
-  scan_tc::Params prm{q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per, hist};
+  scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
+                      hist};
   scan_tc::index_score_tc_kernel<<<dim3((unsigned)chunks, (unsigned)B), scan_tc::kThreads, scan_tc::kSmemBytes,
                                    stream>>>(map, prm);
-  CSA2_CHECK_LAUNCH();
-  return CSA2_OK;
-}
-
-// Launch helpers shared with the fused path in capi.cu.
-int csa2_launch_index_score_simple(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
-                                   const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                                   const int32_t* n_visible, const int32_t* positions, int64_t n_pos,
-                                   float* scores, cudaStream_t stream) {
-  if (n_pos == 0 || B == 0) return CSA2_OK;
-  dim3 grid((unsigned)((n_pos + 127) / 128), (unsigned)B);
-  index_score_simple_kernel<<<grid, 128, 0, stream>>>(q_data, q_e8m0, w, ik_data, ik_scale, cap, n_visible,
-                                                      positions, n_pos, scores);
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
 }

@@ -53,6 +53,8 @@ constexpr int kSmemBytes = kOffHist + kTopkHistBins * 4 + 1024;  // + alignment 
 static_assert(kOffQ % 1024 == 0, "q operand must be 1024-byte aligned");
 
 struct Params {
+  const uint8_t* ik_data;  // read directly (cp.async) in the positions mode
+  const int32_t* positions;  // optional [B][n_pos] cache positions; NULL = 0..n_pos-1
   const uint8_t* q_data;
   const uint8_t* q_e8m0;
   const float* w;
@@ -83,23 +85,27 @@ __global__ void __launch_bounds__(kThreads, 3)
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + kOffHist);
   const bool with_hist = p.hist != nullptr;
+  const bool pos_mode = p.positions != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int64_t n_tiles_all = (p.n_pos + kTileRows - 1) / kTileRows;
   int64_t nv = (int64_t)p.n_visible[b];
+  // positions mode: a listed position is scored when it is below n_visible
+  // (and the capacity); dense mode: entries 0..nv-1 of the list
+  const int64_t nv_pos = nv < 0 ? 0 : (nv > p.cap ? p.cap : nv);
   nv = nv < 0 ? 0 : (nv > p.n_pos ? p.n_pos : nv);
   const int64_t t_begin = (int64_t)blockIdx.x * p.tiles_per_cta;
   int64_t t_end_all = t_begin + p.tiles_per_cta;
   if (t_end_all > n_tiles_all) t_end_all = n_tiles_all;
-  int64_t t_end = (nv + kTileRows - 1) / kTileRows;
+  int64_t t_end = pos_mode ? t_end_all : (nv + kTileRows - 1) / kTileRows;
   if (t_end > t_end_all) t_end = t_end_all;
   const int n_tiles = t_end > t_begin ? (int)(t_end - t_begin) : 0;
 
   // ---- set-up: barriers, the q operand (B) and its scales, tensor memory ----
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&full[s], pos_mode ? 32 : 1);  // positions mode: one cp.async arrival per producer lane
       tc::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -130,7 +136,45 @@ __global__ void __launch_bounds__(kThreads, 3)
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp && pos_mode) {
+    // ---- gather producer: lane l copies rows 4l..4l+3 of each tile (64 data
+    // bytes in four 16-byte chunks at their SW64 places, 4 scale bytes);
+    // rows whose position is not visible are zero-filled ----
+    const int32_t* plist = p.positions + (int64_t)b * p.n_pos;
+    int32_t pv[4];
+    const auto fetch = [&](int i) {
+      const int64_t base = (t_begin + i) * kTileRows + lane * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) pv[q] = base + q < p.n_pos ? plist[base + q] : -1;
+    };
+    if (n_tiles > 0) fetch(0);
+    int i = 0;
+    for (; i < n_tiles; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const bool ok = tc::mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, &g_index_error);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      int32_t cur[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cur[q] = pv[q];
+      if (i + 1 < n_tiles) fetch(i + 1);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t r = (uint32_t)(lane * 4 + q);
+        const bool valid = cur[q] >= 0 && cur[q] < nv_pos;
+        const int64_t src = (int64_t)b * p.cap + (valid ? cur[q] : 0);
+        const uint32_t nb = valid ? 16u : 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tc::cp_async_16(sA + s * kTileBytes + tc::sw64_offset(r, (uint32_t)c), p.ik_data + src * kIkBytes + c * 16,
+                          nb);
+        tc::cp_async_4(sSfRaw + s * kSfBytes + r * 4, p.ik_scale + src * kIkScales, valid ? 4u : 0u);
+      }
+      tc::cp_async_mbar_arrive(&full[s]);
+    }
+    tc::cp_async_wait_all();  // nothing of this lane is in flight when the CTA ends
+    __syncwarp();
+  } else if (warp == kProducerWarp) {
     // ---- TMA producer ----
     if (lane == 0) {
       int issued = 0;
@@ -218,9 +262,14 @@ __global__ void __launch_bounds__(kThreads, 3)
       float sc = 0.0f;
 #pragma unroll
       for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);
-      const int64_t pos = (t_begin + i) * kTileRows + row;
-      if (pos < p.n_pos) out[pos] = pos < nv ? sc : -INFINITY;
-      if (with_hist && pos < nv && score_is_candidate(sc))
+      const int64_t li = (t_begin + i) * kTileRows + row;  // list index
+      bool valid = li < nv;
+      if (pos_mode) {
+        const int32_t pp = li < p.n_pos ? p.positions[(int64_t)b * p.n_pos + li] : -1;
+        valid = pp >= 0 && pp < nv_pos;
+      }
+      if (li < p.n_pos) out[li] = valid ? sc : -INFINITY;
+      if (with_hist && valid && score_is_candidate(sc))
         atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
     }
     // positions of this CTA's range past the visible entries

@@ -35,16 +35,20 @@ namespace csa2 {
 
 __device__ int g_topk_error = 0;
 
-constexpr int kHistBits = kTopkHistBits;  // 11
-constexpr int kHistBins = kTopkHistBins;  // 2048
+constexpr int kHistBits = kTopkHistBits;  // 12: first level, top key bits
+constexpr int kHistBins = kTopkHistBins;  // 4096
+constexpr int kHist2Bits = 11;            // second level, the next key bits of bin t
+constexpr int kHist2Bins = 1 << kHist2Bits;
+constexpr int kRadixBits = 11;            // bits per pass of the exact radix select
+constexpr int kRadixBins = 1 << kRadixBits;
 constexpr int kSelThreads = 256;
 constexpr int kPerThread = 16;                      // consecutive scores per select thread
 constexpr int kSelTile = kSelThreads * kPerThread;  // 4096 scores
 constexpr int kMaxRegions = 8192;                   // regions per row (their offsets live in shared memory)
 constexpr int kFinThreads = 512;
-constexpr int kFinPerThread = 8;
+constexpr int kFinPerThread = 16;
 constexpr int kTieCap = 1024;                       // second-level ties ranked in shared memory
-constexpr int kHist2Shift = 32 - 2 * kHistBits;     // 10: second-level digit is key bits [20, 10]
+constexpr int kHist2Shift = 32 - kHistBits - kHist2Bits;  // 9: second-level digit is key bits [19, 9]
 
 struct RowCounters {
   int32_t t;       // threshold bin (-1: fewer candidates than k)
@@ -53,8 +57,8 @@ struct RowCounters {
 };
 
 struct TopkWs {
-  uint32_t* hist;     // [B][kHistBins]  top 11 key bits
-  uint32_t* hist2;    // [B][kHistBins]  next 11 key bits of the keys in bin t
+  uint32_t* hist;     // [B][kHistBins]  top 12 key bits
+  uint32_t* hist2;    // [B][kHist2Bins] next 11 key bits of the keys in bin t
   RowCounters* cnt;   // [B]
   uint32_t* rcount;   // [B][n_regions]  keys each region wrote
   uint2* cand;        // [B][n]  (key, position); region r owns [r*region, r*region + its scores)
@@ -78,7 +82,7 @@ __host__ __device__ inline size_t topk_ws_layout(int32_t B, int64_t n, int32_t k
   topk_regions(n, &region, &nr);
   size_t off = 0;
   size_t hist = off;   off = align_up(off + (size_t)B * kHistBins * 4, 256);
-  size_t hist2 = off;  off = align_up(off + (size_t)B * kHistBins * 4, 256);
+  size_t hist2 = off;  off = align_up(off + (size_t)B * kHist2Bins * 4, 256);
   size_t cnt = off;    off = align_up(off + (size_t)B * sizeof(RowCounters), 256);
   size_t rcount = off; off = align_up(off + (size_t)B * nr * 4, 256);
   size_t cand = off;   off = align_up(off + (size_t)B * (size_t)(n > 0 ? n : 1) * 8, 256);
@@ -96,7 +100,9 @@ __host__ __device__ inline size_t topk_ws_layout(int32_t B, int64_t n, int32_t k
 
 // The histograms and counters (the leading part of the layout) start at zero.
 __host__ __device__ inline size_t topk_ws_zero_bytes(int32_t B) {
-  return align_up(2 * align_up((size_t)B * kHistBins * 4, 256) + (size_t)B * sizeof(RowCounters), 256);
+  return align_up(align_up((size_t)B * kHistBins * 4, 256) + align_up((size_t)B * kHist2Bins * 4, 256) +
+                      (size_t)B * sizeof(RowCounters),
+                  256);
 }
 
 __device__ __forceinline__ bool load_candidate(const float* __restrict__ scores, const int32_t* __restrict__ positions,
@@ -199,17 +205,17 @@ __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, u
   return bin;
 }
 
-// One warp finds, in a global histogram of kHistBins counts, the first bin
+// One warp finds, in a global histogram of kHist2Bins counts, the first bin
 // from the top at which the running count reaches `need` (-1 if the total is
 // below it) and the count strictly above that bin. Lane l owns bins
-// [kHistBins - 64(l+1), kHistBins - 64 l); a warp scan over the lanes finds the
+// [kHist2Bins - 64(l+1), kHist2Bins - 64 l); a warp scan over the lanes finds the
 // owning lane, then the lanes split that lane's 64 bins two apiece. The row
 // must be 256-byte aligned; counts are read through L2 (__ldcg) because other
 // CTAs of an earlier kernel wrote them with atomics.
 __device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need, uint32_t* above_out) {
-  static_assert(kHistBins == 32 * 64, "one warp covers the histogram 64 bins a lane");
+  static_assert(kHist2Bins == 32 * 64, "one warp covers the histogram 64 bins a lane");
   const int lane = threadIdx.x & 31;
-  const uint4* p = reinterpret_cast<const uint4*>(gh + kHistBins - 64 * (lane + 1));
+  const uint4* p = reinterpret_cast<const uint4*>(gh + kHist2Bins - 64 * (lane + 1));
   uint32_t s = 0;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -229,7 +235,7 @@ __device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need
   }
   const int c = __ffs(__ballot_sync(0xffffffffu, incl >= need)) - 1;
   const uint32_t excl_c = __shfl_sync(0xffffffffu, incl - s, c);
-  const int top_c = kHistBins - 64 * c;
+  const int top_c = kHist2Bins - 64 * c;
   // lane l: bins top_c-1-2l (.y) and top_c-2-2l (.x)
   const uint2 v = __ldcg(reinterpret_cast<const uint2*>(gh + top_c - 2 - 2 * lane));
   const uint32_t ps = v.x + v.y;
@@ -260,11 +266,11 @@ __device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need
 // many keys equal to the threshold are still needed.
 template <typename KeyFn>
 __device__ uint32_t radix_select_desc(int count, uint32_t need, int fixed_bits, uint32_t prefix,
-                                      KeyFn keyfn, uint32_t* hist /*kHistBins*/, uint32_t* scratch,
+                                      KeyFn keyfn, uint32_t* hist /*kRadixBins*/, uint32_t* scratch,
                                       uint32_t* r_left) {
   int done_bits = fixed_bits;
   while (done_bits < 32) {
-    int pass_bits = min(kHistBits, 32 - done_bits);
+    int pass_bits = min(kRadixBits, 32 - done_bits);
     int nb = 1 << pass_bits;
     int nbins = nb < (int)blockDim.x ? (int)blockDim.x : nb;  // pad to a multiple of blockDim
     for (int i = threadIdx.x; i < nbins; i += blockDim.x) hist[i] = 0;
@@ -436,7 +442,7 @@ template <bool kPositions>
 __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
     const int32_t* __restrict__ positions, int32_t k, TopkWs ws) {
-  __shared__ uint32_t h2[kHistBins];
+  __shared__ uint32_t h2[kHist2Bins];
   __shared__ uint32_t s_wsum[kSelThreads / 32];
   __shared__ uint32_t s_wex[kSelThreads / 32];
   __shared__ uint32_t s_scan[33];
@@ -461,14 +467,19 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
   uint32_t ok = lo < nv ? load_run<kPositions>(scores, positions, row_off, lo + (int64_t)threadIdx.x * kPerThread,
                                                nv, vec, key, pos)
                         : 0u;
-  // threshold bin t of the row: thread j sums the 8 bins [2040 - 8j, 2048 - 8j),
+  // threshold bin t of the row: thread j sums the 16 bins [4080 - 16j, 4096 - 16j),
   // a block scan from the top finds the thread whose bins reach k
-  static_assert(kHistBins == 8 * kSelThreads, "8 histogram bins per select thread");
-  const uint4* hp =
-      reinterpret_cast<const uint4*>(ws.hist + (size_t)b * kHistBins + kHistBins - 8 * (threadIdx.x + 1));
-  const uint4 hlo = __ldcg(hp), hhi = __ldcg(hp + 1);  // bins base+0..3, base+4..7
-  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) h2[i] = 0u;
-  const uint32_t hs = hlo.x + hlo.y + hlo.z + hlo.w + hhi.x + hhi.y + hhi.z + hhi.w;
+  constexpr int kBinsPerThread = kHistBins / kSelThreads;
+  static_assert(kBinsPerThread == 16, "16 histogram bins per select thread");
+  const uint4* hp = reinterpret_cast<const uint4*>(ws.hist + (size_t)b * kHistBins +
+                                                   kHistBins - kBinsPerThread * (threadIdx.x + 1));
+  uint4 hv[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) hv[q] = __ldcg(hp + q);  // bins base + 4q .. base + 4q + 3
+  for (int i = threadIdx.x; i < kHist2Bins; i += kSelThreads) h2[i] = 0u;
+  uint32_t hs = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) hs += hv[q].x + hv[q].y + hv[q].z + hv[q].w;
   uint32_t hin = hs;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -499,11 +510,18 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
   {
     const uint32_t hex = s_wex[warp] + hin - hs;  // count in the bins above this thread's
     if (hex < (uint32_t)k && hex + hs >= (uint32_t)k) {
-      const uint32_t v[8] = {hhi.w, hhi.z, hhi.y, hhi.x, hlo.w, hlo.z, hlo.y, hlo.x};  // top bin first
-      uint32_t run = hex;
-      int bin = kHistBins - 8 * (int)threadIdx.x - 1;
+      uint32_t v[kBinsPerThread];  // top bin first
 #pragma unroll
-      for (int i = 0; i < 7; ++i) {
+      for (int q = 0; q < 4; ++q) {
+        v[15 - 4 * q] = hv[q].x;
+        v[14 - 4 * q] = hv[q].y;
+        v[13 - 4 * q] = hv[q].z;
+        v[12 - 4 * q] = hv[q].w;
+      }
+      uint32_t run = hex;
+      int bin = kHistBins - kBinsPerThread * (int)threadIdx.x - 1;
+#pragma unroll
+      for (int i = 0; i < kBinsPerThread - 1; ++i) {
         if (run + v[i] >= (uint32_t)k) break;
         run += v[i];
         --bin;
@@ -529,7 +547,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
       const bool f = ((ok >> e) & 1u) && digit >= t;
       flag |= (uint32_t)f << e;
       if (f && digit == t) {
-        atomicAdd(&h2[(key[e] >> kHist2Shift) & (kHistBins - 1)], 1u);
+        atomicAdd(&h2[(key[e] >> kHist2Shift) & (kHist2Bins - 1)], 1u);
         any_t = true;
       }
     }
@@ -554,8 +572,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
   }
   if (threadIdx.x == 0) rcount[r] = written;
   if (__syncthreads_or(any_t)) {
-    uint32_t* gh2 = ws.hist2 + (size_t)b * kHistBins;
-    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+    uint32_t* gh2 = ws.hist2 + (size_t)b * kHist2Bins;
+    for (int i = threadIdx.x; i < kHist2Bins; i += kSelThreads)
       if (h2[i]) atomicAdd(&gh2[i], h2[i]);
   }
 }
@@ -572,7 +590,7 @@ __device__ void take_all(uint32_t count, LoadFn ld, int32_t k, int32_t* out, uin
 // Takes the `need` largest of `count` (key, position) entries read through
 // `ld`, every key's top `fixed_bits` equal to those of `prefix`: keys above the
 // exact threshold key T are taken, and among keys equal to T the smallest
-// positions. h has kHistBins words (or blockDim.x if more), scratch
+// positions. h has kRadixBins words (or blockDim.x if more), scratch
 // blockDim.x + 8.
 template <typename LoadFn>
 __device__ void resolve_exact(uint32_t count, uint32_t need, int fixed_bits, uint32_t prefix, LoadFn ld, int32_t k,
@@ -645,9 +663,9 @@ __device__ __forceinline__ uint32_t count_below(const int32_t* a, uint32_t len, 
 
 // ---- pass 3: one CTA per row resolves bin t and writes the row -------------
 // Shared memory (dynamic): ties (uint2) [kTieCap], prefix [kMaxRegions + 1],
-// out [CSA2_MAX_TOPK], h [kHistBins], scratch [kFinThreads + 8], tsel [kTieCap].
+// out [CSA2_MAX_TOPK], h [kRadixBins], scratch [kFinThreads + 8], tsel [kTieCap].
 static constexpr size_t kFinSmem =
-    (size_t)kTieCap * 8 + (size_t)(kMaxRegions + 1 + CSA2_MAX_TOPK + kHistBins + kFinThreads + 8 + kTieCap) * 4;
+    (size_t)kTieCap * 8 + (size_t)(kMaxRegions + 1 + CSA2_MAX_TOPK + kRadixBins + kFinThreads + 8 + kTieCap) * 4;
 
 __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n, int32_t k, TopkWs ws,
                                                                        int32_t* __restrict__ idx, int dense) {
@@ -656,7 +674,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   uint32_t* prefix = reinterpret_cast<uint32_t*>(fsm + (size_t)kTieCap * 8);
   int32_t* out = reinterpret_cast<int32_t*>(prefix + kMaxRegions + 1);
   uint32_t* h = reinterpret_cast<uint32_t*>(out + CSA2_MAX_TOPK);
-  uint32_t* scratch = h + kHistBins;
+  uint32_t* scratch = h + kRadixBins;
   int32_t* tsel = reinterpret_cast<int32_t*>(scratch + kFinThreads + 8);
   __shared__ uint32_t s_nout, s_ntie, s_nsel, s_above2;
   __shared__ int s_t2;
@@ -678,7 +696,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   for (int j = j0; j < j1; ++j) local += __ldcg(rc + j);
   if (need_res && threadIdx.x < 32) {
     uint32_t above2;
-    const int t2 = warp_threshold_bin(ws.hist2 + (size_t)b * kHistBins, r, &above2);
+    const int t2 = warp_threshold_bin(ws.hist2 + (size_t)b * kHist2Bins, r, &above2);
     if (threadIdx.x == 0) {
       s_t2 = t2;
       s_above2 = above2;
@@ -704,7 +722,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   if (need_res) {
     t2 = s_t2;
     if (t2 >= 0) {
-      c_t2 = __ldcg(ws.hist2 + (size_t)b * kHistBins + t2);
+      c_t2 = __ldcg(ws.hist2 + (size_t)b * kHist2Bins + t2);
       r2 = r - s_above2;
       res_ties = r2 < c_t2;
     }
@@ -738,7 +756,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
       for (int e = 0; e < kFinPerThread; ++e) {
         if (!((valid >> e) & 1u)) continue;
         const int digit = (int)(c[e].x >> (32 - kHistBits));
-        const int d2 = (int)((c[e].x >> kHist2Shift) & (kHistBins - 1));
+        const int d2 = (int)((c[e].x >> kHist2Shift) & (kHist2Bins - 1));
         const bool at_t = need_res && digit == t;
         const bool taken = !at_t || d2 > t2 || (d2 == t2 && !res_ties);
         def |= (uint32_t)taken << e;
