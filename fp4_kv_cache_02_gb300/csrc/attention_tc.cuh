@@ -212,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mma_commit(bar);
   }
   __syncwarp();
-  bool ok = tc::mbar_wait_bounded(bar, 0, s_abort, &g_attn_error);
+  // warp-uniform outcomes: the tcgen05.ld below needs the whole warp
+  bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar, 0, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
   // ---- softmax over the chunk's rows; warp w: rows 32*(w%4).., heads 32*(w/4).. ----
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mma_commit(bar);
   }
   __syncwarp();
-  ok = ok && tc::mbar_wait_bounded(bar, 1, s_abort, &g_attn_error);
+  ok = __all_sync(0xffffffffu, ok && tc::mbar_wait_bounded(bar, 1, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
   // ---- partial O (unnormalised, fp32) and (max, sum) to the workspace ----

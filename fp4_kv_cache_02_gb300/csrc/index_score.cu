@@ -8,9 +8,9 @@
 //
 //   s[b][i] = sum_h w[b][h] * ReLU( qhat[b][h] . khat[b][p_i] )
 //
-// The decode scan (contiguous entries, or a positions list for Reindex
-// layers) runs on the tensor cores (index_score_tc.cuh); the CUDA-core
-// kernel here serves the prefill scan.
+// Both scans run on the tensor cores: the decode scan over contiguous entries
+// or a positions list of a Reindex layer (index_score_tc.cuh), and the causal
+// prefill scan of a chunk of queries (prefill_score_tc.cuh).
 #include "common.cuh"
 
 namespace csa2 {
@@ -20,78 +20,7 @@ __device__ int g_index_error = 0;
 }  // namespace csa2
 
 #include "index_score_tc.cuh"
-
-namespace csa2 {
-
-// Dequantise one query's MXFP4 q into shared memory [32][128] fp32.
-__device__ __forceinline__ void load_qhat(const uint8_t* __restrict__ q_data,
-                                          const uint8_t* __restrict__ q_e8m0, float* qs) {
-  for (int i = threadIdx.x; i < kIdxHeads * kIdxDim; i += blockDim.x) {
-    int h = i / kIdxDim, c = i % kIdxDim;
-    uint32_t byte = q_data[h * kIkBytes + c / 2];
-    uint32_t code = (c & 1) ? (byte >> 4) : (byte & 0xF);
-    qs[i] = e2m1_to_f32(code) * e8m0_to_f32(q_e8m0[h * kIkScales + c / 32]);
-  }
-}
-
-// Score of one key row against the shared qhat: per 32-channel block the key
-// values are decoded into registers and folded into 32 per-head partial dots.
-__device__ __forceinline__ float score_row(const uint8_t* __restrict__ kd,
-                                           const uint8_t* __restrict__ ksc,
-                                           const float* qs, const float* ws) {
-  float dot[kIdxHeads];
-#pragma unroll
-  for (int h = 0; h < kIdxHeads; ++h) dot[h] = 0.0f;
-  uint32_t scales = *reinterpret_cast<const uint32_t*>(ksc);
-#pragma unroll 1
-  for (int kb = 0; kb < 4; ++kb) {
-    uint4 v = *reinterpret_cast<const uint4*>(kd + kb * 16);
-    float s = e8m0_to_f32((scales >> (8 * kb)) & 0xFF);
-    uint32_t words[4] = {v.x, v.y, v.z, v.w};
-    float kv[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) kv[i] = e2m1_to_f32((words[i / 8] >> (4 * (i % 8))) & 0xF) * s;
-#pragma unroll
-    for (int h = 0; h < kIdxHeads; ++h) {
-      const float* qrow = qs + h * kIdxDim + kb * 32;
-      float acc = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc = fmaf(qrow[i], kv[i], acc);
-      dot[h] += acc;
-    }
-  }
-  float s = 0.0f;
-#pragma unroll
-  for (int h = 0; h < kIdxHeads; ++h) s = fmaf(ws[h], fmaxf(dot[h], 0.0f), s);
-  return s;
-}
-
-// Prefill: grid (ceil(n_entries / blockDim), T); query t sees 0..p0+t.
-__global__ void __launch_bounds__(128) prefill_score_simple_kernel(
-    const uint8_t* __restrict__ q_data, const uint8_t* __restrict__ q_e8m0,
-    const float* __restrict__ w, const uint8_t* __restrict__ ik_data,
-    const uint8_t* __restrict__ ik_scale, int64_t n_entries, int64_t p0,
-    float* __restrict__ scores) {
-  __shared__ float qs[kIdxHeads * kIdxDim];
-  __shared__ float ws[kIdxHeads];
-  const int t = blockIdx.y;
-  const int64_t first = (int64_t)blockIdx.x * blockDim.x;
-  const int64_t last_visible = p0 + t;
-  int64_t i = first + threadIdx.x;
-  if (first > last_visible) {  // whole block masked
-    if (i < n_entries) scores[(int64_t)t * n_entries + i] = -INFINITY;
-    return;
-  }
-  load_qhat(q_data + (int64_t)t * kIdxHeads * kIkBytes, q_e8m0 + (int64_t)t * kIdxHeads * kIkScales, qs);
-  if (threadIdx.x < kIdxHeads) ws[threadIdx.x] = w[t * kIdxHeads + threadIdx.x];
-  __syncthreads();
-  if (i >= n_entries) return;
-  float out = -INFINITY;
-  if (i <= last_visible) out = score_row(ik_data + i * kIkBytes, ik_scale + i * kIkScales, qs, ws);
-  scores[(int64_t)t * n_entries + i] = out;
-}
-
-}  // namespace csa2
+#include "prefill_score_tc.cuh"
 
 using namespace csa2;
 
@@ -178,11 +107,41 @@ extern "C" int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_
                                         int64_t n_entries, int64_t p0, float* scores, csa2_stream_t stream) {
   if (!q_data || !q_e8m0 || !w || !ik_data || !ik_scale || !scores) return CSA2_ERR_INVALID_ARG;
   if (T < 0 || n_entries < 0 || p0 < 0 || p0 + T > n_entries) return CSA2_ERR_INVALID_ARG;
-  if (!csa2_aligned(ik_data, 16) || !csa2_aligned(ik_scale, 4)) return CSA2_ERR_ALIGNMENT;
+  if (!csa2_aligned(ik_data, 16) || !csa2_aligned(ik_scale, 4) || !csa2_aligned(q_data, 16) ||
+      !csa2_aligned(q_e8m0, 4) || !csa2_aligned(w, 4))
+    return CSA2_ERR_ALIGNMENT;
+  if ((int64_t)T * kIdxHeads > 0x7FFFFFFFLL || n_entries > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
   if (T == 0 || n_entries == 0) return CSA2_OK;
-  dim3 grid((unsigned)((n_entries + 127) / 128), (unsigned)T);
-  prefill_score_simple_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(q_data, q_e8m0, w, ik_data, ik_scale,
-                                                                       n_entries, p0, scores);
+  auto encode = tensor_map_encoder();
+  if (!encode) return CSA2_ERR_CUDA;
+  using namespace prefill_tc;
+  CUtensorMap map_ik, map_q;
+  cuuint64_t kdims[2] = {(cuuint64_t)kIkBytes, (cuuint64_t)n_entries};
+  cuuint64_t kstr[1] = {(cuuint64_t)kIkBytes};
+  cuuint32_t kbox[2] = {(cuuint32_t)kIkBytes, (cuuint32_t)kTileRows};
+  cuuint64_t qdims[2] = {(cuuint64_t)kIkBytes, (cuuint64_t)T * kIdxHeads};
+  cuuint32_t qbox[2] = {(cuuint32_t)kIkBytes, 256};
+  cuuint32_t estr[2] = {1, 1};
+  if (encode(&map_ik, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)ik_data, kdims, kstr, kbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+      encode(&map_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q_data, qdims, kstr, qbox, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return CSA2_ERR_CUDA;
+  static bool attr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
+  if (!attr[dev]) {
+    if (cudaFuncSetAttribute(prefill_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+        cudaSuccess)
+      return CSA2_ERR_CUDA;
+    attr[dev] = true;
+  }
+  const int64_t tiles = (n_entries + kTileRows - 1) / kTileRows;
+  dim3 grid((unsigned)((tiles + kChunkTiles - 1) / kChunkTiles), (unsigned)((T + kQBlock - 1) / kQBlock));
+  Params prm{q_e8m0, w, ik_scale, n_entries, p0, T, scores};
+  prefill_score_tc_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(map_ik, map_q, prm);
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
 }

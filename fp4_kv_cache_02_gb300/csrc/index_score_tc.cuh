@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&acc_full[a], 1);
-      tc::mbar_init(&acc_empty[a], 128);
+      tc::mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
     }
     *s_abort = 0;
     tc::fence_mbar_init();
@@ -252,13 +252,15 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
-      if (!tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error)) break;
+      // warp-uniform outcome: tcgen05.ld below needs the whole warp
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error))) break;
       tc::tc_fence_after();
       uint32_t r[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_base + acc_col(a), r);
       tc::tmem_ld_wait();
       tc::tc_fence_before();
-      tc::mbar_arrive(&acc_empty[a]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
       float sc = 0.0f;
 #pragma unroll
       for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);

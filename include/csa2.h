@@ -253,10 +253,15 @@ int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0,
  * encoder-side prefill indexer cost in notes section 4.4 item 4).
  * T queries at positions p0 .. p0+T-1 of one sequence; query t sees entries
  * 0 .. p0+t (itself included).
- *   q_data [T][32][64], q_e8m0 [T][32][4], w [T][32]
- *   ik planes of the sequence with n_entries >= p0 + T entries
+ *   q_data [T][32][64] (16-byte aligned), q_e8m0 [T][32][4], w [T][32]
+ *   ik planes of the sequence with n_entries >= p0 + T entries (ik_data
+ *     16-byte aligned, ik_scale 4-byte aligned; no padding rows needed)
  *   scores [T][n_entries] fp32 out, -inf beyond each query's prefix.
- * Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ * Runs on the tensor cores: blocks of 32 queries against 128-entry key
+ * tiles (block-scaled MXF4 products), a fp32 ReLU-weighted epilogue.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED_SHAPE (T*32 or n_entries above
+ * 2^31-1), CUDA; a bounded device wait that runs out is reported by
+ * csa2_get_last_error as TIMEOUT.
  */
 int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
                              const float* w, int32_t T,

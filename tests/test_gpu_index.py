@@ -190,6 +190,25 @@ def test_prefill_index_score(csa2):
         assert np.all(s[t, N0 + t + 1:] == -np.inf)
 
 
+@pytest.mark.parametrize("T,N0", [(37, 9000), (64, 130), (1, 0)])
+def test_prefill_index_score_blocks_chunks_and_ragged_edges(csa2, T, N0):
+    """Query blocks of 32 with a ragged last block, key chunks of 64 tiles with
+    a ragged last tile, and the causal edge running through the tiles."""
+    from fp4_kv_cache_02_gb300.inputs import prefill_chunk
+    d = prefill_chunk(94, T, N0)
+    N = N0 + T
+    qd, qs = oracle.quant_mxfp4(d["q_idx"].reshape(-1, 128))
+    qd, qs = qd.reshape(T, 32, 64), qs.reshape(T, 32, 4)
+    ikd, iks = oracle.quant_mxfp4(d["ik"])
+    scores = torch.empty(T, N, dtype=torch.float32, device="cuda")
+    csa2.csa2_prefill_index_score(dev(qd), dev(qs), dev(d["w"]), dev(ikd), dev(iks), N0, scores)
+    s = scores.cpu().numpy()
+    for t in sorted({0, T // 2, T - 1}):
+        ref = oracle.index_score(qd[t], qs[t], d["w"][t], ikd, iks, n=N0 + t + 1)[0]
+        _scores_close(s[t, :N0 + t + 1], ref)
+        assert np.all(s[t, N0 + t + 1:] == -np.inf)
+
+
 def test_index_score_block_scales_land_on_their_own_rows_and_blocks(csa2):
     """Keys and queries whose 32-channel blocks carry very different power-of-two
     magnitudes: a scale applied to the wrong key row, head or channel block
