@@ -246,8 +246,9 @@ def run_gpu(args):
         stages.append(("reindex_topk", st_reindex))
     stages.append(("sparse_attn", st_attn))
     # our kernels per step: quant 1; fused scan + select + finalize 3; pool: block max, histogram, select,
-    # finalize, expand 5; reindex: quant, scan, histogram, select, finalize 5; attention partial + combine
-    n_launches = 1 + 3 + (5 + 5 if reindex else 0) + 2 * math.ceil(B * L / 256)
+    # finalize, expand 5; reindex: quant, scan (builds its own histogram), select, finalize 4; attention
+    # partial + combine per 256 query-layers
+    n_launches = 1 + 3 + (5 + 4 if reindex else 0) + 2 * math.ceil(B * L / 256)
 
     def step(ev=None):
         for j, (_, fn) in enumerate(stages):
@@ -341,9 +342,15 @@ def run_gpu(args):
     tp = os.path.join(ROOT, "profiles", "index_score_traffic.json")
     if os.path.exists(tp):
         try:
-            traffic = json.load(open(tp)).get("dram_bytes_per_launch")
+            rec = json.load(open(tp))
+            # the ncu figure of this workload's scan launch, when one was taken
+            if rec.get("workload") == wl.name and B == wl.B:
+                traffic = rec.get("dram_bytes_per_launch")
         except (ValueError, OSError):
             traffic = None
+    # attention: gathered latents + SWA rows + Q in + bf16 O out, per query-layer
+    attn_bytes = B * L * (K * KV_BYTES_PER_ENTRY + W * 512 + 2 * 64 * 512 * 2)
+    attn_ms = stage_ms[[nm for nm, _ in stages].index("sparse_attn")]
     qps = world * B / (ms_max * 1e-3)
     line = {
         "metric": METRIC,
@@ -370,6 +377,10 @@ def run_gpu(args):
                      "peak": hbm_peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
                      "frac": round(scan_gbs / hbm_peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": scan_bytes},
+        "kernel_rooflines": {
+            "sparse_attn": {"bound": "hbm", "achieved": round(attn_bytes / (attn_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
+                            "unit": "GB/s", "frac": round(attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                            "algorithmic_bytes_per_step": attn_bytes, "note": "partial + combine kernels"}},
         "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "gpu_launches": args.steps * n_launches,
