@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            const float* __restrict__ part_ml, int32_t n_split,
                                                            int32_t q0, uint16_t* __restrict__ out,
                                                            float* __restrict__ out_f32, float* __restrict__ lse) {
+  pdl_begin();
   constexpr int kHeadsPerCta = 8;
   __shared__ float scale_s[kHeadsPerCta][16];
   __shared__ float inv_l[kHeadsPerCta];
@@ -175,12 +176,10 @@ static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, f
   for (int32_t q0 = 0; q0 < n_q; q0 += kQueriesPerLaunch) {
     int32_t nq = n_q - q0 < kQueriesPerLaunch ? n_q - q0 : kQueriesPerLaunch;
     a.q0 = q0;
-    attn_tc::attn_partial_tc_kernel<<<dim3((unsigned)a.n_split, (unsigned)nq), attn_tc::kThreads,
-                                       attn_tc::kSmemBytes, stream>>>(qmap, a);
-    CSA2_CHECK_LAUNCH();
-    attn_combine_kernel<<<dim3((unsigned)nq, kHeads / 8), 256, 0, stream>>>(a.part_o, a.part_ml, a.n_split, q0, out,
-                                                                         out_f32, lse);
-    CSA2_CHECK_LAUNCH();
+    CSA2_LAUNCH_PDL(attn_tc::attn_partial_tc_kernel, dim3((unsigned)a.n_split, (unsigned)nq), dim3(attn_tc::kThreads),
+                    (size_t)attn_tc::kSmemBytes, stream, qmap, a);
+    CSA2_LAUNCH_PDL(attn_combine_kernel, dim3((unsigned)nq, kHeads / 8), dim3(256), 0, stream, a.part_o, a.part_ml,
+                    a.n_split, q0, out, out_f32, lse);
   }
   return CSA2_OK;
 }

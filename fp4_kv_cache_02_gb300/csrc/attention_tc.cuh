@@ -74,6 +74,7 @@ __device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32], int lan
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);

@@ -17,6 +17,7 @@ __device__ int g_codec_error = 0;
 // ---- MXFP4: one thread per 32-element block ---------------------------------
 __global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t n_blocks,
                                    uint8_t* __restrict__ data, uint8_t* __restrict__ e8m0) {
+  pdl_begin();
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= n_blocks) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
@@ -191,9 +192,8 @@ extern "C" int csa2_quant_mxfp4(const void* x_bf16, int64_t rows, int32_t cols, 
   if (!csa2_aligned(x_bf16, 16) || !csa2_aligned(data, 16)) return CSA2_ERR_ALIGNMENT;
   int64_t nb = rows * (cols / 32);
   if (nb == 0) return CSA2_OK;
-  quant_mxfp4_kernel<<<grid_for(nb, 256), 256, 0, (cudaStream_t)stream>>>(
-      (const uint16_t*)x_bf16, nb, data, e8m0);
-  CSA2_CHECK_LAUNCH();
+  CSA2_LAUNCH_PDL(quant_mxfp4_kernel, grid_for(nb, 256), dim3(256), 0, (cudaStream_t)stream,
+                  (const uint16_t*)x_bf16, nb, data, e8m0);
   return CSA2_OK;
 }
 

@@ -87,6 +87,16 @@ __device__ __forceinline__ bool score_is_candidate(float s) {
   return !(isnan(s) || s == -INFINITY);
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// The kernels of the decode chain begin here: wait until the kernel before this
+// one in the stream has completed and its writes are visible, then allow the
+// next kernel's CTAs to be scheduled (they park at their own wait). Launched
+// without the programmatic-serialization attribute, both are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
   return __uint_as_float(((uint32_t)b) << 16);
 }
@@ -97,6 +107,32 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 #define CSA2_CHECK_LAUNCH()                                 \
   do {                                                      \
     if (cudaPeekAtLastError() != cudaSuccess) {             \
+      (void)cudaGetLastError();                             \
+      return CSA2_ERR_CUDA;                                 \
+    }                                                       \
+  } while (0)
+
+// Launches a kernel that begins with pdl_begin() so that its launch overlaps the
+// tail of the previous kernel in the stream. Returns the launch status.
+template <typename... KArgs, typename... Args>
+static inline cudaError_t csa2_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                          cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+#define CSA2_LAUNCH_PDL(...)                                 \
+  do {                                                      \
+    if (csa2_launch_pdl(__VA_ARGS__) != cudaSuccess) {      \
       (void)cudaGetLastError();                             \
       return CSA2_ERR_CUDA;                                 \
     }                                                       \

@@ -96,9 +96,8 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
   }
   scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
                       hist};
-  scan_tc::index_score_tc_kernel<<<dim3((unsigned)chunks, (unsigned)B), scan_tc::kThreads, scan_tc::kSmemBytes,
-                                   stream>>>(map, prm);
-  CSA2_CHECK_LAUNCH();
+  CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)chunks, (unsigned)B), dim3(scan_tc::kThreads),
+                  (size_t)scan_tc::kSmemBytes, stream, map, prm);
   return CSA2_OK;
 }
 

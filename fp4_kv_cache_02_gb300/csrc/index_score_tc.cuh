@@ -69,6 +69,7 @@ struct Params {
 
 __global__ void __launch_bounds__(kThreads, 3)
     index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap_ik, Params p) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);

@@ -123,6 +123,7 @@ __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, u
 __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
     const int32_t* __restrict__ positions, int64_t chunk, int32_t k, TopkWs ws) {
+  pdl_begin();
   __shared__ uint32_t sh[kHistBins];
   const int b = blockIdx.y;
   for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sh[i] = 0;
@@ -442,6 +443,7 @@ template <bool kPositions>
 __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
     const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_valid,
     const int32_t* __restrict__ positions, int32_t k, TopkWs ws) {
+  pdl_begin();
   __shared__ uint32_t h2[kHist2Bins];
   __shared__ uint32_t s_wsum[kSelThreads / 32];
   __shared__ uint32_t s_wex[kSelThreads / 32];
@@ -669,6 +671,7 @@ static constexpr size_t kFinSmem =
 
 __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n, int32_t k, TopkWs ws,
                                                                        int32_t* __restrict__ idx, int dense) {
+  pdl_begin();
   extern __shared__ __align__(16) unsigned char fsm[];
   uint2* ties = reinterpret_cast<uint2*>(fsm);
   uint32_t* prefix = reinterpret_cast<uint32_t*>(fsm + (size_t)kTieCap * 8);
@@ -866,6 +869,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
 // bmax[b][j] = max of scores[b][block*j .. block*j+block) within [0, n_visible[b]).
 __global__ void block_max_kernel(const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_visible,
                                  int32_t block, int64_t nb, float* __restrict__ bmax) {
+  pdl_begin();
   const int b = blockIdx.y;
   int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= nb) return;
@@ -883,6 +887,7 @@ __global__ void block_max_kernel(const float* __restrict__ scores, int64_t n, co
 
 __global__ void pool_expand_kernel(const int32_t* __restrict__ blocks, int32_t n_blocks, int32_t block,
                                    const int32_t* __restrict__ n_visible, int64_t n, int32_t* __restrict__ pool) {
+  pdl_begin();
   const int b = blockIdx.y;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (int64_t)n_blocks * block) return;
@@ -959,13 +964,15 @@ int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t
   topk_ws_layout(B, n, k, &ws, (char*)workspace);
   dim3 grid((unsigned)ws.n_regions, (unsigned)B);
   if (positions)
-    topk_select_kernel<true><<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, k, ws);
+    CSA2_LAUNCH_PDL(topk_select_kernel<true>, grid, dim3(kSelThreads), 0, stream, scores, n, n_valid, positions, k, ws);
   else
-    topk_select_kernel<false><<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, nullptr, k, ws);
+    CSA2_LAUNCH_PDL(topk_select_kernel<false>, grid, dim3(kSelThreads), 0, stream, scores, n, n_valid,
+                    (const int32_t*)nullptr, k, ws);
   CSA2_CHECK_LAUNCH();
   int rc = topk_finalize_attr();
   if (rc) return rc;
-  topk_finalize_kernel<<<(unsigned)B, kFinThreads, kFinSmem, stream>>>(n, k, ws, idx, positions == nullptr);
+  CSA2_LAUNCH_PDL(topk_finalize_kernel, dim3((unsigned)B), dim3(kFinThreads), kFinSmem, stream, n, k, ws, idx,
+                  (int)(positions == nullptr));
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
 }
@@ -980,7 +987,7 @@ int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n
   int64_t chunk = topk_chunk(B, n);
   int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
   dim3 grid((unsigned)chunks, (unsigned)B);
-  topk_hist_kernel<<<grid, kSelThreads, 0, stream>>>(scores, n, n_valid, positions, chunk, k, ws);
+  CSA2_LAUNCH_PDL(topk_hist_kernel, grid, dim3(kSelThreads), 0, stream, scores, n, n_valid, positions, chunk, k, ws);
   CSA2_CHECK_LAUNCH();
   return csa2_topk_from_hist(scores, B, n, n_valid, positions, k, idx, workspace, stream);
 }
@@ -1018,7 +1025,7 @@ int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int3
   off += align_up((size_t)B * n_blocks * 4, 256);
   if (nb > 0) {
     dim3 g1((unsigned)((nb + 255) / 256), (unsigned)B);
-    block_max_kernel<<<g1, 256, 0, stream>>>(scores, n, n_visible, block, nb, bmax);
+    CSA2_LAUNCH_PDL(block_max_kernel, g1, dim3(256), 0, stream, scores, n, n_visible, block, nb, bmax);
     CSA2_CHECK_LAUNCH();
   }
   int rc = csa2_launch_topk(bmax, B, nb, nullptr, nullptr, n_blocks, blocks, base + off, workspace_bytes - off,
@@ -1026,7 +1033,8 @@ int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int3
   if (rc) return rc;
   int64_t total = (int64_t)n_blocks * block;
   dim3 g2((unsigned)((total + 255) / 256), (unsigned)B);
-  pool_expand_kernel<<<g2, 256, 0, stream>>>(blocks, n_blocks, block, n_visible, n, pool);
+  CSA2_LAUNCH_PDL(pool_expand_kernel, g2, dim3(256), 0, stream, (const int32_t*)blocks, n_blocks, block, n_visible, n,
+                  pool);
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
 }
