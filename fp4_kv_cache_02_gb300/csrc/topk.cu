@@ -865,6 +865,14 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   for (uint32_t i = threadIdx.x; i < (uint32_t)k; i += kFinThreads) dst[i] = i < nout ? out[i] : -1;
 }
 
+// Clears the leading `words` 16-byte words of a workspace (the histograms and
+// counters) as a kernel, so the clear joins the chain of dependent launches.
+__global__ void zero_kernel(uint4* __restrict__ p, int64_t words) {
+  pdl_begin();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // ---- block pool ---------------------------------------------------------------
 // bmax[b][j] = max of scores[b][block*j .. block*j+block) within [0, n_visible[b]).
 __global__ void block_max_kernel(const float* __restrict__ scores, int64_t n, const int32_t* __restrict__ n_visible,
@@ -943,7 +951,7 @@ extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
   return topk_ws_layout(B, n, k, nullptr, nullptr);
 }
 
-// Clears the histogram and counters of a Top-K workspace (enqueued on
+// Clears the histogram and counters of a Top-K workspace (a kernel enqueued on
 // `stream`) and returns the per-row histogram [B][kTopkHistBins] that a
 // producer of the scores may fill (the decode scan does it in its epilogue).
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
@@ -952,7 +960,10 @@ int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t w
   if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
   TopkWs ws;
   topk_ws_layout(B, n, k, &ws, (char*)workspace);
-  if (cudaMemsetAsync(workspace, 0, topk_ws_zero_bytes(B), stream) != cudaSuccess) return CSA2_ERR_CUDA;
+  const int64_t words = (int64_t)(topk_ws_zero_bytes(B) / 16);  // a multiple of 256 bytes
+  if (words > 0)
+    CSA2_LAUNCH_PDL(zero_kernel, dim3((unsigned)((words + 255) / 256 < 304 ? (words + 255) / 256 : 304)), dim3(256),
+                    0, stream, (uint4*)workspace, words);
   if (hist) *hist = ws.hist;
   return CSA2_OK;
 }
