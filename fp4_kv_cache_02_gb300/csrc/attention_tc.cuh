@@ -28,7 +28,7 @@ namespace csa2 {
 namespace attn_tc {
 
 constexpr int kRowsTc = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: 4 TMEM lane quadrants x 4
 constexpr int kOffR = 0;                                   // 8 blocks x [128 t][128 B]  = 128 KiB
 constexpr int kOffQ = kOffR + kHeadDim * kRowsTc * 2;      // 8 blocks x [64 h][128 B]   =  64 KiB
 constexpr int kOffP = kOffQ;  // P (2 parts x 2 blocks x [64 h][128 B] = 32 KiB) reuses Q once S^T is done
@@ -52,14 +52,15 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// Transpose-reduce across a warp: lane L holds v[0..31] (one value per head);
-// afterwards lane L returns the reduction over all 32 lanes of head L. Each
-// stage halves the values a lane keeps: 16 + 8 + 4 + 2 + 1 shuffles. v is
+// Transpose-reduce across a warp: lane L holds v[0..N) (one value per head,
+// N = 16 or 32); afterwards lane L returns the reduction over all 32 lanes of
+// head L mod N. Each stage halves the values a lane keeps (N/2 + ... + 1
+// shuffles); for N = 16 a last shuffle joins the two half-warps. v is
 // overwritten.
-template <bool kMax>
-__device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32], int lane) {
+template <bool kMax, int N>
+__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
 #pragma unroll
-  for (int width = 16; width >= 1; width >>= 1) {
+  for (int width = N / 2; width >= 1; width >>= 1) {
     const bool up = (lane & width) != 0;
 #pragma unroll
     for (int i = 0; i < width; ++i) {
@@ -69,7 +70,12 @@ __device__ __forceinline__ float warp_transpose_reduce32(float (&v)[32], int lan
       v[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-  return v[0];
+  float r = v[0];
+  if (N == 16) {
+    const float o = __shfl_xor_sync(0xffffffffu, r, 16);
+    r = kMax ? fmaxf(r, o) : r + o;
+  }
+  return r;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -109,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tma_load_2d(sQ + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
-  {
-    const uint32_t byte = (uint32_t)tid;  // kThreads == 256: one entry each
+  if (tid < 256) {
+    const uint32_t byte = (uint32_t)tid;
     lut_fp4x2[byte] = pack_bf16x2(e2m1_to_f32(byte & 0xF), e2m1_to_f32(byte >> 4));
     __nv_bfloat16 e = __float2bfloat16_rn(e4m3_to_f32(byte));  // exact (4 significant bits)
     lut_e4m3[byte] = *reinterpret_cast<uint16_t*>(&e);
@@ -141,18 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   // ---- gather + dequantise R: [128 t][512 c] bf16 as 8 blocks [128 t][128 B] ----
-  // warp w owns rows 16w..16w+15; pass j covers 8 rows x one 64-channel block,
-  // 4 lanes per row, each lane 16 channels (two 16-byte chunks). All 16 loads
-  // of a thread are issued before any is used.
+  // warp w owns rows 8w..8w+7; pass j covers them in 64-channel block j, 4
+  // lanes per row, each lane 16 channels (two 16-byte chunks). All loads of a
+  // thread are issued before any is used.
   {
-    constexpr int kPasses = 16;
+    constexpr int kPasses = 8;
     uint4 raw[kPasses];
     uint32_t sc[kPasses];
 #pragma unroll
     for (int jj = 0; jj < kPasses; ++jj) {
-      const int j = jj;
-      const int r = warp * 16 + (j & 1) * 8 + (lane >> 2);
-      const int blk = (j >> 1) * 4 + (lane & 3);
+      const int r = warp * 8 + (lane >> 2);
+      const int blk = jj * 4 + (lane & 3);
       const int kind = row_valid[r];
       const int64_t src = row_src[r];
       raw[jj] = make_uint4(0u, 0u, 0u, 0u);
@@ -168,9 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 #pragma unroll
     for (int jj = 0; jj < kPasses; ++jj) {
-      const int j = jj;
-      const int r = warp * 16 + (j & 1) * 8 + (lane >> 2);
-      const int blk = (j >> 1) * 4 + (lane & 3);
+      const int r = warp * 8 + (lane >> 2);
+      const int blk = jj * 4 + (lane & 3);
       const int kind = row_valid[r];
       uint32_t o[8];
       if (kind == 1) {
@@ -217,37 +221,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar, 0, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
-  // ---- softmax over the chunk's rows; warp w: rows 32*(w%4).., heads 32*(w/4).. ----
-  const int rq = warp & 3, hb = (warp >> 2) * 32;
+  // ---- softmax over the chunk's rows; warp w: rows 32*(w%4).., heads 16*(w/4).. ----
+  constexpr int kHpw = 16;  // heads per warp
+  const int rq = warp & 3, hb = (warp >> 2) * kHpw;
   const int row = rq * 32 + lane;
   const bool rv = ok && row_valid[row] != 0;
   const uint32_t s_addr = tmem + ((uint32_t)(rq * 32) << 16) + kColS + hb;
-  float p[32];
+  float p[kHpw];
   auto load_scores = [&]() {
-    uint32_t r[32];
+    uint32_t r[kHpw];
     if (ok) {
-      tc::tmem_ld_32x32b_x32(s_addr, r);
+      tc::tmem_ld_32x32b_x16(s_addr, r);
       tc::tmem_ld_wait();
     }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) p[j] = rv ? __uint_as_float(r[j]) * a.sm_scale : -INFINITY;
+    for (int j = 0; j < kHpw; ++j) p[j] = rv ? __uint_as_float(r[j]) * a.sm_scale : -INFINITY;
   };
   load_scores();
-  // per-head max over the warp's 32 rows lands in lane (head - hb)
-  red[rq][hb + lane] = warp_transpose_reduce32<true>(p, lane);
+  // per-head max over the warp's 32 rows lands in lane (head - hb) mod 16
+  {
+    const float m = warp_transpose_reduce<true, kHpw>(p, lane);
+    if (lane < kHpw) red[rq][hb + lane] = m;
+  }
   __syncthreads();
   if (tid < kHeads) m_s[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
   __syncthreads();
   // P = exp(S - m) from a second read of S; P_hi = bf16(P), P_lo = bf16(P - P_hi)
   load_scores();
 #pragma unroll
-  for (int j = 0; j < 32; ++j) p[j] = (p[j] == -INFINITY) ? 0.0f : expf(p[j] - m_s[hb + j]);
+  for (int j = 0; j < kHpw; ++j) p[j] = (p[j] == -INFINITY) ? 0.0f : expf(p[j] - m_s[hb + j]);
   // P parts, K-major for the PV MMA: [64 h][128 t] as 2 blocks of [64 h][128 B]
   {
     uint8_t* blkp = sP + (row >> 6) * (kHeads * 128);
     const uint32_t chunk = (uint32_t)(row & 63) >> 3, within = ((uint32_t)row & 7u) * 2u;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < kHpw; ++j) {
       const int h = hb + j;
       const __nv_bfloat16 hi = __float2bfloat16_rn(p[j]);
       const __nv_bfloat16 lo = __float2bfloat16_rn(p[j] - __bfloat162float(hi));
@@ -257,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncthreads();  // red[] reads for m_s are done before it is reused for the sums
-  red[rq][hb + lane] = warp_transpose_reduce32<false>(p, lane);
+  {
+    const float l = warp_transpose_reduce<false, kHpw>(p, lane);
+    if (lane < kHpw) red[rq][hb + lane] = l;
+  }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
@@ -292,9 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- partial O (unnormalised, fp32) and (max, sum) to the workspace ----
   float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
   if (ok) {
-    // warp w: channel lanes of quadrant w%4, channel blocks mb = 2*(w/4) .. +1
-    for (int mbi = 0; mbi < 2; ++mbi) {
-      const int mb = 2 * (warp >> 2) + mbi;
+    // warp w: channel lanes of quadrant w%4, channel block mb = w/4
+    for (int mbi = 0; mbi < 1; ++mbi) {
+      const int mb = warp >> 2;
       const int c = mb * 128 + rq * 32 + lane;
       for (int hh = 0; hh < kHeads; hh += 32) {
         uint32_t r[32];
