@@ -222,24 +222,24 @@ def run_gpu(args):
 
     # the step as named stages (each a sequence of public C-ABI calls)
     def st_quant():
-        csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc, stream)
+        csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc)
 
     def st_index():
         if reindex:
             csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx_full,
-                                 iws, pool_blocks=NBLK, pool=pool, stream=stream)
+                                 iws, pool_blocks=NBLK, pool=pool)
         else:
             csa2.csa2_index_topk(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
-                                 iws, stream=stream)
+                                 iws)
 
     def st_reindex():
-        csa2.csa2_quant_mxfp4(inp["q_re"], qr_data, qr_sc, stream)
+        csa2.csa2_quant_mxfp4(inp["q_re"], qr_data, qr_sc)
         csa2.csa2_index_topk(qr_data, qr_sc, inp["w_re"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx,
-                             rws, positions=pool, stream=stream)
+                             rws, positions=pool)
 
     def st_attn():
         csa2.csa2_sparse_attn_decode(inp["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], idx, inp["swa"],
-                                     out, aws, stream=stream)
+                                     out, aws)
 
     stages = [("quant_q", st_quant), ("index_topk_pool" if reindex else "index_topk", st_index)]
     if reindex:
@@ -265,7 +265,41 @@ def run_gpu(args):
     assert csa2.csa2_get_last_error() == 0
 
     nst = len(stages)
+    # (1) eager steps with an event between stages: the per-stage breakdown
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_l2()
+        step(evs[i])
+    torch.cuda.synchronize()
+    stage = [0.0] * nst
+    eager_total = 0.0
+    for e in evs:
+        for j in range(nst):
+            stage[j] += e[j].elapsed_time(e[j + 1])
+        eager_total += e[0].elapsed_time(e[nst])
+    stage_ms = [s_ / args.steps for s_ in stage]
+    eager_ms = eager_total / args.steps
+
+    # (2) the step captured once as a CUDA graph (the kernels' programmatic
+    # dependent launches become graph edges) and replayed: the timed number
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream(device)
+        side.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream(device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            flush_l2()
+            graph.replay()
+        torch.cuda.synchronize()
+        assert csa2.csa2_get_last_error() == 0
+    run_step = graph.replay if graph is not None else step
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local_rank) as clk:
         if world > 1:
             torch.distributed.barrier()
@@ -273,19 +307,14 @@ def run_gpu(args):
         torch.cuda.nvtx.range_push("timed_steps")   # lets ncu filter to the timed region
         for i in range(args.steps):
             flush_l2()                     # L2 flush between timed steps, outside the events
-            step(evs[i])
+            ev_a[i].record(stream)
+            run_step()
+            ev_b[i].record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    stage = [0.0] * nst
-    total = 0.0
-    for e in evs:
-        for j in range(nst):
-            stage[j] += e[j].elapsed_time(e[j + 1])
-        total += e[0].elapsed_time(e[nst])
-    ms = total / args.steps
-    stage_ms = [s / args.steps for s in stage]
+    ms = sum(a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)) / args.steps
     ms_max = reduce_max(ms, world, device)
 
     # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed) ----
@@ -319,12 +348,21 @@ def run_gpu(args):
     for _ in range(args.warmup):
         e2e_step()
     torch.cuda.synchronize()
+    run_e2e = e2e_step
+    if not args.no_graph:
+        e2e_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(e2e_graph):
+            e2e_step()
+        for _ in range(args.warmup):
+            e2e_graph.replay()
+        torch.cuda.synchronize()
+        run_e2e = e2e_graph.replay
     e2e_ms = 0.0
     for _ in range(args.steps):
         flush_l2()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        e2e_step()
+        run_e2e()
         b_.record(stream)
         b_.synchronize()
         e2e_ms += a.elapsed_time(b_)
@@ -369,6 +407,8 @@ def run_gpu(args):
                    "visible_entries": N, "layers_sharing_topk": L,
                    "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
                    "l2": "flushed between steps (512 MiB write + 512 MiB read)", "parallelism": f"dp{world} (sequences)"},
+        "launch": "CUDA graph of the step (programmatic dependent launches)" if graph is not None else "eager",
+        "ms_per_step_eager": round(eager_ms, 5),
         "stages_ms": dict([(nm, round(v, 5)) for (nm, _), v in zip(stages, stage_ms)] +
                           [("index_score_alone", round(scan_ms, 5))]),
         "entries_scored_per_s": round(world * B * (N + (NBLK * 8 if reindex else 0)) / (ms_max * 1e-3), 1),
@@ -493,6 +533,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph of the step")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 4],
