@@ -41,15 +41,28 @@ constexpr uint32_t kColO = 64;     // O^T: 4 blocks x 64 columns, lanes = channe
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
 // exact bf16x2 product (operands with <= 2 and <= 4 significant bits)
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Four E2M1 codes (the 16-bit x: channel i in bits 4i..4i+3) to four exact
+// bf16 values in two bf16x2 words, in registers: the magnitudes come from two
+// 8-entry byte tables (low and high byte of the bf16 of 0, 0.5, 1, 1.5, 2, 3,
+// 4, 6) picked by prmt, the signs from a sign-replicating prmt.
+__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t x, uint32_t& v01, uint32_t& v23) {
+  constexpr uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;  // low bytes, magnitudes 0..3 and 4..7
+  constexpr uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;  // high bytes
+  const uint32_t sel = x & 0x7777u;
+  const uint32_t lo4 = __byte_perm(kLoA, kLoB, sel);
+  uint32_t hi4 = __byte_perm(kHiA, kHiB, sel);
+  // msb of bytes: x << 4 holds the signs of channels 0 and 2, x those of 1 and 3
+  uint32_t smask;
+  asm("prmt.b32 %0, %1, %2, 0x9D8C;" : "=r"(smask) : "r"(x), "r"(x << 4));
+  hi4 |= smask & 0x80808080u;
+  v01 = __byte_perm(lo4, hi4, 0x5140);
+  v23 = __byte_perm(lo4, hi4, 0x7362);
 }
 
 // Transpose-reduce across a warp: lane L holds v[0..N) (one value per head,
@@ -93,7 +106,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 20);
   __shared__ float red[4][kHeads];
   __shared__ float m_s[kHeads], l_s[kHeads];
-  __shared__ uint32_t lut_fp4x2[256];  // byte of two E2M1 codes -> two bf16 values
   __shared__ uint16_t lut_e4m3[256];   // E4M3 byte -> bf16 value
   __shared__ int row_valid[kRowsTc];  // 0 none, 1 selected latent, 2 SWA row
   __shared__ int64_t row_src[kRowsTc];  // entry index in the plane, or SWA byte offset
@@ -117,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   if (tid < 256) {
     const uint32_t byte = (uint32_t)tid;
-    lut_fp4x2[byte] = pack_bf16x2(e2m1_to_f32(byte & 0xF), e2m1_to_f32(byte >> 4));
     __nv_bfloat16 e = __float2bfloat16_rn(e4m3_to_f32(byte));  // exact (4 significant bits)
     lut_e4m3[byte] = *reinterpret_cast<uint16_t*>(&e);
   }
@@ -182,7 +193,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s2 = s1 | (s1 << 16);
         const uint32_t w[2] = {raw[jj].x, raw[jj].y};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = mul_bf16x2(lut_fp4x2[(w[e >> 2] >> (8 * (e & 3))) & 0xFFu], s2);
+        for (int e = 0; e < 8; e += 2) {
+          uint32_t v01, v23;
+          e2m1x4_to_bf16((w[e >> 2] >> (8 * (e & 3))) & 0xFFFFu, v01, v23);
+          o[e] = mul_bf16x2(v01, s2);
+          o[e + 1] = mul_bf16x2(v23, s2);
+        }
       } else {
         const uint32_t w[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};  // zero for invalid rows
 #pragma unroll
