@@ -73,17 +73,29 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
     if (lse) lse[(int64_t)qi * kHeads + h] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
   }
   __syncthreads();
+  // each float4 of the output: the loads of all splits go out together (up to
+  // 8 at a time), so a thread waits on L2 once per output, not once per split
+  constexpr int kBatch = 8;
   for (int i = tid; i < kHeadsPerCta * kHeadDim / 4; i += blockDim.x) {
     const int hl = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
     const int h = h0 + hl;
+    const float* base = part_o + ((int64_t)lq * n_split * kHeads + h) * kHeadDim + c4 * 4;
+    const int64_t split_stride = (int64_t)kHeads * kHeadDim;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < n_split; ++s) {
-      const float f = scale_s[hl][s];
-      if (f == 0.0f) continue;
-      const float4 v =
-          *reinterpret_cast<const float4*>(part_o + (((int64_t)lq * n_split + s) * kHeads + h) * kHeadDim + c4 * 4);
-      acc.x = fmaf(v.x, f, acc.x); acc.y = fmaf(v.y, f, acc.y);
-      acc.z = fmaf(v.z, f, acc.z); acc.w = fmaf(v.w, f, acc.w);
+    for (int s0 = 0; s0 < n_split; s0 += kBatch) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        v[j] = s0 + j < n_split ? *reinterpret_cast<const float4*>(base + (s0 + j) * split_stride)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (s0 + j >= n_split) break;
+        const float f = scale_s[hl][s0 + j];  // fixed split order
+        if (f == 0.0f) continue;
+        acc.x = fmaf(v[j].x, f, acc.x); acc.y = fmaf(v[j].y, f, acc.y);
+        acc.z = fmaf(v[j].z, f, acc.z); acc.w = fmaf(v[j].w, f, acc.w);
+      }
     }
     const float il = inv_l[hl];
     acc.x *= il; acc.y *= il; acc.z *= il; acc.w *= il;
