@@ -245,10 +245,10 @@ def run_gpu(args):
     if reindex:
         stages.append(("reindex_topk", st_reindex))
     stages.append(("sparse_attn", st_attn))
-    # our kernels per step: quant 1; workspace clear + scan (fused histogram) + select + finalize 4; pool:
-    # block max, clear, histogram, select, finalize, expand 6; reindex: quant, clear, scan, select,
-    # finalize 5; attention partial + combine per 256 query-layers
-    n_launches = 1 + 4 + (6 + 5 if reindex else 0) + 2 * math.ceil(B * L / 256)
+    # our kernels per step: quant 1; workspace clear + scan (fused histogram and, with the pool, block
+    # maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex: quant,
+    # clear, scan, select, finalize 5; attention partial + combine per 256 query-layers
+    n_launches = 1 + 4 + (5 + 5 if reindex else 0) + 2 * math.ceil(B * L / 256)
 
     def step(ev=None):
         for j, (_, fn) in enumerate(stages):

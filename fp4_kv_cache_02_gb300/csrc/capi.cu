@@ -6,7 +6,7 @@
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
-                               uint32_t* hist, cudaStream_t stream);
+                               uint32_t* hist, float* bmax, cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -16,6 +16,9 @@ int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n
 int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
                            int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+int csa2_launch_pool_from_bmax(const float* bmax, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
+                               int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
 extern "C" int csa2_version(void) { return 100; }
 
@@ -71,7 +74,7 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                    nullptr, (cudaStream_t)stream);
+                                    nullptr, nullptr, (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -81,6 +84,9 @@ extern "C" size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_pos, int32
   size_t scores = al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
   size_t t = csa2_topk_workspace_size(B, n_pos, k);
   if (pool_blocks > 0) {
+    // block maxima (written by the scan) get their own slice; the pool's
+    // Top-K reuses the Full Top-K's scratch after it
+    scores += al256((size_t)B * (size_t)((n_pos + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK + 1) * 4);
     size_t p = csa2_block_pool_workspace_size(B, n_pos, CSA2_POOL_BLOCK, pool_blocks);
     if (p > t) t = p;
   }
@@ -106,18 +112,23 @@ extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, con
   cudaStream_t s = (cudaStream_t)stream;
   float* scores = (float*)workspace;
   size_t off = al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
+  float* bmax = nullptr;
+  if (pool_blocks > 0) {
+    bmax = (float*)((char*)workspace + off);
+    off += al256((size_t)B * (size_t)((n_pos + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK + 1) * 4);
+  }
   char* rest = (char*)workspace + off;
   size_t rest_bytes = workspace_bytes - off;
-  // the scan's epilogue builds the Top-K histogram
+  // the scan's epilogue builds the Top-K histogram (and the pool's block maxima)
   uint32_t* hist = nullptr;
   rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist);
   if (rc) return rc;
   rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                  hist, s);
+                                  hist, bmax, s);
   if (rc) return rc;
   rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);
   if (rc) return rc;
   if (pool_blocks > 0)
-    rc = csa2_launch_block_pool(scores, B, n_pos, n_visible, CSA2_POOL_BLOCK, pool_blocks, pool, rest, rest_bytes, s);
+    rc = csa2_launch_pool_from_bmax(bmax, B, n_pos, n_visible, CSA2_POOL_BLOCK, pool_blocks, pool, rest, rest_bytes, s);
   return rc;
 }

@@ -65,6 +65,7 @@ struct Params {
   float* scores;
   int32_t tiles_per_cta;
   uint32_t* hist;  // optional [B][kTopkHistBins] Top-K histogram (zeroed by the caller)
+  float* bmax;     // optional [B][ceil(n_pos / 8)] block maxima for the candidate pool (dense mode)
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -272,6 +273,15 @@ __global__ void __launch_bounds__(kThreads, 3)
         valid = pp >= 0 && pp < nv_pos;
       }
       if (li < p.n_pos) out[li] = valid ? sc : -INFINITY;
+      if (p.bmax) {
+        // maximum over the block of 8 consecutive entries (8 consecutive lanes);
+        // entries past n_visible and NaN scores take no part
+        float v = valid && !isnan(sc) ? sc : -INFINITY;
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        if ((lane & 7) == 0 && li < p.n_pos) p.bmax[(int64_t)b * ((p.n_pos + 7) / 8) + li / 8] = v;
+      }
       if (with_hist && valid && score_is_candidate(sc))
         atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
     }
@@ -280,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 3)
     int64_t hi = t_end_all * kTileRows;
     if (hi > p.n_pos) hi = p.n_pos;
     for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
+    if (p.bmax && hi > lo) {
+      float* bm = p.bmax + (int64_t)b * ((p.n_pos + 7) / 8);
+      for (int64_t j = lo / 8 + threadIdx.x; j < (hi + 7) / 8; j += 128) bm[j] = -INFINITY;
+    }
   }
   tc::tc_fence_before();
   __syncthreads();

@@ -1022,6 +1022,28 @@ extern "C" size_t csa2_block_pool_workspace_size(int32_t B, int64_t n, int32_t b
   return off;
 }
 
+// Pool from block maxima already in place: Top-n_blocks of the maxima, then the
+// positions of the chosen blocks. `workspace` holds the chosen blocks and the
+// Top-K scratch.
+int csa2_launch_pool_from_bmax(const float* bmax, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
+                               int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  if (B == 0) return CSA2_OK;
+  const int64_t nb = (n + block - 1) / block;
+  char* base = (char*)workspace;
+  int32_t* blocks = (int32_t*)base;
+  const size_t off = align_up((size_t)B * n_blocks * 4, 256);
+  if (workspace_bytes < off) return CSA2_ERR_WORKSPACE;
+  int rc = csa2_launch_topk(bmax, B, nb, nullptr, nullptr, n_blocks, blocks, base + off, workspace_bytes - off,
+                            stream);
+  if (rc) return rc;
+  const int64_t total = (int64_t)n_blocks * block;
+  dim3 g2((unsigned)((total + 255) / 256), (unsigned)B);
+  CSA2_LAUNCH_PDL(pool_expand_kernel, g2, dim3(256), 0, stream, (const int32_t*)blocks, n_blocks, block, n_visible, n,
+                  pool);
+  return CSA2_OK;
+}
+
 int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
                            int32_t n_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
@@ -1032,22 +1054,12 @@ int csa2_launch_block_pool(const float* scores, int32_t B, int64_t n, const int3
   char* base = (char*)workspace;
   float* bmax = (float*)base;
   size_t off = align_up((size_t)B * (size_t)(nb > 0 ? nb : 1) * 4, 256);
-  int32_t* blocks = (int32_t*)(base + off);
-  off += align_up((size_t)B * n_blocks * 4, 256);
   if (nb > 0) {
     dim3 g1((unsigned)((nb + 255) / 256), (unsigned)B);
     CSA2_LAUNCH_PDL(block_max_kernel, g1, dim3(256), 0, stream, scores, n, n_visible, block, nb, bmax);
-    CSA2_CHECK_LAUNCH();
   }
-  int rc = csa2_launch_topk(bmax, B, nb, nullptr, nullptr, n_blocks, blocks, base + off, workspace_bytes - off,
-                            stream);
-  if (rc) return rc;
-  int64_t total = (int64_t)n_blocks * block;
-  dim3 g2((unsigned)((total + 255) / 256), (unsigned)B);
-  CSA2_LAUNCH_PDL(pool_expand_kernel, g2, dim3(256), 0, stream, (const int32_t*)blocks, n_blocks, block, n_visible, n,
-                  pool);
-  CSA2_CHECK_LAUNCH();
-  return CSA2_OK;
+  return csa2_launch_pool_from_bmax(bmax, B, n, n_visible, block, n_blocks, pool, base + off, workspace_bytes - off,
+                                    stream);
 }
 
 extern "C" int csa2_block_pool(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
