@@ -66,6 +66,13 @@ def _load():
         "csa2_topk_static": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp]),
         "csa2_block_pool_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_block_pool": (ctypes.c_int, [vp, i32, i64, vp, i32, i32, vp, vp, sz, vp]),
+        "csa2_block_max": (ctypes.c_int, [vp, i32, i64, vp, i32, vp, vp]),
+        "csa2_topk_candidates": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, i64, vp, vp]),
+        "csa2_topk_merge_workspace_size": (sz, [i32, i32, i32, i32]),
+        "csa2_topk_merge": (ctypes.c_int, [vp, i32, i32, i32, i32, vp, vp, sz, vp]),
+        "csa2_shard_positions": (ctypes.c_int, [vp, i32, i32, i64, i64, vp, vp]),
+        "csa2_shard_pool": (ctypes.c_int, [vp, i32, i32, i32, i64, i64, vp, vp, vp]),
+        "csa2_attn_merge": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp, vp]),
         "csa2_index_topk_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_index_topk": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp,
                                            vp, sz, vp]),
@@ -239,6 +246,55 @@ def csa2_prefill_index_score(q_data, q_e8m0, w, ik_data, ik_scale, p0, scores, s
           p0, _p(scores), _s(stream))
 
 
+def csa2_block_max(scores, bmax, n_visible=None, block=POOL_BLOCK, stream=None):
+    """scores [B,n] fp32 -> bmax [B,ceil(n/block)] fp32."""
+    _req(scores, torch.float32, "scores"); _req(bmax, torch.float32, "bmax")
+    _req(n_visible, torch.int32, "n_visible", allow_none=True)
+    B, n = scores.shape
+    _call("csa2_block_max", _p(scores), B, n, _p(n_visible), block, _p(bmax), _s(stream))
+
+
+# ---- context sharding: exchange steps -------------------------------------------
+
+def csa2_topk_candidates(scores, idx, offset, cand, positions=None, stream=None):
+    """scores [B,n] fp32, idx [B,k] int32 columns -> cand [B,k,2] int32 pairs
+    (fp32 score bits, global position)."""
+    _req(scores, torch.float32, "scores"); _req(idx, torch.int32, "idx"); _req(cand, torch.int32, "cand")
+    _req(positions, torch.int32, "positions", allow_none=True)
+    B, n = scores.shape
+    _call("csa2_topk_candidates", _p(scores), B, n, _p(positions), _p(idx), idx.shape[1], int(offset), _p(cand),
+          _s(stream))
+
+
+def csa2_topk_merge(cand, k_out, idx, workspace, stream=None):
+    """cand [R,B,k,2] int32 pairs gathered in rank order -> idx [B,k_out] global positions."""
+    _req(cand, torch.int32, "cand"); _req(idx, torch.int32, "idx"); _req(workspace, torch.uint8, "workspace")
+    R, B, k = cand.shape[0], cand.shape[1], cand.shape[2]
+    _call("csa2_topk_merge", _p(cand), R, B, k, k_out, _p(idx), _p(workspace), workspace.numel(), _s(stream))
+
+
+def csa2_shard_positions(idx, lo, hi, local_idx, stream=None):
+    _req(idx, torch.int32, "idx"); _req(local_idx, torch.int32, "local_idx")
+    B, k = idx.shape
+    _call("csa2_shard_positions", _p(idx), B, k, int(lo), int(hi), _p(local_idx), _s(stream))
+
+
+def csa2_shard_pool(blocks, lo, hi, pool, n_visible=None, block=POOL_BLOCK, stream=None):
+    _req(blocks, torch.int32, "blocks"); _req(pool, torch.int32, "pool")
+    _req(n_visible, torch.int32, "n_visible", allow_none=True)
+    B, nb = blocks.shape
+    _call("csa2_shard_pool", _p(blocks), B, nb, block, int(lo), int(hi), _p(n_visible), _p(pool), _s(stream))
+
+
+def csa2_attn_merge(parts, lses, out, out_f32=None, lse_out=None, stream=None):
+    """parts [R,...,64,512] fp32, lses [R,...,64] fp32 -> out [...,64,512] bf16."""
+    _req(parts, torch.float32, "parts"); _req(lses, torch.float32, "lses"); _req(out, torch.bfloat16, "out")
+    _req(out_f32, torch.float32, "out_f32", allow_none=True); _req(lse_out, torch.float32, "lse_out", allow_none=True)
+    R = parts.shape[0]
+    n_q = parts[0].numel() // (HEADS * HEAD_DIM)
+    _call("csa2_attn_merge", _p(parts), _p(lses), R, n_q, _p(out), _p(out_f32), _p(lse_out), _s(stream))
+
+
 # ---- attention ------------------------------------------------------------------
 
 def csa2_sparse_attn_decode(q, kv_data, kv_scale, n_visible, idx, swa, out, workspace, out_f32=None, lse=None,
@@ -309,6 +365,10 @@ def pool_workspace(B, n, block=POOL_BLOCK, n_blocks=POOL_BLOCKS, device="cuda"):
 
 def index_topk_workspace(B, n_pos, k, pool_blocks=0, device="cuda"):
     return _ws(_lib.csa2_index_topk_workspace_size(B, n_pos, k, pool_blocks), device)
+
+
+def merge_workspace(R, B, k, k_out, device="cuda"):
+    return _ws(_lib.csa2_topk_merge_workspace_size(R, B, k, k_out), device)
 
 
 def attn_workspace(n_queries, k, n_swa, device="cuda"):

@@ -1013,6 +1013,16 @@ extern "C" int csa2_topk(const float* scores, int32_t B, int64_t n, const int32_
                           (cudaStream_t)stream);
 }
 
+extern "C" int csa2_block_max(const float* scores, int32_t B, int64_t n, const int32_t* n_visible, int32_t block,
+                              float* bmax, csa2_stream_t stream) {
+  if (!scores || !bmax || B < 0 || n < 0 || block <= 0) return CSA2_ERR_INVALID_ARG;
+  const int64_t nb = (n + block - 1) / block;
+  if (B == 0 || nb == 0) return CSA2_OK;
+  CSA2_LAUNCH_PDL(block_max_kernel, dim3((unsigned)((nb + 255) / 256), (unsigned)B), dim3(256), 0,
+                  (cudaStream_t)stream, scores, n, n_visible, block, nb, bmax);
+  return CSA2_OK;
+}
+
 extern "C" size_t csa2_block_pool_workspace_size(int32_t B, int64_t n, int32_t block, int32_t n_blocks) {
   if (B <= 0 || n < 0 || block <= 0 || n_blocks <= 0) return 0;
   int64_t nb = (n + block - 1) / block;

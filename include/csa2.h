@@ -228,6 +228,95 @@ int csa2_block_pool(const float* scores, int32_t B, int64_t n,
                     int32_t* pool, void* workspace, size_t workspace_bytes,
                     csa2_stream_t stream);
 
+/**
+ * Block maxima (report section 2.3.2: a block's score is the maximum index
+ * score among its positions).
+ *   bmax[b][j] = max of the non-NaN scores[b][block*j .. block*j+block) within
+ *   [0, n_visible[b]) (n_visible may be NULL: all n), -inf for none.
+ *   bmax [B][ceil(n / block)] fp32 out. Errors: INVALID_ARG, CUDA.
+ */
+int csa2_block_max(const float* scores, int32_t B, int64_t n,
+                   const int32_t* n_visible, int32_t block, float* bmax,
+                   csa2_stream_t stream);
+
+/* ======================================================================== */
+/* Context sharding: the exchange steps of a step split across ranks          */
+/* ======================================================================== */
+/* A rank owns the contiguous entries [lo, hi) of every sequence (its planes
+ * hold them at local positions 0 .. hi-lo-1). Exact because a global Top-K
+ * winner is in its own range's local Top-K (report section 2.3: Top-K over
+ * all entries; section 2.3.2: the best blocks likewise), and attention over
+ * disjoint row sets merges by log-sum-exp (section 2.3: one softmax over the
+ * selected and SWA rows). A candidate is an 8-byte pair {fp32 score, int32
+ * global position}; -1 marks an empty slot (its score is -inf). */
+
+/**
+ * Candidates of a local Top-K: cand[b][j] = {scores[b][c], pos(c) + offset}
+ * for c = idx[b][j], pos(c) = positions[b][c] (positions non-NULL) or c;
+ * {-inf, -1} where c < 0, c >= n or pos(c) < 0.
+ *   scores [B][n] fp32, positions [B][n] int32 or NULL, idx [B][k] int32
+ *   columns (from csa2_topk without positions), cand [B][k] pairs out
+ *   (8-byte aligned). Errors: INVALID_ARG, UNSUPPORTED_SHAPE (a position
+ *   above 2^31-1), ALIGNMENT, CUDA.
+ */
+int csa2_topk_candidates(const float* scores, int32_t B, int64_t n,
+                         const int32_t* positions, const int32_t* idx,
+                         int32_t k, int64_t offset, void* cand,
+                         csa2_stream_t stream);
+
+/** Bytes of workspace csa2_topk_merge needs. */
+size_t csa2_topk_merge_workspace_size(int32_t R, int32_t B, int32_t k,
+                                      int32_t k_out);
+
+/**
+ * Merge of R ranks' candidates: idx[b] = the global positions of the k_out
+ * best candidates of row b over all ranks, as csa2_topk orders and pads them
+ * (ascending position, -1 at the end).
+ *   cand [R][B][k] pairs (each rank's csa2_topk_candidates, gathered in rank
+ *   order), idx [B][k_out] int32 out, 1 <= k_out <= CSA2_MAX_TOPK.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, WORKSPACE, CUDA.
+ */
+int csa2_topk_merge(const void* cand, int32_t R, int32_t B, int32_t k,
+                    int32_t k_out, int32_t* idx, void* workspace,
+                    size_t workspace_bytes, csa2_stream_t stream);
+
+/**
+ * local_idx[b][j] = idx[b][j] - lo when lo <= idx[b][j] < hi, else -1: the
+ * merged global positions that fall into this rank's range, as local ones
+ * (the attention's idx).
+ *   idx, local_idx [B][k] int32. Errors: INVALID_ARG, CUDA.
+ */
+int csa2_shard_positions(const int32_t* idx, int32_t B, int32_t k,
+                         int64_t lo, int64_t hi, int32_t* local_idx,
+                         csa2_stream_t stream);
+
+/**
+ * The merged pool restricted to this rank: for the global block ids
+ * blocks[b][j] (-1 = unused), pool[b][j*block + r] = p - lo for the position
+ * p = blocks[b][j]*block + r when lo <= p < hi and p - lo < n_visible[b]
+ * (n_visible local, may be NULL), else -1.
+ *   blocks [B][n_blocks] int32, pool [B][n_blocks*block] int32 out.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, CUDA.
+ */
+int csa2_shard_pool(const int32_t* blocks, int32_t B, int32_t n_blocks,
+                    int32_t block, int64_t lo, int64_t hi,
+                    const int32_t* n_visible, int32_t* pool,
+                    csa2_stream_t stream);
+
+/**
+ * Merges R partial attention outputs of disjoint row sets in rank order
+ * 0..R-1: out = sum_r exp(lse_r - L) / S * o_r with L = max_r lse_r,
+ * S = sum_r exp(lse_r - L); lse_out = L + log S. A set with lse = -inf (no
+ * rows) contributes nothing; a query-head with no rows at all gets 0, -inf.
+ *   parts [R][n_q][64][512] fp32 (each rank's out_f32, 16-byte aligned),
+ *   lses [R][n_q][64] fp32 (each rank's lse), out_bf16 [n_q][64][512] out
+ *   (8-byte aligned), out_f32 (nullable, 16-byte aligned) and lse_out
+ *   [n_q][64] (nullable). Errors: INVALID_ARG, ALIGNMENT, CUDA.
+ */
+int csa2_attn_merge(const float* parts, const float* lses, int32_t R,
+                    int32_t n_q, void* out_bf16, float* out_f32,
+                    float* lse_out, csa2_stream_t stream);
+
 /** Bytes of workspace csa2_index_topk needs (pool_blocks 0 = no pool). */
 size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_pos, int32_t k,
                                       int32_t pool_blocks);

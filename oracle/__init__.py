@@ -84,6 +84,8 @@ def lib():
             L.orc_topk.argtypes = [f32p, i32p, i64, i32, i32p]
             L.orc_block_pool.restype = i32
             L.orc_block_pool.argtypes = [f32p, i64, i32, i32, i32p]
+            L.orc_block_max.argtypes = [f32p, i64, i32, f32p]
+            L.orc_attn_merge.argtypes = [f64p, f64p, i32, i32, i32, f64p, f64p]
             L.orc_sparse_attn.argtypes = [f32p, i32, i32, u8p, u8p, i32p, i32, u8p, i32, d, f64p, f64p]
             L.orc_decode_batch.restype = ctypes.c_uint64
             L.orc_decode_batch.argtypes = [i32, i64, i32p, u8p, u8p, f32p, u8p, u8p, u8p, u8p,
@@ -225,6 +227,27 @@ def block_pool(scores, block=8, n_blocks=2048):
     pool = np.zeros(block * n_blocks, np.int32)
     kept = lib().orc_block_pool(_p(scores), scores.size, block, n_blocks, _p(pool))
     return pool, int(kept)
+
+
+def block_max(scores, block=8):
+    """Block maxima of one row: [ceil(n / block)] fp32."""
+    scores = _c(scores, np.float32)
+    nb = (scores.size + block - 1) // block
+    bmax = np.zeros(nb, np.float32)
+    lib().orc_block_max(_p(scores), scores.size, block, _p(bmax))
+    return bmax
+
+
+def attn_merge(outs, lses):
+    """outs [R, H, D], lses [R, H] (float64): the attention over the union of
+    the R disjoint row sets. Returns (out [H, D], lse [H]) float64."""
+    outs = _c(outs, np.float64)
+    lses = _c(lses, np.float64)
+    R, H, D = outs.shape
+    out = np.zeros((H, D), np.float64)
+    lse = np.zeros(H, np.float64)
+    lib().orc_attn_merge(_p(outs), _p(lses), R, H, D, _p(out), _p(lse))
+    return out, lse
 
 
 def sparse_attn(q, kv_data, kv_scale, idx, swa, sm_scale=1.0):

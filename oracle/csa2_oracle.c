@@ -326,19 +326,24 @@ static int by_int_asc(const void* a, const void* b) {
   return (x > y) - (x < y);
 }
 
+void orc_block_max(const float* scores, int64_t n, int block, float* bmax) {
+  int64_t nb = (n + block - 1) / block, b, p;
+  for (b = 0; b < nb; ++b) {
+    float m = -INFINITY;
+    for (p = b * block; p < (b + 1) * block && p < n; ++p)
+      if (scores[p] > m) m = scores[p];
+    bmax[b] = m;
+  }
+}
+
 int orc_block_pool(const float* scores, int64_t n, int block, int n_blocks,
                    int32_t* pool) {
   int64_t nb = (n + block - 1) / block, b;
   float* bmax = (float*)malloc(sizeof(float) * (size_t)(nb > 0 ? nb : 1));
   int32_t* kept = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_blocks > 0 ? n_blocks : 1));
   int j, r, n_kept;
-  for (b = 0; b < nb; ++b) {
-    int64_t p;
-    float m = -INFINITY;
-    for (p = b * block; p < (b + 1) * block && p < n; ++p)
-      if (scores[p] > m) m = scores[p];
-    bmax[b] = m;
-  }
+  (void)b;
+  orc_block_max(scores, n, block, bmax);
   /* the best blocks by (max desc, block asc) are a Top-K over block maxima */
   n_kept = orc_topk(bmax, NULL, nb, n_blocks, kept);
   qsort(kept, (size_t)n_kept, sizeof(int32_t), by_int_asc);
@@ -445,6 +450,34 @@ uint64_t orc_decode_batch(int B, int64_t cap, const int32_t* n_visible,
   }
   (void)n_threads;
   return macs;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Attention over a union of disjoint row sets ([R] 2.3: one softmax over     */
+/* all rows a query attends to, split here by where the rows live)           */
+/* ------------------------------------------------------------------------ */
+
+void orc_attn_merge(const double* outs, const double* lses, int R, int H,
+                    int D, double* out, double* lse) {
+  int r, h, c;
+  for (h = 0; h < H; ++h) {
+    double m = -INFINITY, l = 0.0;
+    for (r = 0; r < R; ++r)
+      if (lses[(int64_t)r * H + h] > m) m = lses[(int64_t)r * H + h];
+    for (c = 0; c < D; ++c) out[(int64_t)h * D + c] = 0.0;
+    if (m == -INFINITY) {
+      lse[h] = -INFINITY;
+      continue;
+    }
+    for (r = 0; r < R; ++r) l += exp(lses[(int64_t)r * H + h] - m);
+    lse[h] = m + log(l);
+    for (r = 0; r < R; ++r) {
+      double wgt = exp(lses[(int64_t)r * H + h] - lse[h]);
+      if (lses[(int64_t)r * H + h] == -INFINITY) continue;
+      for (c = 0; c < D; ++c)
+        out[(int64_t)h * D + c] += wgt * outs[((int64_t)r * H + h) * D + c];
+    }
+  }
 }
 
 int orc_max_threads(void) {

@@ -79,6 +79,10 @@ int orc_topk(const float* scores, const int32_t* positions, int64_t n, int k,
 int orc_block_pool(const float* scores, int64_t n, int block, int n_blocks,
                    int32_t* pool);
 
+/* Block maxima alone: bmax[b] = max of scores over block b within [0, n)
+ * (NaN skipped), -inf for a block with no score.                           */
+void orc_block_max(const float* scores, int64_t n, int block, float* bmax);
+
 /* ---- sparse attention -----------------------------------------------------
  * One query: q [H][D] (values already bf16-exact), rows = dequantised main KV
  * of idx[0..k) (negative entries skipped) followed by the n_swa SWA rows.
@@ -88,6 +92,15 @@ void orc_sparse_attn(const float* q, int H, int D, const uint8_t* kv_data,
                      const uint8_t* kv_scale, const int32_t* idx, int k,
                      const uint8_t* swa, int n_swa, double sm_scale,
                      double* out, double* lse);
+
+/* ---- merge of attention over disjoint row sets ------------------------------
+ * R partial results (out_r [H][D], lse_r [H]) of one query, each the softmax
+ * attention over its own rows, merged into the attention over the union of
+ * the rows: since softmax weights over the union are exp(s - LSE) with
+ * LSE = log sum_r exp(lse_r), out = sum_r exp(lse_r - LSE) * out_r.
+ * A set with lse = -inf has no rows; all -inf gives out 0, lse -inf.        */
+void orc_attn_merge(const double* outs, const double* lses, int R, int H,
+                    int D, double* out, double* lse);
 
 /* ---- whole decode step for a batch (the timed CPU baseline) --------------
  * For each of the B sequences (OpenMP over sequences): score all n_visible[b]
