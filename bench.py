@@ -335,6 +335,9 @@ def run_gpu(args):
         scan_ms += a.elapsed_time(b_)
     scan_ms /= args.steps
 
+    # ---- the fused KV append, for its roofline and its decode latency ----
+    app = measure_append(csa2, torch, B, device, args.steps, flush_l2, stream)
+
     # ---- end to end: per-step inputs from pinned host memory, outputs back ----
     # Each step copies its inputs host -> device and its outputs (attention
     # output, Top-K indices) device -> host. The copies run on their own streams
@@ -459,7 +462,13 @@ def run_gpu(args):
         "kernel_rooflines": {
             "sparse_attn": {"bound": "hbm", "achieved": round(attn_bytes / (attn_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
                             "unit": "GB/s", "frac": round(attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                            "algorithmic_bytes_per_step": attn_bytes, "note": "partial + combine kernels"}},
+                            "algorithmic_bytes_per_step": attn_bytes, "note": "partial + combine kernels"},
+            "kv_append": {"bound": "hbm", "achieved": round(app["bulk_bytes"] / (app["bulk_ms"] * 1e-3) / 1e9, 1),
+                          "peak": hbm_peak, "unit": "GB/s",
+                          "frac": round(app["bulk_bytes"] / (app["bulk_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
+                          "algorithmic_bytes_per_launch": app["bulk_bytes"], "entries_per_launch": app["entries"],
+                          "decode_append_us": round(app["decode_us"], 2),
+                          "note": "timed alone, outside the step: bf16 latent + key in, 356 B entry out"}},
         "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "note": "copies on their own streams overlap neighbouring steps (two buffer sets); inputs exceed L2"},
@@ -471,6 +480,46 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return line
+
+
+APPEND_ENTRIES = 131072            # bulk append: entries per launch, over the batch
+APPEND_BYTES_PER_ENTRY = 512 * 2 + 128 * 2 + KV_BYTES_PER_ENTRY + IK_BYTES_PER_ENTRY   # bf16 in, packed out
+
+
+def measure_append(csa2, torch, B, device, steps, flush_l2, stream):
+    """csa2_kv_append timed alone: (1) a bulk append of APPEND_ENTRIES new
+    entries spread over the B sequences into empty planes (inputs larger than
+    L2, flushed between launches), against the HBM roofline; (2) the decode
+    case, one entry per sequence, as a latency."""
+    from fp4_kv_cache_02_gb300.inputs import device_normal
+    T = APPEND_ENTRIES // B
+    kv = device_normal((B, T, 512), 91, device)
+    ik = device_normal((B, T, 128), 92, device)
+    planes = [torch.empty(B, T, w, dtype=torch.uint8, device=device) for w in (256, 32, 64, 4)]
+    nv0 = torch.zeros(B, dtype=torch.int32, device=device)
+    nv1 = torch.empty_like(nv0)
+
+    def timed(kv_, ik_, n):
+        tot = 0.0
+        for _ in range(n):
+            flush_l2()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            csa2.csa2_kv_append(kv_, ik_, *planes, nv0, n_visible_out=nv1, stream=stream)
+            b_.record(stream)
+            b_.synchronize()
+            tot += a.elapsed_time(b_)
+        return tot / n
+
+    timed(kv, ik, 3)
+    bulk_ms = timed(kv, ik, steps)
+    one_kv, one_ik = kv[:, :1].contiguous(), ik[:, :1].contiguous()
+    timed(one_kv, one_ik, 3)
+    decode_ms = timed(one_kv, one_ik, steps)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    nbytes = B * T * APPEND_BYTES_PER_ENTRY
+    return {"bulk_ms": bulk_ms, "bulk_bytes": nbytes, "entries": B * T, "decode_us": decode_ms * 1e3}
 
 
 # ---------------------------------------------------------------------------- CPU oracle

@@ -60,6 +60,7 @@ def _load():
         "csa2_unpack_kv_fp4": (ctypes.c_int, [vp, vp, i64, vp, vp]),
         "csa2_pack_fp8_e4m3": (ctypes.c_int, [vp, i64, vp, vp]),
         "csa2_unpack_fp8_e4m3": (ctypes.c_int, [vp, i64, vp, vp]),
+        "csa2_kv_append": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, vp, vp]),
         "csa2_index_score": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32]),
         "csa2_topk": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp, sz, vp]),
@@ -179,6 +180,18 @@ def csa2_pack_fp8_e4m3(x, out, stream=None):
 def csa2_unpack_fp8_e4m3(inp, out, stream=None):
     _req(inp, torch.uint8, "in"); _req(out, torch.bfloat16, "out")
     _call("csa2_unpack_fp8_e4m3", _p(inp), inp.numel(), _p(out), _s(stream))
+
+
+def csa2_kv_append(kv, ik, kv_data, kv_scale, ik_data, ik_scale, n_visible, n_visible_out=None, stream=None):
+    """kv [B,T,512] bf16 (RoPE'd latents), ik [B,T,128] bf16 -> entries at
+    n_visible[b] + t of the planes [B,cap,...]; n_visible_out (may be n_visible)."""
+    _req(kv, torch.bfloat16, "kv"); _req(ik, torch.bfloat16, "ik")
+    for t, n in ((kv_data, "kv_data"), (kv_scale, "kv_scale"), (ik_data, "ik_data"), (ik_scale, "ik_scale")):
+        _req(t, torch.uint8, n)
+    _req(n_visible, torch.int32, "n_visible"); _req(n_visible_out, torch.int32, "n_visible_out", allow_none=True)
+    B, T = kv.shape[0], kv.shape[1]
+    _call("csa2_kv_append", _p(kv), _p(ik), B, T, _p(kv_data), _p(kv_scale), _p(ik_data), _p(ik_scale),
+          kv_data.shape[1], _p(n_visible), _p(n_visible_out), _s(stream))
 
 
 # ---- indexer, pool, Top-K -----------------------------------------------------

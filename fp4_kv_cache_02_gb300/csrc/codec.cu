@@ -7,8 +7,10 @@
 //
 // These kernels are memory bound and off the per-query hot loop except for
 // the indexer-q quantisation; they use one thread per scale block with
-// 16-byte vector loads.
-#include "common.cuh"
+// 16-byte vector loads. The fused KV append (a new entry's main-KV latent,
+// quantised after RoPE, and its indexer key, written at the sequence's next
+// position) uses one warp per entry and the same block encoders.
+#include "codec_blocks.cuh"
 
 namespace csa2 {
 
@@ -27,37 +29,11 @@ __global__ void quant_mxfp4_kernel(const uint16_t* __restrict__ x, int64_t n_blo
     uint4 v = src[i];
     w[4 * i + 0] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
   }
-  // amax over the block, on the bf16 bit patterns with the sign cleared
-  uint32_t amax_bits = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    amax_bits = max(amax_bits, (w[i] & 0x7FFFu));
-    amax_bits = max(amax_bits, ((w[i] >> 16) & 0x7FFFu));
-  }
-  // floor(log2(amax)) is the unbiased exponent field for a normal amax;
-  // subnormal or zero amax clamps to -127.
-  int exp_field = (int)(amax_bits >> 7);  // bf16 exponent field
-  int X = exp_field == 0 ? -127 : (exp_field - 127) - 2;
-  X = X < -127 ? -127 : (X > 127 ? 127 : X);
-  // 2^-X as fp32 (X = 127 gives the subnormal 2^-127)
-  float inv = X == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - X) << 23);
-  uint32_t out[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      uint32_t pair0 = w[4 * i + 2 * j], pair1 = w[4 * i + 2 * j + 1];
-      float a0 = bf16_bits_to_f32(pair0 & 0xFFFFu) * inv;
-      float a1 = bf16_bits_to_f32(pair0 >> 16) * inv;
-      float a2 = bf16_bits_to_f32(pair1 & 0xFFFFu) * inv;
-      float a3 = bf16_bits_to_f32(pair1 >> 16) * inv;
-      word |= (cvt_e2m1x2(a0, a1) | (cvt_e2m1x2(a2, a3) << 8)) << (16 * j);
-    }
-    out[i] = word;
-  }
-  *reinterpret_cast<uint4*>(data + blk * 16) = make_uint4(out[0], out[1], out[2], out[3]);
-  e8m0[blk] = (uint8_t)(X + 127);
+  uint4 d;
+  uint8_t e;
+  encode_mxfp4_block(w, d, e);
+  *reinterpret_cast<uint4*>(data + blk * 16) = d;
+  e8m0[blk] = e;
 }
 
 __global__ void dequant_mxfp4_kernel(const uint8_t* __restrict__ data,
@@ -87,34 +63,12 @@ __global__ void pack_kv_fp4_kernel(const uint16_t* __restrict__ x, int64_t n_blo
   if (blk >= n_blocks) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + blk * 16);
   uint4 v0 = src[0], v1 = src[1];
-  uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  float f[16];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    f[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-    f[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    amax = fmaxf(amax, fabsf(f[2 * i]));
-    amax = fmaxf(amax, fabsf(f[2 * i + 1]));
-  }
-  float q = __fdiv_rn(amax, 6.0f);
-  uint32_t sc = cvt_e4m3x2(q, 0.0f) & 0xFFu;
-  float s = e4m3_to_f32(sc);
-  uint32_t out0 = 0, out1 = 0;
-  if (s != 0.0f) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t byte = cvt_e2m1x2(__fdiv_rn(f[2 * i], s), __fdiv_rn(f[2 * i + 1], s));
-      out0 |= byte << (8 * i);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t byte = cvt_e2m1x2(__fdiv_rn(f[8 + 2 * i], s), __fdiv_rn(f[8 + 2 * i + 1], s));
-      out1 |= byte << (8 * i);
-    }
-  }
-  *reinterpret_cast<uint2*>(kv_data + blk * 8) = make_uint2(out0, out1);
-  kv_scale[blk] = (uint8_t)sc;
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  uint2 d;
+  uint8_t sc;
+  encode_kv_fp4_block(w, d, sc);
+  *reinterpret_cast<uint2*>(kv_data + blk * 8) = d;
+  kv_scale[blk] = sc;
 }
 
 __global__ void unpack_kv_fp4_kernel(const uint8_t* __restrict__ kv_data,
@@ -165,6 +119,69 @@ __global__ void unpack_fp8_kernel(const uint8_t* __restrict__ in, int64_t n, uin
   if (i >= n) return;
   __nv_bfloat16 b = __float2bfloat16_rn(e4m3_to_f32(in[i]));
   out[i] = *reinterpret_cast<uint16_t*>(&b);
+}
+
+// ---- fused append: one warp per new entry (b, t) ----------------------------
+// Lane l encodes main-KV block l (channels 16l .. 16l+15); lanes 0..3 also
+// encode indexer-key block l (channels 32l .. 32l+31). The entry goes to
+// position n_visible[b] + t. A sequence whose T entries do not fit below the
+// capacity (or whose count is negative) gets none of them, keeps its count
+// and records a device error.
+constexpr int kAppendWarps = 8;
+
+__global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
+    const uint16_t* __restrict__ kv, const uint16_t* __restrict__ ik, int32_t B, int32_t T,
+    uint8_t* __restrict__ kv_data, uint8_t* __restrict__ kv_scale, uint8_t* __restrict__ ik_data,
+    uint8_t* __restrict__ ik_scale, int64_t cap, const int32_t* __restrict__ n_visible,
+    int32_t* __restrict__ n_visible_out) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int64_t e = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (e >= (int64_t)B * T) return;
+  const int b = (int)(e / T), t = (int)(e % T);
+  const int64_t nv = n_visible[b];
+  const bool fits = nv >= 0 && nv + T <= cap;
+  if (n_visible_out && t == 0 && lane == 0) n_visible_out[b] = (int32_t)(fits ? nv + T : nv);
+  if (!fits) {
+    if (lane == 0 && t == 0) record_error(&g_codec_error, CSA2_ERR_DEVICE);
+    return;
+  }
+  const int64_t p = nv + t;
+  const int64_t row = (int64_t)b * cap + p;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(kv + e * kHeadDim + lane * 16);
+    const uint4 v0 = src[0], v1 = src[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint2 d;
+    uint8_t sc;
+    encode_kv_fp4_block(w, d, sc);
+    *reinterpret_cast<uint2*>(kv_data + row * kKvBytes + lane * 8) = d;
+    kv_scale[row * kKvScales + lane] = sc;
+  }
+  if (lane < kIdxDim / 32) {
+    const uint4* src = reinterpret_cast<const uint4*>(ik + e * kIdxDim + lane * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = src[i];
+      w[4 * i + 0] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    uint4 d;
+    uint8_t sc;
+    encode_mxfp4_block(w, d, sc);
+    *reinterpret_cast<uint4*>(ik_data + row * (kIdxDim / 2) + lane * 16) = d;
+    ik_scale[row * (kIdxDim / 32) + lane] = sc;
+  }
+}
+
+// In-place advance of the visible counts, after the append grid has finished
+// reading them (its programmatic dependency waits for the whole grid).
+__global__ void advance_visible_kernel(int32_t* __restrict__ n_visible, int32_t B, int32_t T, int64_t cap) {
+  pdl_begin();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int64_t nv = n_visible[b];
+  if (nv >= 0 && nv + T <= cap) n_visible[b] = (int32_t)(nv + T);
 }
 
 }  // namespace csa2
@@ -249,5 +266,26 @@ extern "C" int csa2_unpack_fp8_e4m3(const uint8_t* in, int64_t n, void* out_bf16
   if (n == 0) return CSA2_OK;
   unpack_fp8_kernel<<<grid_for(n, 256), 256, 0, (cudaStream_t)stream>>>(in, n, (uint16_t*)out_bf16);
   CSA2_CHECK_LAUNCH();
+  return CSA2_OK;
+}
+
+extern "C" int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t B, int32_t T, uint8_t* kv_data,
+                              uint8_t* kv_scale, uint8_t* ik_data, uint8_t* ik_scale, int64_t cap,
+                              const int32_t* n_visible, int32_t* n_visible_out, csa2_stream_t stream) {
+  if (!kv_bf16 || !ik_bf16 || !kv_data || !kv_scale || !ik_data || !ik_scale || !n_visible) return CSA2_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || cap < 0) return CSA2_ERR_INVALID_ARG;
+  if (cap > 0x7FFFFFFFLL) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!csa2_aligned(kv_bf16, 16) || !csa2_aligned(ik_bf16, 16) || !csa2_aligned(kv_data, 8) ||
+      !csa2_aligned(ik_data, 16))
+    return CSA2_ERR_ALIGNMENT;
+  if (B == 0 || T == 0) return CSA2_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool in_place = n_visible_out == n_visible;
+  const int64_t entries = (int64_t)B * T;
+  CSA2_LAUNCH_PDL(kv_append_kernel, grid_for(entries, kAppendWarps), dim3(kAppendWarps * 32), 0, s,
+                  (const uint16_t*)kv_bf16, (const uint16_t*)ik_bf16, B, T, kv_data, kv_scale, ik_data, ik_scale, cap,
+                  n_visible, in_place ? (int32_t*)nullptr : n_visible_out);
+  if (in_place)
+    CSA2_LAUNCH_PDL(advance_visible_kernel, grid_for(B, 256), dim3(256), 0, s, n_visible_out, B, T, cap);
   return CSA2_OK;
 }

@@ -136,6 +136,28 @@ int csa2_pack_fp8_e4m3(const void* x_bf16, int64_t n, uint8_t* out,
 int csa2_unpack_fp8_e4m3(const uint8_t* in, int64_t n, void* out_bf16,
                          csa2_stream_t stream);
 
+/**
+ * Fused KV append (report section 2.4.4: the main-KV latent is quantised
+ * after RoPE into E2M1 with one E4M3 scale per 16 channels, no global scale;
+ * the indexer key into OCP MXFP4): T new entries per sequence, written at
+ * positions n_visible[b] .. n_visible[b] + T - 1 of its planes.
+ *   kv_bf16 [B][T][512] bf16 (the RoPE'd latents, 16-byte aligned),
+ *   ik_bf16 [B][T][128] bf16 (the indexer keys, 16-byte aligned);
+ *   kv planes [B][cap][256] / [B][cap][32] (kv_data 8-byte aligned),
+ *   ik planes [B][cap][64] / [B][cap][4] (ik_data 16-byte aligned);
+ *   n_visible [B] int32; n_visible_out [B] int32 (nullable) receives
+ *   n_visible + T. It may be n_visible itself (advanced in place).
+ * The bytes written equal csa2_pack_kv_fp4 and csa2_quant_mxfp4 of the same
+ * rows. A sequence whose T entries do not fit below cap gets none of them and
+ * keeps its count; csa2_get_last_error then reports DEVICE.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (cap above 2^31-1), ALIGNMENT, CUDA.
+ */
+int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t B,
+                   int32_t T, uint8_t* kv_data, uint8_t* kv_scale,
+                   uint8_t* ik_data, uint8_t* ik_scale, int64_t cap,
+                   const int32_t* n_visible, int32_t* n_visible_out,
+                   csa2_stream_t stream);
+
 /* ======================================================================== */
 /* Lightning indexer, pool and Top-K                                         */
 /* ======================================================================== */

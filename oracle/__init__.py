@@ -182,6 +182,29 @@ def unpack_fp8(b):
     return out
 
 
+def kv_append(kv, ik, kv_data, kv_scale, ik_data, ik_scale, n_visible):
+    """Appends T new entries per sequence ([R] 2.4.4: the main-KV latent is
+    quantised after RoPE to E2M1 + E4M3/16, the indexer key to MXFP4): row t
+    of sequence b goes to position n_visible[b] + t of its planes. A sequence
+    whose T rows do not fit below the capacity is left unchanged. Updates the
+    planes in place; returns the new visible counts.
+      kv float32 [B, T, 512], ik float32 [B, T, 128] (bf16-exact values);
+      planes [B, cap, 256] / [B, cap, 32] / [B, cap, 64] / [B, cap, 4] u8."""
+    kv = _c(kv, np.float32)
+    ik = _c(ik, np.float32)
+    B, T = kv.shape[0], kv.shape[1]
+    cap = kv_data.shape[1]
+    out = np.array(n_visible, np.int32).copy()
+    for b in range(B):
+        nv = int(n_visible[b])
+        if nv < 0 or nv + T > cap or T == 0:
+            continue
+        kv_data[b, nv:nv + T], kv_scale[b, nv:nv + T] = pack_kv_fp4(kv[b])
+        ik_data[b, nv:nv + T], ik_scale[b, nv:nv + T] = quant_mxfp4(ik[b])
+        out[b] = nv + T
+    return out
+
+
 def main_kv_entry_bytes() -> int:
     return lib().orc_main_kv_entry_bytes()
 

@@ -178,3 +178,41 @@ def test_fp8_pack_matches_library_cast(orc):
     assert np.array_equal(got, ref)
     assert np.array_equal(orc.unpack_fp8(got),
                           torch.from_numpy(got).view(torch.float8_e4m3fn).double().numpy())
+
+
+# ---- fused KV append: placement around the pinned codecs ------------------------
+
+def _rows(rng, shape):
+    return bf16_round(rng.standard_normal(shape).astype(np.float32) * 3.0)
+
+
+def test_kv_append_step_by_step_builds_the_bulk_packed_planes(orc):
+    """Appending entries a few at a time must give the planes that packing the
+    whole sequence at once gives (the bulk codec calls are pinned above)."""
+    rng = np.random.default_rng(61)
+    B, cap, n = 2, 64, 40
+    kv, ik = _rows(rng, (B, n, 512)), _rows(rng, (B, n, 128))
+    planes = [np.full((B, cap, w), 0xA5, np.uint8) for w in (256, 32, 64, 4)]
+    nv = np.zeros(B, np.int32)
+    for lo, hi in ((0, 1), (1, 8), (8, 9), (9, 40)):
+        nv = orc.kv_append(kv[:, lo:hi], ik[:, lo:hi], *planes, nv)
+        assert list(nv) == [hi, hi]
+    for b in range(B):
+        d, s = orc.pack_kv_fp4(kv[b])
+        qd, qs = orc.quant_mxfp4(ik[b])
+        assert np.array_equal(planes[0][b, :n], d) and np.array_equal(planes[1][b, :n], s)
+        assert np.array_equal(planes[2][b, :n], qd) and np.array_equal(planes[3][b, :n], qs)
+        for pl in planes:
+            assert np.all(pl[b, n:] == 0xA5)     # nothing past the visible entries is touched
+
+
+def test_kv_append_that_does_not_fit_changes_nothing(orc):
+    rng = np.random.default_rng(62)
+    B, cap, T = 3, 16, 4
+    kv, ik = _rows(rng, (B, T, 512)), _rows(rng, (B, T, 128))
+    planes = [np.full((B, cap, w), 0x5A, np.uint8) for w in (256, 32, 64, 4)]
+    nv = orc.kv_append(kv, ik, *planes, np.array([12, 13, -1], np.int32))
+    assert list(nv) == [16, 13, -1]
+    assert not np.all(planes[0][0, 12:] == 0x5A)
+    for pl in planes:
+        assert np.all(pl[1:] == 0x5A)
