@@ -9,10 +9,11 @@
 // SWA KV); mer.dev notes section 1 (64 heads of dim 512; the 512-dim KV latent
 // is shared as K and V).
 //
-// Work split: one CTA per (query, chunk of 128 rows) computes an
-// unnormalised partial (m, l, O) of its rows on the tensor cores
-// (attention_tc.cuh); a second kernel merges the chunks of a query in fixed
-// chunk order, so results are deterministic.
+// Work split: one CTA per (query, chunk of rows) computes an unnormalised
+// partial (m, l, O) of its rows on the tensor cores (attention_tc.cuh); a
+// second kernel merges the chunks of a query in fixed chunk order, so results
+// are deterministic. The chunk size (32 .. 160 rows) is picked per launch so
+// that the CTAs fill the SMs in as few waves as possible.
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -36,10 +37,13 @@ struct AttnArgs {
   int32_t n_swa;
   float sm_scale;
   int32_t n_split;
+  int32_t rows;             // rows per chunk (a multiple of 32, at most 160)
   float* part_o;            // [n_q][n_split][64][512]
   float* part_ml;           // [n_q][n_split][64][2]
   int32_t q0;               // first query of this launch
 };
+
+constexpr int kMaxSplitCombine = 32;
 
 // grid (n_q_in_launch, 8), block 256: merge the splits of 8 heads of one
 // query, in fixed split order.
@@ -49,7 +53,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restri
                                                            float* __restrict__ out_f32, float* __restrict__ lse) {
   pdl_begin();
   constexpr int kHeadsPerCta = 8;
-  __shared__ float scale_s[kHeadsPerCta][16];
+  __shared__ float scale_s[kHeadsPerCta][kMaxSplitCombine];
   __shared__ float inv_l[kHeadsPerCta];
   const int lq = blockIdx.x;
   const int qi = q0 + lq;
@@ -125,7 +129,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-static constexpr int kMaxSplit = 16;  // k + n_swa <= 1024 rows per query
+static constexpr int kMaxSplit = kMaxSplitCombine;  // k + n_swa <= 32 x 160 rows per query
 static constexpr int kQueriesPerLaunch = 256;
 
 int csa2_read_and_clear_attn_error(cudaStream_t s) {
@@ -138,15 +142,61 @@ int csa2_read_and_clear_attn_error(cudaStream_t s) {
   return v;
 }
 
-static inline int attn_splits(int32_t k, int32_t n_swa) {
-  return (k + n_swa + attn_tc::kRowsTc - 1) / attn_tc::kRowsTc;
+static int sm_count() {
+  constexpr int kMaxDevices = 64;
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  if (!count[dev]) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 152;
+    count[dev] = c;
+  }
+  return count[dev];
+}
+
+// Rows per chunk for n_q queries of `total` rows each: the multiple of 32 (at
+// most 160) with the smallest estimated time = waves x (fixed + per-row cost)
+// plus the combine's per-split cost. The costs are the kernel's measured phase
+// times on GB300 (about 7.5 us per CTA plus 0.047 us per row).
+static int attn_rows(int32_t n_q, int32_t total) {
+  if (total <= 0) return 32;
+  const int n_sm = sm_count();
+  double best = 1e300;
+  int best_rows = -1;
+  for (int rows = 32; rows <= attn_tc::kMaxRows; rows += 32) {
+    const int splits = (total + rows - 1) / rows;
+    if (splits > kMaxSplit) continue;
+    const int64_t ctas = (int64_t)n_q * splits;
+    const int64_t waves = (ctas + n_sm - 1) / n_sm;
+    const double t = (double)waves * (7.5 + 0.047 * rows) + 0.05 * splits;
+    if (t < best - 1e-9) {
+      best = t;
+      best_rows = rows;
+    }
+  }
+  return best_rows;
+}
+
+static inline int attn_queries_per_launch(int32_t n_queries) {
+  return n_queries < kQueriesPerLaunch ? n_queries : kQueriesPerLaunch;
+}
+
+// splits per query; 0 when k + n_swa needs more than kMaxSplit chunks
+static inline int attn_splits(int32_t n_queries, int32_t k, int32_t n_swa, int* rows_out) {
+  const int32_t total = k + n_swa;
+  const int rows = attn_rows(attn_queries_per_launch(n_queries), total);
+  if (rows < 0) return 0;
+  if (rows_out) *rows_out = rows;
+  const int splits = (total + rows - 1) / rows;
+  return splits < 1 ? 1 : splits;
 }
 
 extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, int32_t n_swa) {
   if (n_queries <= 0 || k < 0 || n_swa < 0) return 0;
   // partials are indexed by query within one launch of at most kQueriesPerLaunch
-  int32_t nq = n_queries < kQueriesPerLaunch ? n_queries : kQueriesPerLaunch;
-  int ns = attn_splits(k, n_swa);
+  int32_t nq = attn_queries_per_launch(n_queries);
+  int ns = attn_splits(n_queries, k, n_swa, nullptr);
   if (ns < 1) ns = 1;
   size_t o = (size_t)nq * ns * kHeads * kHeadDim * 4;
   o = (o + 255) / 256 * 256;
@@ -155,12 +205,11 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, 
 
 static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, float* lse, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
-  a.n_split = attn_splits(a.k, a.n_swa);
-  if (a.n_split < 1) a.n_split = 1;
-  if (a.n_split > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  a.n_split = attn_splits(n_q, a.k, a.n_swa, &a.rows);
+  if (a.n_split < 1 || a.n_split > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
   size_t need = csa2_sparse_attn_workspace_size(n_q, a.k, a.n_swa);
   if (!ws || ws_bytes < need || !csa2_aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
-  int32_t nq_ws = n_q < kQueriesPerLaunch ? n_q : kQueriesPerLaunch;
+  int32_t nq_ws = attn_queries_per_launch(n_q);
   size_t o_bytes = (size_t)nq_ws * a.n_split * kHeads * kHeadDim * 4;
   o_bytes = (o_bytes + 255) / 256 * 256;
   a.part_o = (float*)ws;
@@ -204,8 +253,9 @@ extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
   if (!q_bf16 || !kv_data || !kv_scale || !n_visible || !idx || !out_bf16) return CSA2_ERR_INVALID_ARG;
   if (B < 0 || L < 1 || k < 0 || n_swa < 0 || cap < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
-  if (k > CSA2_MAX_TOPK || n_swa > 512 || attn_splits(k, n_swa) > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 8) || !csa2_aligned(out_bf16, 8) ||
+  if (k > CSA2_MAX_TOPK || n_swa > 512 || k + n_swa > kMaxSplit * attn_tc::kMaxRows)
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 2) || !csa2_aligned(out_bf16, 8) ||
       (swa && !csa2_aligned(swa, 16)) || (out_f32 && !csa2_aligned(out_f32, 16)))
     return CSA2_ERR_ALIGNMENT;
   if (B == 0) return CSA2_OK;
@@ -233,8 +283,9 @@ extern "C" int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T, const uin
   if (!q_bf16 || !kv_data || !kv_scale || !idx || !out_bf16) return CSA2_ERR_INVALID_ARG;
   if (T < 0 || k < 0 || n_swa < 0 || n_entries < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
-  if (k > CSA2_MAX_TOPK || n_swa > 512 || attn_splits(k, n_swa) > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 8) || !csa2_aligned(out_bf16, 8) ||
+  if (k > CSA2_MAX_TOPK || n_swa > 512 || k + n_swa > kMaxSplit * attn_tc::kMaxRows)
+    return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 2) || !csa2_aligned(out_bf16, 8) ||
       (swa && !csa2_aligned(swa, 16)) || (out_f32 && !csa2_aligned(out_f32, 16)))
     return CSA2_ERR_ALIGNMENT;
   if (T == 0) return CSA2_OK;

@@ -6,18 +6,23 @@
 // layer's SWA rows in one softmax; mer.dev notes section 1: 64 heads of dim
 // 512 share the 512-channel latent as K and V.
 //
-// One CTA takes one query (64 heads) and one chunk of 128 rows (selected
-// latents or SWA rows):
-//   1. gather + dequantise the chunk into shared memory as bf16 R[t][c]
-//      (exact: E2M1 x E4M3 has at most 6 significant bits), laid out as
-//      128-byte-swizzled blocks of 64 channels;
-//   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (M = 128 rows, N = 64 heads,
-//      K = 512; both operands K-major), accumulated in tensor memory;
+// One CTA takes one query (64 heads) and one chunk of `rows` rows (selected
+// latents and/or SWA rows; rows is a multiple of 32, at most 160, chosen by
+// the host so that the grid fills the SMs in as few waves as possible):
+//   1. all row loads are issued up front; the chunk is dequantised into
+//      shared memory as bf16 R[t][c] (exact: E2M1 x E4M3 has at most 6
+//      significant bits) in 128-byte-swizzled blocks of 64 channels, the low
+//      256 channels first;
+//   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (M = 128 rows per tile, one
+//      or two tiles; N = 64 heads; K = 512 in two halves of 256 channels, so
+//      that only half of Q is resident: the first half's MMAs run while the
+//      high channels are dequantised and the second half of Q loads);
 //   3. per-head max and sum over the chunk's rows; P = exp(S - max) split
-//      into bf16 hi + lo parts (keeps the P.V product at fp32-level accuracy);
-//   4. O^T[c][h] = sum_t R[t][c] P[h][t] on the tensor cores (M = 128 channels
-//      x 4 blocks, N = 64 heads, K = 128 rows), reading the same R tile as an
-//      MN-major operand, once with P_hi and once with P_lo;
+//      into bf16 hi + lo parts (keeps the P.V product at fp32-level accuracy),
+//      stacked as 128 B-operand rows (64 hi, 64 lo);
+//   4. O^T[c][n] = sum_t R[t][c] P[n][t] on the tensor cores (M = 128 channels
+//      x 4 blocks, N = 128, K = rows), reading the same R tile as an MN-major
+//      operand; O = O_hi + O_lo when read back;
 //   5. the unnormalised partial O and the chunk's (max, sum) per head go to the
 //      workspace; attn_combine_kernel merges the chunks in fixed order.
 #pragma once
@@ -27,19 +32,22 @@
 namespace csa2 {
 namespace attn_tc {
 
-constexpr int kRowsTc = 128;
-constexpr int kThreads = 512;  // 16 warps: 4 TMEM lane quadrants x 4
-constexpr int kOffR = 0;                                   // 8 blocks x [128 t][128 B]  = 128 KiB
-constexpr int kOffQ = kOffR + kHeadDim * kRowsTc * 2;      // 8 blocks x [64 h][128 B]   =  64 KiB
-constexpr int kOffP = kOffQ;  // P (2 parts x 2 blocks x [64 h][128 B] = 32 KiB) reuses Q once S^T is done
-constexpr int kPBytes = kHeads * kRowsTc * 2;              // 16 KiB per P part
-constexpr int kOffMisc = kOffQ + kHeadDim * kHeads * 2;
+constexpr int kMaxRows = 160;   // rows per CTA: a multiple of 32, at most 160
+constexpr int kThreads = 512;   // 16 warps: 4 TMEM lane quadrants x 4
+constexpr int kBlkR = kMaxRows * 128;                     // one 64-channel block of R: [160 t][128 B]
+constexpr int kOffR = 0;                                  // 8 blocks                        = 160 KiB
+constexpr int kOffQP = kOffR + 8 * kBlkR;                 // Q half (4 x [64 h][128 B]) or P = 48 KiB
+constexpr int kQHalfBytes = kHeads * 256 * 2;             // 32 KiB
+constexpr int kPBlk = 2 * kHeads * 128;                   // P: per 64 rows, [128 n][128 B]  = 16 KiB
+constexpr int kOffMisc = kOffQP + 3 * kPBlk;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S^T: 64 columns (heads), lanes = rows
-constexpr uint32_t kColO = 64;     // O^T: 4 blocks x 64 columns, lanes = channels
+constexpr uint32_t kColS = 0;      // S^T: tile t at columns 64t .. 64t+63 (heads), lanes = rows
+constexpr uint32_t kColO = 0;      // O^T: 4 blocks x 128 columns (64 hi + 64 lo), lanes = channels;
+                                   // written once S^T has been read
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kQHalfBytes <= 3 * kPBlk, "Q half fits the P region");
 
 // exact bf16x2 product (operands with <= 2 and <= 4 significant bits)
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
@@ -98,33 +106,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   uint8_t* sR = sm + kOffR;
-  uint8_t* sQ = sm + kOffQ;
-  uint8_t* sP = sm + kOffP;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffMisc);
-  uint64_t* q_bar = bar + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 16);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 20);
+  uint8_t* sQP = sm + kOffQP;
+  uint64_t* bar_s0 = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T over channels 0..255 done
+  uint64_t* bar_s1 = bar_s0 + 1;                                 // S^T complete
+  uint64_t* bar_pv = bar_s0 + 2;                                 // O^T complete
+  uint64_t* q_bar = bar_s0 + 3;                                  // Q halves (two phases)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 32);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 36);
   __shared__ float red[4][kHeads];
   __shared__ float m_s[kHeads], l_s[kHeads];
-  __shared__ uint16_t lut_e4m3[256];   // E4M3 byte -> bf16 value
-  __shared__ int row_valid[kRowsTc];  // 0 none, 1 selected latent, 2 SWA row
-  __shared__ int64_t row_src[kRowsTc];  // entry index in the plane, or SWA byte offset
+  __shared__ uint16_t lut_e4m3[256];     // E4M3 byte -> bf16 value
+  __shared__ int row_valid[kMaxRows];    // 0 none, 1 selected latent, 2 SWA row
+  __shared__ int64_t row_src[kMaxRows];  // entry index in the plane, or SWA byte offset
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lq = blockIdx.y;
   const int qi = a.q0 + lq;
   const int seq = qi / a.L;
   const int split = blockIdx.x;
+  const int rows = a.rows;
+  const int n_tiles = (rows + 127) >> 7;
 
-  // ---- Q: [64 h][512 c] bf16 -> 8 TMA boxes of [64 h][64 c] = [64][128 B], SW128 ----
+  // ---- Q channels 0..255: 4 TMA boxes of [64 h][64 c] = [64][128 B], SW128 ----
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(bar_s0, 1);
+    tc::mbar_init(bar_s1, 1);
+    tc::mbar_init(bar_pv, 1);
     tc::mbar_init(q_bar, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(q_bar, kHeads * kHeadDim * 2);
-    for (int blk = 0; blk < kHeadDim / 64; ++blk)
-      tc::tma_load_2d(sQ + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
+    tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
+    for (int blk = 0; blk < 4; ++blk)
+      tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   if (tid < 256) {
@@ -135,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- rows of this chunk: position (or SWA row), validity ----
   const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
   const int32_t* idx_row = a.idx + (int64_t)seq * a.k;
-  if (tid < kRowsTc) {
-    const int t = split * kRowsTc + tid;
+  if (tid < rows) {
+    const int t = split * rows + tid;
     int valid = 0;
     int64_t src = 0;
     if (t < a.k) {
@@ -157,132 +170,201 @@ __global__ void __launch_bounds__(kThreads, 1)
     row_src[tid] = src;
   }
   __syncthreads();
-  // ---- gather + dequantise R: [128 t][512 c] bf16 as 8 blocks [128 t][128 B] ----
-  // warp w owns rows 8w..8w+7; pass j covers them in 64-channel block j, 4
-  // lanes per row, each lane 16 channels (two 16-byte chunks). All loads of a
-  // thread are issued before any is used.
-  {
-    constexpr int kPasses = 8;
-    uint4 raw[kPasses];
-    uint32_t sc[kPasses];
+
+  // ---- gather: all loads first. Pass ps covers rows 64ps .. 64ps+63: warp w
+  // rows 64ps + 4w .. +3, 8 lanes per row; lane `sub` holds channels
+  // 32sub .. 32sub+31 of the low half and of the high half of the row ----
+  constexpr int kPasses = (kMaxRows + 63) / 64;
+  const int grp = lane >> 3, sub = lane & 7;
+  uint4 raw[kPasses][4];
 #pragma unroll
-    for (int jj = 0; jj < kPasses; ++jj) {
-      const int r = warp * 8 + (lane >> 2);
-      const int blk = jj * 4 + (lane & 3);
-      const int kind = row_valid[r];
-      const int64_t src = row_src[r];
-      raw[jj] = make_uint4(0u, 0u, 0u, 0u);
-      sc[jj] = 0u;
-      if (kind == 1) {
-        const uint2 v = *reinterpret_cast<const uint2*>(a.kv_data + src * kKvBytes + blk * 8);
-        raw[jj].x = v.x;
-        raw[jj].y = v.y;
-        sc[jj] = a.kv_scale[src * kKvScales + blk];
-      } else if (kind == 2) {
-        raw[jj] = *reinterpret_cast<const uint4*>(a.swa + src + blk * 16);
-      }
+  for (int ps = 0; ps < kPasses; ++ps) {
+    const int r = ps * 64 + warp * 4 + grp;
+    const int kind = r < rows ? row_valid[r] : 0;
+    const int64_t src = r < rows ? row_src[r] : 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw[ps][i] = make_uint4(0u, 0u, 0u, 0u);
+    if (kind == 1) {
+      const uint8_t* d = a.kv_data + src * kKvBytes + sub * 16;
+      raw[ps][0] = *reinterpret_cast<const uint4*>(d);
+      raw[ps][1] = *reinterpret_cast<const uint4*>(d + 128);
+      const uint8_t* sc = a.kv_scale + src * kKvScales + sub * 2;
+      raw[ps][2].x = (uint32_t)*reinterpret_cast<const uint16_t*>(sc) |
+                     ((uint32_t)*reinterpret_cast<const uint16_t*>(sc + 16) << 16);
+    } else if (kind == 2) {
+      const uint8_t* e = a.swa + src + sub * 32;
+      raw[ps][0] = *reinterpret_cast<const uint4*>(e);
+      raw[ps][1] = *reinterpret_cast<const uint4*>(e + 16);
+      raw[ps][2] = *reinterpret_cast<const uint4*>(e + 256);
+      raw[ps][3] = *reinterpret_cast<const uint4*>(e + 272);
     }
+  }
+  // dequantise one half (channels 256h .. 256h+255) of every row into R
+  auto dequant_half = [&](const int half) {
 #pragma unroll
-    for (int jj = 0; jj < kPasses; ++jj) {
-      const int r = warp * 8 + (lane >> 2);
-      const int blk = jj * 4 + (lane & 3);
+    for (int ps = 0; ps < kPasses; ++ps) {
+      const int r = ps * 64 + warp * 4 + grp;
+      if (r >= rows) continue;
       const int kind = row_valid[r];
-      uint32_t o[8];
+      uint32_t o[16];
       if (kind == 1) {
-        const uint32_t s1 = lut_e4m3[sc[jj]];
-        const uint32_t s2 = s1 | (s1 << 16);
-        const uint32_t w[2] = {raw[jj].x, raw[jj].y};
+        const uint4 d = raw[ps][half];
+        const uint32_t scb = (raw[ps][2].x >> (16 * half)) & 0xFFFFu;
+        const uint32_t sa = lut_e4m3[scb & 0xFFu], sb = lut_e4m3[scb >> 8];
+        const uint32_t sa2 = sa | (sa << 16), sb2 = sb | (sb << 16);
+        const uint32_t w[4] = {d.x, d.y, d.z, d.w};  // w[i]: channels 8i .. 8i+7 of the lane's 32
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          uint32_t v01, v23;
-          e2m1x4_to_bf16((w[e >> 2] >> (8 * (e & 3))) & 0xFFFFu, v01, v23);
-          o[e] = mul_bf16x2(v01, s2);
-          o[e + 1] = mul_bf16x2(v23, s2);
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t v01, v23;
+            e2m1x4_to_bf16((w[i] >> (16 * hh)) & 0xFFFFu, v01, v23);
+            const uint32_t s2 = i < 2 ? sa2 : sb2;   // channels 0..15: scale a, 16..31: scale b
+            o[4 * i + 2 * hh] = mul_bf16x2(v01, s2);
+            o[4 * i + 2 * hh + 1] = mul_bf16x2(v23, s2);
+          }
         }
-      } else {
-        const uint32_t w[4] = {raw[jj].x, raw[jj].y, raw[jj].z, raw[jj].w};  // zero for invalid rows
+      } else if (kind == 2) {
+        const uint4 x = raw[ps][2 * half], y = raw[ps][2 * half + 1];
+        const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 16; ++e) {
           const uint32_t pair = w[e >> 1] >> (16 * (e & 1));
           o[e] = (uint32_t)lut_e4m3[pair & 0xFFu] | ((uint32_t)lut_e4m3[(pair >> 8) & 0xFFu] << 16);
         }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = 0u;   // invalid rows are zero: P = 0 must not meet NaN
       }
-      uint8_t* region = sR + (blk >> 2) * (kRowsTc * 128);
-      const uint32_t c0 = (uint32_t)(blk & 3) * 2;
-      *reinterpret_cast<uint4*>(region + tc::sw128_offset(r, c0)) = make_uint4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<uint4*>(region + tc::sw128_offset(r, c0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+      uint8_t* region = sR + (half * 4 + (sub >> 1)) * kBlkR;
+      const uint32_t c0 = (uint32_t)(sub & 1) * 4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(region + tc::sw128_offset((uint32_t)r, c0 + j)) =
+            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    }
+  };
+  // S^T (+)= R[:, 256kh .. +255] . Q[:, 256kh .. +255]^T for every tile of 128 rows
+  auto issue_s = [&](const uint32_t tmem, const int kh) {
+    constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 0, 0);
+    const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQP);
+    for (int t = 0; t < n_tiles; ++t)
+      for (int kk = 0; kk < 16; ++kk) {
+        const uint32_t blk = (uint32_t)(kh * 4) + ((uint32_t)kk >> 2), off = ((uint32_t)kk & 3u) * 32u;
+        const uint64_t ad = tc::smem_desc(r_addr + blk * kBlkR + (uint32_t)t * (128u * 128u) + off, 0, 1024,
+                                          tc::kSwizzle128B);
+        const uint64_t bd = tc::smem_desc(q_addr + ((uint32_t)kk >> 2) * (kHeads * 128) + off, 0, 1024,
+                                          tc::kSwizzle128B);
+        tc::mma_bf16(tmem + kColS + 64u * (uint32_t)t, ad, bd, idesc, (kh | kk) ? 1u : 0u);
+      }
+  };
+
+  dequant_half(0);
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  bool lead_ok = true;   // meaningful in thread 0
+  if (tid == 0) {
+    lead_ok = tc::mbar_wait_bounded(q_bar, 0, s_abort, &g_attn_error);
+    if (lead_ok) {
+      issue_s(tmem, 0);
+      tc::mma_commit(bar_s0);
+    }
+  }
+  dequant_half(1);
+  if (tid == 0 && lead_ok) {
+    // the Q buffer takes channels 256..511 once the first MMAs have read it
+    lead_ok = tc::mbar_wait_bounded(bar_s0, 0, s_abort, &g_attn_error);
+    if (lead_ok) {
+      tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
+      for (int blk = 0; blk < 4; ++blk)
+        tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, 256 + blk * 64, qi * kHeads, q_bar);
     }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-
-  // ---- S^T = R . Q^T : M = 128 rows, N = 64 heads, K = 512 ----
-  bool q_ok = tc::mbar_wait_bounded(q_bar, 0, s_abort, &g_attn_error);
-  if (tid == 0 && q_ok) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 0, 0);
-    const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQ);
-    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-      const uint32_t blk = (uint32_t)kk >> 2, off = ((uint32_t)kk & 3u) * 32u;
-      const uint64_t ad = tc::smem_desc(r_addr + blk * (kRowsTc * 128) + off, 0, 1024, tc::kSwizzle128B);
-      const uint64_t bd = tc::smem_desc(q_addr + blk * (kHeads * 128) + off, 0, 1024, tc::kSwizzle128B);
-      tc::mma_bf16(tmem + kColS, ad, bd, idesc, kk > 0 ? 1u : 0u);
+  if (tid == 0 && lead_ok) {
+    lead_ok = tc::mbar_wait_bounded(q_bar, 1, s_abort, &g_attn_error);
+    if (lead_ok) {
+      issue_s(tmem, 1);
+      tc::mma_commit(bar_s1);
     }
-    tc::mma_commit(bar);
   }
+  if (tid == 0 && !lead_ok) *s_abort = 1;
   __syncwarp();
   // warp-uniform outcomes: the tcgen05.ld below needs the whole warp
-  bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar, 0, s_abort, &g_attn_error));
+  const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_s1, 0, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
-  // ---- softmax over the chunk's rows; warp w: rows 32*(w%4).., heads 16*(w/4).. ----
+  // ---- softmax over the chunk's rows. Warp w reads TMEM lanes 32(w%4) .. (rows
+  // 32(w%4) + lane of tile 0, and rows 128 + lane of tile 1 for w%4 == 0) and
+  // heads 16(w/4) .. +15 ----
   constexpr int kHpw = 16;  // heads per warp
   const int rq = warp & 3, hb = (warp >> 2) * kHpw;
-  const int row = rq * 32 + lane;
-  const bool rv = ok && row_valid[row] != 0;
-  const uint32_t s_addr = tmem + ((uint32_t)(rq * 32) << 16) + kColS + hb;
-  float p[kHpw];
+  const int row0 = rq * 32 + lane, row1 = 128 + lane;
+  const bool two = n_tiles > 1 && rq == 0;  // warp-uniform
+  const bool rv0 = s_ok && row0 < rows && row_valid[row0] != 0;
+  const bool rv1 = s_ok && two && row1 < rows && row_valid[row1] != 0;
+  float p0[kHpw], p1[kHpw];
   auto load_scores = [&]() {
-    uint32_t r[kHpw];
-    if (ok) {
-      tc::tmem_ld_32x32b_x16(s_addr, r);
+    uint32_t r0[kHpw], r1[kHpw];
+    if (s_ok) {
+      tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(rq * 32) << 16) + kColS + hb, r0);
+      if (two) tc::tmem_ld_32x32b_x16(tmem + kColS + 64u + hb, r1);
       tc::tmem_ld_wait();
     }
 #pragma unroll
-    for (int j = 0; j < kHpw; ++j) p[j] = rv ? __uint_as_float(r[j]) * a.sm_scale : -INFINITY;
+    for (int j = 0; j < kHpw; ++j) {
+      p0[j] = rv0 ? __uint_as_float(r0[j]) * a.sm_scale : -INFINITY;
+      p1[j] = rv1 ? __uint_as_float(r1[j]) * a.sm_scale : -INFINITY;
+    }
   };
   load_scores();
-  // per-head max over the warp's 32 rows lands in lane (head - hb) mod 16
+  // per-head max over the warp's rows lands in lane (head - hb) mod 16
   {
-    const float m = warp_transpose_reduce<true, kHpw>(p, lane);
+    float v[kHpw];
+#pragma unroll
+    for (int j = 0; j < kHpw; ++j) v[j] = fmaxf(p0[j], p1[j]);
+    const float m = warp_transpose_reduce<true, kHpw>(v, lane);
     if (lane < kHpw) red[rq][hb + lane] = m;
   }
   __syncthreads();
   if (tid < kHeads) m_s[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
   __syncthreads();
-  // P = exp(S - m) from a second read of S; P_hi = bf16(P), P_lo = bf16(P - P_hi)
+  // P = exp(S - m) from a second read of S; P_hi = bf16(P), P_lo = bf16(P - P_hi),
+  // stored K-major for the PV MMA as B-operand rows n = h (hi) and 64 + h (lo):
+  // per 64 rows t a block of [128 n][128 B]
   load_scores();
 #pragma unroll
-  for (int j = 0; j < kHpw; ++j) p[j] = (p[j] == -INFINITY) ? 0.0f : expf(p[j] - m_s[hb + j]);
-  // P parts, K-major for the PV MMA: [64 h][128 t] as 2 blocks of [64 h][128 B]
-  {
-    uint8_t* blkp = sP + (row >> 6) * (kHeads * 128);
-    const uint32_t chunk = (uint32_t)(row & 63) >> 3, within = ((uint32_t)row & 7u) * 2u;
+  for (int j = 0; j < kHpw; ++j) {
+    const float m = m_s[hb + j];
+    p0[j] = (p0[j] == -INFINITY) ? 0.0f : expf(p0[j] - m);
+    p1[j] = (p1[j] == -INFINITY) ? 0.0f : expf(p1[j] - m);
+  }
+  auto store_p = [&](const int t, const float (&pv)[kHpw]) {
+    uint8_t* blkp = sQP + (t >> 6) * kPBlk;
+    const uint32_t chunk = (uint32_t)(t & 63) >> 3, within = ((uint32_t)t & 7u) * 2u;
 #pragma unroll
     for (int j = 0; j < kHpw; ++j) {
-      const int h = hb + j;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(p[j]);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(p[j] - __bfloat162float(hi));
-      const uint32_t off = tc::sw128_offset((uint32_t)h, chunk) + within;
-      *reinterpret_cast<__nv_bfloat16*>(blkp + off) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(blkp + kPBytes + off) = lo;
+      const uint32_t h = (uint32_t)(hb + j);
+      const __nv_bfloat16 hi = __float2bfloat16_rn(pv[j]);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(pv[j] - __bfloat162float(hi));
+      *reinterpret_cast<__nv_bfloat16*>(blkp + tc::sw128_offset(h, chunk) + within) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(blkp + tc::sw128_offset(h + kHeads, chunk) + within) = lo;
     }
-  }
+  };
+  if (row0 < rows) store_p(row0, p0);
+  if (two && row1 < rows) store_p(row1, p1);
   __syncthreads();  // red[] reads for m_s are done before it is reused for the sums
   {
-    const float l = warp_transpose_reduce<false, kHpw>(p, lane);
+    float v[kHpw];
+#pragma unroll
+    for (int j = 0; j < kHpw; ++j) v[j] = p0[j] + p1[j];
+    const float l = warp_transpose_reduce<false, kHpw>(v, lane);
     if (lane < kHpw) red[rq][hb + lane] = l;
   }
   tc::fence_proxy_async_smem();
@@ -291,45 +373,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   if (tid < kHeads) l_s[tid] = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
 
-  // ---- O^T = R^T . P^T : 4 x (M = 128 channels), N = 64 heads, K = 128 rows ----
-  if (tid == 0 && ok) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 1, 0);  // A (channels x rows) is MN-major
-    const uint32_t r_addr = tc::smem_u32(sR), p_addr = tc::smem_u32(sP);
+  // ---- O^T = R^T . [P_hi; P_lo]^T : 4 x (M = 128 channels), N = 128, K = rows ----
+  if (tid == 0 && s_ok) {
+    constexpr uint32_t idesc = tc::idesc_bf16(128, 128, 1, 0);  // A (channels x rows) is MN-major
+    const uint32_t r_addr = tc::smem_u32(sR), p_addr = tc::smem_u32(sQP);
+    const int ksteps = rows / 16;
     for (int mb = 0; mb < 4; ++mb) {
-      for (int part = 0; part < 2; ++part) {
-        for (int kk = 0; kk < kRowsTc / 16; ++kk) {
-          // A: channels 128*mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
-          //    rows 16*kk .. +15 (8-row groups: SBO apart)
-          const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)(2 * mb) * (kRowsTc * 128) + (uint32_t)kk * 16u * 128u,
-                                            kRowsTc * 128, 1024, tc::kSwizzle128B);
-          // B: P part, heads 0..63, rows 16*kk .. +15 (64-row K blocks of 128 B)
-          const uint64_t bd = tc::smem_desc(p_addr + (uint32_t)part * kPBytes + (uint32_t)(kk >> 2) * (kHeads * 128) +
-                                                ((uint32_t)kk & 3u) * 32u,
-                                            0, 1024, tc::kSwizzle128B);
-          tc::mma_bf16(tmem + kColO + 64u * (uint32_t)mb, ad, bd, idesc, (part | kk) ? 1u : 0u);
-        }
+      for (int kk = 0; kk < ksteps; ++kk) {
+        // A: channels 128mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
+        //    rows 16kk .. +15 (8-row groups: SBO apart)
+        const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)(2 * mb) * kBlkR + (uint32_t)kk * 16u * 128u, kBlkR,
+                                          1024, tc::kSwizzle128B);
+        // B: 128 P rows (hi, lo), rows t = 16kk .. +15 inside the 64-row block kk/4
+        const uint64_t bd = tc::smem_desc(p_addr + (uint32_t)(kk >> 2) * kPBlk + ((uint32_t)kk & 3u) * 32u, 0, 1024,
+                                          tc::kSwizzle128B);
+        tc::mma_bf16(tmem + kColO + 128u * (uint32_t)mb, ad, bd, idesc, kk ? 1u : 0u);
       }
     }
-    tc::mma_commit(bar);
+    tc::mma_commit(bar_pv);
   }
   __syncwarp();
-  ok = __all_sync(0xffffffffu, ok && tc::mbar_wait_bounded(bar, 1, s_abort, &g_attn_error));
+  const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, 0, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
-  // ---- partial O (unnormalised, fp32) and (max, sum) to the workspace ----
+  // ---- partial O = O_hi + O_lo (unnormalised, fp32) and (max, sum) to the workspace ----
   float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
   if (ok) {
     // warp w: channel lanes of quadrant w%4, channel block mb = w/4
-    for (int mbi = 0; mbi < 1; ++mbi) {
-      const int mb = warp >> 2;
-      const int c = mb * 128 + rq * 32 + lane;
-      for (int hh = 0; hh < kHeads; hh += 32) {
-        uint32_t r[32];
-        tc::tmem_ld_32x32b_x32(tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)mb + (uint32_t)hh, r);
-        tc::tmem_ld_wait();
+    const int mb = warp >> 2;
+    const int c = mb * 128 + rq * 32 + lane;
+    const uint32_t base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 128u * (uint32_t)mb;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) po[(hh + j) * kHeadDim + c] = __uint_as_float(r[j]);
-      }
+    for (int hh = 0; hh < kHeads; hh += 32) {
+      uint32_t rh[32], rl[32];
+      tc::tmem_ld_32x32b_x32(base + (uint32_t)hh, rh);
+      tc::tmem_ld_32x32b_x32(base + (uint32_t)(kHeads + hh), rl);
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) po[(hh + j) * kHeadDim + c] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
     }
   }
   if (tid < kHeads) {

@@ -405,6 +405,8 @@ size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k,
  *   out [B][L][64][512] bf16; out_f32 (nullable) the same before the bf16
  *   rounding; lse (nullable) [B][L][64] natural-log sum of exp(S), -inf for
  *   a query with no rows (its output is 0).
+ *   k + n_swa <= 5120. q, swa and out_f32 16-byte aligned, out 8-byte
+ *   aligned, the planes as in the conventions above.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, WORKSPACE, CUDA.
  */
 int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
