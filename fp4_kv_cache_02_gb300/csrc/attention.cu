@@ -14,6 +14,7 @@
 // second kernel merges the chunks of a query in fixed chunk order, so results
 // are deterministic. The chunk size (32 .. 160 rows) is picked per launch so
 // that the CTAs fill the SMs in as few waves as possible.
+#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
@@ -41,72 +42,102 @@ struct AttnArgs {
   float* part_o;            // [n_q][n_split][64][512]
   float* part_ml;           // [n_q][n_split][64][2]
   int32_t q0;               // first query of this launch
+  int32_t fused;            // the n_split CTAs of a query form a cluster and merge in shared memory
+  uint16_t* out;            // [n_q][64][512] bf16 (fused path)
+  float* out_f32;           // nullable (fused path)
+  float* lse;               // nullable (fused path)
 };
 
 constexpr int kMaxSplitCombine = 32;
 
-// grid (n_q_in_launch, 8), block 256: merge the splits of 8 heads of one
-// query, in fixed split order.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float* __restrict__ part_o,
-                                                           const float* __restrict__ part_ml, int32_t n_split,
-                                                           int32_t q0, uint16_t* __restrict__ out,
-                                                           float* __restrict__ out_f32, float* __restrict__ lse) {
+// grid (n_q_in_launch, 8), block 512: merge the splits of 8 heads of one
+// query, in fixed split order. Thread t owns the float4 columns t and t + 512
+// of the CTA's [8 heads][512] output; it issues the loads of its first batch of
+// splits before the (max, sum) of the splits are read and turned into weights.
+constexpr int kCombineThreads = 512;
+__global__ void __launch_bounds__(kCombineThreads) attn_combine_kernel(const float* __restrict__ part_o,
+                                                                       const float* __restrict__ part_ml,
+                                                                       int32_t n_split, int32_t q0,
+                                                                       uint16_t* __restrict__ out,
+                                                                       float* __restrict__ out_f32,
+                                                                       float* __restrict__ lse) {
   pdl_begin();
   constexpr int kHeadsPerCta = 8;
+  constexpr int kBatch = 8;                      // splits loaded together
+  constexpr int kItems = kHeadsPerCta * kHeadDim / 4 / kCombineThreads;  // 2 float4 per thread
+  __shared__ float ml_s[kMaxSplitCombine][kHeadsPerCta][2];
   __shared__ float scale_s[kHeadsPerCta][kMaxSplitCombine];
   __shared__ float inv_l[kHeadsPerCta];
   const int lq = blockIdx.x;
   const int qi = q0 + lq;
   const int h0 = blockIdx.y * kHeadsPerCta;
   const int tid = threadIdx.x;
-  if (tid < kHeadsPerCta) {
-    const int h = h0 + tid;
-    float M = -INFINITY;
-    for (int s = 0; s < n_split; ++s) {
-      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + h) * 2;
-      if (ml[1] > 0.0f) M = fmaxf(M, ml[0]);
-    }
-    float Lsum = 0.0f;
-    for (int s = 0; s < n_split; ++s) {
-      const float* ml = part_ml + (((int64_t)lq * n_split + s) * kHeads + h) * 2;
-      const float f = (ml[1] > 0.0f) ? expf(ml[0] - M) : 0.0f;
-      scale_s[tid][s] = f;
-      Lsum += ml[1] * f;
-    }
-    inv_l[tid] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-    if (lse) lse[(int64_t)qi * kHeads + h] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
-  }
-  __syncthreads();
-  // each float4 of the output: the loads of all splits go out together (up to
-  // 8 at a time), so a thread waits on L2 once per output, not once per split
-  constexpr int kBatch = 8;
-  for (int i = tid; i < kHeadsPerCta * kHeadDim / 4; i += blockDim.x) {
-    const int hl = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
-    const int h = h0 + hl;
-    const float* base = part_o + ((int64_t)lq * n_split * kHeads + h) * kHeadDim + c4 * 4;
-    const int64_t split_stride = (int64_t)kHeads * kHeadDim;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < n_split; s0 += kBatch) {
-      float4 v[kBatch];
+  const int64_t split_stride = (int64_t)kHeads * kHeadDim;
+  const float* qbase = part_o + (int64_t)lq * n_split * split_stride + (int64_t)h0 * kHeadDim;
+  float4 v[kItems][kBatch];
+  auto load_batch = [&](int s0) {
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int i = tid + u * kCombineThreads;  // [hl][c4] within the CTA's heads
 #pragma unroll
       for (int j = 0; j < kBatch; ++j)
-        v[j] = s0 + j < n_split ? *reinterpret_cast<const float4*>(base + (s0 + j) * split_stride)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u][j] = s0 + j < n_split ? *reinterpret_cast<const float4*>(qbase + (s0 + j) * split_stride + i * 4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_batch(0);
+  if (tid < n_split * kHeadsPerCta) {
+    const int sp = tid / kHeadsPerCta, hl = tid % kHeadsPerCta;
+    const float2 ml = *reinterpret_cast<const float2*>(part_ml + (((int64_t)lq * n_split + sp) * kHeads + h0 + hl) * 2);
+    ml_s[sp][hl][0] = ml.x;
+    ml_s[sp][hl][1] = ml.y;
+  }
+  __syncthreads();
+  if (tid < kHeadsPerCta) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < n_split; ++sp)
+      if (ml_s[sp][tid][1] > 0.0f) M = fmaxf(M, ml_s[sp][tid][0]);
+    float Lsum = 0.0f;
+    for (int sp = 0; sp < n_split; ++sp) {
+      const float f = ml_s[sp][tid][1] > 0.0f ? expf(ml_s[sp][tid][0] - M) : 0.0f;
+      scale_s[tid][sp] = f;
+      Lsum += ml_s[sp][tid][1] * f;
+    }
+    inv_l[tid] = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+    if (lse) lse[(int64_t)qi * kHeads + h0 + tid] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
+  }
+  __syncthreads();
+  float4 acc[kItems];
+#pragma unroll
+  for (int u = 0; u < kItems; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < n_split; s0 += kBatch) {
+    if (s0 > 0) load_batch(s0);
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int hl = (tid + u * kCombineThreads) / (kHeadDim / 4);
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         if (s0 + j >= n_split) break;
         const float f = scale_s[hl][s0 + j];  // fixed split order
-        if (f == 0.0f) continue;
-        acc.x = fmaf(v[j].x, f, acc.x); acc.y = fmaf(v[j].y, f, acc.y);
-        acc.z = fmaf(v[j].z, f, acc.z); acc.w = fmaf(v[j].w, f, acc.w);
+        acc[u].x = fmaf(v[u][j].x, f, acc[u].x);
+        acc[u].y = fmaf(v[u][j].y, f, acc[u].y);
+        acc[u].z = fmaf(v[u][j].z, f, acc[u].z);
+        acc[u].w = fmaf(v[u][j].w, f, acc[u].w);
       }
     }
+  }
+#pragma unroll
+  for (int u = 0; u < kItems; ++u) {
+    const int i = tid + u * kCombineThreads;
+    const int hl = i / (kHeadDim / 4), c4 = i % (kHeadDim / 4);
     const float il = inv_l[hl];
-    acc.x *= il; acc.y *= il; acc.z *= il; acc.w *= il;
-    const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4 * 4;
-    if (out_f32) *reinterpret_cast<float4*>(out_f32 + o) = acc;
-    __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(out + o) = make_uint2(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1));
+    float4 r = acc[u];
+    r.x *= il; r.y *= il; r.z *= il; r.w *= il;
+    const int64_t o = ((int64_t)qi * kHeads + h0 + hl) * kHeadDim + c4 * 4;
+    if (out_f32) *reinterpret_cast<float4*>(out_f32 + o) = r;
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(r.x, r.y), b1 = __floats2bfloat162_rn(r.z, r.w);
+    *reinterpret_cast<uint2*>(out + o) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
   }
 }
 
@@ -155,49 +186,113 @@ static int sm_count() {
   return count[dev];
 }
 
-// Rows per chunk for n_q queries of `total` rows each: the multiple of 32 (at
-// most 160) with the smallest estimated time = waves x (fixed + per-row cost)
-// plus the combine's per-split cost. The costs are the kernel's measured phase
-// times on GB300 (about 7.5 us per CTA plus 0.047 us per row).
-static int attn_rows(int32_t n_q, int32_t total) {
-  if (total <= 0) return 32;
+static constexpr int kMaxClusterSplit = attn_tc::kMaxClusterChunks;  // portable cluster size
+
+// Opts the partial kernel into its dynamic shared memory, once per device.
+static int attn_kernel_attr() {
+  constexpr int kMaxDevices = 64;
+  static bool done[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
+  if (!done[dev]) {
+    if (cudaFuncSetAttribute(attn_tc::attn_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_tc::kSmemBytes) != cudaSuccess)
+      return CSA2_ERR_CUDA;
+    done[dev] = true;
+  }
+  return CSA2_OK;
+}
+
+// How many clusters of `size` partial CTAs can be resident at once (0 when a
+// cluster of that size cannot run), cached per device.
+static int attn_max_clusters(int size) {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices][kMaxClusterSplit + 1];
+  static bool filled[kMaxDevices][kMaxClusterSplit + 1];
+  int dev = 0;
+  if (size < 1 || size > kMaxClusterSplit) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!filled[dev][size]) {
+    int n = 0;
+    if (attn_kernel_attr() == CSA2_OK) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)size, 1, 1);
+      cfg.blockDim = dim3(attn_tc::kThreads);
+      cfg.dynamicSmemBytes = attn_tc::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)size;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, (void*)attn_tc::attn_partial_tc_kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+      }
+    }
+    cache[dev][size] = n;
+    filled[dev][size] = true;
+  }
+  return cache[dev][size];
+}
+
+struct AttnPlan {
+  int rows;    // rows per chunk
+  int splits;  // chunks per query
+  bool fused;  // chunks of a query form a cluster and merge in shared memory
+};
+
+// The chunking of n_q queries of `total` rows each: rows per chunk a multiple
+// of 32 (at most 160), merged either inside a cluster (at most 8 chunks) or by
+// the combine kernel, whichever has the smaller estimated time = waves x
+// (fixed + per-row cost) + merge cost. The costs are the kernels' measured
+// times on GB300: about 7.5 us per CTA plus 0.047 us per row; the cluster
+// merge about 2.5 us plus 0.6 us per chunk (it waits for the slowest chunk of
+// the cluster); the combine kernel about 6 us plus 0.05 us per chunk.
+static AttnPlan attn_plan(int32_t n_q, int32_t total) {
+  AttnPlan best_plan{-1, 0, false};
+  if (total <= 0) return AttnPlan{32, 1, false};
   const int n_sm = sm_count();
   double best = 1e300;
-  int best_rows = -1;
   for (int rows = 32; rows <= attn_tc::kMaxRows; rows += 32) {
     const int splits = (total + rows - 1) / rows;
     if (splits > kMaxSplit) continue;
-    const int64_t ctas = (int64_t)n_q * splits;
-    const int64_t waves = (ctas + n_sm - 1) / n_sm;
-    const double t = (double)waves * (7.5 + 0.047 * rows) + 0.05 * splits;
+    const double cta = 7.5 + 0.047 * rows;
+    const int64_t waves = ((int64_t)n_q * splits + n_sm - 1) / n_sm;
+    const double t = (double)waves * cta + 6.0 + 0.05 * splits;
     if (t < best - 1e-9) {
       best = t;
-      best_rows = rows;
+      best_plan = AttnPlan{rows, splits, false};
+    }
+    const int clusters = splits <= kMaxClusterSplit ? attn_max_clusters(splits) : 0;
+    if (clusters > 0) {
+      const int64_t cwaves = ((int64_t)n_q + clusters - 1) / clusters;
+      const double tc_ = (double)cwaves * (cta + 2.5 + 0.6 * splits);
+      if (tc_ < best - 1e-9) {
+        best = tc_;
+        best_plan = AttnPlan{rows, splits, true};
+      }
     }
   }
-  return best_rows;
+  return best_plan;
 }
 
 static inline int attn_queries_per_launch(int32_t n_queries) {
   return n_queries < kQueriesPerLaunch ? n_queries : kQueriesPerLaunch;
 }
 
-// splits per query; 0 when k + n_swa needs more than kMaxSplit chunks
-static inline int attn_splits(int32_t n_queries, int32_t k, int32_t n_swa, int* rows_out) {
-  const int32_t total = k + n_swa;
-  const int rows = attn_rows(attn_queries_per_launch(n_queries), total);
-  if (rows < 0) return 0;
-  if (rows_out) *rows_out = rows;
-  const int splits = (total + rows - 1) / rows;
-  return splits < 1 ? 1 : splits;
+static inline AttnPlan attn_plan_for(int32_t n_queries, int32_t k, int32_t n_swa) {
+  return attn_plan(attn_queries_per_launch(n_queries), k + n_swa);
 }
 
 extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, int32_t n_swa) {
   if (n_queries <= 0 || k < 0 || n_swa < 0) return 0;
   // partials are indexed by query within one launch of at most kQueriesPerLaunch
   int32_t nq = attn_queries_per_launch(n_queries);
-  int ns = attn_splits(n_queries, k, n_swa, nullptr);
-  if (ns < 1) ns = 1;
+  const AttnPlan plan = attn_plan_for(n_queries, k, n_swa);
+  if (plan.fused) return 256;  // the chunks merge in shared memory
+  int ns = plan.splits < 1 ? 1 : plan.splits;
   size_t o = (size_t)nq * ns * kHeads * kHeadDim * 4;
   o = (o + 255) / 256 * 256;
   return o + (size_t)nq * ns * kHeads * 2 * 4;
@@ -205,8 +300,14 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, 
 
 static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, float* lse, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
-  a.n_split = attn_splits(n_q, a.k, a.n_swa, &a.rows);
-  if (a.n_split < 1 || a.n_split > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  const AttnPlan plan = attn_plan_for(n_q, a.k, a.n_swa);
+  if (plan.rows < 0 || plan.splits < 1 || plan.splits > kMaxSplit) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  a.n_split = plan.splits;
+  a.rows = plan.rows;
+  a.fused = plan.fused ? 1 : 0;
+  a.out = out;
+  a.out_f32 = out_f32;
+  a.lse = lse;
   size_t need = csa2_sparse_attn_workspace_size(n_q, a.k, a.n_swa);
   if (!ws || ws_bytes < need || !csa2_aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
   int32_t nq_ws = attn_queries_per_launch(n_q);
@@ -214,13 +315,7 @@ static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, f
   o_bytes = (o_bytes + 255) / 256 * 256;
   a.part_o = (float*)ws;
   a.part_ml = (float*)((char*)ws + o_bytes);
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_tc::attn_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attn_tc::kSmemBytes) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    attr = true;
-  }
+  if (attn_kernel_attr() != CSA2_OK) return CSA2_ERR_CUDA;
   // Q rows of all queries as a 2-D bf16 tensor [n_q * 64][512], loaded in
   // [64 heads][64 channels] boxes with the 128-byte swizzle the MMA reads.
   auto encode = tensor_map_encoder();
@@ -237,10 +332,19 @@ static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, f
   for (int32_t q0 = 0; q0 < n_q; q0 += kQueriesPerLaunch) {
     int32_t nq = n_q - q0 < kQueriesPerLaunch ? n_q - q0 : kQueriesPerLaunch;
     a.q0 = q0;
-    CSA2_LAUNCH_PDL(attn_tc::attn_partial_tc_kernel, dim3((unsigned)a.n_split, (unsigned)nq), dim3(attn_tc::kThreads),
-                    (size_t)attn_tc::kSmemBytes, stream, qmap, a);
-    CSA2_LAUNCH_PDL(attn_combine_kernel, dim3((unsigned)nq, kHeads / 8), dim3(256), 0, stream, a.part_o, a.part_ml,
-                    a.n_split, q0, out, out_f32, lse);
+    if (a.fused) {
+      if (csa2_launch_pdl_cluster(attn_tc::attn_partial_tc_kernel, dim3((unsigned)a.n_split, (unsigned)nq),
+                                  dim3(attn_tc::kThreads), (size_t)attn_tc::kSmemBytes, stream, (unsigned)a.n_split,
+                                  qmap, a) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return CSA2_ERR_CUDA;
+      }
+    } else {
+      CSA2_LAUNCH_PDL(attn_tc::attn_partial_tc_kernel, dim3((unsigned)a.n_split, (unsigned)nq),
+                      dim3(attn_tc::kThreads), (size_t)attn_tc::kSmemBytes, stream, qmap, a);
+      CSA2_LAUNCH_PDL(attn_combine_kernel, dim3((unsigned)nq, kHeads / 8), dim3(kCombineThreads), 0, stream, a.part_o,
+                      a.part_ml, a.n_split, q0, out, out_f32, lse);
+    }
   }
   return CSA2_OK;
 }

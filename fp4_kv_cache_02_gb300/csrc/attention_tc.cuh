@@ -23,8 +23,12 @@
 //   4. O^T[c][n] = sum_t R[t][c] P[n][t] on the tensor cores (M = 128 channels
 //      x 4 blocks, N = 128, K = rows), reading the same R tile as an MN-major
 //      operand; O = O_hi + O_lo when read back;
-//   5. the unnormalised partial O and the chunk's (max, sum) per head go to the
-//      workspace; attn_combine_kernel merges the chunks in fixed order.
+//   5. the chunks of a query merge: when they form one thread-block cluster
+//      (at most 8 chunks) each scales its O by exp(m - M) / L into its shared
+//      memory and each rank sums a slice of the heads over the cluster in rank
+//      order through distributed shared memory, writing the output directly;
+//      otherwise the unnormalised partial O and (max, sum) go to the workspace
+//      and attn_combine_kernel merges the chunks in the same fixed order.
 #pragma once
 
 #include "tc_common.cuh"
@@ -33,6 +37,7 @@ namespace csa2 {
 namespace attn_tc {
 
 constexpr int kMaxRows = 160;   // rows per CTA: a multiple of 32, at most 160
+constexpr int kMaxClusterChunks = 8;  // chunks of a query merged inside one cluster
 constexpr int kThreads = 512;   // 16 warps: 4 TMEM lane quadrants x 4
 constexpr int kBlkR = kMaxRows * 128;                     // one 64-channel block of R: [160 t][128 B]
 constexpr int kOffR = 0;                                  // 8 blocks                        = 160 KiB
@@ -101,7 +106,9 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
-  pdl_begin();
+  // barriers, tensor memory and the E4M3 table need nothing from the preceding
+  // kernel; its outputs (the indices, possibly Q) are read after pdl_wait()
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
@@ -135,15 +142,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(q_bar, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
-    tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
-    for (int blk = 0; blk < 4; ++blk)
-      tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   if (tid < 256) {
     const uint32_t byte = (uint32_t)tid;
     __nv_bfloat16 e = __float2bfloat16_rn(e4m3_to_f32(byte));  // exact (4 significant bits)
     lut_e4m3[byte] = *reinterpret_cast<uint16_t*>(&e);
+  }
+  pdl_wait();
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
+    for (int blk = 0; blk < 4; ++blk)
+      tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
   }
   // ---- rows of this chunk: position (or SWA row), validity ----
   const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
@@ -396,27 +406,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, 0, s_abort, &g_attn_error));
   tc::tc_fence_after();
 
-  // ---- partial O = O_hi + O_lo (unnormalised, fp32) and (max, sum) to the workspace ----
-  float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
-  if (ok) {
-    // warp w: channel lanes of quadrant w%4, channel block mb = w/4
-    const int mb = warp >> 2;
-    const int c = mb * 128 + rq * 32 + lane;
-    const uint32_t base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 128u * (uint32_t)mb;
+  // warp w reads the O^T lanes of quadrant w%4 in channel block mb = w/4
+  const int mb = warp >> 2;
+  const int c_own = mb * 128 + rq * 32 + lane;
+  const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 128u * (uint32_t)mb;
+  if (a.fused) {
+    // ---- merge inside the cluster of this query's chunks (rank = split) ----
+    // each chunk stores its unnormalised O as [h][c] fp32 in its own shared
+    // memory; after one cluster barrier every CTA reads all chunks' (m, l),
+    // forms the weights exp(m_j - M) / L, and rank r sums heads
+    // [64r/n, 64(r+1)/n) over the chunks in fixed order, writing the output.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int nsp = a.n_split;
+    const int rank = (int)cl.block_rank();
+    __shared__ float w_s[kMaxClusterChunks][kHeads];   // m_j, then the weights
+    __shared__ float f_l[kMaxClusterChunks][kHeads];   // l_j
+    float* o_s = reinterpret_cast<float*>(sR);  // 128 KiB of the R tile, free after the PV product
 #pragma unroll
     for (int hh = 0; hh < kHeads; hh += 32) {
       uint32_t rh[32], rl[32];
-      tc::tmem_ld_32x32b_x32(base + (uint32_t)hh, rh);
-      tc::tmem_ld_32x32b_x32(base + (uint32_t)(kHeads + hh), rl);
-      tc::tmem_ld_wait();
+      if (ok) {
+        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, rh);
+        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)(kHeads + hh), rl);
+        tc::tmem_ld_wait();
+      }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) po[(hh + j) * kHeadDim + c] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+      for (int j = 0; j < 32; ++j)
+        o_s[(hh + j) * kHeadDim + c_own] = ok ? __uint_as_float(rh[j]) + __uint_as_float(rl[j]) : 0.0f;
     }
-  }
-  if (tid < kHeads) {
-    float* ml = a.part_ml + (((int64_t)lq * a.n_split + split) * kHeads + tid) * 2;
-    ml[0] = m_s[tid];
-    ml[1] = ok ? l_s[tid] : 0.0f;
+    if (tid < kHeads && !ok) l_s[tid] = 0.0f;
+    cl.sync();
+    // (m, l) of every chunk, one remote load each
+    if (tid < nsp * kHeads) {
+      const int j = tid / kHeads, h = tid % kHeads;
+      const float lj = *cl.map_shared_rank(&l_s[h], j);
+      const float mj = *cl.map_shared_rank(&m_s[h], j);
+      w_s[j][h] = lj > 0.0f ? mj : -INFINITY;
+      f_l[j][h] = lj;
+    }
+    __syncthreads();
+    if (tid < kHeads) {
+      float M = -INFINITY;
+      for (int j = 0; j < nsp; ++j) M = fmaxf(M, w_s[j][tid]);
+      float Lsum = 0.0f;
+      for (int j = 0; j < nsp; ++j)
+        if (f_l[j][tid] > 0.0f) Lsum += f_l[j][tid] * expf(w_s[j][tid] - M);
+      for (int j = 0; j < nsp; ++j)
+        w_s[j][tid] = (f_l[j][tid] > 0.0f && Lsum > 0.0f) ? expf(w_s[j][tid] - M) / Lsum : 0.0f;
+      if (rank == 0 && a.lse) a.lse[(int64_t)qi * kHeads + tid] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
+    }
+    __syncthreads();
+    const int h0 = kHeads * rank / nsp, h1 = kHeads * (rank + 1) / nsp;
+    for (int i = tid; i < (h1 - h0) * (kHeadDim / 4); i += kThreads) {
+      const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
+      float4 v[kMaxClusterChunks];
+#pragma unroll
+      for (int j = 0; j < kMaxClusterChunks; ++j)
+        if (j < nsp) v[j] = *reinterpret_cast<const float4*>(cl.map_shared_rank(o_s, j) + h * kHeadDim + c4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < kMaxClusterChunks; ++j) {   // fixed rank order
+        if (j >= nsp) break;
+        const float f = w_s[j][h];
+        acc.x = fmaf(v[j].x, f, acc.x);
+        acc.y = fmaf(v[j].y, f, acc.y);
+        acc.z = fmaf(v[j].z, f, acc.z);
+        acc.w = fmaf(v[j].w, f, acc.w);
+      }
+      const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4;
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(a.out + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+    }
+    cl.sync();  // the other ranks have finished reading this CTA's shared memory
+  } else {
+    // ---- partial O = O_hi + O_lo (unnormalised, fp32) and (max, sum) to the workspace ----
+    float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
+    if (ok) {
+#pragma unroll
+      for (int hh = 0; hh < kHeads; hh += 32) {
+        uint32_t rh[32], rl[32];
+        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, rh);
+        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)(kHeads + hh), rl);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          po[(hh + j) * kHeadDim + c_own] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
+      }
+    }
+    if (tid < kHeads) {
+      float* ml = a.part_ml + (((int64_t)lq * a.n_split + split) * kHeads + tid) * 2;
+      ml[0] = m_s[tid];
+      ml[1] = ok ? l_s[tid] : 0.0f;
+    }
   }
   tc::tc_fence_before();
   __syncthreads();

@@ -6,7 +6,7 @@
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
-                               uint32_t* hist, float* bmax, cudaStream_t stream);
+                               uint32_t* hist, float* bmax, int early_reads, cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -74,7 +74,7 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                    nullptr, nullptr, (cudaStream_t)stream);
+                                    nullptr, nullptr, 0, (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -124,7 +124,7 @@ extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, con
   rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist);
   if (rc) return rc;
   rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                  hist, bmax, s);
+                                  hist, bmax, 1, s);  // just after the workspace clear
   if (rc) return rc;
   rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);
   if (rc) return rc;

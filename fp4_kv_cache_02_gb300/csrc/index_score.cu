@@ -61,11 +61,13 @@ static int device_sm_count() {
 
 // Tensor-core scan of list entries 0..n_pos-1 of every sequence: cache
 // positions 0..n_pos-1 (TMA tiles) or, with a positions list, the listed ones
-// (gathered row by row).
+// (gathered row by row). early_reads: the kernel just before in the stream
+// writes nothing the scan reads (it only clears the Top-K workspace), so the
+// scan's loads may start before that kernel ends.
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
-                               uint32_t* hist, float* bmax, cudaStream_t stream) {
+                               uint32_t* hist, float* bmax, int early_reads, cudaStream_t stream) {
   if (n_pos == 0 || B == 0) return CSA2_OK;
   if (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)) return CSA2_ERR_ALIGNMENT;
   auto encode = tensor_map_encoder();
@@ -95,7 +97,7 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
     attr = true;
   }
   scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
-                      hist, positions ? nullptr : bmax};
+                      hist, positions ? nullptr : bmax, early_reads};
   CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)chunks, (unsigned)B), dim3(scan_tc::kThreads),
                   (size_t)scan_tc::kSmemBytes, stream, map, prm);
   return CSA2_OK;

@@ -66,11 +66,18 @@ struct Params {
   int32_t tiles_per_cta;
   uint32_t* hist;  // optional [B][kTopkHistBins] Top-K histogram (zeroed by the caller)
   float* bmax;     // optional [B][ceil(n_pos / 8)] block maxima for the candidate pool (dense mode)
+  // 1 when the preceding kernel in the stream writes only the workspace (the
+  // histogram clear): then the cache, q and positions are read at once and
+  // only the epilogue's writes wait for that kernel
+  int32_t early_reads;
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
     index_score_tc_kernel(const __grid_constant__ CUtensorMap tmap_ik, Params p) {
-  pdl_begin();
+  if (p.early_reads)
+    pdl_launch_dependents();
+  else
+    pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
@@ -245,6 +252,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     __syncwarp();
   } else {
     // ---- epilogue: warps 0..3, one key row per thread ----
+    if (p.early_reads) pdl_wait();  // the scores, maxima and histogram are written below
     float wr[kIdxHeads];
 #pragma unroll
     for (int h = 0; h < kIdxHeads; ++h) wr[h] = p.w[(int64_t)b * kIdxHeads + h];
@@ -302,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     tc::tmem_dealloc(tmem, kTmemCols);
   }
   if (with_hist) {
+    if (p.early_reads) pdl_wait();
     uint32_t* gh = p.hist + (int64_t)b * kTopkHistBins;
     for (int i = threadIdx.x; i < kTopkHistBins; i += kThreads)
       if (s_hist[i]) atomicAdd(&gh[i], s_hist[i]);
