@@ -83,6 +83,18 @@ def peaks():
     return 6800.0, "fallback"
 
 
+FP4_PER_BF16 = 13.5 / 2.25   # nominal dense FP4 : BF16 tensor rate
+
+
+def tensor_peak_tflops():
+    """(bf16 TFLOP/s of a kernel timed alone, its source)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -337,6 +349,7 @@ def run_gpu(args):
 
     # ---- the fused KV append, for its roofline and its decode latency ----
     app = measure_append(csa2, torch, B, device, args.steps, flush_l2, stream)
+    pre = measure_prefill(csa2, torch, device, max(3, min(args.steps, 10)), flush_l2, stream) if args.prefill else None
 
     # ---- end to end: per-step inputs from pinned host memory, outputs back ----
     # Each step copies its inputs host -> device and its outputs (attention
@@ -475,6 +488,21 @@ def run_gpu(args):
         "gpu_launches": args.steps * n_launches,
         "clocks": clk.summary(),
     }
+    if pre is not None:
+        bf16_peak, bf16_kind = tensor_peak_tflops()
+        fp4_peak = bf16_peak * FP4_PER_BF16
+        sc_tf = pre["scan_flops"] / (pre["scan_ms"] * 1e-3) / 1e12
+        at_tf = pre["attn_flops"] / (pre["attn_ms"] * 1e-3) / 1e12
+        line["kernel_rooflines"]["prefill_index_score"] = {
+            "bound": "tensor", "achieved": round(sc_tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+            "frac": round(sc_tf / fp4_peak, 4), "ms": round(pre["scan_ms"], 4), "pairs": pre["pairs"],
+            "peak_kind": f"{bf16_kind} bf16 x {FP4_PER_BF16:g} (nominal FP4:BF16)",
+            "note": "4,096 queries at 126,976.., causal; 2 x 4,096 FLOP per (query, entry) pair"}
+        line["kernel_rooflines"]["prefill_attention_replay"] = {
+            "bound": "tensor", "achieved": round(at_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
+            "frac": round(at_tf / bf16_peak, 4), "ms": round(pre["attn_ms"], 4),
+            "peak_kind": f"{bf16_kind} bf16",
+            "note": "4,096 queries x (512 + 128 rows), Bounded-Replay cut at swa row 64; QK + PV FLOPs"}
     if not args.no_cpu_baseline and wid == WORKLOAD_ID:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if world > 1:
@@ -484,6 +512,58 @@ def run_gpu(args):
 
 APPEND_ENTRIES = 131072            # bulk append: entries per launch, over the batch
 APPEND_BYTES_PER_ENTRY = 512 * 2 + 128 * 2 + KV_BYTES_PER_ENTRY + IK_BYTES_PER_ENTRY   # bf16 in, packed out
+
+
+PREFILL_T, PREFILL_P0, PREFILL_REPLAY_ROW = 4096, 126976, 64
+
+
+def measure_prefill(csa2, torch, device, steps, flush_l2, stream):
+    """The prefill pair of kernels timed alone on the prefill workload (4,096
+    queries at positions 126,976 .. 131,071 of one sequence): the causal
+    indexer scan (4,096 MAC per query-entry pair, FP4 tensor cores) and the
+    sparse attention with the Bounded-Replay cut (512 selected + 128 SWA rows
+    per query; QK and PV on bf16 tensor cores)."""
+    from fp4_kv_cache_02_gb300.inputs import device_normal, device_uniform
+    T, p0, W, K = PREFILL_T, PREFILL_P0, 128, 512
+    N = p0 + T
+    q_data, q_sc = csa2.quant_mxfp4(device_normal((T, 32, 128), 71, device))
+    w = device_uniform((T, 32), 72, device).float().contiguous()
+    ik_data, ik_sc = csa2.quant_mxfp4(device_normal((N, 128), 73, device))
+    scores = torch.empty(T, N, dtype=torch.float32, device=device)
+    kv_data, kv_sc = csa2.pack_kv_fp4(device_normal((N, 512), 74, device))
+    Q = device_normal((T, 64, 512), 75, device, scale=1.0 / math.sqrt(512))
+    swa = csa2.pack_fp8(device_normal((T + W - 1, 512), 76, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(77)
+    lim = torch.arange(p0 + 1, p0 + T + 1, device=device, dtype=torch.float64)[:, None]
+    idx = (torch.rand(T, K, generator=g, device=device, dtype=torch.float64) * lim).to(torch.int32).contiguous()
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device=device)
+    aws = csa2.attn_workspace(T, K, W, device=device)
+
+    def timed(fn, n):
+        tot = 0.0
+        for _ in range(n):
+            flush_l2()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b_.record(stream)
+            b_.synchronize()
+            tot += a.elapsed_time(b_)
+        return tot / n
+
+    scan = lambda: csa2.csa2_prefill_index_score(q_data, q_sc, w, ik_data, ik_sc, p0, scores, stream=stream)
+    attn = lambda: csa2.csa2_sparse_attn_prefill_replay(Q, kv_data, kv_sc, idx, swa, W, PREFILL_REPLAY_ROW, out, aws,
+                                                        stream=stream)
+    timed(scan, 2)
+    scan_ms = timed(scan, steps)
+    timed(attn, 2)
+    attn_ms = timed(attn, steps)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    pairs = T * p0 + T * (T + 1) // 2
+    return {"scan_ms": scan_ms, "scan_flops": 2 * 4096 * pairs, "pairs": pairs,
+            "attn_ms": attn_ms, "attn_flops": 2 * 2 * T * 64 * (K + W) * 512}
 
 
 def measure_append(csa2, torch, B, device, steps, flush_l2, stream):
@@ -623,6 +703,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph of the step")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="skip the prefill scan and attention timings reported beside the decode step")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 4],

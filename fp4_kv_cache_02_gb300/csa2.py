@@ -83,6 +83,8 @@ def _load():
                                                    vp, vp, vp, vp, sz, vp]),
         "csa2_sparse_attn_prefill": (ctypes.c_int, [vp, i32, vp, vp, i64, vp, i32, vp, i32, f32, vp, vp,
                                                     vp, vp, sz, vp]),
+        "csa2_sparse_attn_prefill_replay": (ctypes.c_int, [vp, i32, vp, vp, i64, vp, i32, vp, i32, i32, f32, vp,
+                                                           vp, vp, vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -339,6 +341,22 @@ def csa2_sparse_attn_prefill(q, kv_data, kv_scale, idx, swa, n_swa, out, workspa
     k = idx.shape[1]
     _call("csa2_sparse_attn_prefill", _p(q), T, _p(kv_data), _p(kv_scale), n_entries, _p(idx), k, _p(swa), n_swa,
           float(sm_scale), _p(out), _p(out_f32), _p(lse), _p(workspace), workspace.numel(), _s(stream))
+
+
+def csa2_sparse_attn_prefill_replay(q, kv_data, kv_scale, idx, swa, n_swa, replay_row, out, workspace, out_f32=None,
+                                    lse=None, sm_scale=1.0, stream=None):
+    """csa2_sparse_attn_prefill with the Bounded-Replay cut: query t uses swa
+    rows max(t, replay_row) .. t + n_swa - 1."""
+    _req(q, torch.bfloat16, "q"); _req(kv_data, torch.uint8, "kv_data"); _req(kv_scale, torch.uint8, "kv_scale")
+    _req(idx, torch.int32, "idx"); _req(out, torch.bfloat16, "out"); _req(workspace, torch.uint8, "workspace")
+    _req(swa, torch.uint8, "swa", allow_none=True)
+    _req(out_f32, torch.float32, "out_f32", allow_none=True); _req(lse, torch.float32, "lse", allow_none=True)
+    T = q.shape[0]
+    n_entries = kv_data.shape[0]
+    k = idx.shape[1]
+    _call("csa2_sparse_attn_prefill_replay", _p(q), T, _p(kv_data), _p(kv_scale), n_entries, _p(idx), k, _p(swa),
+          n_swa, int(replay_row), float(sm_scale), _p(out), _p(out_f32), _p(lse), _p(workspace), workspace.numel(),
+          _s(stream))
 
 
 # ---- allocating helpers (torch memory plumbing + the entry points above) --------

@@ -36,6 +36,7 @@ struct AttnArgs {
   const uint8_t* swa;       // SWA bytes
   int64_t swa_q_stride;     // bytes between consecutive queries' windows
   int32_t n_swa;
+  int32_t swa_first_row;    // prefill: SWA rows before this row of the array are masked (Bounded Replay)
   float sm_scale;
   int32_t n_split;
   int32_t rows;             // rows per chunk (a multiple of 32, at most 160)
@@ -375,17 +376,18 @@ extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
   a.swa = swa;
   a.swa_q_stride = (int64_t)n_swa * kHeadDim;
   a.n_swa = n_swa;
+  a.swa_first_row = INT32_MIN;  // decode windows are never truncated
   a.sm_scale = sm_scale;
   return launch_attn(a, B * L, (uint16_t*)out_bf16, out_f32, lse, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
-extern "C" int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T, const uint8_t* kv_data,
-                                        const uint8_t* kv_scale, int64_t n_entries, const int32_t* idx, int32_t k,
-                                        const uint8_t* swa, int32_t n_swa, float sm_scale, void* out_bf16,
-                                        float* out_f32, float* lse, void* workspace, size_t workspace_bytes,
-                                        csa2_stream_t stream) {
+extern "C" int csa2_sparse_attn_prefill_replay(const void* q_bf16, int32_t T, const uint8_t* kv_data,
+                                               const uint8_t* kv_scale, int64_t n_entries, const int32_t* idx,
+                                               int32_t k, const uint8_t* swa, int32_t n_swa, int32_t replay_row,
+                                               float sm_scale, void* out_bf16, float* out_f32, float* lse,
+                                               void* workspace, size_t workspace_bytes, csa2_stream_t stream) {
   if (!q_bf16 || !kv_data || !kv_scale || !idx || !out_bf16) return CSA2_ERR_INVALID_ARG;
-  if (T < 0 || k < 0 || n_swa < 0 || n_entries < 0) return CSA2_ERR_INVALID_ARG;
+  if (T < 0 || k < 0 || n_swa < 0 || n_entries < 0 || replay_row < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
   if (k > CSA2_MAX_TOPK || n_swa > 512 || k + n_swa > kMaxSplit * attn_tc::kMaxRows)
     return CSA2_ERR_UNSUPPORTED_SHAPE;
@@ -406,6 +408,16 @@ extern "C" int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T, const uin
   a.swa = swa;
   a.swa_q_stride = kHeadDim;  // query t uses rows t .. t + n_swa - 1
   a.n_swa = n_swa;
+  a.swa_first_row = replay_row;
   a.sm_scale = sm_scale;
   return launch_attn(a, T, (uint16_t*)out_bf16, out_f32, lse, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+extern "C" int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T, const uint8_t* kv_data,
+                                        const uint8_t* kv_scale, int64_t n_entries, const int32_t* idx, int32_t k,
+                                        const uint8_t* swa, int32_t n_swa, float sm_scale, void* out_bf16,
+                                        float* out_f32, float* lse, void* workspace, size_t workspace_bytes,
+                                        csa2_stream_t stream) {
+  return csa2_sparse_attn_prefill_replay(q_bf16, T, kv_data, kv_scale, n_entries, idx, k, swa, n_swa, 0, sm_scale,
+                                         out_bf16, out_f32, lse, workspace, workspace_bytes, stream);
 }

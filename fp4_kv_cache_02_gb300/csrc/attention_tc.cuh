@@ -173,8 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (t < a.k + a.n_swa) {
-      valid = 2;                                       // SWA row
-      src = (int64_t)qi * a.swa_q_stride + (int64_t)(t - a.k) * kHeadDim;
+      // SWA row; in prefill row j of query qi is row qi + j of the array, and
+      // rows before swa_first_row lie before a Bounded Replay start
+      if ((int64_t)qi + (t - a.k) >= (int64_t)a.swa_first_row) {
+        valid = 2;
+        src = (int64_t)qi * a.swa_q_stride + (int64_t)(t - a.k) * kHeadDim;
+      }
     }
     row_valid[tid] = valid;
     row_src[tid] = src;

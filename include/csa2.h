@@ -434,6 +434,27 @@ int csa2_sparse_attn_prefill(const void* q_bf16, int32_t T,
                              void* workspace, size_t workspace_bytes,
                              csa2_stream_t stream);
 
+/**
+ * Sparse prefill attention with the Bounded-Replay SWA mask (notes section 6:
+ * after the SWA cache of a prefix was evicted, only the last n_win tokens are
+ * replayed and the sliding window is cut at the replay start s, so the query
+ * at position i sees SWA positions [max(s, i - W + 1), i]).
+ *   As csa2_sparse_attn_prefill, with replay_row >= 0 the first row of the swa
+ *   array inside the replay segment: query t uses rows
+ *   max(t, replay_row) .. t + n_swa - 1. With swa row r holding position
+ *   p0 - (n_swa - 1) + r, replay_row = s - p0 + n_swa - 1 (0: no truncation).
+ * Errors: as csa2_sparse_attn_decode.
+ */
+int csa2_sparse_attn_prefill_replay(const void* q_bf16, int32_t T,
+                                    const uint8_t* kv_data,
+                                    const uint8_t* kv_scale, int64_t n_entries,
+                                    const int32_t* idx, int32_t k,
+                                    const uint8_t* swa, int32_t n_swa,
+                                    int32_t replay_row, float sm_scale,
+                                    void* out_bf16, float* out_f32, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    csa2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

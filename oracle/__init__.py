@@ -290,6 +290,15 @@ def sparse_attn(q, kv_data, kv_scale, idx, swa, sm_scale=1.0):
     return out, lse
 
 
+def bounded_replay_window(i, s, W):
+    """SWA positions visible to the query at position i when the SWA state is
+    rebuilt by Bounded Replay from position s ([B] 6): the sliding window of
+    the W most recent positions ending at i, cut at the replay start s.
+    Returns the half-open range (lo, hi) of positions, lo = max(s, i - W + 1),
+    hi = i + 1."""
+    return max(s, i - W + 1), i + 1
+
+
 def decode_batch(n_visible, q_data, q_e8m0, w, ik_data, ik_scale, kv_data, kv_scale,
                  Q, swa, k=512, sm_scale=1.0, n_threads=0):
     """Whole decode step for B sequences (score -> Top-k -> attention for the L

@@ -94,6 +94,38 @@ def test_decode_attention_is_deterministic(csa2):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("replay_row", [0, 5, 60, 140])
+def test_prefill_attention_with_bounded_replay_matches_oracle(csa2, replay_row):
+    """Query t at position i = N0 + t sees SWA positions [max(s, i - W + 1), i]
+    when the SWA state was replayed from s; swa row r holds position
+    N0 - (W - 1) + r, so the replay start maps to row replay_row."""
+    T, N0, k, W = 20, 1000, 64, 128
+    d = prefill_chunk(97, T, N0)
+    kvd, kvs = oracle.pack_kv_fp4(d["kv"])
+    swa = oracle.pack_fp8(d["swa"].reshape(-1)).reshape(T + W - 1, 512)
+    rng = np.random.default_rng(5)
+    idx = np.stack([rng.permutation(N0 + t + 1)[:k] for t in range(T)]).astype(np.int32)
+    idx[3, :] = -1                   # a query with SWA rows only (or, when cut away, no rows at all)
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty(T, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(T, 64, dtype=torch.float32, device="cuda")
+    csa2.csa2_sparse_attn_prefill_replay(dev(d["Q"]).to(torch.bfloat16), dev(kvd), dev(kvs), dev(idx), dev(swa), W,
+                                         replay_row, out, csa2.attn_workspace(T, k, W), out_f32=out32, lse=lse)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    o, l = out32.cpu().numpy(), lse.cpu().numpy()
+    s_pos = N0 - (W - 1) + replay_row
+    for t in range(T):
+        lo, hi = oracle.bounded_replay_window(N0 + t, s_pos, W)
+        rows = swa[lo - (N0 - (W - 1)):hi - (N0 - (W - 1))]
+        ref, ref_lse = oracle.sparse_attn(d["Q"][t], kvd, kvs, idx[t], rows if len(rows) else None)
+        if np.all(np.isneginf(ref_lse)):
+            assert np.all(o[t] == 0) and np.all(np.isneginf(l[t]))
+            continue
+        assert attn_row_error(o[t], ref) <= ATTN_ROW_TOL
+        np.testing.assert_allclose(l[t], ref_lse, rtol=1e-5, atol=1e-5)
+
+
 def test_prefill_attention_matches_oracle(csa2):
     T, N0, k, W = 5, 1000, 64, 128
     d = prefill_chunk(98, T, N0)

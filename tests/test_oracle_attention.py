@@ -115,3 +115,20 @@ def test_decode_batch_composes_score_topk_attention(orc):
         for l in range(L):
             o, _ = orc.sparse_attn(Q[b, l], kvd[b], kvs[b], ref_idx, swa[b, l])
             assert np.array_equal(out[b, l], o)
+
+
+# ---- Bounded Replay ([B] 6): the cut sliding window ------------------------------
+
+def test_bounded_replay_window_properties(orc):
+    W = 128
+    for i in range(0, 600, 7):
+        for s in range(0, i + 1, 5):
+            lo, hi = orc.bounded_replay_window(i, s, W)
+            vis = list(range(lo, hi))
+            assert vis[-1] == i                     # the query's own position is always visible
+            assert all(p >= s for p in vis)         # nothing before the replay start
+            assert len(vis) == min(W, i - s + 1)    # W positions unless the replay cut is closer
+    # a replay start far enough back leaves the plain sliding window
+    assert orc.bounded_replay_window(1000, 0, W) == (1000 - W + 1, 1001)
+    # replay starting at the query itself: only its own row
+    assert orc.bounded_replay_window(50, 50, W) == (50, 51)
