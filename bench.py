@@ -498,6 +498,18 @@ def run_gpu(args):
             "frac": round(sc_tf / fp4_peak, 4), "ms": round(pre["scan_ms"], 4), "pairs": pre["pairs"],
             "peak_kind": f"{bf16_kind} bf16 x {FP4_PER_BF16:g} (nominal FP4:BF16)",
             "note": "4,096 queries at 126,976.., causal; 2 x 4,096 FLOP per (query, entry) pair"}
+        cs_tf = pre["cscan_flops"] / (pre["cscan_ms"] * 1e-3) / 1e12
+        line["kernel_rooflines"]["prefill_index_score_compressed_m2"] = {
+            "bound": "tensor", "achieved": round(cs_tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+            "frac": round(cs_tf / fp4_peak, 4), "ms": round(pre["cscan_ms"], 4), "pairs": pre["cpairs"],
+            "peak_kind": f"{bf16_kind} bf16 x {FP4_PER_BF16:g} (nominal FP4:BF16)",
+            "note": "encoder Full layer: 4,096 queries at token 253,952.. over complete 2-token entries"}
+        cmp_gbs = pre["cmp_bytes"] / (pre["cmp_ms"] * 1e-3) / 1e9
+        line["kernel_rooflines"]["compress_kv_m2"] = {
+            "bound": "hbm", "achieved": round(cmp_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(cmp_gbs / hbm_peak, 4), "ms": round(pre["cmp_ms"], 4),
+            "algorithmic_bytes_per_launch": pre["cmp_bytes"], "entries_per_launch": pre["cmp_entries"],
+            "note": "262,144 tokens of C and Z (bf16) in, 131,072 packed 288-byte entries out"}
         line["kernel_rooflines"]["prefill_attention_replay"] = {
             "bound": "tensor", "achieved": round(at_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
             "frac": round(at_tf / bf16_peak, 4), "ms": round(pre["attn_ms"], 4),
@@ -555,15 +567,35 @@ def measure_prefill(csa2, torch, device, steps, flush_l2, stream):
     scan = lambda: csa2.csa2_prefill_index_score(q_data, q_sc, w, ik_data, ik_sc, p0, scores, stream=stream)
     attn = lambda: csa2.csa2_sparse_attn_prefill_replay(Q, kv_data, kv_sc, idx, swa, W, PREFILL_REPLAY_ROW, out, aws,
                                                         stream=stream)
+    # encoder Full layer at m = 2: the same 4,096 queries at token positions
+    # 253,952 .. see the complete compressed entries (126,976 .. 129,024 of them)
+    m, tok0 = 2, 2 * p0
+    cscan = lambda: csa2.csa2_prefill_index_score_compressed(q_data, q_sc, w, ik_data, ik_sc, tok0, m, scores,
+                                                               stream=stream)
     timed(scan, 2)
     scan_ms = timed(scan, steps)
     timed(attn, 2)
     attn_ms = timed(attn, steps)
+    timed(cscan, 2)
+    cscan_ms = timed(cscan, steps)
+    del scores
+    # the compressor: 262,144 tokens of C and Z (bf16) into 131,072 packed entries
+    n_tok = 2 * 131072
+    C = device_normal((n_tok, 512), 78, device)
+    Z = device_normal((n_tok, 512), 79, device)
+    bias = device_normal((m, 512), 80, device).float().contiguous()
+    cmp = lambda: csa2.csa2_compress_kv(C, Z, bias, m, kv_data, kv_sc, stream=stream)
+    timed(cmp, 2)
+    cmp_ms = timed(cmp, steps)
     torch.cuda.synchronize()
     assert csa2.csa2_get_last_error() == 0
     pairs = T * p0 + T * (T + 1) // 2
+    cpairs = sum((tok0 + t + 1) // m for t in range(T))
     return {"scan_ms": scan_ms, "scan_flops": 2 * 4096 * pairs, "pairs": pairs,
-            "attn_ms": attn_ms, "attn_flops": 2 * 2 * T * 64 * (K + W) * 512}
+            "attn_ms": attn_ms, "attn_flops": 2 * 2 * T * 64 * (K + W) * 512,
+            "cscan_ms": cscan_ms, "cscan_flops": 2 * 4096 * cpairs, "cpairs": cpairs,
+            "cmp_ms": cmp_ms, "cmp_bytes": n_tok * 2 * 512 * 2 + (n_tok // m) * KV_BYTES_PER_ENTRY,
+            "cmp_entries": n_tok // m}
 
 
 def measure_append(csa2, torch, B, device, steps, flush_l2, stream):

@@ -78,6 +78,8 @@ def _load():
         "csa2_index_topk": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp,
                                            vp, sz, vp]),
         "csa2_prefill_index_score": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, i64, vp, vp]),
+        "csa2_prefill_index_score_compressed": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, i64, i32, vp, vp]),
+        "csa2_compress_kv": (ctypes.c_int, [vp, vp, vp, i64, i32, vp, vp, vp, vp]),
         "csa2_sparse_attn_workspace_size": (sz, [i32, i32, i32]),
         "csa2_sparse_attn_decode": (ctypes.c_int, [vp, i32, i32, vp, vp, i64, vp, vp, i32, vp, i32, f32,
                                                    vp, vp, vp, vp, sz, vp]),
@@ -196,6 +198,17 @@ def csa2_kv_append(kv, ik, kv_data, kv_scale, ik_data, ik_scale, n_visible, n_vi
           kv_data.shape[1], _p(n_visible), _p(n_visible_out), _s(stream))
 
 
+def csa2_compress_kv(c, z, bias, m, kv_data, kv_scale, out=None, stream=None):
+    """c, z [n_tokens,512] bf16, bias [m,512] fp32 -> entries [n_tokens/m] packed
+    into kv_data [.,256] / kv_scale [.,32]; out [n_tokens/m,512] bf16 (optional)."""
+    _req(c, torch.bfloat16, "c"); _req(z, torch.bfloat16, "z"); _req(bias, torch.float32, "bias")
+    _req(kv_data, torch.uint8, "kv_data"); _req(kv_scale, torch.uint8, "kv_scale")
+    _req(out, torch.bfloat16, "out", allow_none=True)
+    n_tokens = c.numel() // 512
+    _call("csa2_compress_kv", _p(c), _p(z), _p(bias), n_tokens, int(m), _p(kv_data), _p(kv_scale), _p(out),
+          _s(stream))
+
+
 # ---- indexer, pool, Top-K -----------------------------------------------------
 
 def csa2_index_score(q_data, q_e8m0, w, ik_data, ik_scale, n_visible, scores, positions=None, stream=None):
@@ -308,6 +321,15 @@ def csa2_attn_merge(parts, lses, out, out_f32=None, lse_out=None, stream=None):
     R = parts.shape[0]
     n_q = parts[0].numel() // (HEADS * HEAD_DIM)
     _call("csa2_attn_merge", _p(parts), _p(lses), R, n_q, _p(out), _p(out_f32), _p(lse_out), _s(stream))
+
+
+def csa2_prefill_index_score_compressed(q_data, q_e8m0, w, ik_data, ik_scale, p0, m, scores, stream=None):
+    for t, n in ((q_data, "q_data"), (q_e8m0, "q_e8m0"), (ik_data, "ik_data"), (ik_scale, "ik_scale")):
+        _req(t, torch.uint8, n)
+    _req(w, torch.float32, "w"); _req(scores, torch.float32, "scores")
+    T, n_entries = scores.shape
+    _call("csa2_prefill_index_score_compressed", _p(q_data), _p(q_e8m0), _p(w), T, _p(ik_data), _p(ik_scale),
+          n_entries, int(p0), int(m), _p(scores), _s(stream))
 
 
 # ---- attention ------------------------------------------------------------------

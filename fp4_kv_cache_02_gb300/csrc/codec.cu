@@ -174,6 +174,67 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
   }
 }
 
+// ---- compressor: one warp per compressed entry --------------------------------
+// entry e of m tokens (rows em .. em+m-1): per channel c the weights are a
+// softmax over the block's tokens of Z[row][c] + bias[a][c], and the entry is
+// the weighted sum of C[row][c]; it is rounded to bf16 and packed like the
+// latent of csa2_kv_append. Lane l owns channels 16l .. 16l+15 (one E4M3 block).
+__global__ void __launch_bounds__(kAppendWarps * 32) compress_kv_kernel(
+    const uint16_t* __restrict__ C, const uint16_t* __restrict__ Z, const float* __restrict__ bias, int64_t n_out,
+    int32_t m, uint8_t* __restrict__ kv_data, uint8_t* __restrict__ kv_scale, uint16_t* __restrict__ out_bf16) {
+  pdl_begin();
+  const int lane = threadIdx.x & 31;
+  const int64_t e = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (e >= n_out) return;
+  const int c0 = lane * 16;
+  auto load16 = [&](const uint16_t* base, int64_t row, float (&v)[16]) {
+    const uint4* src = reinterpret_cast<const uint4*>(base + row * kHeadDim + c0);
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+      v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+  };
+  float mx[16], den[16], num[16], z[16], c[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) mx[i] = -INFINITY;
+  for (int a = 0; a < m; ++a) {
+    load16(Z, e * m + a, z);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mx[i] = fmaxf(mx[i], z[i] + bias[a * kHeadDim + c0 + i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) den[i] = num[i] = 0.0f;
+  for (int a = 0; a < m; ++a) {
+    load16(Z, e * m + a, z);
+    load16(C, e * m + a, c);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float wgt = expf(z[i] + bias[a * kHeadDim + c0 + i] - mx[i]);
+      den[i] += wgt;
+      num[i] = fmaf(wgt, c[i], num[i]);
+    }
+  }
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(num[2 * i] / den[2 * i], num[2 * i + 1] / den[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  if (out_bf16) {
+    uint4* dst = reinterpret_cast<uint4*>(out_bf16 + e * kHeadDim + c0);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  uint2 d;
+  uint8_t sc;
+  encode_kv_fp4_block(w, d, sc);
+  *reinterpret_cast<uint2*>(kv_data + e * kKvBytes + lane * 8) = d;
+  kv_scale[e * kKvScales + lane] = sc;
+}
+
 // In-place advance of the visible counts, after the append grid has finished
 // reading them (its programmatic dependency waits for the whole grid).
 __global__ void advance_visible_kernel(int32_t* __restrict__ n_visible, int32_t B, int32_t T, int64_t cap) {
@@ -287,5 +348,21 @@ extern "C" int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t 
                   n_visible, in_place ? (int32_t*)nullptr : n_visible_out);
   if (in_place)
     CSA2_LAUNCH_PDL(advance_visible_kernel, grid_for(B, 256), dim3(256), 0, s, n_visible_out, B, T, cap);
+  return CSA2_OK;
+}
+
+extern "C" int csa2_compress_kv(const void* c_bf16, const void* z_bf16, const float* bias, int64_t n_tokens,
+                                int32_t m, uint8_t* kv_data, uint8_t* kv_scale, void* out_bf16,
+                                csa2_stream_t stream) {
+  if (!c_bf16 || !z_bf16 || !bias || !kv_data || !kv_scale || n_tokens < 0 || m < 1) return CSA2_ERR_INVALID_ARG;
+  if (n_tokens % m) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  if (!csa2_aligned(c_bf16, 16) || !csa2_aligned(z_bf16, 16) || !csa2_aligned(kv_data, 8) ||
+      (out_bf16 && !csa2_aligned(out_bf16, 16)))
+    return CSA2_ERR_ALIGNMENT;
+  const int64_t n_out = n_tokens / m;
+  if (n_out == 0) return CSA2_OK;
+  CSA2_LAUNCH_PDL(compress_kv_kernel, grid_for(n_out, kAppendWarps), dim3(kAppendWarps * 32), 0,
+                  (cudaStream_t)stream, (const uint16_t*)c_bf16, (const uint16_t*)z_bf16, bias, n_out, m, kv_data,
+                  kv_scale, (uint16_t*)out_bf16);
   return CSA2_OK;
 }

@@ -103,11 +103,12 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
   return CSA2_OK;
 }
 
-extern "C" int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w,
-                                        int32_t T, const uint8_t* ik_data, const uint8_t* ik_scale,
-                                        int64_t n_entries, int64_t p0, float* scores, csa2_stream_t stream) {
+extern "C" int csa2_prefill_index_score_compressed(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w,
+                                                   int32_t T, const uint8_t* ik_data, const uint8_t* ik_scale,
+                                                   int64_t n_entries, int64_t p0, int32_t m, float* scores,
+                                                   csa2_stream_t stream) {
   if (!q_data || !q_e8m0 || !w || !ik_data || !ik_scale || !scores) return CSA2_ERR_INVALID_ARG;
-  if (T < 0 || n_entries < 0 || p0 < 0 || p0 + T > n_entries) return CSA2_ERR_INVALID_ARG;
+  if (T < 0 || n_entries < 0 || p0 < 0 || m < 1 || (p0 + T) / m > n_entries) return CSA2_ERR_INVALID_ARG;
   if (!csa2_aligned(ik_data, 16) || !csa2_aligned(ik_scale, 4) || !csa2_aligned(q_data, 16) ||
       !csa2_aligned(q_e8m0, 4) || !csa2_aligned(w, 4))
     return CSA2_ERR_ALIGNMENT;
@@ -141,8 +142,15 @@ extern "C" int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_
   }
   const int64_t tiles = (n_entries + kTileRows - 1) / kTileRows;
   dim3 grid((unsigned)((tiles + kChunkTiles - 1) / kChunkTiles), (unsigned)((T + kQBlock - 1) / kQBlock));
-  Params prm{q_e8m0, w, ik_scale, n_entries, p0, T, scores};
+  Params prm{q_e8m0, w, ik_scale, n_entries, p0, T, m, scores};
   prefill_score_tc_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(map_ik, map_q, prm);
   CSA2_CHECK_LAUNCH();
   return CSA2_OK;
+}
+
+extern "C" int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w,
+                                        int32_t T, const uint8_t* ik_data, const uint8_t* ik_scale,
+                                        int64_t n_entries, int64_t p0, float* scores, csa2_stream_t stream) {
+  return csa2_prefill_index_score_compressed(q_data, q_e8m0, w, T, ik_data, ik_scale, n_entries, p0, 1, scores,
+                                             stream);
 }

@@ -70,8 +70,9 @@ struct Params {
   const float* w;          // [T][32]
   const uint8_t* ik_scale; // [n_entries][4]
   int64_t n_entries;
-  int64_t p0;
+  int64_t p0;              // token position of query 0
   int32_t T;
+  int32_t m;               // tokens per entry: query t sees entries j < (p0 + t + 1) / m
   float* scores;           // [T][n_entries]
 };
 
@@ -115,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t tiles_all = (p.n_entries + kTileRows - 1) / kTileRows;
   // entries visible to the block's last query, in tiles
   const int64_t last_t = min((int64_t)t0 + kQBlock, (int64_t)p.T) - 1;
-  int64_t vis_tiles = (p.p0 + last_t) / kTileRows + 1;
+  const int64_t last_vis = (p.p0 + last_t + 1) / p.m;        // entries the last query sees
+  int64_t vis_tiles = (last_vis + kTileRows - 1) / kTileRows;
   if (vis_tiles > tiles_all) vis_tiles = tiles_all;
   const int64_t c0 = (int64_t)blockIdx.x * kChunkTiles;
   const int64_t c1 = min(c0 + kChunkTiles, tiles_all);
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = u / kGroups, g = u % kGroups;
       const int a = u % kAcc;
       const int64_t j = (c0 + i) * kTileRows + quad * 32 + lane;  // this thread's entry
+      const int64_t jm_last = j * p.m + (p.m - 1);                 // its last token
       // warp-uniform outcome: tcgen05.ld below needs the whole warp
       if (!__all_sync(0xffffffffu,
                       tc::mbar_wait_bounded(&acc_full[a], (uint32_t)(u / kAcc) & 1u, s_abort, &g_index_error)))
@@ -300,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float e = sum_f32x2(am0) + sum_f32x2(am1) + 0.5f * (sum_f32x2(aa0) + sum_f32x2(aa1));
         const int t = t0 + qi + k;
-        if (t < p.T && j < p.n_entries) p.scores[(int64_t)t * p.n_entries + j] = j <= p.p0 + t ? e : -INFINITY;
+        // entry j (tokens jm .. jm+m-1) is complete at the query's position p0 + t
+        if (t < p.T && j < p.n_entries) p.scores[(int64_t)t * p.n_entries + j] = jm_last <= p.p0 + t ? e : -INFINITY;
       }
     }
     // tiles of the chunk past every query of the block

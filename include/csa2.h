@@ -158,6 +158,26 @@ int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t B,
                    const int32_t* n_visible, int32_t* n_visible_out,
                    csa2_stream_t stream);
 
+/**
+ * Sequence compressor of the encoder's Full layers (the paperglide summary of
+ * DeepSeek-V4, "Compressed Sparse Attention": every m tokens merge into one
+ * compressed entry; the notes' section 4.1: CSA2 blocks do not overlap and
+ * the merge is softmax-weighted). For entry e (tokens em .. em+m-1) and
+ * channel c:  w_a = softmax_a( Z[em+a][c] + bias[a][c] ),
+ *             entry[e][c] = sum_a w_a * C[em+a][c]   (fp32),
+ * rounded to bf16 and packed as the main-KV latent (E2M1 + E4M3/16, the bytes
+ * csa2_pack_kv_fp4 writes for that bf16 row).
+ *   c_bf16, z_bf16 [n_tokens][512] bf16 (16-byte aligned), bias [m][512]
+ *   fp32; n_tokens a multiple of m. Entries 0 .. n_tokens/m - 1 of kv_data
+ *   [..][256] (8-byte aligned) and kv_scale [..][32] are written (offset the
+ *   plane pointers to append); out_bf16 [n_tokens/m][512] (nullable, 16-byte
+ *   aligned) receives the bf16 entries.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE (n_tokens % m), ALIGNMENT, CUDA.
+ */
+int csa2_compress_kv(const void* c_bf16, const void* z_bf16, const float* bias,
+                     int64_t n_tokens, int32_t m, uint8_t* kv_data,
+                     uint8_t* kv_scale, void* out_bf16, csa2_stream_t stream);
+
 /* ======================================================================== */
 /* Lightning indexer, pool and Top-K                                         */
 /* ======================================================================== */
@@ -379,6 +399,23 @@ int csa2_prefill_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
                              const uint8_t* ik_data, const uint8_t* ik_scale,
                              int64_t n_entries, int64_t p0, float* scores,
                              csa2_stream_t stream);
+
+/**
+ * Prefill indexer scores over compressed entries (notes section 4.4 item 4:
+ * the encoder's Full layers score each query against the visible compressed
+ * entries, about 3,072 N^2 multiply-adds at m = 2): as
+ * csa2_prefill_index_score with p0 the token position of query 0 and m tokens
+ * per entry; query t sees the complete entries j < floor((p0 + t + 1) / m).
+ * m = 1 is csa2_prefill_index_score. Requires floor((p0 + T) / m) <= n_entries.
+ * Errors: as csa2_prefill_index_score.
+ */
+int csa2_prefill_index_score_compressed(const uint8_t* q_data,
+                                        const uint8_t* q_e8m0, const float* w,
+                                        int32_t T, const uint8_t* ik_data,
+                                        const uint8_t* ik_scale,
+                                        int64_t n_entries, int64_t p0,
+                                        int32_t m, float* scores,
+                                        csa2_stream_t stream);
 
 /* ======================================================================== */
 /* Sparse attention                                                          */

@@ -85,6 +85,7 @@ def lib():
             L.orc_block_pool.restype = i32
             L.orc_block_pool.argtypes = [f32p, i64, i32, i32, i32p]
             L.orc_block_max.argtypes = [f32p, i64, i32, f32p]
+            L.orc_compress_kv.argtypes = [f64p, f64p, f64p, i64, i32, i32, f64p]
             L.orc_attn_merge.argtypes = [f64p, f64p, i32, i32, i32, f64p, f64p]
             L.orc_sparse_attn.argtypes = [f32p, i32, i32, u8p, u8p, i32p, i32, u8p, i32, d, f64p, f64p]
             L.orc_decode_batch.restype = ctypes.c_uint64
@@ -203,6 +204,28 @@ def kv_append(kv, ik, kv_data, kv_scale, ik_data, ik_scale, n_visible):
         ik_data[b, nv:nv + T], ik_scale[b, nv:nv + T] = quant_mxfp4(ik[b])
         out[b] = nv + T
     return out
+
+
+def compress_kv(C, Z, bias, m):
+    """Softmax-weighted merge of every m tokens into one entry ([V4] CSA; [B]
+    4.1). C, Z [n_tokens, D], bias [m, D] -> float64 [n_tokens // m, D]."""
+    C = _c(C, np.float64)
+    Z = _c(Z, np.float64)
+    bias = _c(bias, np.float64)
+    n, D = C.shape
+    out = np.zeros((n // m, D), np.float64)
+    lib().orc_compress_kv(_p(C), _p(Z), _p(bias), n, m, D, _p(out))
+    return out
+
+
+def compressed_visible(pos, m):
+    """Complete compressed entries visible to a query at token position pos:
+    entry j covers tokens jm .. jm+m-1 and is visible once its last token is at
+    or before pos."""
+    j = 0
+    while (j + 1) * m - 1 <= pos:
+        j += 1
+    return j
 
 
 def main_kv_entry_bytes() -> int:

@@ -480,6 +480,32 @@ void orc_attn_merge(const double* outs, const double* lses, int R, int H,
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Sequence compressor ([V4] "Compressed Sparse Attention": m tokens merge    */
+/* into one compressed entry by a softmax over the group; [B] 4.1: CSA2       */
+/* blocks do not overlap)                                                    */
+/* ------------------------------------------------------------------------ */
+
+void orc_compress_kv(const double* C, const double* Z, const double* bias,
+                     int64_t n_tokens, int m, int D, double* out) {
+  int64_t e, n_out = n_tokens / m;
+  int a, c;
+  for (e = 0; e < n_out; ++e)
+    for (c = 0; c < D; ++c) {
+      double mx = -INFINITY, den = 0.0, num = 0.0;
+      for (a = 0; a < m; ++a) {
+        double s = Z[(e * m + a) * D + c] + bias[a * D + c];
+        if (s > mx) mx = s;
+      }
+      for (a = 0; a < m; ++a) {
+        double wgt = exp(Z[(e * m + a) * D + c] + bias[a * D + c] - mx);
+        den += wgt;
+        num += wgt * C[(e * m + a) * D + c];
+      }
+      out[e * D + c] = num / den;
+    }
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -93,6 +93,14 @@ void orc_sparse_attn(const float* q, int H, int D, const uint8_t* kv_data,
                      const uint8_t* swa, int n_swa, double sm_scale,
                      double* out, double* lse);
 
+/* ---- sequence compressor (CSA: every m tokens merge into one entry; CSA2
+ * blocks do not overlap; softmax-weighted merge). For entry e and channel c:
+ * w_a = softmax over a = 0..m-1 of Z[em+a][c] + bias[a][c];
+ * out[e][c] = sum_a w_a C[em+a][c]. C, Z [n_tokens][D], bias [m][D],
+ * out [n_tokens/m][D], all in double.                                       */
+void orc_compress_kv(const double* C, const double* Z, const double* bias,
+                     int64_t n_tokens, int m, int D, double* out);
+
 /* ---- merge of attention over disjoint row sets ------------------------------
  * R partial results (out_r [H][D], lse_r [H]) of one query, each the softmax
  * attention over its own rows, merged into the attention over the union of
