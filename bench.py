@@ -264,8 +264,8 @@ def run_gpu(args):
     stages.append(("sparse_attn", st_attn))
     # our kernels per step: quant 1; workspace clear + scan (fused histogram and, with the pool, block
     # maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex: quant,
-    # clear, scan, select, finalize 5; attention partial + combine per 256 query-layers
-    n_launches = 1 + 4 + (5 + 5 if reindex else 0) + 2 * math.ceil(B * L / 256)
+    # clear, scan, select, finalize 5; attention: partials (+ combine) per 256 query-layers, as planned
+    n_launches = 1 + 4 + (5 + 5 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
 
     def step(ev=None):
         for j, (_, fn) in enumerate(stages):

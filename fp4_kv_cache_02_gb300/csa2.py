@@ -81,6 +81,7 @@ def _load():
         "csa2_prefill_index_score_compressed": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, i64, i32, vp, vp]),
         "csa2_compress_kv": (ctypes.c_int, [vp, vp, vp, i64, i32, vp, vp, vp, vp]),
         "csa2_sparse_attn_workspace_size": (sz, [i32, i32, i32]),
+        "csa2_sparse_attn_kernel_launches": (ctypes.c_int, [i32, i32, i32]),
         "csa2_sparse_attn_decode": (ctypes.c_int, [vp, i32, i32, vp, vp, i64, vp, vp, i32, vp, i32, f32,
                                                    vp, vp, vp, vp, sz, vp]),
         "csa2_sparse_attn_prefill": (ctypes.c_int, [vp, i32, vp, vp, i64, vp, i32, vp, i32, f32, vp, vp,

@@ -299,6 +299,14 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, 
   return o + (size_t)nq * ns * kHeads * 2 * 4;
 }
 
+extern "C" int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k, int32_t n_swa) {
+  if (n_queries <= 0 || k < 0 || n_swa < 0) return 0;
+  const AttnPlan plan = attn_plan_for(n_queries, k, n_swa);
+  if (plan.rows < 0) return 0;
+  const int batches = (n_queries + kQueriesPerLaunch - 1) / kQueriesPerLaunch;
+  return batches * (plan.fused ? 1 : 2);
+}
+
 static int launch_attn(AttnArgs a, int32_t n_q, uint16_t* out, float* out_f32, float* lse, void* ws, size_t ws_bytes,
                        cudaStream_t stream) {
   const AttnPlan plan = attn_plan_for(n_q, a.k, a.n_swa);

@@ -426,6 +426,12 @@ int csa2_prefill_index_score_compressed(const uint8_t* q_data,
 size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k,
                                        int32_t n_swa);
 
+/** Kernel launches one attention call makes for n_queries on the current
+ *  device (the chunks of a query merge in a cluster or in a second kernel,
+ *  whichever the launch plan finds faster); 0 for invalid sizes. */
+int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k,
+                                     int32_t n_swa);
+
 /**
  * Sparse decode attention (report section 2.3: each query attends to the
  * selected entries together with the layer-local SWA KV; section 2.3.1:
