@@ -5,8 +5,8 @@ sequences of the Full-layer decode workload (32 sequences x 65,536 visible
 entries; 32 x 128 MXFP4 indexer, Top-512, 64 x 512 attention over the 512
 selected FP4 latents + 128 FP8 SWA rows):
 
-    csa2_quant_mxfp4 (indexer q)  ->  csa2_index_topk (scan + Top-512)
-      ->  csa2_sparse_attn_decode
+    csa2_index_topk_bf16 (indexer q -> MXFP4 in the scan's prologue, scan,
+      Top-512)  ->  csa2_sparse_attn_decode
 
 with the KV cache resident in HBM. The timed region holds exactly --steps
 steps, each bracketed by CUDA events on the launching stream, with an L2
@@ -222,8 +222,6 @@ def run_gpu(args):
     if reindex:
         pool = torch.empty(B, NBLK * 8, dtype=torch.int32, device=device)
         idx_full = torch.empty(B, K, dtype=torch.int32, device=device)
-        qr_data = torch.empty(B, 32, 64, dtype=torch.uint8, device=device)
-        qr_sc = torch.empty(B, 32, 4, dtype=torch.uint8, device=device)
         rws = csa2.index_topk_workspace(B, NBLK * 8, K, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
@@ -238,34 +236,31 @@ def run_gpu(args):
     io = {k_: inp[k_] for k_ in ("q_idx", "w", "Q", "swa", "q_re", "w_re")}
     io["out"], io["idx"] = out, idx
 
-    def st_quant():
-        csa2.csa2_quant_mxfp4(io["q_idx"], q_data, q_sc)
-
+    # the indexer q goes in as bf16: the scan quantises it to MXFP4 in its prologue
     def st_index():
         if reindex:
-            csa2.csa2_index_topk(q_data, q_sc, io["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, idx_full,
-                                 iws, pool_blocks=NBLK, pool=pool)
+            csa2.csa2_index_topk_bf16(io["q_idx"], io["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K,
+                                      idx_full, iws, pool_blocks=NBLK, pool=pool)
         else:
-            csa2.csa2_index_topk(q_data, q_sc, io["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K, io["idx"],
-                                 iws)
+            csa2.csa2_index_topk_bf16(io["q_idx"], io["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K,
+                                      io["idx"], iws)
 
     def st_reindex():
-        csa2.csa2_quant_mxfp4(io["q_re"], qr_data, qr_sc)
-        csa2.csa2_index_topk(qr_data, qr_sc, io["w_re"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K,
-                             io["idx"], rws, positions=pool)
+        csa2.csa2_index_topk_bf16(io["q_re"], io["w_re"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], K,
+                                  io["idx"], rws, positions=pool)
 
     def st_attn():
         csa2.csa2_sparse_attn_decode(io["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], io["idx"], io["swa"],
                                      io["out"], aws)
 
-    stages = [("quant_q", st_quant), ("index_topk_pool" if reindex else "index_topk", st_index)]
+    stages = [("index_topk_pool" if reindex else "index_topk", st_index)]
     if reindex:
         stages.append(("reindex_topk", st_reindex))
     stages.append(("sparse_attn", st_attn))
-    # our kernels per step: quant 1; workspace clear + scan (fused histogram and, with the pool, block
-    # maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex: quant,
-    # clear, scan, select, finalize 5; attention: partials (+ combine) per 256 query-layers, as planned
-    n_launches = 1 + 4 + (5 + 5 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
+    # our kernels per step: workspace clear + scan (q quantisation, fused histogram and, with the pool,
+    # block maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex:
+    # clear, scan, select, finalize 4; attention: partials (+ combine) per 256 query-layers, as planned
+    n_launches = 4 + (5 + 4 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
 
     def step(ev=None):
         for j, (_, fn) in enumerate(stages):
@@ -335,6 +330,7 @@ def run_gpu(args):
     ms_max = reduce_max(ms, world, device)
 
     # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed) ----
+    csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc)
     scan_ms = 0.0
     for _ in range(args.steps):
         flush_l2()

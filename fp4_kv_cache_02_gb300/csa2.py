@@ -77,6 +77,8 @@ def _load():
         "csa2_index_topk_workspace_size": (sz, [i32, i64, i32, i32]),
         "csa2_index_topk": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp,
                                            vp, sz, vp]),
+        "csa2_index_topk_bf16": (ctypes.c_int, [vp, vp, i32, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, sz,
+                                                vp]),
         "csa2_prefill_index_score": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, i64, vp, vp]),
         "csa2_prefill_index_score_compressed": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, i64, i32, vp, vp]),
         "csa2_compress_kv": (ctypes.c_int, [vp, vp, vp, i64, i32, vp, vp, vp, vp]),
@@ -264,6 +266,21 @@ def csa2_index_topk(q_data, q_e8m0, w, ik_data, ik_scale, n_visible, k, idx, wor
         n_pos = positions.shape[1] if positions is not None else cap
     _call("csa2_index_topk", _p(q_data), _p(q_e8m0), _p(w), B, _p(ik_data), _p(ik_scale), cap, _p(n_visible),
           _p(positions), n_pos, k, _p(idx), pool_blocks, _p(pool), _p(workspace), workspace.numel(), _s(stream))
+
+
+def csa2_index_topk_bf16(q, w, ik_data, ik_scale, n_visible, k, idx, workspace, positions=None, n_pos=None,
+                         pool_blocks=0, pool=None, stream=None):
+    """csa2_index_topk with q [B,32,128] bf16, quantised inside the scan."""
+    _req(q, torch.bfloat16, "q")
+    for t, n in ((ik_data, "ik_data"), (ik_scale, "ik_scale"), (workspace, "workspace")):
+        _req(t, torch.uint8, n)
+    _req(w, torch.float32, "w"); _req(n_visible, torch.int32, "n_visible"); _req(idx, torch.int32, "idx")
+    _req(positions, torch.int32, "positions", allow_none=True); _req(pool, torch.int32, "pool", allow_none=True)
+    B, cap = ik_data.shape[0], ik_data.shape[1]
+    if n_pos is None:
+        n_pos = positions.shape[1] if positions is not None else cap
+    _call("csa2_index_topk_bf16", _p(q), _p(w), B, _p(ik_data), _p(ik_scale), cap, _p(n_visible), _p(positions),
+          n_pos, k, _p(idx), pool_blocks, _p(pool), _p(workspace), workspace.numel(), _s(stream))
 
 
 def csa2_prefill_index_score(q_data, q_e8m0, w, ik_data, ik_scale, p0, scores, stream=None):

@@ -425,7 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nsp = a.n_split;
     const int rank = (int)cl.block_rank();
     __shared__ float w_s[kMaxClusterChunks][kHeads];   // m_j, then the weights
-    __shared__ float f_l[kMaxClusterChunks][kHeads];   // l_j
+    __shared__ float f_l[kMaxClusterChunks][kHeads];   // l_j, then l_j exp(m_j - M)
+    __shared__ float e_s[kMaxClusterChunks][kHeads];   // exp(m_j - M)
+    __shared__ float M_s[kHeads];
     float* o_s = reinterpret_cast<float*>(sR);  // 128 KiB of the R tile, free after the PV product
 #pragma unroll
     for (int hh = 0; hh < kHeads; hh += 32) {
@@ -441,48 +443,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tid < kHeads && !ok) l_s[tid] = 0.0f;
     cl.sync();
-    // (m, l) of every chunk, one remote load each
+    // rank r sums heads [64r/n, 64(r+1)/n): items i = tid + kThreads u are
+    // float4 columns of that slice; the remote loads of the first two items
+    // go out before the weights are formed
+    const int h0 = kHeads * rank / nsp, h1 = kHeads * (rank + 1) / nsp;
+    const int n_items = (h1 - h0) * (kHeadDim / 4);
+    float4 v[2][kMaxClusterChunks];
+    auto load_items = [&](const int i0) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kThreads;
+        const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
+#pragma unroll
+        for (int j = 0; j < kMaxClusterChunks; ++j)
+          if (j < nsp && i < n_items)
+            v[u][j] = *reinterpret_cast<const float4*>(cl.map_shared_rank(o_s, j) + h * kHeadDim + c4);
+      }
+    };
+    load_items(tid);
+    // (m, l) of every chunk, one remote load each; e_j = l_j exp(m_j - M)
     if (tid < nsp * kHeads) {
       const int j = tid / kHeads, h = tid % kHeads;
       const float lj = *cl.map_shared_rank(&l_s[h], j);
-      const float mj = *cl.map_shared_rank(&m_s[h], j);
-      w_s[j][h] = lj > 0.0f ? mj : -INFINITY;
+      w_s[j][h] = lj > 0.0f ? *cl.map_shared_rank(&m_s[h], j) : -INFINITY;
       f_l[j][h] = lj;
     }
     __syncthreads();
-    if (tid < kHeads) {
+    // thread (j, h): M = max_j m_j, e_j = exp(m_j - M), then L = sum_j l_j e_j in
+    // fixed order and the weight e_j / L (m_s and l_s stay as they are: the
+    // other CTAs of the cluster may still be reading them)
+    if (tid < nsp * kHeads) {
+      const int j = tid / kHeads, h = tid % kHeads;
       float M = -INFINITY;
-      for (int j = 0; j < nsp; ++j) M = fmaxf(M, w_s[j][tid]);
-      float Lsum = 0.0f;
-      for (int j = 0; j < nsp; ++j)
-        if (f_l[j][tid] > 0.0f) Lsum += f_l[j][tid] * expf(w_s[j][tid] - M);
-      for (int j = 0; j < nsp; ++j)
-        w_s[j][tid] = (f_l[j][tid] > 0.0f && Lsum > 0.0f) ? expf(w_s[j][tid] - M) / Lsum : 0.0f;
-      if (rank == 0 && a.lse) a.lse[(int64_t)qi * kHeads + tid] = Lsum > 0.0f ? M + logf(Lsum) : -INFINITY;
+      for (int jj = 0; jj < nsp; ++jj) M = fmaxf(M, w_s[jj][h]);
+      const float e = f_l[j][h] > 0.0f ? expf(w_s[j][h] - M) : 0.0f;
+      e_s[j][h] = e;
+      f_l[j][h] *= e;  // l_j e_j, read by every j below
+      if (j == 0) M_s[h] = M;
     }
     __syncthreads();
-    const int h0 = kHeads * rank / nsp, h1 = kHeads * (rank + 1) / nsp;
-    for (int i = tid; i < (h1 - h0) * (kHeadDim / 4); i += kThreads) {
-      const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
-      float4 v[kMaxClusterChunks];
+    if (tid < nsp * kHeads) {
+      const int j = tid / kHeads, h = tid % kHeads;
+      float Lsum = 0.0f;
+      for (int jj = 0; jj < nsp; ++jj) Lsum += f_l[jj][h];   // fixed order
+      w_s[j][h] = Lsum > 0.0f ? e_s[j][h] / Lsum : 0.0f;
+      if (j == 0 && rank == 0 && a.lse) a.lse[(int64_t)qi * kHeads + h] = Lsum > 0.0f ? M_s[h] + logf(Lsum) : -INFINITY;
+    }
+    __syncthreads();
+    for (int i0 = tid; i0 < n_items; i0 += 2 * kThreads) {
+      if (i0 != tid) load_items(i0);
 #pragma unroll
-      for (int j = 0; j < kMaxClusterChunks; ++j)
-        if (j < nsp) v[j] = *reinterpret_cast<const float4*>(cl.map_shared_rank(o_s, j) + h * kHeadDim + c4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kThreads;
+        if (i >= n_items) break;
+        const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int j = 0; j < kMaxClusterChunks; ++j) {   // fixed rank order
-        if (j >= nsp) break;
-        const float f = w_s[j][h];
-        acc.x = fmaf(v[j].x, f, acc.x);
-        acc.y = fmaf(v[j].y, f, acc.y);
-        acc.z = fmaf(v[j].z, f, acc.z);
-        acc.w = fmaf(v[j].w, f, acc.w);
+        for (int j = 0; j < kMaxClusterChunks; ++j) {   // fixed rank order
+          if (j >= nsp) break;
+          const float f = w_s[j][h];
+          acc.x = fmaf(v[u][j].x, f, acc.x);
+          acc.y = fmaf(v[u][j].y, f, acc.y);
+          acc.z = fmaf(v[u][j].z, f, acc.z);
+          acc.w = fmaf(v[u][j].w, f, acc.w);
+        }
+        const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4;
+        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
+        const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(a.out + o) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
       }
-      const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4;
-      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
-      const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(a.out + o) =
-          make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
     }
     cl.sync();  // the other ranks have finished reading this CTA's shared memory
   } else {

@@ -6,7 +6,8 @@
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
-                               uint32_t* hist, float* bmax, int early_reads, cudaStream_t stream);
+                               uint32_t* hist, float* bmax, int early_reads, const void* q_bf16,
+                               cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -74,7 +75,7 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                    nullptr, nullptr, 0, (cudaStream_t)stream);
+                                    nullptr, nullptr, 0, nullptr, (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -93,12 +94,13 @@ extern "C" size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_pos, int32
   return scores + t;
 }
 
-extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
-                               const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
-                               const int32_t* n_visible, const int32_t* positions, int64_t n_pos, int32_t k,
-                               int32_t* idx, int32_t pool_blocks, int32_t* pool, void* workspace,
-                               size_t workspace_bytes, csa2_stream_t stream) {
-  int rc = check_index_args(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos);
+static int index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const void* q_bf16, const float* w, int32_t B,
+                      const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap, const int32_t* n_visible,
+                      const int32_t* positions, int64_t n_pos, int32_t k, int32_t* idx, int32_t pool_blocks,
+                      int32_t* pool, void* workspace, size_t workspace_bytes, csa2_stream_t stream) {
+  int rc = q_bf16 ? check_index_args((const uint8_t*)q_bf16, (const uint8_t*)q_bf16, w, B, ik_data, ik_scale, cap,
+                                     n_visible, n_pos)
+                  : check_index_args(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos);
   if (rc) return rc;
   if (!idx) return CSA2_ERR_INVALID_ARG;
   if (k <= 0 || k > CSA2_MAX_TOPK || pool_blocks < 0 || pool_blocks > CSA2_MAX_TOPK)
@@ -124,11 +126,30 @@ extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, con
   rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist);
   if (rc) return rc;
   rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                  hist, bmax, 1, s);  // just after the workspace clear
+                                  hist, bmax, 1, q_bf16, s);  // just after the workspace clear
   if (rc) return rc;
   rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);
   if (rc) return rc;
   if (pool_blocks > 0)
     rc = csa2_launch_pool_from_bmax(bmax, B, n_pos, n_visible, CSA2_POOL_BLOCK, pool_blocks, pool, rest, rest_bytes, s);
   return rc;
+}
+
+extern "C" int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
+                               const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
+                               const int32_t* n_visible, const int32_t* positions, int64_t n_pos, int32_t k,
+                               int32_t* idx, int32_t pool_blocks, int32_t* pool, void* workspace,
+                               size_t workspace_bytes, csa2_stream_t stream) {
+  return index_topk(q_data, q_e8m0, nullptr, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, k, idx,
+                    pool_blocks, pool, workspace, workspace_bytes, stream);
+}
+
+extern "C" int csa2_index_topk_bf16(const void* q_bf16, const float* w, int32_t B, const uint8_t* ik_data,
+                                    const uint8_t* ik_scale, int64_t cap, const int32_t* n_visible,
+                                    const int32_t* positions, int64_t n_pos, int32_t k, int32_t* idx,
+                                    int32_t pool_blocks, int32_t* pool, void* workspace, size_t workspace_bytes,
+                                    csa2_stream_t stream) {
+  if (!q_bf16) return CSA2_ERR_INVALID_ARG;
+  return index_topk(nullptr, nullptr, q_bf16, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, k, idx,
+                    pool_blocks, pool, workspace, workspace_bytes, stream);
 }

@@ -22,6 +22,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "codec_blocks.cuh"
 #include "tc_common.cuh"
 
 namespace csa2 {
@@ -70,6 +71,9 @@ struct Params {
   // histogram clear): then the cache, q and positions are read at once and
   // only the epilogue's writes wait for that kernel
   int32_t early_reads;
+  // optional [B][32][128] bf16 indexer q: quantised to MXFP4 in the prologue
+  // (the same block encoder as csa2_quant_mxfp4) instead of reading q_data
+  const uint16_t* q_bf16;
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -124,12 +128,31 @@ __global__ void __launch_bounds__(kThreads, 3)
     *s_abort = 0;
     tc::fence_mbar_init();
   }
-  if (threadIdx.x < 128) {
+  if (threadIdx.x < 128 && p.q_bf16) {
+    // q: head r, channels 32c .. 32c+31 -> one MXFP4 block: 16 bytes at its
+    // SW64 place and the E8M0 byte, the four bytes of a head gathered by shuffles
+    const int r = threadIdx.x >> 2, c = threadIdx.x & 3;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q_bf16 + ((int64_t)b * kIdxHeads + r) * kIdxDim + c * 32);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = src[i];
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    uint4 d;
+    uint8_t e;
+    encode_mxfp4_block(w, d, e);
+    *reinterpret_cast<uint4*>(sQ + tc::sw64_offset(r, c)) = d;
+    uint32_t sb = (uint32_t)e << (8 * c);
+    sb |= __shfl_xor_sync(0xffffffffu, sb, 1);
+    sb |= __shfl_xor_sync(0xffffffffu, sb, 2);
+    if (c == 0) *reinterpret_cast<uint4*>(sSfb + r * 16) = make_uint4(sb, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  } else if (threadIdx.x < 128) {
     // q: 32 rows x 64 B, K-major with the 64-byte swizzle
     const int r = threadIdx.x >> 2, c = threadIdx.x & 3;
     uint4 v = *reinterpret_cast<const uint4*>(p.q_data + ((int64_t)b * kIdxHeads + r) * kIkBytes + c * 16);
     *reinterpret_cast<uint4*>(sQ + tc::sw64_offset(r, c)) = v;
-  } else if (threadIdx.x < 160) {
+  } else if (threadIdx.x < 160 && !p.q_bf16) {
     // scales of q for tcgen05.cp: row i holds the four E8M0 bytes of head i
     // (bytes for rows i+32, i+64, i+96 do not exist for N = 32 and are 2^0)
     const int i = threadIdx.x - 128;

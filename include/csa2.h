@@ -380,6 +380,20 @@ int csa2_index_topk(const uint8_t* q_data, const uint8_t* q_e8m0,
                     size_t workspace_bytes, csa2_stream_t stream);
 
 /**
+ * csa2_index_topk with the indexer q given in bf16: the scan quantises it to
+ * MXFP4 in its prologue with the same block encoder as csa2_quant_mxfp4 (same
+ * bytes, so the same scores and indices), saving that kernel and its launch.
+ *   q_bf16 [B][32][128] bf16 (16-byte aligned); the rest as csa2_index_topk.
+ */
+int csa2_index_topk_bf16(const void* q_bf16, const float* w, int32_t B,
+                         const uint8_t* ik_data, const uint8_t* ik_scale,
+                         int64_t cap, const int32_t* n_visible,
+                         const int32_t* positions, int64_t n_pos, int32_t k,
+                         int32_t* idx, int32_t pool_blocks, int32_t* pool,
+                         void* workspace, size_t workspace_bytes,
+                         csa2_stream_t stream);
+
+/**
  * Prefill indexer scores with causal masking (report section 2.3; the
  * encoder-side prefill indexer cost in notes section 4.4 item 4).
  * T queries at positions p0 .. p0+T-1 of one sequence; query t sees entries

@@ -236,3 +236,46 @@ def test_index_score_block_scales_land_on_their_own_rows_and_blocks(csa2):
         ref = oracle.index_score(qd[b], qs[b], w[b], ikd[b], iks[b], n=int(nv[b]))[0]
         _scores_close(s[b, :nv[b]], ref)
         assert np.all(s[b, nv[b]:] == -np.inf)
+
+
+@pytest.mark.parametrize("mode", ["dense", "pool", "positions"])
+def test_index_topk_from_bf16_q_equals_quantise_then_index(csa2, mode):
+    """The scan that quantises q itself must give the bytes, scores, indices and
+    pool of csa2_quant_mxfp4 followed by csa2_index_topk."""
+    case = DecodeCase(workload=88, Ns=[20000, 7000, 130], reindex=(mode == "pool"), planted_blocks=4 if mode == "pool" else 0)
+    g = case.to_device()
+    B, cap, k = case.B, case.cap, 512
+    q16 = g["q_idx"]
+    qd = torch.empty(B, 32, 64, dtype=torch.uint8, device="cuda")
+    qs = torch.empty(B, 32, 4, dtype=torch.uint8, device="cuda")
+    csa2.csa2_quant_mxfp4(q16, qd, qs)
+    kw = {}
+    n_pos = cap
+    if mode == "pool":
+        kw = dict(pool_blocks=64)
+    if mode == "positions":
+        rng = np.random.default_rng(3)
+        pos = np.stack([np.sort(rng.choice(cap, 3000, replace=False)) for _ in range(B)]).astype(np.int32)
+        pos[:, ::9] = -1
+        kw = dict(positions=dev(pos))
+        n_pos = 3000
+    outs = []
+    for fused in (False, True):
+        idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
+        pool = torch.empty(B, 64 * 8, dtype=torch.int32, device="cuda") if mode == "pool" else None
+        ws = csa2.index_topk_workspace(B, n_pos, k, 64 if mode == "pool" else 0)
+        ws.fill_(0x5A)
+        if fused:
+            csa2.csa2_index_topk_bf16(q16, g["w"], g["ik_data"], g["ik_scale"], g["n_visible"], k, idx, ws,
+                                      pool=pool, **kw)
+        else:
+            csa2.csa2_index_topk(qd, qs, g["w"], g["ik_data"], g["ik_scale"], g["n_visible"], k, idx, ws, pool=pool,
+                                 **kw)
+        torch.cuda.synchronize()
+        assert csa2.csa2_get_last_error() == 0
+        scores = ws[:B * n_pos * 4].view(torch.float32).view(B, n_pos).clone()
+        outs.append((idx.clone(), None if pool is None else pool.clone(), scores))
+    assert torch.equal(outs[0][0], outs[1][0])
+    if mode == "pool":
+        assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2], outs[1][2])
