@@ -352,6 +352,11 @@ def csa2_prefill_index_score_compressed(q_data, q_e8m0, w, ik_data, ik_scale, p0
 
 # ---- attention ------------------------------------------------------------------
 
+def csa2_sparse_attn_kernel_launches(n_queries, k, n_swa) -> int:
+    """Kernel launches one attention call makes on the current device."""
+    return int(_lib.csa2_sparse_attn_kernel_launches(n_queries, k, n_swa))
+
+
 def csa2_sparse_attn_decode(q, kv_data, kv_scale, n_visible, idx, swa, out, workspace, out_f32=None, lse=None,
                             sm_scale=1.0, stream=None):
     """q [B,L,64,512] bf16; kv planes [B,cap,256]/[B,cap,32]; idx [B,k]; swa [B,L,n_swa,512] u8."""
