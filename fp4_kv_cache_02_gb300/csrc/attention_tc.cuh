@@ -352,12 +352,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   // P = exp(S - m) from a second read of S; P_hi = bf16(P), P_lo = bf16(P - P_hi),
   // stored K-major for the PV MMA as B-operand rows n = h (hi) and 64 + h (lo):
   // per 64 rows t a block of [128 n][128 B]
-  load_scores();
+  // the scores are still in p0 / p1 (the reduction worked on a copy);
+  // exp(s - m) = 2^(s log2 e - m log2 e); only the warps of lane quadrant 0
+  // hold rows of the second tile
+  constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
   for (int j = 0; j < kHpw; ++j) {
-    const float m = m_s[hb + j];
-    p0[j] = (p0[j] == -INFINITY) ? 0.0f : expf(p0[j] - m);
-    p1[j] = (p1[j] == -INFINITY) ? 0.0f : expf(p1[j] - m);
+    const float ml = m_s[hb + j] * kLog2e;
+    p0[j] = (p0[j] == -INFINITY) ? 0.0f : exp2f(fmaf(p0[j], kLog2e, -ml));
+  }
+  if (two) {
+#pragma unroll
+    for (int j = 0; j < kHpw; ++j) {
+      const float ml = m_s[hb + j] * kLog2e;
+      p1[j] = (p1[j] == -INFINITY) ? 0.0f : exp2f(fmaf(p1[j], kLog2e, -ml));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kHpw; ++j) p1[j] = 0.0f;
   }
   auto store_p = [&](const int t, const float (&pv)[kHpw]) {
     uint8_t* blkp = sQP + (t >> 6) * kPBlk;
