@@ -14,9 +14,9 @@
 //      significant bits) in 128-byte-swizzled blocks of 64 channels, the low
 //      256 channels first;
 //   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (M = 128 rows per tile, one
-//      or two tiles; N = 64 heads; K = 512 in two halves of 256 channels, so
-//      that only half of Q is resident: the first half's MMAs run while the
-//      high channels are dequantised and the second half of Q loads);
+//      or two tiles; N = 64 heads; K = 512 in quarters of 128 channels held
+//      in three slots: quarter 3 loads into quarter 0's slot once its MMAs are
+//      done, while the high channels are dequantised);
 //   3. per-head max and sum over the chunk's rows; P = exp(S - max) split
 //      into bf16 hi + lo parts (keeps the P.V product at fp32-level accuracy),
 //      stacked as 128 B-operand rows (64 hi, 64 lo);
@@ -42,7 +42,7 @@ constexpr int kThreads = 512;   // 16 warps: 4 TMEM lane quadrants x 4
 constexpr int kBlkR = kMaxRows * 128;                     // one 64-channel block of R: [160 t][128 B]
 constexpr int kOffR = 0;                                  // 8 blocks                        = 160 KiB
 constexpr int kOffQP = kOffR + 8 * kBlkR;                 // Q half (4 x [64 h][128 B]) or P = 48 KiB
-constexpr int kQHalfBytes = kHeads * 256 * 2;             // 32 KiB
+constexpr int kQQuarterBytes = kHeads * 128 * 2;          // 16 KiB: channels 128q .. 128q+127
 constexpr int kPBlk = 2 * kHeads * 128;                   // P: per 64 rows, [128 n][128 B]  = 16 KiB
 constexpr int kOffMisc = kOffQP + 3 * kPBlk;
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;
@@ -52,7 +52,7 @@ constexpr uint32_t kColO = 0;      // O^T: 4 blocks x 128 columns (64 hi + 64 lo
                                    // written once S^T has been read
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kQHalfBytes <= 3 * kPBlk, "Q half fits the P region");
+static_assert(3 * kQQuarterBytes <= 3 * kPBlk, "three Q quarters fit the P region");
 
 // exact bf16x2 product (operands with <= 2 and <= 4 significant bits)
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
@@ -114,12 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   uint8_t* sR = sm + kOffR;
   uint8_t* sQP = sm + kOffQP;
-  uint64_t* bar_s0 = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T over channels 0..255 done
+  uint64_t* bar_s0 = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T over channels 0..127 done
   uint64_t* bar_s1 = bar_s0 + 1;                                 // S^T complete
   uint64_t* bar_pv = bar_s0 + 2;                                 // O^T complete
-  uint64_t* q_bar = bar_s0 + 3;                                  // Q halves (two phases)
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 32);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 36);
+  uint64_t* q_full = bar_s0 + 3;                                 // 3 Q slots (slot 0 twice)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 48);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 52);
   __shared__ float red[4][kHeads];
   __shared__ float m_s[kHeads], l_s[kHeads];
   __shared__ uint16_t lut_e4m3[256];     // E4M3 byte -> bf16 value
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(bar_s0, 1);
     tc::mbar_init(bar_s1, 1);
     tc::mbar_init(bar_pv, 1);
-    tc::mbar_init(q_bar, 1);
+    for (int q = 0; q < 3; ++q) tc::mbar_init(&q_full[q], 1);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -150,11 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     lut_e4m3[byte] = *reinterpret_cast<uint16_t*>(&e);
   }
   pdl_wait();
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
-    for (int blk = 0; blk < 4; ++blk)
-      tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, blk * 64, qi * kHeads, q_bar);
-  }
+  // Q quarter q (channels 128q .. +127, two boxes of [64 h][64 c]) into slot
+  // q % 3 of the Q/P region: quarters 0-2 now, quarter 3 once quarter 0's
+  // MMAs have read slot 0
+  auto load_q_quarter = [&](const int q) {
+    uint8_t* slot = sQP + (q % 3) * kQQuarterBytes;
+    tc::mbar_arrive_expect_tx(&q_full[q % 3], kQQuarterBytes);
+    for (int blk = 0; blk < 2; ++blk)
+      tc::tma_load_2d(slot + blk * (kHeads * 128), &tmap_q, q * 128 + blk * 64, qi * kHeads, &q_full[q % 3]);
+  };
+  if (tid == 0)
+    for (int q = 0; q < 3; ++q) load_q_quarter(q);
   // ---- rows of this chunk: position (or SWA row), validity ----
   const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
   const int32_t* idx_row = a.idx + (int64_t)seq * a.k;
@@ -258,18 +264,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
     }
   };
-  // S^T (+)= R[:, 256kh .. +255] . Q[:, 256kh .. +255]^T for every tile of 128 rows
-  auto issue_s = [&](const uint32_t tmem, const int kh) {
+  // S^T (+)= R[:, 128q .. +127] . Q[:, 128q .. +127]^T for every tile of 128 rows
+  auto issue_s = [&](const uint32_t tmem, const int q) {
     constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 0, 0);
-    const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQP);
+    const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQP) + (uint32_t)((q % 3) * kQQuarterBytes);
     for (int t = 0; t < n_tiles; ++t)
-      for (int kk = 0; kk < 16; ++kk) {
-        const uint32_t blk = (uint32_t)(kh * 4) + ((uint32_t)kk >> 2), off = ((uint32_t)kk & 3u) * 32u;
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t blk = (uint32_t)(q * 2) + ((uint32_t)kk >> 2), off = ((uint32_t)kk & 3u) * 32u;
         const uint64_t ad = tc::smem_desc(r_addr + blk * kBlkR + (uint32_t)t * (128u * 128u) + off, 0, 1024,
                                           tc::kSwizzle128B);
         const uint64_t bd = tc::smem_desc(q_addr + ((uint32_t)kk >> 2) * (kHeads * 128) + off, 0, 1024,
                                           tc::kSwizzle128B);
-        tc::mma_bf16(tmem + kColS + 64u * (uint32_t)t, ad, bd, idesc, (kh | kk) ? 1u : 0u);
+        tc::mma_bf16(tmem + kColS + 64u * (uint32_t)t, ad, bd, idesc, (q | kk) ? 1u : 0u);
       }
   };
 
@@ -281,31 +287,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   bool lead_ok = true;   // meaningful in thread 0
   if (tid == 0) {
-    lead_ok = tc::mbar_wait_bounded(q_bar, 0, s_abort, &g_attn_error);
+    lead_ok = tc::mbar_wait_bounded(&q_full[0], 0, s_abort, &g_attn_error);
     if (lead_ok) {
       issue_s(tmem, 0);
       tc::mma_commit(bar_s0);
+      lead_ok = tc::mbar_wait_bounded(&q_full[1], 0, s_abort, &g_attn_error);
+      if (lead_ok) issue_s(tmem, 1);
     }
   }
   dequant_half(1);
   if (tid == 0 && lead_ok) {
-    // the Q buffer takes channels 256..511 once the first MMAs have read it
+    // slot 0 takes quarter 3 once quarter 0's MMAs have read it
     lead_ok = tc::mbar_wait_bounded(bar_s0, 0, s_abort, &g_attn_error);
-    if (lead_ok) {
-      tc::mbar_arrive_expect_tx(q_bar, kQHalfBytes);
-      for (int blk = 0; blk < 4; ++blk)
-        tc::tma_load_2d(sQP + blk * (kHeads * 128), &tmap_q, 256 + blk * 64, qi * kHeads, q_bar);
-    }
+    if (lead_ok) load_q_quarter(3);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   if (tid == 0 && lead_ok) {
-    lead_ok = tc::mbar_wait_bounded(q_bar, 1, s_abort, &g_attn_error);
+    lead_ok = tc::mbar_wait_bounded(&q_full[2], 0, s_abort, &g_attn_error);
     if (lead_ok) {
-      issue_s(tmem, 1);
-      tc::mma_commit(bar_s1);
+      issue_s(tmem, 2);
+      lead_ok = tc::mbar_wait_bounded(&q_full[0], 1, s_abort, &g_attn_error);
+      if (lead_ok) {
+        issue_s(tmem, 3);
+        tc::mma_commit(bar_s1);
+      }
     }
   }
   if (tid == 0 && !lead_ok) *s_abort = 1;
