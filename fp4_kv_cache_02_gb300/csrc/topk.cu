@@ -46,7 +46,7 @@ constexpr int kPerThread = 16;                      // consecutive scores per se
 constexpr int kSelTile = kSelThreads * kPerThread;  // 4096 scores
 constexpr int kMaxRegions = 8192;                   // regions per row (their offsets live in shared memory)
 constexpr int kFinThreads = 512;
-constexpr int kFinPerThread = 16;
+constexpr int kFinPerThread = 4;
 constexpr int kTieCap = 1024;                       // second-level ties ranked in shared memory
 constexpr int kHist2Shift = 32 - kHistBits - kHist2Bits;  // 9: second-level digit is key bits [19, 9]
 
@@ -213,16 +213,24 @@ __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, u
 // owning lane, then the lanes split that lane's 64 bins two apiece. The row
 // must be 256-byte aligned; counts are read through L2 (__ldcg) because other
 // CTAs of an earlier kernel wrote them with atomics.
-__device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need, uint32_t* above_out) {
-  static_assert(kHist2Bins == 32 * 64, "one warp covers the histogram 64 bins a lane");
+// Sum of the 64 bins lane l owns (the loads can be issued before `need` is known).
+__device__ __forceinline__ uint32_t warp_hist_lane_sum(const uint32_t* __restrict__ gh) {
   const int lane = threadIdx.x & 31;
   const uint4* p = reinterpret_cast<const uint4*>(gh + kHist2Bins - 64 * (lane + 1));
+  uint4 v[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __ldcg(p + i);
   uint32_t s = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint4 v = __ldcg(p + i);
-    s += v.x + v.y + v.z + v.w;
-  }
+  for (int i = 0; i < 16; ++i) s += v[i].x + v[i].y + v[i].z + v[i].w;
+  return s;
+}
+
+__device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need, uint32_t* above_out,
+                                  uint32_t* count_out = nullptr, const uint32_t* lane_sum = nullptr) {
+  static_assert(kHist2Bins == 32 * 64, "one warp covers the histogram 64 bins a lane");
+  const int lane = threadIdx.x & 31;
+  const uint32_t s = lane_sum ? *lane_sum : warp_hist_lane_sum(gh);
   uint32_t incl = s;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -249,12 +257,15 @@ __device__ int warp_threshold_bin(const uint32_t* __restrict__ gh, uint32_t need
   const int c2 = __ffs(__ballot_sync(0xffffffffu, excl_c + incl2 >= need)) - 1;
   uint32_t base = excl_c + __shfl_sync(0xffffffffu, incl2 - ps, c2);
   const uint32_t hy = __shfl_sync(0xffffffffu, v.y, c2);
+  const uint32_t hx = __shfl_sync(0xffffffffu, v.x, c2);
   int bin;
   if (base + hy >= need) {
     bin = top_c - 1 - 2 * c2;
+    if (count_out) *count_out = hy;
   } else {
     bin = top_c - 2 - 2 * c2;
     base += hy;
+    if (count_out) *count_out = hx;
   }
   *above_out = base;
   return bin;
@@ -520,11 +531,14 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
         v[13 - 4 * q] = hv[q].z;
         v[12 - 4 * q] = hv[q].w;
       }
-      uint32_t run = hex;
+      uint32_t run = hex, cnt_t = v[kBinsPerThread - 1];
       int bin = kHistBins - kBinsPerThread * (int)threadIdx.x - 1;
 #pragma unroll
       for (int i = 0; i < kBinsPerThread - 1; ++i) {
-        if (run + v[i] >= (uint32_t)k) break;
+        if (run + v[i] >= (uint32_t)k) {
+          cnt_t = v[i];
+          break;
+        }
         run += v[i];
         --bin;
       }
@@ -532,6 +546,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
       if (r == 0) {
         ws.cnt[b].t = bin;
         ws.cnt[b].above = run;
+        ws.cnt[b].pad[0] = cnt_t;  // keys in bin t
       }
     }
   }
@@ -679,16 +694,20 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   uint32_t* h = reinterpret_cast<uint32_t*>(out + CSA2_MAX_TOPK);
   uint32_t* scratch = h + kRadixBins;
   int32_t* tsel = reinterpret_cast<int32_t*>(scratch + kFinThreads + 8);
-  __shared__ uint32_t s_nout, s_ntie, s_nsel, s_above2;
+  __shared__ uint32_t s_nout, s_ntie, s_nsel, s_above2, s_ct2;
   __shared__ int s_t2;
   const int b = blockIdx.x;
   const int R = ws.n_regions;
   const int64_t row_off = (int64_t)b * n;
   const uint2* cand = ws.cand + row_off;
   int32_t* dst = idx + (size_t)b * k;
+  // the row's counters, its region sizes and (warp 0) its second-level
+  // histogram are loaded together
+  uint32_t h2_sum = 0;
+  if (threadIdx.x < 32) h2_sum = warp_hist_lane_sum(ws.hist2 + (size_t)b * kHist2Bins);
   const int t = __ldcg(&ws.cnt[b].t);
   const uint32_t above = __ldcg(&ws.cnt[b].above);
-  const uint32_t c_t = t >= 0 ? __ldcg(ws.hist + (size_t)b * kHistBins + t) : 0u;
+  const uint32_t c_t = t >= 0 ? __ldcg(&ws.cnt[b].pad[0]) : 0u;  // keys in bin t, recorded by the select
   const uint32_t r = t >= 0 ? (uint32_t)k - above : 0u;  // still needed from bin t
   const bool need_res = t >= 0 && r < c_t;
   // region sizes -> offsets (the loads are in flight while warp 0 finds t2)
@@ -698,11 +717,12 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   uint32_t local = 0;
   for (int j = j0; j < j1; ++j) local += __ldcg(rc + j);
   if (need_res && threadIdx.x < 32) {
-    uint32_t above2;
-    const int t2 = warp_threshold_bin(ws.hist2 + (size_t)b * kHist2Bins, r, &above2);
+    uint32_t above2, c2 = 0;
+    const int t2 = warp_threshold_bin(ws.hist2 + (size_t)b * kHist2Bins, r, &above2, &c2, &h2_sum);
     if (threadIdx.x == 0) {
       s_t2 = t2;
       s_above2 = above2;
+      s_ct2 = c2;
     }
   }
   if (threadIdx.x == 0) {
@@ -725,7 +745,7 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   if (need_res) {
     t2 = s_t2;
     if (t2 >= 0) {
-      c_t2 = __ldcg(ws.hist2 + (size_t)b * kHist2Bins + t2);
+      c_t2 = s_ct2;
       r2 = r - s_above2;
       res_ties = r2 < c_t2;
     }
