@@ -72,3 +72,62 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     lib.csa2_sparse_attn_workspace_size.restype = ctypes.c_size_t
     lib.csa2_sparse_attn_workspace_size.argtypes = [ctypes.c_int32] * 3
     assert lib.csa2_sparse_attn_workspace_size(32, 512, 128) > 0
+
+
+def test_host_argument_checks_of_the_newer_entry_points(lib):
+    """Append, compressor, replay prefill, Bounded-Replay and exchange steps:
+    null pointers, bad sizes and misalignment are refused on the host; empty
+    work returns OK without enqueuing anything."""
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    fake = vp(1 << 20)
+    odd = vp((1 << 20) + 8)
+    lib.csa2_kv_append.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, vp, vp]
+    assert lib.csa2_kv_append(None, fake, 1, 1, fake, fake, fake, fake, 128, fake, None, None) == -1
+    assert lib.csa2_kv_append(fake, fake, -1, 1, fake, fake, fake, fake, 128, fake, None, None) == -1
+    assert lib.csa2_kv_append(odd, fake, 1, 1, fake, fake, fake, fake, 128, fake, None, None) == -3
+    assert lib.csa2_kv_append(fake, fake, 0, 1, fake, fake, fake, fake, 128, fake, None, None) == 0
+    assert lib.csa2_kv_append(fake, fake, 4, 0, fake, fake, fake, fake, 128, fake, fake, None) == 0
+    lib.csa2_compress_kv.argtypes = [vp, vp, vp, i64, i32, vp, vp, vp, vp]
+    assert lib.csa2_compress_kv(fake, fake, fake, 10, 0, fake, fake, None, None) == -1     # m < 1
+    assert lib.csa2_compress_kv(fake, fake, fake, 10, 4, fake, fake, None, None) == -2     # partial block
+    assert lib.csa2_compress_kv(odd, fake, fake, 8, 2, fake, fake, None, None) == -3
+    assert lib.csa2_compress_kv(fake, fake, fake, 0, 2, fake, fake, None, None) == 0
+    lib.csa2_prefill_index_score_compressed.argtypes = [vp, vp, vp, i32, vp, vp, i64, i64, i32, vp, vp]
+    # entries visible to the last query beyond the plane: refused
+    assert lib.csa2_prefill_index_score_compressed(fake, fake, fake, 8, fake, fake, 100, 200, 2, fake, None) == -1
+    assert lib.csa2_prefill_index_score_compressed(fake, fake, fake, 8, fake, fake, 100, 0, 0, fake, None) == -1
+    lib.csa2_sparse_attn_prefill_replay.argtypes = [vp, i32, vp, vp, i64, vp, i32, vp, i32, i32, ctypes.c_float,
+                                                    vp, vp, vp, vp, sz, vp]
+    assert lib.csa2_sparse_attn_prefill_replay(fake, 4, fake, fake, 100, fake, 8, fake, 16, -1, 1.0, fake, None,
+                                               None, fake, 1 << 30, None) == -1      # negative replay row
+    assert lib.csa2_sparse_attn_prefill_replay(fake, 0, fake, fake, 100, fake, 8, fake, 16, 3, 1.0, fake, None,
+                                               None, fake, 1 << 30, None) == 0
+    lib.csa2_topk_candidates.argtypes = [vp, i32, i64, vp, vp, i32, i64, vp, vp]
+    assert lib.csa2_topk_candidates(fake, 1, 10, None, fake, 0, 0, fake, None) == -1
+    assert lib.csa2_topk_candidates(fake, 1, 10, None, fake, 4, 0, vp((1 << 20) + 4), None) == -3
+    assert lib.csa2_topk_candidates(fake, 1, 10, None, fake, 4, (1 << 31) - 5, fake, None) == -2
+    lib.csa2_topk_merge.argtypes = [vp, i32, i32, i32, i32, vp, vp, sz, vp]
+    assert lib.csa2_topk_merge(fake, 2, 1, 8, 0, fake, fake, 1 << 20, None) == -2
+    assert lib.csa2_topk_merge(fake, 2, 1, 8, 8, fake, fake, 16, None) == -6
+    lib.csa2_shard_positions.argtypes = [vp, i32, i32, i64, i64, vp, vp]
+    assert lib.csa2_shard_positions(fake, 1, 8, 10, 5, fake, None) == -1                  # hi < lo
+    lib.csa2_shard_pool.argtypes = [vp, i32, i32, i32, i64, i64, vp, vp, vp]
+    assert lib.csa2_shard_pool(fake, 1, 8, 0, 0, 8, None, fake, None) == -1
+    lib.csa2_attn_merge.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp]
+    assert lib.csa2_attn_merge(fake, fake, 0, 1, fake, None, None, None) == -1
+    assert lib.csa2_attn_merge(odd, fake, 2, 1, fake, None, None, None) == -3
+    assert lib.csa2_attn_merge(fake, fake, 2, 0, fake, None, None, None) == 0
+    lib.csa2_block_max.argtypes = [vp, i32, i64, vp, i32, vp, vp]
+    assert lib.csa2_block_max(fake, 1, 10, None, 0, fake, None) == -1
+    assert lib.csa2_block_max(fake, 0, 10, None, 8, fake, None) == 0
+    lib.csa2_index_topk_bf16.argtypes = [vp, vp, i32, vp, vp, i64, vp, vp, i64, i32, vp, i32, vp, vp, sz, vp]
+    assert lib.csa2_index_topk_bf16(None, fake, 1, fake, fake, 128, fake, None, 128, 8, fake, 0, None, fake,
+                                    1 << 30, None) == -1
+
+
+def test_merge_workspace_and_launch_counts_are_host_arithmetic(lib):
+    lib.csa2_topk_merge_workspace_size.restype = ctypes.c_size_t
+    lib.csa2_topk_merge_workspace_size.argtypes = [ctypes.c_int32] * 4
+    a = lib.csa2_topk_merge_workspace_size(4, 32, 512, 512)
+    assert a >= 2 * 32 * 4 * 512 * 4
+    assert lib.csa2_topk_merge_workspace_size(0, 32, 512, 512) == 0
