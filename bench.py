@@ -151,6 +151,14 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def step_config(wl, B, N, L, K, W, world):
+    """The `config` object of the bench line, shared by both arms."""
+    return {"workload": wl.name if B == wl.B else f"{wl.name}_batch{B}", "sequences_per_gpu": B,
+            "visible_entries": N, "layers_sharing_topk": L,
+            "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
+            "l2": "flushed between steps (512 MiB write + 512 MiB read)", "parallelism": f"dp{world} (sequences)"}
+
+
 # ---------------------------------------------------------------------------- GPU arm
 
 def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device):
@@ -454,10 +462,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e2m1/e4m3/e8m0 storage; fp32 scores; bf16 attention with fp32 accumulate",
         "data": "synthetic N(0,1) caches drawn on the device, packed by the library",
-        "config": {"workload": wl.name if B == wl.B else f"{wl.name}_batch{B}", "sequences_per_gpu": B,
-                   "visible_entries": N, "layers_sharing_topk": L,
-                   "indexer": "32 heads x 128 MXFP4", "topk": K, "heads": 64, "head_dim": 512, "swa": W,
-                   "l2": "flushed between steps (512 MiB write + 512 MiB read)", "parallelism": f"dp{world} (sequences)"},
+        "config": step_config(wl, B, N, L, K, W, world),
         "launch": "CUDA graph of the step (programmatic dependent launches)" if graph is not None else "eager",
         "ms_per_step_eager": round(eager_ms, 5),
         "stages_ms": dict([(nm, round(v, 5)) for (nm, _), v in zip(stages, stage_ms)] +
@@ -716,7 +721,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(qps, 3), "unit": "queries/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (oracle)", "data": "synthetic",
-        "config": {"workload": "full_decode_b32_n65536", "visible_entries": N, "topk": 512},
+        "config": step_config(WORKLOADS[WORKLOAD_ID], WORKLOADS[WORKLOAD_ID].B, N, WORKLOADS[WORKLOAD_ID].L, 512,
+                              128, world),
         "cpu_baseline": {"value": round(qps, 3), "unit": "queries/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n_seq} sequence(s) x {N} entries per step"},
         "e2e": {"value": round(qps, 3), "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
