@@ -50,7 +50,9 @@ constexpr int kOffBars = kOffSfb + 512;
 constexpr int kNumBars = 2 * kStages + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kOffHist = kOffMisc + 16;               // Top-K histogram of this CTA's scores
-constexpr int kSmemBytes = kOffHist + kTopkHistBins * 4 + 1024;  // + alignment slack
+constexpr int kRing = 16;                             // tile index of each tile in flight (claimed mode)
+constexpr int kOffRing = kOffHist + kTopkHistBins * 4;
+constexpr int kSmemBytes = kOffRing + kRing * 4 + 1024;  // + alignment slack
 static_assert(kOffQ % 1024 == 0, "q operand must be 1024-byte aligned");
 
 struct Params {
@@ -74,6 +76,15 @@ struct Params {
   // optional [B][32][128] bf16 indexer q: quantised to MXFP4 in the prologue
   // (the same block encoder as csa2_quant_mxfp4) instead of reading q_data
   const uint16_t* q_bf16;
+  // optional tile counters, sequence b's at tile_ctr[b * tile_ctr_stride],
+  // zero when the preceding kernel ends (dense mode): after its first
+  // `claim0` tiles (a fixed range, read at once) each CTA of a sequence claims
+  // `claim` tiles at a time from the counter, so that CTAs with a larger share
+  // of the memory bandwidth take more tiles
+  int32_t* tile_ctr;
+  int32_t tile_ctr_stride;
+  int32_t claim0;
+  int32_t claim;
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -97,8 +108,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + kOffHist);
+  volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(sm + kOffRing);
   const bool with_hist = p.hist != nullptr;
   const bool pos_mode = p.positions != nullptr;
+  // claimed mode: tiles come from the sequence's counter, their indices pass
+  // from the producer to the MMA warp and the epilogue through s_ring; a tile
+  // index of -1 ends the stream
+  const bool claimed = !pos_mode && p.tile_ctr != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
@@ -114,6 +130,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   int64_t t_end = pos_mode ? t_end_all : (nv + kTileRows - 1) / kTileRows;
   if (t_end > t_end_all) t_end = t_end_all;
   const int n_tiles = t_end > t_begin ? (int)(t_end - t_begin) : 0;
+  // claimed mode: tiles 0 .. t_vis-1 of the sequence hold visible entries
+  const int64_t t_vis_ = (nv + kTileRows - 1) / kTileRows;
+  const int32_t t_vis = (int32_t)(t_vis_ < n_tiles_all ? t_vis_ : n_tiles_all);
 
   // ---- set-up: barriers, the q operand (B) and its scales, tensor memory ----
   if (threadIdx.x == 0) {
@@ -210,16 +229,52 @@ __global__ void __launch_bounds__(kThreads, 3)
     // ---- TMA producer ----
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < n_tiles; ++i) {
+      const auto issue = [&](int i, int64_t tile) -> bool {
         const int s = i % kStages;
         const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, &g_index_error)) break;
-        const int64_t row0 = (t_begin + i) * kTileRows;
+        if (!tc::mbar_wait_bounded(&empty[s], ph ^ 1u, s_abort, &g_index_error)) return false;
+        const int64_t row0 = tile * kTileRows;
+        if (claimed) s_ring[i % kRing] = (int32_t)tile;
         tc::mbar_arrive_expect_tx(&full[s], kTileBytes + kSfBytes);
         tc::tma_load_3d(sA + s * kTileBytes, &tmap_ik, 0, (int32_t)row0, b, &full[s]);
         tc::bulk_load(sSfRaw + s * kSfBytes, p.ik_scale + ((int64_t)b * p.cap + row0) * kIkScales, kSfBytes,
                       &full[s]);
-        ++issued;
+        return true;
+      };
+      if (claimed) {
+        bool ok = true;
+        // the fixed first range: tiles [x * claim0, x * claim0 + claim0)
+        const int32_t c0 = (int32_t)blockIdx.x * p.claim0;
+        for (int32_t t = c0; ok && t < c0 + p.claim0 && t < t_vis; ++t) {
+          ok = issue(issued, t);
+          if (ok) ++issued;
+        }
+        // the counter is cleared by the preceding kernel
+        if (p.early_reads) pdl_wait();
+        const int32_t base = (int32_t)gridDim.x * p.claim0;
+        const int32_t step = p.claim > 0 ? p.claim : 1;
+        while (ok && base < t_vis) {
+          const int32_t c = base + atomicAdd(p.tile_ctr + (int64_t)b * p.tile_ctr_stride, step);
+          if (c >= t_vis) break;
+          const int32_t ce = c + step < t_vis ? c + step : t_vis;
+          for (int32_t t = c; ok && t < ce; ++t) {
+            ok = issue(issued, t);
+            if (ok) ++issued;
+          }
+        }
+        if (ok) {
+          // the end of the stream: one more stage, no bytes, tile index -1
+          const int s = issued % kStages;
+          if (tc::mbar_wait_bounded(&empty[s], ((uint32_t)(issued / kStages) & 1u) ^ 1u, s_abort, &g_index_error)) {
+            s_ring[issued % kRing] = -1;
+            tc::mbar_arrive(&full[s]);
+          }
+        }
+      } else {
+        for (int i = 0; i < n_tiles; ++i) {
+          if (!issue(i, t_begin + i)) break;
+          ++issued;
+        }
       }
       if (*s_abort) {
         // let copies already in flight land before the CTA's memory goes away
@@ -236,11 +291,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     const uint64_t bdesc1 = tc::smem_desc(q_addr + 32, 0, 512, tc::kSwizzle64B);
     constexpr uint32_t idesc0 = tc::idesc_mxf4(128, 32, 0, 0);
     constexpr uint32_t idesc1 = tc::idesc_mxf4(128, 32, 2, 2);
-    if (lane == 0 && n_tiles > 0)
+    // q's scales into tensor memory, for every CTA that may score a tile (in
+    // claimed mode any CTA of the sequence may)
+    if (lane == 0 && (claimed || n_tiles > 0))
       tc::tmem_cp_32x128_x4(tmem + kSfbCol, tc::smem_desc(tc::smem_u32(sSfb), 0, 128, tc::kSwizzleNone));
     __syncwarp();
     int last = -1;
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = 0; claimed || i < n_tiles; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       const int a = i & 1;
@@ -248,6 +305,10 @@ __global__ void __launch_bounds__(kThreads, 3)
       bool ok = tc::mbar_wait_bounded(&acc_empty[a], aph ^ 1u, s_abort, &g_index_error) &&
                 tc::mbar_wait_bounded(&full[s], ph, s_abort, &g_index_error);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (claimed && s_ring[i % kRing] < 0) {
+        if (lane == 0) tc::mbar_arrive(&acc_full[a]);  // passes the end on to the epilogue
+        break;
+      }
       // scales of keys lane, lane+32, lane+64, lane+96 -> one 16-byte row
       const uint32_t* raw = reinterpret_cast<const uint32_t*>(sSfRaw + s * kSfBytes);
       uint4 v = make_uint4(raw[lane], raw[lane + 32], raw[lane + 64], raw[lane + 96]);
@@ -282,11 +343,13 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int row = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     float* out = p.scores + (int64_t)b * p.n_pos;
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = 0; claimed || i < n_tiles; ++i) {
       const int a = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
       // warp-uniform outcome: tcgen05.ld below needs the whole warp
       if (!__all_sync(0xffffffffu, tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error))) break;
+      const int64_t tile = claimed ? (int64_t)s_ring[i % kRing] : t_begin + i;
+      if (tile < 0) break;
       tc::tc_fence_after();
       uint32_t r[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_base + acc_col(a), r);
@@ -297,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       float sc = 0.0f;
 #pragma unroll
       for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);
-      const int64_t li = (t_begin + i) * kTileRows + row;  // list index
+      const int64_t li = tile * kTileRows + row;  // list index
       bool valid = li < nv;
       if (pos_mode) {
         const int32_t pp = li < p.n_pos ? p.positions[(int64_t)b * p.n_pos + li] : -1;
@@ -316,14 +379,19 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (with_hist && valid && score_is_candidate(sc))
         atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
     }
-    // positions of this CTA's range past the visible entries
-    const int64_t lo = (t_begin > t_end ? t_begin : t_end) * kTileRows;
-    int64_t hi = t_end_all * kTileRows;
-    if (hi > p.n_pos) hi = p.n_pos;
-    for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
-    if (p.bmax && hi > lo) {
-      float* bm = p.bmax + (int64_t)b * ((p.n_pos + 7) / 8);
-      for (int64_t j = lo / 8 + threadIdx.x; j < (hi + 7) / 8; j += 128) bm[j] = -INFINITY;
+    // tiles past the visible entries: this CTA's range, or in claimed mode
+    // every gridDim.x-th tile from t_vis + blockIdx.x
+    const int64_t fill_lo = claimed ? t_vis + (int64_t)blockIdx.x : (t_begin > t_end ? t_begin : t_end);
+    const int64_t fill_hi = claimed ? n_tiles_all : t_end_all;
+    const int64_t fill_step = claimed ? (int64_t)gridDim.x : 1;
+    for (int64_t t = fill_lo; t < fill_hi; t += fill_step) {
+      const int64_t lo = t * kTileRows;
+      const int64_t hi = lo + kTileRows < p.n_pos ? lo + kTileRows : p.n_pos;
+      for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
+      if (p.bmax) {
+        float* bm = p.bmax + (int64_t)b * ((p.n_pos + 7) / 8);
+        for (int64_t j = lo / 8 + threadIdx.x; j < (hi + 7) / 8; j += 128) bm[j] = -INFINITY;
+      }
     }
   }
   tc::tc_fence_before();

@@ -53,8 +53,10 @@ constexpr int kHist2Shift = 32 - kHistBits - kHist2Bits;  // 9: second-level dig
 struct RowCounters {
   int32_t t;       // threshold bin (-1: fewer candidates than k)
   uint32_t above;  // candidates in bins above t
-  uint32_t pad[6];
+  uint32_t pad[5];
+  int32_t scan_tiles;  // tiles claimed by the decode scan that fills the histogram
 };
+static_assert(sizeof(RowCounters) == 32 && offsetof(RowCounters, scan_tiles) % 4 == 0, "row counter layout");
 
 struct TopkWs {
   uint32_t* hist;     // [B][kHistBins]  top 12 key bits
@@ -973,9 +975,10 @@ extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {
 
 // Clears the histogram and counters of a Top-K workspace (a kernel enqueued on
 // `stream`) and returns the per-row histogram [B][kTopkHistBins] that a
-// producer of the scores may fill (the decode scan does it in its epilogue).
+// producer of the scores may fill (the decode scan does it in its epilogue),
+// and the per-row tile counters (zeroed too) it may claim its tiles from.
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
-                      cudaStream_t stream, uint32_t** hist) {
+                      cudaStream_t stream, uint32_t** hist, int32_t** scan_ctr, int32_t* scan_ctr_stride) {
   size_t need = topk_ws_layout(B, n, k, nullptr, nullptr);
   if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
   TopkWs ws;
@@ -985,6 +988,8 @@ int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t w
     CSA2_LAUNCH_PDL(zero_kernel, dim3((unsigned)((words + 255) / 256 < 304 ? (words + 255) / 256 : 304)), dim3(256),
                     0, stream, (uint4*)workspace, words);
   if (hist) *hist = ws.hist;
+  if (scan_ctr) *scan_ctr = &ws.cnt[0].scan_tiles;
+  if (scan_ctr_stride) *scan_ctr_stride = (int32_t)(sizeof(RowCounters) / sizeof(int32_t));
   return CSA2_OK;
 }
 
@@ -1011,7 +1016,7 @@ int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t
 int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
                      int32_t k, int32_t* idx, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B == 0) return CSA2_OK;
-  int rc = csa2_topk_prepare(B, n, k, workspace, workspace_bytes, stream, nullptr);
+  int rc = csa2_topk_prepare(B, n, k, workspace, workspace_bytes, stream, nullptr, nullptr, nullptr);
   if (rc) return rc;
   TopkWs ws;
   topk_ws_layout(B, n, k, &ws, (char*)workspace);

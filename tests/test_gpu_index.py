@@ -172,6 +172,26 @@ def test_index_topk_with_pool_and_reindex(csa2):
         check_topk(rs, got_r[b], k, positions=pos)
 
 
+def test_index_topk_scans_every_tile_once_when_claimed(csa2):
+    """Long ragged rows, 8 sequences: past a fixed first range per CTA the
+    fused scan's CTAs claim tiles from a per-row counter. The workspace starts
+    filled with huge finite scores, so a visible tile that no CTA scored would
+    rank first and break the Top-K against the oracle."""
+    Ns = [60001, 50000, 65536, 45000, 61234, 58000, 47000, 64000]
+    case = DecodeCase(workload=94, Ns=Ns, gen_device="cuda")
+    g = case.to_device()
+    k = 512
+    idx = torch.empty(case.B, k, dtype=torch.int32, device="cuda")
+    ws = csa2.index_topk_workspace(case.B, case.cap, k)
+    ws.fill_(0x7F)  # every float of the workspace reads 3.39e38
+    csa2.csa2_index_topk(g["q_data"], g["q_e8m0"], g["w"], g["ik_data"], g["ik_scale"], g["n_visible"], k, idx, ws)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    got = idx.cpu().numpy()
+    for b in range(case.B):
+        check_topk(case.oracle_scores(b), got[b], k)
+
+
 def test_prefill_index_score(csa2):
     from fp4_kv_cache_02_gb300.inputs import prefill_chunk
     T, N0 = 6, 2000
