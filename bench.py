@@ -337,15 +337,17 @@ def run_gpu(args):
     ms = sum(a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)) / args.steps
     ms_max = reduce_max(ms, world, device)
 
-    # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed) ----
+    # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed),
+    # scheduled as inside the step: tiles claimed from per-sequence counters ----
     csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc)
+    tile_ctr = torch.zeros(2 * B, dtype=torch.int32, device=device)
     scan_ms = 0.0
     for _ in range(args.steps):
         flush_l2()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        csa2.csa2_index_score(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"], scores,
-                              stream=stream)
+        csa2.csa2_index_score_claimed(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"],
+                                      scores, tile_ctr, stream=stream)
         b_.record(stream)
         b_.synchronize()
         scan_ms += a.elapsed_time(b_)

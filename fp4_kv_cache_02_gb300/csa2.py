@@ -62,6 +62,7 @@ def _load():
         "csa2_unpack_fp8_e4m3": (ctypes.c_int, [vp, i64, vp, vp]),
         "csa2_kv_append": (ctypes.c_int, [vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, vp, vp]),
         "csa2_index_score": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, vp, i64, vp, vp]),
+        "csa2_index_score_claimed": (ctypes.c_int, [vp, vp, vp, i32, vp, vp, i64, vp, i64, vp, vp, vp]),
         "csa2_topk_workspace_size": (sz, [i32, i64, i32]),
         "csa2_topk": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp, sz, vp]),
         "csa2_topk_static": (ctypes.c_int, [vp, i32, i64, vp, vp, i32, vp, vp]),
@@ -225,6 +226,21 @@ def csa2_index_score(q_data, q_e8m0, w, ik_data, ik_scale, n_visible, scores, po
     n_pos = scores.shape[1]
     _call("csa2_index_score", _p(q_data), _p(q_e8m0), _p(w), B, _p(ik_data), _p(ik_scale), cap,
           _p(n_visible), _p(positions), n_pos, _p(scores), _s(stream))
+
+
+def csa2_index_score_claimed(q_data, q_e8m0, w, ik_data, ik_scale, n_visible, scores, tile_counters, stream=None):
+    """As csa2_index_score without positions; tile_counters [2*B] int32, zero
+    before the first call and left zero by every call."""
+    for t, n in ((q_data, "q_data"), (q_e8m0, "q_e8m0"), (ik_data, "ik_data"), (ik_scale, "ik_scale")):
+        _req(t, torch.uint8, n)
+    _req(w, torch.float32, "w"); _req(n_visible, torch.int32, "n_visible"); _req(scores, torch.float32, "scores")
+    _req(tile_counters, torch.int32, "tile_counters")
+    B, cap = ik_data.shape[0], ik_data.shape[1]
+    n_pos = scores.shape[1]
+    if tile_counters.numel() < 2 * B:
+        raise ValueError("tile_counters needs 2 * B int32")
+    _call("csa2_index_score_claimed", _p(q_data), _p(q_e8m0), _p(w), B, _p(ik_data), _p(ik_scale), cap,
+          _p(n_visible), n_pos, _p(scores), _p(tile_counters), _s(stream))
 
 
 def csa2_topk(scores, k, idx, workspace, n_valid=None, positions=None, stream=None):

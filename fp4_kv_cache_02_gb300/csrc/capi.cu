@@ -7,7 +7,8 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
                                uint32_t* hist, float* bmax, int early_reads, const void* q_bf16,
-                               int32_t* tile_ctr, int32_t tile_ctr_stride, cudaStream_t stream);
+                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done,
+                               cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist, int32_t** scan_ctr, int32_t* scan_ctr_stride);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -75,7 +76,21 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                    nullptr, nullptr, 0, nullptr, nullptr, 0, (cudaStream_t)stream);
+                                    nullptr, nullptr, 0, nullptr, nullptr, 0, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int csa2_index_score_claimed(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
+                                        const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
+                                        const int32_t* n_visible, int64_t n_pos, float* scores,
+                                        int32_t* tile_counters, csa2_stream_t stream) {
+  int rc = check_index_args(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, n_pos);
+  if (rc) return rc;
+  if (!scores || !tile_counters || n_pos > cap) return CSA2_ERR_INVALID_ARG;
+  if (!csa2_aligned(tile_counters, 8)) return CSA2_ERR_ALIGNMENT;
+  // sequence b's counter and finished-CTA count: tile_counters[2b], [2b + 1]
+  return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, nullptr, n_pos, scores,
+                                    nullptr, nullptr, 0, nullptr, tile_counters, 2, tile_counters + 1,
+                                    (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
@@ -128,7 +143,8 @@ static int index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const void* 
   rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist, &scan_ctr, &scan_ctr_stride);
   if (rc) return rc;
   rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                  hist, bmax, 1, q_bf16, scan_ctr, scan_ctr_stride, s);  // just after the workspace clear
+                                  hist, bmax, 1, q_bf16, scan_ctr, scan_ctr_stride, nullptr,
+                                  s);  // just after the workspace clear
   if (rc) return rc;
   rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);
   if (rc) return rc;

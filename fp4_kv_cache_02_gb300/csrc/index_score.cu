@@ -68,7 +68,8 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
                                uint32_t* hist, float* bmax, int early_reads, const void* q_bf16,
-                               int32_t* tile_ctr, int32_t tile_ctr_stride, cudaStream_t stream) {
+                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done,
+                               cudaStream_t stream) {
   if (n_pos == 0 || B == 0) return CSA2_OK;
   if (q_bf16 ? !csa2_aligned(q_bf16, 16) : (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)))
     return CSA2_ERR_ALIGNMENT;
@@ -102,7 +103,8 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
   // pipeline's depth, then claims of two tiles
   scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
                       hist, positions ? nullptr : bmax, early_reads, (const uint16_t*)q_bf16,
-                      positions ? nullptr : tile_ctr, tile_ctr_stride, scan_tc::kStages, 2};
+                      positions ? nullptr : tile_ctr, tile_ctr_stride, scan_tc::kStages, 2,
+                      positions ? nullptr : tile_done};
   CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)chunks, (unsigned)B), dim3(scan_tc::kThreads),
                   (size_t)scan_tc::kSmemBytes, stream, map, prm);
   return CSA2_OK;

@@ -85,6 +85,9 @@ struct Params {
   int32_t tile_ctr_stride;
   int32_t claim0;
   int32_t claim;
+  // optional, beside tile_ctr (same stride): CTAs of the sequence that have
+  // finished; the last one puts both words back to zero for the next launch
+  int32_t* tile_done;
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -399,6 +402,15 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (warp == kMmaWarp) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (claimed && p.tile_done && threadIdx.x == 0) {
+    // every CTA of the sequence has made its last claim once all have arrived here
+    __threadfence();
+    int32_t* done = p.tile_done + (int64_t)b * p.tile_ctr_stride;
+    if (atomicAdd(done, 1) == (int32_t)gridDim.x - 1) {
+      p.tile_ctr[(int64_t)b * p.tile_ctr_stride] = 0;
+      *done = 0;
+    }
   }
   if (with_hist) {
     if (p.early_reads) pdl_wait();

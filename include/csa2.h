@@ -202,6 +202,26 @@ int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0,
                      int64_t n_pos, float* scores, csa2_stream_t stream);
 
 /**
+ * The same scores as csa2_index_score with positions == NULL, with another
+ * schedule. csa2_index_score gives each CTA a fixed range of a sequence's
+ * 128-entry tiles. Here, after one fixed pipeline depth, the CTAs of a
+ * sequence claim tiles two at a time from a counter, so CTAs with a larger
+ * share of the memory bandwidth take more (csa2_index_topk schedules its scan
+ * this way, with counters in its workspace).
+ *   tile_counters [2 * B] int32, device, 8-byte aligned, owned by the caller:
+ *   all zero before the first call; every call that completes leaves them
+ *   zero again. Calls that may run at the same time need their own buffers.
+ *   Other arguments as csa2_index_score (n_pos <= cap).
+ * Errors: INVALID_ARG (also a NULL tile_counters), ALIGNMENT, CUDA.
+ */
+int csa2_index_score_claimed(const uint8_t* q_data, const uint8_t* q_e8m0,
+                             const float* w, int32_t B, const uint8_t* ik_data,
+                             const uint8_t* ik_scale, int64_t cap,
+                             const int32_t* n_visible, int64_t n_pos,
+                             float* scores, int32_t* tile_counters,
+                             csa2_stream_t stream);
+
+/**
  * Bytes of workspace csa2_topk needs for B rows of n scores and a given k.
  */
 size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k);

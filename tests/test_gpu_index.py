@@ -192,6 +192,33 @@ def test_index_topk_scans_every_tile_once_when_claimed(csa2):
         check_topk(case.oracle_scores(b), got[b], k)
 
 
+def test_claimed_scan_equals_fixed_ranges_and_leaves_counters_zero(csa2):
+    """csa2_index_score_claimed gives the bytes csa2_index_score gives (same
+    kernel, tiles claimed from counters instead of fixed ranges), on long
+    ragged rows where most CTAs claim past a fixed first range, and leaves its
+    counters at zero for the next call."""
+    Ns = [60001, 50000, 65536, 45000, 61234, 58000, 47000, 64000]
+    case = DecodeCase(workload=94, Ns=Ns, gen_device="cuda")
+    g = case.to_device()
+    ref = torch.empty(case.B, case.cap, dtype=torch.float32, device="cuda")
+    csa2.csa2_index_score(g["q_data"], g["q_e8m0"], g["w"], g["ik_data"], g["ik_scale"], g["n_visible"], ref)
+    ctr = torch.zeros(2 * case.B, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        got = torch.full_like(ref, 3.0e38)
+        csa2.csa2_index_score_claimed(g["q_data"], g["q_e8m0"], g["w"], g["ik_data"], g["ik_scale"], g["n_visible"],
+                                      got, ctr)
+        torch.cuda.synchronize()
+        assert csa2.csa2_get_last_error() == 0
+        assert torch.equal(got, ref)
+        assert int(ctr.abs().sum()) == 0
+    # and the scores themselves against the oracle on two rows
+    r = ref.cpu().numpy()
+    for b in (3, 7):
+        s_ = case.oracle_scores(b)
+        _scores_close(r[b, :Ns[b]], s_)
+        assert np.all(r[b, Ns[b]:] == -np.inf)
+
+
 def test_prefill_index_score(csa2):
     from fp4_kv_cache_02_gb300.inputs import prefill_chunk
     T, N0 = 6, 2000

@@ -59,6 +59,11 @@ def test_host_argument_checks_without_gpu(lib):
     assert lib.csa2_topk(fake, 1, 100, None, None, 8, fake, fake, 16, None) == -6   # workspace too small
     lib.csa2_index_score.argtypes = [vp, vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, vp, vp]
     assert lib.csa2_index_score(fake, fake, fake, 1, fake, fake, 100, fake, None, 100, fake, None) == -3  # cap % 128
+    lib.csa2_index_score_claimed.argtypes = [vp, vp, vp, ctypes.c_int32, vp, vp, ctypes.c_int64, vp, ctypes.c_int64,
+                                             vp, vp, vp]
+    assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 128, fake, None, None) == -1
+    assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 256, fake, fake, None) == -1
+    assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 128, fake, vp(4100), None) == -3
     lib.csa2_status_string.restype = ctypes.c_char_p
     assert lib.csa2_status_string(-6) == b"workspace too small or misaligned"
 
