@@ -6,7 +6,10 @@
 // s = sum_h w_h ReLU(q_h . k) with 32 heads x 128 channels, q and k both
 // MXFP4 (E2M1 values, one E8M0 scale per 32).
 //
-// One CTA scans a contiguous run of 128-key tiles of one sequence:
+// One CTA scans 128-key tiles of one sequence: a contiguous run, or (claimed
+// mode, dense rows) a fixed first range of one pipeline depth and then tiles
+// claimed two at a time from the sequence's counter, so that CTAs with a
+// larger share of the memory bandwidth take more of them:
 //   warp 4       TMA producer: 128 x 64 B E2M1 tile (3-D tensor map, 64-byte
 //                swizzle) + the tile's 512 B of E8M0 scales (bulk copy) per
 //                pipeline stage;
