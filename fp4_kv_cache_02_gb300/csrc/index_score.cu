@@ -105,7 +105,7 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
                       hist, positions ? nullptr : bmax, early_reads, (const uint16_t*)q_bf16,
                       positions ? nullptr : tile_ctr, tile_ctr_stride, scan_tc::kStages, 2,
                       positions ? nullptr : tile_done};
-  CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)chunks, (unsigned)B), dim3(scan_tc::kThreads),
+  CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)B, (unsigned)chunks), dim3(scan_tc::kThreads),
                   (size_t)scan_tc::kSmemBytes, stream, map, prm);
   return CSA2_OK;
 }

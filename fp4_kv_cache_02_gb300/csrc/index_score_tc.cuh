@@ -123,14 +123,17 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool claimed = !pos_mode && p.tile_ctr != nullptr;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
+  // grid (sequences, chunks): consecutive CTAs belong to different sequences,
+  // so each sequence's CTAs spread over the SMs of both dies
+  const int b = blockIdx.x;
+  const int chunk = blockIdx.y, n_chunks = gridDim.y;
   const int64_t n_tiles_all = (p.n_pos + kTileRows - 1) / kTileRows;
   int64_t nv = (int64_t)p.n_visible[b];
   // positions mode: a listed position is scored when it is below n_visible
   // (and the capacity); dense mode: entries 0..nv-1 of the list
   const int64_t nv_pos = nv < 0 ? 0 : (nv > p.cap ? p.cap : nv);
   nv = nv < 0 ? 0 : (nv > p.n_pos ? p.n_pos : nv);
-  const int64_t t_begin = (int64_t)blockIdx.x * p.tiles_per_cta;
+  const int64_t t_begin = (int64_t)chunk * p.tiles_per_cta;
   int64_t t_end_all = t_begin + p.tiles_per_cta;
   if (t_end_all > n_tiles_all) t_end_all = n_tiles_all;
   int64_t t_end = pos_mode ? t_end_all : (nv + kTileRows - 1) / kTileRows;
@@ -250,14 +253,14 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (claimed) {
         bool ok = true;
         // the fixed first range: tiles [x * claim0, x * claim0 + claim0)
-        const int32_t c0 = (int32_t)blockIdx.x * p.claim0;
+        const int32_t c0 = (int32_t)chunk * p.claim0;
         for (int32_t t = c0; ok && t < c0 + p.claim0 && t < t_vis; ++t) {
           ok = issue(issued, t);
           if (ok) ++issued;
         }
         // the counter is cleared by the preceding kernel
         if (p.early_reads) pdl_wait();
-        const int32_t base = (int32_t)gridDim.x * p.claim0;
+        const int32_t base = (int32_t)n_chunks * p.claim0;
         const int32_t step = p.claim > 0 ? p.claim : 1;
         while (ok && base < t_vis) {
           const int32_t c = base + atomicAdd(p.tile_ctr + (int64_t)b * p.tile_ctr_stride, step);
@@ -386,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
     }
     // tiles past the visible entries: this CTA's range, or in claimed mode
-    // every gridDim.x-th tile from t_vis + blockIdx.x
-    const int64_t fill_lo = claimed ? t_vis + (int64_t)blockIdx.x : (t_begin > t_end ? t_begin : t_end);
+    // every n_chunks-th tile from t_vis + chunk
+    const int64_t fill_lo = claimed ? t_vis + (int64_t)chunk : (t_begin > t_end ? t_begin : t_end);
     const int64_t fill_hi = claimed ? n_tiles_all : t_end_all;
-    const int64_t fill_step = claimed ? (int64_t)gridDim.x : 1;
+    const int64_t fill_step = claimed ? (int64_t)n_chunks : 1;
     for (int64_t t = fill_lo; t < fill_hi; t += fill_step) {
       const int64_t lo = t * kTileRows;
       const int64_t hi = lo + kTileRows < p.n_pos ? lo + kTileRows : p.n_pos;
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     // every CTA of the sequence has made its last claim once all have arrived here
     __threadfence();
     int32_t* done = p.tile_done + (int64_t)b * p.tile_ctr_stride;
-    if (atomicAdd(done, 1) == (int32_t)gridDim.x - 1) {
+    if (atomicAdd(done, 1) == n_chunks - 1) {
       p.tile_ctr[(int64_t)b * p.tile_ctr_stride] = 0;
       *done = 0;
     }
