@@ -219,6 +219,25 @@ def test_claimed_scan_equals_fixed_ranges_and_leaves_counters_zero(csa2):
         assert np.all(r[b, Ns[b]:] == -np.inf)
 
 
+def test_claimed_scan_edges(csa2):
+    """Claimed scan on a small ragged case: an empty row, a row of one entry,
+    rows shorter than the fixed first ranges, n_pos below the capacity; the
+    bytes equal the fixed-range scan's and the counters return to zero."""
+    case = DecodeCase(workload=95, Ns=[0, 1, 700, 4093, 129])
+    g = case.to_device()
+    for n_pos in (case.cap, case.cap - 128):
+        ref = torch.empty(case.B, n_pos, dtype=torch.float32, device="cuda")
+        csa2.csa2_index_score(g["q_data"], g["q_e8m0"], g["w"], g["ik_data"], g["ik_scale"], g["n_visible"], ref)
+        ctr = torch.zeros(2 * case.B, dtype=torch.int32, device="cuda")
+        got = torch.full_like(ref, 3.0e38)
+        csa2.csa2_index_score_claimed(g["q_data"], g["q_e8m0"], g["w"], g["ik_data"], g["ik_scale"], g["n_visible"],
+                                      got, ctr)
+        torch.cuda.synchronize()
+        assert csa2.csa2_get_last_error() == 0
+        assert torch.equal(got, ref)
+        assert int(ctr.abs().sum()) == 0
+
+
 def test_prefill_index_score(csa2):
     from fp4_kv_cache_02_gb300.inputs import prefill_chunk
     T, N0 = 6, 2000
