@@ -64,6 +64,7 @@ def test_host_argument_checks_without_gpu(lib):
     assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 128, fake, None, None) == -1
     assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 256, fake, fake, None) == -1
     assert lib.csa2_index_score_claimed(fake, fake, fake, 1, fake, fake, 128, fake, 128, fake, vp(4100), None) == -3
+    assert lib.csa2_index_score_claimed(fake, fake, fake, 0, fake, fake, 128, fake, 128, fake, fake, None) == 0  # B = 0
     lib.csa2_status_string.restype = ctypes.c_char_p
     assert lib.csa2_status_string(-6) == b"workspace too small or misaligned"
 
