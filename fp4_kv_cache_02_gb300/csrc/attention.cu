@@ -191,17 +191,8 @@ static constexpr int kMaxClusterSplit = attn_tc::kMaxClusterChunks;  // portable
 
 // Opts the partial kernel into its dynamic shared memory, once per device.
 static int attn_kernel_attr() {
-  constexpr int kMaxDevices = 64;
-  static bool done[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
-  if (!done[dev]) {
-    if (cudaFuncSetAttribute(attn_tc::attn_partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attn_tc::kSmemBytes) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    done[dev] = true;
-  }
-  return CSA2_OK;
+  static Csa2PerDeviceOnce optin;
+  return csa2_smem_optin((const void*)attn_tc::attn_partial_tc_kernel, attn_tc::kSmemBytes, optin);
 }
 
 // How many clusters of `size` partial CTAs can be resident at once (0 when a

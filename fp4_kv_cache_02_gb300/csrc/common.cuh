@@ -11,6 +11,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/csa2.h"
 
 namespace csa2 {
@@ -164,6 +166,31 @@ static inline cudaError_t csa2_launch_pdl_cluster(void (*kernel)(KArgs...), dim3
       return CSA2_ERR_CUDA;                                 \
     }                                                       \
   } while (0)
+
+// Per-device "done" flags of one one-time set-up step, with the lock that
+// orders the first calls of several host threads.
+struct Csa2PerDeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  bool done[kMaxDevices] = {};
+};
+
+// Opts `kernel` into `bytes` of dynamic shared memory on the current device,
+// once per device (the attribute is per device; a kernel launched on a device
+// where it was never set fails to launch above 48 KB).
+static inline int csa2_smem_optin(const void* kernel, int bytes, Csa2PerDeviceOnce& once) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= Csa2PerDeviceOnce::kMaxDevices) return CSA2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (!once.done[dev]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return CSA2_ERR_CUDA;
+    }
+    once.done[dev] = true;
+  }
+  return CSA2_OK;
+}
 
 static inline bool csa2_aligned(const void* p, uintptr_t a) {
   return (((uintptr_t)p) & (a - 1)) == 0;

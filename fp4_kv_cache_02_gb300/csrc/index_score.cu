@@ -92,13 +92,9 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
   if (chunks > tiles) chunks = tiles;
   const int64_t per = (tiles + chunks - 1) / chunks;
   chunks = (tiles + per - 1) / per;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(scan_tc::index_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             scan_tc::kSmemBytes) != cudaSuccess)
-      return CSA2_ERR_CUDA;
-    attr = true;
-  }
+  static Csa2PerDeviceOnce optin;
+  if (csa2_smem_optin((const void*)scan_tc::index_score_tc_kernel, scan_tc::kSmemBytes, optin) != CSA2_OK)
+    return CSA2_ERR_CUDA;
   // claimed tiles (dense mode with counters): a fixed first range of one
   // pipeline's depth, then claims of two tiles
   scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
@@ -138,15 +134,8 @@ extern "C" int csa2_prefill_index_score_compressed(const uint8_t* q_data, const 
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return CSA2_ERR_CUDA;
-  static bool attr[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return CSA2_ERR_CUDA;
-  if (!attr[dev]) {
-    if (cudaFuncSetAttribute(prefill_score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return CSA2_ERR_CUDA;
-    attr[dev] = true;
-  }
+  static Csa2PerDeviceOnce optin;
+  if (csa2_smem_optin((const void*)prefill_score_tc_kernel, kSmemBytes, optin) != CSA2_OK) return CSA2_ERR_CUDA;
   const int64_t tiles = (n_entries + kTileRows - 1) / kTileRows;
   dim3 grid((unsigned)((tiles + kChunkTiles - 1) / kChunkTiles), (unsigned)((T + kQBlock - 1) / kQBlock));
   Params prm{q_e8m0, w, ik_scale, n_entries, p0, T, m, scores};

@@ -953,19 +953,8 @@ static int64_t topk_chunk(int32_t B, int64_t n) {
 
 // Opts the finalize kernel into its dynamic shared memory, once per device.
 static int topk_finalize_attr() {
-  constexpr int kMaxDevices = 64;
-  static bool done[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CSA2_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!done[dev]) {
-    if (cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFinSmem) !=
-        cudaSuccess)
-      return CSA2_ERR_CUDA;
-    done[dev] = true;
-  }
-  return CSA2_OK;
+  static Csa2PerDeviceOnce optin;
+  return csa2_smem_optin((const void*)topk_finalize_kernel, (int)kFinSmem, optin);
 }
 
 extern "C" size_t csa2_topk_workspace_size(int32_t B, int64_t n, int32_t k) {

@@ -256,14 +256,16 @@ int csa2_topk(const float* scores, int32_t B, int64_t n,
  *     exits.
  *   - The first call on a device looks up the buffer's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the life of the
+ *     process: it is not valid after cudaDeviceReset, so a caller that resets
+ *     a device must not call this entry point on it again.
  *   - All calls share the one buffer and it keeps the last call's contents;
  *     the call clears what must start at zero. Calls that overlap on the GPU
  *     (different streams, or different host threads) race on the buffer:
  *     order them on one stream.
  *   - Returns CSA2_ERR_SCRATCH_LIMIT when csa2_topk_workspace_size(B, n, k)
- *     exceeds CSA2_TOPK_STATIC_SCRATCH_BYTES (32 MiB: e.g. 32 rows of 65,536
- *     scores at k = 512 fit), and otherwise the errors of csa2_topk.
+ *     exceeds CSA2_TOPK_STATIC_SCRATCH_BYTES (32 MiB: at k = 512, up to 61
+ *     rows of 65,536 scores fit), and otherwise the errors of csa2_topk.
  */
 #define CSA2_TOPK_STATIC_SCRATCH_BYTES (32u << 20)
 int csa2_topk_static(const float* scores, int32_t B, int64_t n,

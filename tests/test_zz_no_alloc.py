@@ -59,3 +59,24 @@ def test_static_topk_refuses_problems_larger_than_its_buffer(csa2):
     with pytest.raises(csa2.Csa2Error) as e:
         csa2.csa2_topk_static(s, 512, idx)
     assert e.value.status == -8
+
+
+def test_static_topk_limit_is_the_workspace_size(csa2):
+    # the largest batch of 65,536-score rows whose csa2_topk workspace fits the
+    # buffer is accepted and equals csa2_topk; one more row is refused
+    n, k = 65536, 512
+    size = csa2.lib().csa2_topk_workspace_size
+    B = 1
+    while size(B + 1, n, k) <= csa2.TOPK_STATIC_SCRATCH_BYTES:
+        B += 1
+    assert size(B, n, k) <= csa2.TOPK_STATIC_SCRATCH_BYTES < size(B + 1, n, k)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(78)
+    s = torch.randn(B + 1, n, generator=g, device="cuda")
+    ref, got = _run_both(csa2, s[:B].contiguous(), k)
+    assert torch.equal(ref, got)
+    idx = torch.empty(B + 1, k, dtype=torch.int32, device="cuda")
+    with pytest.raises(csa2.Csa2Error) as e:
+        csa2.csa2_topk_static(s, k, idx)
+    assert e.value.status == -8
+    assert csa2.csa2_get_last_error() == 0
