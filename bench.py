@@ -23,6 +23,13 @@ inputs (the same kernel; inside csa2_index_topk it also builds the Top-K
 histogram in its epilogue); `cpu_baseline` is the CPU oracle on a bounded
 sample.
 
+The line's `workloads` object holds the other workloads, each measured the
+same way on its own caches: the single-query decode (4,096 entries; its
+latency per query), the Reindex decode with the 2,048 x 8 block pool (8 x
+1,048,576 entries), the long-context decode with 1 Full + 3 Reuse layers
+(4 x 1,048,576), and the prefill chunk as a pipeline (4,096 queries after
+126,976 entries: q -> MXFP4, causal scan, Top-512, sparse attention).
+
 --impl reference runs the CPU oracle instead (the reference arm).
 Multi-GPU: launched with torch.distributed.run, every rank runs its own
 batch of sequences (weak scaling, no data-path collective).
@@ -161,11 +168,13 @@ def step_config(wl, B, N, L, K, W, world):
 
 # ---------------------------------------------------------------------------- GPU arm
 
-def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device):
+def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device, planted_blocks=0):
     """Synthetic resident caches and per-step inputs, packed with the library's
     own packers on the device (indexer K: MXFP4; main KV: E2M1 + E4M3/16;
-    SWA: E4M3)."""
-    from fp4_kv_cache_02_gb300.inputs import CAP_ALIGN, device_normal, device_uniform, round_up, seed_for
+    SWA: E4M3). With planted_blocks, each sequence's keys hold that many
+    blocks of 8 aligned with its Full-layer query (the Reindex workload)."""
+    from fp4_kv_cache_02_gb300.inputs import (CAP_ALIGN, device_normal, device_planted_keys, device_uniform,
+                                              round_up, seed_for)
     cap = round_up(N, CAP_ALIGN)
     ik_data = torch.empty(B, cap, 64, dtype=torch.uint8, device=device)
     ik_scale = torch.empty(B, cap, 4, dtype=torch.uint8, device=device)
@@ -179,12 +188,16 @@ def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device):
     w_re = torch.empty(B, 32, dtype=torch.float32, device=device) if reindex else None
     for b, s in enumerate(seqs):
         seed = seed_for(wid, s)
-        ik = device_normal((cap, 128), 4 * seed + 1, device)
-        csa2.csa2_quant_mxfp4(ik, ik_data[b], ik_scale[b])
-        kv = device_normal((cap, 512), 4 * seed + 2, device)
-        csa2.csa2_pack_kv_fp4(kv, kv_data[b], kv_scale[b])
         q_idx[b] = device_normal((32, 128), 4 * seed + 3, device)
         w[b] = device_uniform((32,), 4 * seed + 3, device)
+        ik = device_normal((cap, 128), 4 * seed + 1, device)
+        if planted_blocks:
+            device_planted_keys(ik, q_idx[b], w[b], N, planted_blocks, 4 * seed + 7)
+        csa2.csa2_quant_mxfp4(ik, ik_data[b], ik_scale[b])
+        del ik
+        kv = device_normal((cap, 512), 4 * seed + 2, device)
+        csa2.csa2_pack_kv_fp4(kv, kv_data[b], kv_scale[b])
+        del kv
         Q[b] = device_normal((L, 64, 512), 4 * seed + 4, device, scale=1.0 / math.sqrt(512))
         csa2.csa2_pack_fp8_e4m3(device_normal((L, 128, 512), 4 * seed + 5, device), swa[b])
         if reindex:
@@ -196,47 +209,65 @@ def build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device):
                 Q=Q, swa=swa, n_visible=n_visible, q_re=q_re, w_re=w_re)
 
 
-def run_gpu(args):
-    import torch
-    rank, world, local_rank = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-    from fp4_kv_cache_02_gb300 import csa2
-    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
+class Ctx:
+    """What every measurement of one process shares: device, stream, ranks
+    and the L2 flush."""
 
-    wid = args.workload
+    def __init__(self, torch, device, world, rank, local_rank):
+        self.torch, self.device, self.world, self.rank, self.local_rank = torch, device, world, rank, local_rank
+        self.stream = torch.cuda.current_stream(device)
+        self._flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self._flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+
+    def flush_l2(self):
+        self._flush.fill_(1)
+        self._flush_rd.max()
+
+    def timed(self, fn, n):
+        """Mean CUDA-event time (ms) of fn over n launches, L2 flushed before each."""
+        torch = self.torch
+        tot = 0.0
+        for _ in range(n):
+            self.flush_l2()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            fn()
+            b_.record(self.stream)
+            b_.synchronize()
+            tot += a.elapsed_time(b_)
+        return tot / n
+
+
+def measure_decode(csa2, ctx, wid, B, steps, warmup, use_graph=True, with_e2e=True):
+    """One decode workload, measured four ways: (1) eager steps with an event
+    between stages (the per-stage breakdown), (2) the step captured as a CUDA
+    graph and replayed (the timed number, under clock sampling), (3) the
+    indexer scan alone, scheduled as inside the step (its roofline), and (4)
+    end to end with host copies. Each of the `steps` timed steps is preceded
+    by an L2 flush outside its events."""
+    torch, device, stream, world = ctx.torch, ctx.device, ctx.stream, ctx.world
+    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
     wl = WORKLOADS[wid]
-    if wl.kind == "prefill":
-        raise SystemExit("the prefill workload is measured by the parity tests, not by this bench")
     reindex = wl.kind == "reindex"
-    B, N, L, K, W = args.batch or wl.B, wl.N, wl.L, 512, 128
-    seqs = rank_sequences(rank, B)
-    inp = build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device)
+    N, L, K, W = wl.N, wl.L, 512, 128
+    seqs = rank_sequences(ctx.rank, B)
+    inp = build_inputs(csa2, torch, wid, B, N, L, reindex, seqs, device,
+                       planted_blocks=wl.planted_blocks if reindex else 0)
     cap = inp["cap"]
-    stream = torch.cuda.current_stream(device)
+    flush_l2 = ctx.flush_l2
 
     q_data = torch.empty(B, 32, 64, dtype=torch.uint8, device=device)
     q_sc = torch.empty(B, 32, 4, dtype=torch.uint8, device=device)
-    scores = torch.empty(B, cap, dtype=torch.float32, device=device)
     idx = torch.empty(B, K, dtype=torch.int32, device=device)
     out = torch.empty(B, L, 64, 512, dtype=torch.bfloat16, device=device)
     NBLK = 2048
     iws = csa2.index_topk_workspace(B, cap, K, NBLK if reindex else 0, device=device)
     aws = csa2.attn_workspace(B * L, K, W, device=device)
+    pool = idx_full = rws = None
     if reindex:
         pool = torch.empty(B, NBLK * 8, dtype=torch.int32, device=device)
         idx_full = torch.empty(B, K, dtype=torch.int32, device=device)
         rws = csa2.index_topk_workspace(B, NBLK * 8, K, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    flush_rd = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
-
-    def flush_l2():
-        flush.fill_(1)
-        flush_rd.max()
 
     # the step as named stages (each a sequence of public C-ABI calls); the
     # per-step inputs and outputs are looked up in `io`, which the end-to-end
@@ -267,7 +298,7 @@ def run_gpu(args):
     stages.append(("sparse_attn", st_attn))
     # our kernels per step: workspace clear + scan (q quantisation, fused histogram and, with the pool,
     # block maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex:
-    # clear, scan, select, finalize 4; attention: partials (+ combine) per 256 query-layers, as planned
+    # clear, scan, select, finalize 4; attention: as the library plans it for B * L query-layers
     n_launches = 4 + (5 + 4 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
 
     def step(ev=None):
@@ -278,7 +309,7 @@ def run_gpu(args):
         if ev is not None:
             ev[len(stages)].record(stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush_l2()
         step()
     torch.cuda.synchronize()
@@ -286,8 +317,8 @@ def run_gpu(args):
 
     nst = len(stages)
     # (1) eager steps with an event between stages: the per-stage breakdown
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
-    for i in range(args.steps):
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for i in range(steps):
         flush_l2()
         step(evs[i])
     torch.cuda.synchronize()
@@ -297,13 +328,13 @@ def run_gpu(args):
         for j in range(nst):
             stage[j] += e[j].elapsed_time(e[j + 1])
         eager_total += e[0].elapsed_time(e[nst])
-    stage_ms = [s_ / args.steps for s_ in stage]
-    eager_ms = eager_total / args.steps
+    stage_ms = {nm: s_ / steps for (nm, _), s_ in zip(stages, stage)}
+    eager_ms = eager_total / steps
 
     # (2) the step captured once as a CUDA graph (the kernels' programmatic
     # dependent launches become graph edges) and replayed: the timed number
     graph = None
-    if not args.no_graph:
+    if use_graph:
         side = torch.cuda.Stream(device)
         side.wait_stream(torch.cuda.current_stream(device))
         with torch.cuda.stream(side):
@@ -312,20 +343,20 @@ def run_gpu(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step()
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             flush_l2()
             graph.replay()
         torch.cuda.synchronize()
         assert csa2.csa2_get_last_error() == 0
     run_step = graph.replay if graph is not None else step
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clk:
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with ClockSampler(ctx.local_rank) as clk:
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("timed_steps")   # lets ncu filter to the timed region
-        for i in range(args.steps):
+        for i in range(steps):
             flush_l2()                     # L2 flush between timed steps, outside the events
             ev_a[i].record(stream)
             run_step()
@@ -334,30 +365,26 @@ def run_gpu(args):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    ms = sum(a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)) / args.steps
+    ms = sum(a_.elapsed_time(b_) for a_, b_ in zip(ev_a, ev_b)) / steps
     ms_max = reduce_max(ms, world, device)
 
-    # ---- the scan kernel alone, for its roofline (same inputs, L2 flushed),
-    # scheduled as inside the step: tiles claimed from per-sequence counters ----
+    # (3) the scan kernel alone, for its roofline (same inputs, L2 flushed),
+    # scheduled as inside the step: tiles claimed from per-sequence counters
     csa2.csa2_quant_mxfp4(inp["q_idx"], q_data, q_sc)
     tile_ctr = torch.zeros(2 * B, dtype=torch.int32, device=device)
-    scan_ms = 0.0
-    for _ in range(args.steps):
-        flush_l2()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        csa2.csa2_index_score_claimed(q_data, q_sc, inp["w"], inp["ik_data"], inp["ik_scale"], inp["n_visible"],
-                                      scores, tile_ctr, stream=stream)
-        b_.record(stream)
-        b_.synchronize()
-        scan_ms += a.elapsed_time(b_)
-    scan_ms /= args.steps
+    scores = torch.empty(B, cap, dtype=torch.float32, device=device)
+    scan_ms = ctx.timed(lambda: csa2.csa2_index_score_claimed(q_data, q_sc, inp["w"], inp["ik_data"],
+                                                              inp["ik_scale"], inp["n_visible"], scores, tile_ctr,
+                                                              stream=stream), steps)
+    del scores
 
-    # ---- the fused KV append, for its roofline and its decode latency ----
-    app = measure_append(csa2, torch, B, device, args.steps, flush_l2, stream)
-    pre = measure_prefill(csa2, torch, device, max(3, min(args.steps, 10)), flush_l2, stream) if args.prefill else None
+    res = {"wl": wl, "B": B, "N": N, "L": L, "K": K, "W": W, "reindex": reindex, "ms": ms_max,
+           "eager_ms": eager_ms, "stage_ms": stage_ms, "scan_ms": scan_ms, "n_launches": n_launches,
+           "graph": graph is not None, "clocks": clk.summary()}
+    if not with_e2e:
+        return res
 
-    # ---- end to end: per-step inputs from pinned host memory, outputs back ----
+    # (4) end to end: per-step inputs from pinned host memory, outputs back.
     # Each step copies its inputs host -> device and its outputs (attention
     # output, Top-K indices) device -> host, each as one packed buffer (one copy
     # a direction keeps the host's enqueue work small). The copies run on their own streams
@@ -400,7 +427,7 @@ def run_gpu(args):
         for k_ in in_keys:
             d[k_].copy_(inp[k_])
         step()  # eager warm-up with this buffer set
-        if not args.no_graph:
+        if graph is not None:
             g_ = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g_):
                 step()
@@ -435,27 +462,105 @@ def run_gpu(args):
                 d["h_out_flat"].copy_(d["out_flat"], non_blocking=True)
                 d2h_done[sl].record(s_out)
 
-    e2e_loop(max(args.warmup, 2))
+    e2e_loop(max(warmup, 2))
     torch.cuda.synchronize()
     t_a, t_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_a.record(main)
     s_in.wait_stream(main)
     h0 = time.perf_counter()
-    e2e_loop(args.steps)
-    host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
+    e2e_loop(steps)
+    host_ms = (time.perf_counter() - h0) * 1e3 / steps
     s_out.wait_stream(main)
     t_b.record(s_out)
     t_b.synchronize()
-    e2e_ms = reduce_max(t_a.elapsed_time(t_b) / args.steps, world, device)
-    assert torch.equal(slot_io[(args.steps - 1) % 2]["h_idx"].to(device), idx)  # same result as the timed steps
+    e2e_ms = reduce_max(t_a.elapsed_time(t_b) / steps, world, device)
+    assert torch.equal(slot_io[(steps - 1) % 2]["h_idx"].to(device), idx)  # same result as the timed steps
+    res.update({"e2e_ms": e2e_ms, "host_ms": host_ms, "h2d": h2d, "d2h": d2h})
+    return res
+
+
+def decode_summary(res, world, hbm_peak, peak_kind):
+    """The figures of one decode workload: queries/s (device-timed graph
+    replays and end to end), stage times, the indexer scan's HBM roofline and
+    the attention stage's algorithmic bytes over its time."""
+    B, N, L, K, W = res["B"], res["N"], res["L"], res["K"], res["W"]
+    ms = res["ms"]
+    scan_bytes = B * N * IK_BYTES_PER_ENTRY
+    scan_gbs = scan_bytes / (res["scan_ms"] * 1e-3) / 1e9
+    # attention: gathered latents + SWA rows + Q in + bf16 O out, per query-layer
+    attn_bytes = B * L * (K * KV_BYTES_PER_ENTRY + W * 512 + 2 * 64 * 512 * 2)
+    attn_ms = res["stage_ms"]["sparse_attn"]
+    out = {
+        "workload": res["wl"].name, "sequences": world * B, "visible_entries": N, "layers_sharing_topk": L,
+        "queries_per_s": round(world * B / (ms * 1e-3), 1), "ms_per_step": round(ms, 5),
+        "us_per_query": round(ms * 1e3 / B, 3),
+        "entries_scored_per_s": round(world * B * (N + (2048 * 8 if res["reindex"] else 0)) / (ms * 1e-3), 1),
+        "ms_per_step_eager": round(res["eager_ms"], 5),
+        "stages_ms": {k_: round(v, 5) for k_, v in res["stage_ms"].items()},
+        "scan_roofline": {"kernel": "index_score", "bound": "hbm", "achieved": round(scan_gbs, 1),
+                          "peak": hbm_peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
+                          "frac": round(scan_gbs / hbm_peak, 4), "ms": round(res["scan_ms"], 5),
+                          "algorithmic_bytes_per_launch": scan_bytes},
+        "attention": {"algorithmic_bytes_per_step": attn_bytes, "ms": round(attn_ms, 5),
+                      "achieved_gbs": round(attn_bytes / (attn_ms * 1e-3) / 1e9, 1),
+                      "frac": round(attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                      "hbm_floor_us": round(attn_bytes / (hbm_peak * 1e9) * 1e6, 2)},
+        "gpu_launches_per_step": res["n_launches"],
+        "clocks": res["clocks"],
+    }
+    if "e2e_ms" in res:
+        out["e2e"] = {"value": round(world * B / (res["e2e_ms"] * 1e-3), 1), "unit": "queries/s",
+                      "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                      "ms_per_step": round(res["e2e_ms"], 5)}
+    return out
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    from fp4_kv_cache_02_gb300 import csa2
+    from fp4_kv_cache_02_gb300.inputs import WORKLOADS
+
+    ctx = Ctx(torch, device, world, rank, local_rank)
+    wid = args.workload
+    wl = WORKLOADS[wid]
+    B = args.batch or wl.B
+    res = measure_decode(csa2, ctx, wid, B, args.steps, args.warmup, use_graph=not args.no_graph)
+    torch.cuda.empty_cache()
+
+    # ---- the fused KV append, for its roofline and its decode latency ----
+    app = measure_append(csa2, torch, B, device, args.steps, ctx.flush_l2, ctx.stream)
+    pre = measure_prefill(csa2, ctx, max(3, min(args.steps, 10))) if args.prefill else None
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, each its own decode step (or prefill pipeline) ----
+    hbm_peak, peak_kind = peaks()
+    extra = {}
+    for w_ in args.workloads:
+        if w_ == wid or w_ not in WORKLOADS:
+            continue
+        if WORKLOADS[w_].kind == "prefill":
+            continue  # the prefill pipeline comes from measure_prefill
+        r_ = measure_decode(csa2, ctx, w_, WORKLOADS[w_].B, min(args.steps, 100), args.warmup,
+                            use_graph=not args.no_graph)
+        extra[str(w_)] = decode_summary(r_, world, hbm_peak, peak_kind)
+        del r_
+        torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return None
 
-    hbm_peak, peak_kind = peaks()
-    scan_bytes = B * N * IK_BYTES_PER_ENTRY
-    scan_gbs = scan_bytes / (scan_ms * 1e-3) / 1e9
+    ms_max = res["ms"]
+    main_sum = decode_summary(res, world, hbm_peak, peak_kind)
+    scan_bytes = main_sum["scan_roofline"]["algorithmic_bytes_per_launch"]
+    scan_gbs = main_sum["scan_roofline"]["achieved"]
     traffic = None
     tp = os.path.join(ROOT, "profiles", "index_score_traffic.json")
     if os.path.exists(tp):
@@ -466,9 +571,7 @@ def run_gpu(args):
                 traffic = rec.get("dram_bytes_per_launch")
         except (ValueError, OSError):
             traffic = None
-    # attention: gathered latents + SWA rows + Q in + bf16 O out, per query-layer
-    attn_bytes = B * L * (K * KV_BYTES_PER_ENTRY + W * 512 + 2 * 64 * 512 * 2)
-    attn_ms = stage_ms[[nm for nm, _ in stages].index("sparse_attn")]
+    L = res["L"]
     qps = world * B / (ms_max * 1e-3)
     line = {
         "metric": METRIC,
@@ -483,41 +586,44 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "e2m1/e4m3/e8m0 storage; fp32 scores; bf16 attention with fp32 accumulate",
         "data": "synthetic N(0,1) caches drawn on the device, packed by the library",
-        "config": step_config(wl, B, N, L, K, W, world),
-        "launch": "CUDA graph of the step (programmatic dependent launches)" if graph is not None else "eager",
-        "ms_per_step_eager": round(eager_ms, 5),
-        "stages_ms": dict([(nm, round(v, 5)) for (nm, _), v in zip(stages, stage_ms)] +
-                          [("index_score_alone", round(scan_ms, 5))]),
-        "entries_scored_per_s": round(world * B * (N + (NBLK * 8 if reindex else 0)) / (ms_max * 1e-3), 1),
-        "indexer_scan_gbs": round(scan_gbs, 1),
-        "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": round(scan_gbs, 1),
+        "config": step_config(wl, B, res["N"], L, res["K"], res["W"], world),
+        "launch": "CUDA graph of the step (programmatic dependent launches)" if res["graph"] else "eager",
+        "ms_per_step_eager": round(res["eager_ms"], 5),
+        "stages_ms": dict([(nm, round(v, 5)) for nm, v in res["stage_ms"].items()] +
+                          [("index_score_alone", round(res["scan_ms"], 5))]),
+        "entries_scored_per_s": main_sum["entries_scored_per_s"],
+        "indexer_scan_gbs": scan_gbs,
+        "roofline": {"kernel": "index_score", "bound": "hbm", "achieved": scan_gbs,
                      "peak": hbm_peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
-                     "frac": round(scan_gbs / hbm_peak, 4), "traffic": traffic,
+                     "frac": main_sum["scan_roofline"]["frac"], "traffic": traffic,
                      "algorithmic_bytes_per_launch": scan_bytes},
         "kernel_rooflines": {
-            "sparse_attn": {"bound": "hbm", "achieved": round(attn_bytes / (attn_ms * 1e-3) / 1e9, 1), "peak": hbm_peak,
-                            "unit": "GB/s", "frac": round(attn_bytes / (attn_ms * 1e-3) / 1e9 / hbm_peak, 4),
-                            "algorithmic_bytes_per_step": attn_bytes, "note": "partial + combine kernels"},
+            "sparse_attn": {"bound": "hbm", "achieved": main_sum["attention"]["achieved_gbs"], "peak": hbm_peak,
+                            "unit": "GB/s", "frac": main_sum["attention"]["frac"],
+                            "algorithmic_bytes_per_step": main_sum["attention"]["algorithmic_bytes_per_step"]},
             "kv_append": {"bound": "hbm", "achieved": round(app["bulk_bytes"] / (app["bulk_ms"] * 1e-3) / 1e9, 1),
                           "peak": hbm_peak, "unit": "GB/s",
                           "frac": round(app["bulk_bytes"] / (app["bulk_ms"] * 1e-3) / 1e9 / hbm_peak, 4),
                           "algorithmic_bytes_per_launch": app["bulk_bytes"], "entries_per_launch": app["entries"],
                           "decode_append_us": round(app["decode_us"], 2),
                           "note": "timed alone, outside the step: bf16 latent + key in, 356 B entry out"}},
-        "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "queries/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                "host_enqueue_ms_per_step": round(host_ms, 5),
+        "e2e": {"value": main_sum["e2e"]["value"], "unit": "queries/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "ms_per_step": round(res["e2e_ms"], 5), "host_enqueue_ms_per_step": round(res["host_ms"], 5),
                 "note": "one host-to-device copy of the step's inputs and one device-to-host copy of its outputs "
                         "(each a packed buffer), on their own streams, overlapping neighbouring steps (two buffer "
                         "sets); inputs exceed L2"},
-        "gpu_launches": args.steps * n_launches,
-        "clocks": clk.summary(),
+        "gpu_launches": args.steps * res["n_launches"],
+        "clocks": res["clocks"],
     }
+    workloads = {str(wid): main_sum}
+    workloads.update(extra)
     if pre is not None:
         bf16_peak, bf16_kind = tensor_peak_tflops()
         fp4_peak = bf16_peak * FP4_PER_BF16
         sc_tf = pre["scan_flops"] / (pre["scan_ms"] * 1e-3) / 1e12
         at_tf = pre["attn_flops"] / (pre["attn_ms"] * 1e-3) / 1e12
+        rp_tf = pre["attn_flops"] / (pre["replay_ms"] * 1e-3) / 1e12
         line["kernel_rooflines"]["prefill_index_score"] = {
             "bound": "tensor", "achieved": round(sc_tf, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
             "frac": round(sc_tf / fp4_peak, 4), "ms": round(pre["scan_ms"], 4), "pairs": pre["pairs"],
@@ -535,11 +641,28 @@ def run_gpu(args):
             "frac": round(cmp_gbs / hbm_peak, 4), "ms": round(pre["cmp_ms"], 4),
             "algorithmic_bytes_per_launch": pre["cmp_bytes"], "entries_per_launch": pre["cmp_entries"],
             "note": "262,144 tokens of C and Z (bf16) in, 131,072 packed 288-byte entries out"}
-        line["kernel_rooflines"]["prefill_attention_replay"] = {
+        line["kernel_rooflines"]["prefill_attention"] = {
             "bound": "tensor", "achieved": round(at_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
             "frac": round(at_tf / bf16_peak, 4), "ms": round(pre["attn_ms"], 4),
             "peak_kind": f"{bf16_kind} bf16",
-            "note": "4,096 queries x (512 + 128 rows), Bounded-Replay cut at swa row 64; QK + PV FLOPs"}
+            "note": "4,096 queries x (512 selected + 128 SWA rows); QK + PV FLOPs"}
+        line["kernel_rooflines"]["prefill_attention_replay"] = {
+            "bound": "tensor", "achieved": round(rp_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
+            "frac": round(rp_tf / bf16_peak, 4), "ms": round(pre["replay_ms"], 4),
+            "peak_kind": f"{bf16_kind} bf16",
+            "note": "as prefill_attention with the Bounded-Replay cut at swa row 64 (FLOPs counted over 640 rows)"}
+        workloads["3"] = {
+            "workload": WORKLOADS[3].name, "queries": pre["T"], "visible_entries_max": pre["N"],
+            "queries_per_s": round(pre["T"] / (pre["pipeline_ms"] * 1e-3), 1),
+            "ms_per_step": round(pre["pipeline_ms"], 4),
+            "stages_ms": {k_: round(v, 4) for k_, v in pre["stages_ms"].items()},
+            "scan_roofline": {"bound": "tensor", "achieved": round(sc_tf, 1), "peak": round(fp4_peak, 1),
+                              "unit": "TFLOP/s", "frac": round(sc_tf / fp4_peak, 4)},
+            "steps": pre["steps"],
+            "note": "one step = q -> MXFP4, causal scan, Top-512 per query (n_valid = position + 1), sparse "
+                    "attention over 512 selected + the 128-row causal SWA window; eager, L2 flushed before "
+                    "each step"}
+    line["workloads"] = workloads
     if not args.no_cpu_baseline and wid == WORKLOAD_ID:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     if world > 1:
@@ -554,55 +677,72 @@ APPEND_BYTES_PER_ENTRY = 512 * 2 + 128 * 2 + KV_BYTES_PER_ENTRY + IK_BYTES_PER_E
 PREFILL_T, PREFILL_P0, PREFILL_REPLAY_ROW = 4096, 126976, 64
 
 
-def measure_prefill(csa2, torch, device, steps, flush_l2, stream):
-    """The prefill pair of kernels timed alone on the prefill workload (4,096
-    queries at positions 126,976 .. 131,071 of one sequence): the causal
-    indexer scan (4,096 MAC per query-entry pair, FP4 tensor cores) and the
-    sparse attention with the Bounded-Replay cut (512 selected + 128 SWA rows
-    per query; QK and PV on bf16 tensor cores)."""
+def measure_prefill(csa2, ctx, steps):
+    """The prefill workload (4,096 queries at positions 126,976 .. 131,071 of
+    one sequence) as a pipeline, eager, with an event between stages: indexer
+    q -> MXFP4, the causal indexer scan (4,096 MAC per query-entry pair, FP4
+    tensor cores), the Top-512 of each query's visible prefix, and the sparse
+    attention over the 512 selected + the 128-row SWA window (QK and PV on
+    bf16 tensor cores). Beside it, timed alone: the attention with the
+    Bounded-Replay cut, the indexer scan of an encoder Full layer over 2-token
+    compressed entries, and the compressor."""
+    torch, device, stream = ctx.torch, ctx.device, ctx.stream
     from fp4_kv_cache_02_gb300.inputs import device_normal, device_uniform
     T, p0, W, K = PREFILL_T, PREFILL_P0, 128, 512
     N = p0 + T
-    q_data, q_sc = csa2.quant_mxfp4(device_normal((T, 32, 128), 71, device))
+    q_bf = device_normal((T, 32, 128), 71, device)
+    q_data = torch.empty(T, 32, 64, dtype=torch.uint8, device=device)
+    q_sc = torch.empty(T, 32, 4, dtype=torch.uint8, device=device)
     w = device_uniform((T, 32), 72, device).float().contiguous()
     ik_data, ik_sc = csa2.quant_mxfp4(device_normal((N, 128), 73, device))
     scores = torch.empty(T, N, dtype=torch.float32, device=device)
     kv_data, kv_sc = csa2.pack_kv_fp4(device_normal((N, 512), 74, device))
     Q = device_normal((T, 64, 512), 75, device, scale=1.0 / math.sqrt(512))
     swa = csa2.pack_fp8(device_normal((T + W - 1, 512), 76, device))
-    g = torch.Generator(device=device)
-    g.manual_seed(77)
-    lim = torch.arange(p0 + 1, p0 + T + 1, device=device, dtype=torch.float64)[:, None]
-    idx = (torch.rand(T, K, generator=g, device=device, dtype=torch.float64) * lim).to(torch.int32).contiguous()
+    n_valid = torch.arange(p0 + 1, p0 + T + 1, dtype=torch.int32, device=device)
+    idx = torch.empty(T, K, dtype=torch.int32, device=device)
+    tws = csa2.topk_workspace(T, N, K, device=device)
     out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device=device)
     aws = csa2.attn_workspace(T, K, W, device=device)
 
-    def timed(fn, n):
-        tot = 0.0
-        for _ in range(n):
-            flush_l2()
-            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+    stages = [
+        ("quant_q", lambda: csa2.csa2_quant_mxfp4(q_bf, q_data, q_sc, stream=stream)),
+        ("index_score", lambda: csa2.csa2_prefill_index_score(q_data, q_sc, w, ik_data, ik_sc, p0, scores,
+                                                              stream=stream)),
+        ("topk", lambda: csa2.csa2_topk(scores, K, idx, tws, n_valid=n_valid, stream=stream)),
+        ("sparse_attn", lambda: csa2.csa2_sparse_attn_prefill(Q, kv_data, kv_sc, idx, swa, W, out, aws,
+                                                              stream=stream)),
+    ]
+    nst = len(stages)
+    for _ in range(2):
+        ctx.flush_l2()
+        for _, fn in stages:
             fn()
-            b_.record(stream)
-            b_.synchronize()
-            tot += a.elapsed_time(b_)
-        return tot / n
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    for i in range(steps):
+        ctx.flush_l2()
+        for j, (_, fn) in enumerate(stages):
+            evs[i][j].record(stream)
+            fn()
+        evs[i][nst].record(stream)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    stage_ms = {nm: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / steps for j, (nm, _) in enumerate(stages)}
+    pipeline_ms = sum(e[0].elapsed_time(e[nst]) for e in evs) / steps
+    del tws
 
-    scan = lambda: csa2.csa2_prefill_index_score(q_data, q_sc, w, ik_data, ik_sc, p0, scores, stream=stream)
-    attn = lambda: csa2.csa2_sparse_attn_prefill_replay(Q, kv_data, kv_sc, idx, swa, W, PREFILL_REPLAY_ROW, out, aws,
-                                                        stream=stream)
+    replay = lambda: csa2.csa2_sparse_attn_prefill_replay(Q, kv_data, kv_sc, idx, swa, W, PREFILL_REPLAY_ROW, out,
+                                                          aws, stream=stream)
     # encoder Full layer at m = 2: the same 4,096 queries at token positions
     # 253,952 .. see the complete compressed entries (126,976 .. 129,024 of them)
     m, tok0 = 2, 2 * p0
     cscan = lambda: csa2.csa2_prefill_index_score_compressed(q_data, q_sc, w, ik_data, ik_sc, tok0, m, scores,
                                                                stream=stream)
-    timed(scan, 2)
-    scan_ms = timed(scan, steps)
-    timed(attn, 2)
-    attn_ms = timed(attn, steps)
-    timed(cscan, 2)
-    cscan_ms = timed(cscan, steps)
+    ctx.timed(replay, 2)
+    replay_ms = ctx.timed(replay, steps)
+    ctx.timed(cscan, 2)
+    cscan_ms = ctx.timed(cscan, steps)
     del scores
     # the compressor: 262,144 tokens of C and Z (bf16) into 131,072 packed entries
     n_tok = 2 * 131072
@@ -610,14 +750,16 @@ def measure_prefill(csa2, torch, device, steps, flush_l2, stream):
     Z = device_normal((n_tok, 512), 79, device)
     bias = device_normal((m, 512), 80, device).float().contiguous()
     cmp = lambda: csa2.csa2_compress_kv(C, Z, bias, m, kv_data, kv_sc, stream=stream)
-    timed(cmp, 2)
-    cmp_ms = timed(cmp, steps)
+    ctx.timed(cmp, 2)
+    cmp_ms = ctx.timed(cmp, steps)
     torch.cuda.synchronize()
     assert csa2.csa2_get_last_error() == 0
     pairs = T * p0 + T * (T + 1) // 2
     cpairs = sum((tok0 + t + 1) // m for t in range(T))
-    return {"scan_ms": scan_ms, "scan_flops": 2 * 4096 * pairs, "pairs": pairs,
-            "attn_ms": attn_ms, "attn_flops": 2 * 2 * T * 64 * (K + W) * 512,
+    return {"T": T, "N": N, "steps": steps, "pipeline_ms": pipeline_ms, "stages_ms": stage_ms,
+            "scan_ms": stage_ms["index_score"], "scan_flops": 2 * 4096 * pairs, "pairs": pairs,
+            "attn_ms": stage_ms["sparse_attn"], "attn_flops": 2 * 2 * T * 64 * (K + W) * 512,
+            "replay_ms": replay_ms,
             "cscan_ms": cscan_ms, "cscan_flops": 2 * 4096 * cpairs, "cpairs": cpairs,
             "cmp_ms": cmp_ms, "cmp_bytes": n_tok * 2 * 512 * 2 + (n_tok // m) * KV_BYTES_PER_ENTRY,
             "cmp_entries": n_tok // m}
@@ -766,8 +908,13 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--batch", type=int, default=0, help="sequences per GPU (default: the workload's)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=[0, 1, 2, 4],
-                    help="decode workload id (default 1: 32 sequences x 65,536 entries)")
+                    help="decode workload of the headline value (default 1: 32 sequences x 65,536 entries)")
+    ap.add_argument("--workloads", default="0,2,3,4",
+                    help="comma-separated workloads also measured into the line's `workloads` object ('' for none)")
     args = ap.parse_args(argv)
+    args.workloads = [int(x) for x in args.workloads.split(",") if x.strip()]
+    if 3 not in args.workloads:
+        args.prefill = False
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if line is not None:

@@ -163,3 +163,21 @@ def device_uniform(shape, seed: int, device="cuda") -> torch.Tensor:
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32)
+
+
+def device_planted_keys(ik: torch.Tensor, q_idx: torch.Tensor, w: torch.Tensor, n_visible: int,
+                        n_blocks: int, seed: int) -> torch.Tensor:
+    """The planted high-affinity blocks of the Reindex workload, on the device:
+    `n_blocks` blocks of POOL_BLOCK keys, drawn without replacement below
+    `n_visible`, are overwritten in place with u + 0.1 * N(0,1) per channel,
+    where u = sum_h w_h q_h scaled to norm sqrt(128) (the recipe of
+    decode_sequence). ik [cap,128] bf16; returns the sorted block ids."""
+    g = torch.Generator(device=ik.device)
+    g.manual_seed(seed)
+    u = (w.double()[:, None] * q_idx.double()).sum(0)
+    u = u * (math.sqrt(IDX_DIM) / torch.linalg.vector_norm(u))
+    blocks = torch.randperm(n_visible // POOL_BLOCK, generator=g, device=ik.device)[:n_blocks].sort().values
+    noise = torch.randn(n_blocks, POOL_BLOCK, IDX_DIM, generator=g, device=ik.device, dtype=torch.float32)
+    rows = (blocks[:, None] * POOL_BLOCK + torch.arange(POOL_BLOCK, device=ik.device)[None, :]).reshape(-1)
+    ik[rows] = (u.float()[None, None, :] + 0.1 * noise).reshape(-1, IDX_DIM).to(torch.bfloat16)
+    return blocks
