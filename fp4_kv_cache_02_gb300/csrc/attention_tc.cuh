@@ -1,34 +1,38 @@
-// attention_tc.cuh -- tensor-core sparse attention partials (included by
-// attention.cu, which owns g_attn_error, AttnArgs and the combine kernel).
+// attention_tc.cuh -- tensor-core sparse attention (included by attention.cu,
+// which owns g_attn_error and AttnArgs).
 //
 // "DeepSeek-V4.1-Flash: Pushing the Limits of KV Cache Compression", section
 // 2.3: each query attends to its selected main-KV entries together with the
 // layer's SWA rows in one softmax; mer.dev notes section 1: 64 heads of dim
 // 512 share the 512-channel latent as K and V.
 //
-// One CTA takes one query (64 heads) and one chunk of `rows` rows (selected
-// latents and/or SWA rows; rows is a multiple of 32, at most 160, chosen by
-// the host so that the grid fills the SMs in as few waves as possible):
-//   1. all row loads are issued up front; the chunk is dequantised into
-//      shared memory as bf16 R[t][c] (exact: E2M1 x E4M3 has at most 6
-//      significant bits) in 128-byte-swizzled blocks of 64 channels, the low
-//      256 channels first;
-//   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (M = 128 rows per tile, one
-//      or two tiles; N = 64 heads; K = 512 in quarters of 128 channels held
-//      in three slots: quarter 3 loads into quarter 0's slot once its MMAs are
-//      done, while the high channels are dequantised);
-//   3. per-head max and sum over the chunk's rows; P = exp(S - max) split
-//      into bf16 hi + lo parts (keeps the P.V product at fp32-level accuracy),
-//      stacked as 128 B-operand rows (64 hi, 64 lo);
-//   4. O^T[c][n] = sum_t R[t][c] P[n][t] on the tensor cores (M = 128 channels
-//      x 4 blocks, N = 128, K = rows), reading the same R tile as an MN-major
-//      operand; O = O_hi + O_lo when read back;
-//   5. the chunks of a query merge: when they form one thread-block cluster
-//      (at most 8 chunks) each scales its O by exp(m - M) / L into its shared
-//      memory and each rank sums a slice of the heads over the cluster in rank
-//      order through distributed shared memory, writing the output directly;
-//      otherwise the unnormalised partial O and (max, sum) go to the workspace
-//      and attn_combine_kernel merges the chunks in the same fixed order.
+// A query's rows are cut into tiles of 128: the SWA tiles first, then the
+// tiles of selected entries. A thread-block cluster of C CTAs serves one
+// query; CTA r takes the tiles whose index is r modulo C, and each tile gives
+// one partial softmax (m, l, O) over its rows:
+//   1. the rows are loaded (all loads issued at once) and dequantised into
+//      shared memory as fp16 R[t][c] in 128-byte-swizzled blocks of 64
+//      channels. fp16 holds every row value exactly: an E2M1 x E4M3 product
+//      has at most 6 significant bits and lies in [2^-10, 2688]; an E4M3 SWA
+//      value is a subset of fp16;
+//   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (kind::f16, M = 128 rows,
+//      N = 64 heads, K = 512). Q was converted once per CTA from bf16 to fp16
+//      with a power-of-two scale per head (2^k_h puts the head's largest
+//      |q| in [2^14, 2^15)); this is exact for every value above 2^-17 of
+//      that maximum, and S is multiplied back by 2^-k_h in the softmax;
+//   3. per-head max and sum over the tile's rows (four lane-quadrant warps
+//      per group of 16 heads meet at a named barrier); P = 2^(S log2 e - m)
+//      rounded to fp16 (relative error <= 2^-11, against the 2^-9 of bf16)
+//      and stored as the K-major B operand;
+//   4. O^T[c][h] = sum_t R[t][c] P[h][t] on the tensor cores (M = 128
+//      channels x 4 blocks, N = 64, K = 128), the R tile read as an MN-major
+//      operand; the unnormalised O and (m, l) go to the workspace.
+// The SWA tiles depend on nothing the kernel before this one writes, so they
+// run before the programmatic-launch wait; only the selected tiles follow it.
+// Merge: after one cluster barrier (release / acquire) CTA r reads the
+// partials of heads [64r/C, 64(r+1)/C) from the workspace (L2), weighs them
+// by 2^(m_j - M) / L in fixed partial order (deterministic) and writes the
+// output and the log-sum-exp.
 #pragma once
 
 #include "tc_common.cuh"
@@ -36,57 +40,72 @@
 namespace csa2 {
 namespace attn_tc {
 
-constexpr int kMaxRows = 160;   // rows per CTA: a multiple of 32, at most 160
-constexpr int kMaxClusterChunks = 8;  // chunks of a query merged inside one cluster
-constexpr int kThreads = 512;   // 16 warps: 4 TMEM lane quadrants x 4
-constexpr int kBlkR = kMaxRows * 128;                     // one 64-channel block of R: [160 t][128 B]
-constexpr int kOffR = 0;                                  // 8 blocks                        = 160 KiB
-constexpr int kOffQP = kOffR + 8 * kBlkR;                 // Q half (4 x [64 h][128 B]) or P = 48 KiB
-constexpr int kQQuarterBytes = kHeads * 128 * 2;          // 16 KiB: channels 128q .. 128q+127
-constexpr int kPBlk = 2 * kHeads * 128;                   // P: per 64 rows, [128 n][128 B]  = 16 KiB
-constexpr int kOffMisc = kOffQP + 3 * kPBlk;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;
+constexpr int kThreads = 512;                   // 16 warps: 4 TMEM lane quadrants x 4
+constexpr int kRows = 128;                      // rows per tile (M)
+constexpr int kMaxCluster = 8;                  // CTAs of one query (portable cluster size)
+constexpr int kBlkR = kRows * 128;              // one 64-channel block of R: [128 t][128 B] = 16 KiB
+constexpr int kQBlk = kHeads * 128;             // one 64-channel block of Q: [64 h][128 B] = 8 KiB
+constexpr int kPBlk = kHeads * 128;             // 64 rows of P: [64 h][128 B] = 8 KiB
+constexpr int kOffR = 0;                        // 8 blocks = 128 KiB
+constexpr int kOffQ = kOffR + 8 * kBlkR;        // 8 blocks = 64 KiB
+constexpr int kOffP = kOffQ + 8 * kQBlk;        // 2 blocks = 16 KiB
+constexpr int kOffMisc = kOffP + 2 * kPBlk;
+constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;      // S^T: tile t at columns 64t .. 64t+63 (heads), lanes = rows
-constexpr uint32_t kColO = 0;      // O^T: 4 blocks x 128 columns (64 hi + 64 lo), lanes = channels;
-                                   // written once S^T has been read
+constexpr uint32_t kColS = 0;                   // S^T: 64 columns (heads), lanes = rows
+constexpr uint32_t kColO = 64;                  // O^T: 4 blocks x 64 columns (heads), lanes = channels
+constexpr int kMaxPartials = 36;                // 32 tiles of selected rows (k <= 4096) + 4 SWA tiles (<= 512 rows)
 
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(3 * kQQuarterBytes <= 3 * kPBlk, "three Q quarters fit the P region");
+static_assert(kSmemBytes <= 232448 - 4096, "shared memory budget (static arrays included)");
+static_assert(kMaxPartials * kHeads * 3 * 4 <= 8 * kBlkR, "merge scratch fits the R region");
 
-// exact bf16x2 product (operands with <= 2 and <= 4 significant bits)
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
-  __nv_bfloat162 r = __hmul2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
+// kind::f16 with fp16 A/B, fp32 accumulate; a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4)  // D format: f32 (A and B format fields 0: f16)
+         | (a_mn & 1u) << 15 | (b_mn & 1u) << 16 | ((N >> 3) & 63u) << 17 | ((M >> 4) & 31u) << 24;
+}
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Two E4M3 bytes (bits 0..7 and 8..15) to two fp16 values (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(two));
+  return r;
+}
+
+// Two fp32 values to one fp16x2 word (`lo` in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Four E2M1 codes (the 16-bit x: channel i in bits 4i..4i+3) to four exact
-// bf16 values in two bf16x2 words, in registers: the magnitudes come from two
-// 8-entry byte tables (low and high byte of the bf16 of 0, 0.5, 1, 1.5, 2, 3,
-// 4, 6) picked by prmt, the signs from a sign-replicating prmt.
-__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t x, uint32_t& v01, uint32_t& v23) {
-  constexpr uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u;  // low bytes, magnitudes 0..3 and 4..7
-  constexpr uint32_t kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;  // high bytes
-  const uint32_t sel = x & 0x7777u;
-  const uint32_t lo4 = __byte_perm(kLoA, kLoB, sel);
-  uint32_t hi4 = __byte_perm(kHiA, kHiB, sel);
-  // msb of bytes: x << 4 holds the signs of channels 0 and 2, x those of 1 and 3
+// fp16 values in two fp16x2 words. The fp16 of every E2M1 magnitude (0, 0.5,
+// 1, 1.5, 2, 3, 4, 6) has a zero low byte; its high byte comes from an
+// 8-entry byte table picked by prmt, the sign from a sign-replicating prmt.
+__device__ __forceinline__ void e2m1x4_to_f16(uint32_t x, uint32_t& v01, uint32_t& v23) {
+  const uint32_t mag = __byte_perm(0x3E3C3800u, 0x46444240u, x & 0x7777u);
+  // msb of bytes: x << 4 holds the signs of codes 0 and 2, x those of 1 and 3
   uint32_t smask;
   asm("prmt.b32 %0, %1, %2, 0x9D8C;" : "=r"(smask) : "r"(x), "r"(x << 4));
-  hi4 |= smask & 0x80808080u;
-  v01 = __byte_perm(lo4, hi4, 0x5140);
-  v23 = __byte_perm(lo4, hi4, 0x7362);
+  const uint32_t hi4 = mag | (smask & 0x80808080u);
+  v01 = __byte_perm(hi4, 0u, 0x1404u);
+  v23 = __byte_perm(hi4, 0u, 0x3424u);
 }
 
-// Transpose-reduce across a warp: lane L holds v[0..N) (one value per head,
-// N = 16 or 32); afterwards lane L returns the reduction over all 32 lanes of
-// head L mod N. Each stage halves the values a lane keeps (N/2 + ... + 1
-// shuffles); for N = 16 a last shuffle joins the two half-warps. v is
-// overwritten.
-template <bool kMax, int N>
-__device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) {
+// Transpose-reduce across a warp: lane L holds v[0..16) (one value per head);
+// afterwards lane L returns the reduction over all 32 lanes of head L mod 16.
+// v is overwritten.
+template <bool kMax>
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int width = N / 2; width >= 1; width >>= 1) {
+  for (int width = 8; width >= 1; width >>= 1) {
     const bool up = (lane & width) != 0;
 #pragma unroll
     for (int i = 0; i < width; ++i) {
@@ -96,465 +115,384 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&v)[N], int lane) 
       v[i] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
-  float r = v[0];
-  if (N == 16) {
-    const float o = __shfl_xor_sync(0xffffffffu, r, 16);
-    r = kMax ? fmaxf(r, o) : r + o;
-  }
-  return r;
+  const float o = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_release_acquire() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// grid (C, queries of the launch), clusters of C CTAs along x
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_partial_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
-  // barriers, tensor memory and the E4M3 table need nothing from the preceding
-  // kernel; its outputs (the indices, possibly Q) are read after pdl_wait()
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
+  // barriers, tensor memory, Q and the SWA tiles need nothing from the
+  // preceding kernel; its outputs (the indices) are read after pdl_wait()
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = tc::smem_u32(smem_raw);
   uint8_t* sm = smem_raw + (((raw_u32 + 1023u) & ~1023u) - raw_u32);
   uint8_t* sR = sm + kOffR;
-  uint8_t* sQP = sm + kOffQP;
-  uint64_t* bar_s0 = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T over channels 0..127 done
-  uint64_t* bar_s1 = bar_s0 + 1;                                 // S^T complete
-  uint64_t* bar_pv = bar_s0 + 2;                                 // O^T complete
-  uint64_t* q_full = bar_s0 + 3;                                 // 3 Q slots (slot 0 twice)
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 48);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 52);
-  __shared__ float red[4][kHeads];
-  __shared__ float m_s[kHeads], l_s[kHeads];
-  __shared__ uint16_t lut_e4m3[256];     // E4M3 byte -> bf16 value
-  __shared__ int row_valid[kMaxRows];    // 0 none, 1 selected latent, 2 SWA row
-  __shared__ int64_t row_src[kMaxRows];  // entry index in the plane, or SWA byte offset
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sP = sm + kOffP;
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T complete
+  uint64_t* bar_pv = bar_s + 1;                                  // O^T complete
+  uint64_t* q_full = bar_s + 2;                                  // Q landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 24);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 28);
+  __shared__ __align__(16) float red_m[4][kHeads];
+  __shared__ __align__(16) float red_l[4][kHeads];
+  __shared__ float q_mul[kHeads];        // sm_scale * 2^-k_h * log2(e)
+  __shared__ int row_valid[kRows];       // 0 none, 1 selected latent, 2 SWA row
+  __shared__ int64_t row_src[kRows];     // entry index in the plane, or SWA byte offset
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int C = (int)gridDim.x;
+  const int rank = (int)blockIdx.x;
   const int lq = blockIdx.y;
   const int qi = a.q0 + lq;
   const int seq = qi / a.L;
-  const int split = blockIdx.x;
-  const int rows = a.rows;
-  const int n_tiles = (rows + 127) >> 7;
 
-  // ---- Q channels 0..255: 4 TMA boxes of [64 h][64 c] = [64][128 B], SW128 ----
   if (tid == 0) {
-    tc::mbar_init(bar_s0, 1);
-    tc::mbar_init(bar_s1, 1);
+    tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_pv, 1);
-    for (int q = 0; q < 3; ++q) tc::mbar_init(&q_full[q], 1);
+    tc::mbar_init(q_full, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
-  if (tid < 256) {
-    const uint32_t byte = (uint32_t)tid;
-    __nv_bfloat16 e = __float2bfloat16_rn(e4m3_to_f32(byte));  // exact (4 significant bits)
-    lut_e4m3[byte] = *reinterpret_cast<uint16_t*>(&e);
-  }
-  pdl_wait();
-  // Q quarter q (channels 128q .. +127, two boxes of [64 h][64 c]) into slot
-  // q % 3 of the Q/P region: quarters 0-2 now, quarter 3 once quarter 0's
-  // MMAs have read slot 0
-  auto load_q_quarter = [&](const int q) {
-    uint8_t* slot = sQP + (q % 3) * kQQuarterBytes;
-    tc::mbar_arrive_expect_tx(&q_full[q % 3], kQQuarterBytes);
-    for (int blk = 0; blk < 2; ++blk)
-      tc::tma_load_2d(slot + blk * (kHeads * 128), &tmap_q, q * 128 + blk * 64, qi * kHeads, &q_full[q % 3]);
-  };
-  if (tid == 0)
-    for (int q = 0; q < 3; ++q) load_q_quarter(q);
-  // ---- rows of this chunk: position (or SWA row), validity ----
-  const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
-  const int32_t* idx_row = a.idx + (int64_t)seq * a.k;
-  if (tid < rows) {
-    const int t = split * rows + tid;
-    int valid = 0;
-    int64_t src = 0;
-    if (t < a.k) {
-      const int32_t p = idx_row[t];
-      if (p >= 0) {
-        if (p < nv) {
-          valid = 1;                                   // selected latent
-          src = (int64_t)seq * a.kv_seq_stride + p;
-        } else {
-          record_error(&g_attn_error, CSA2_ERR_DEVICE);
-        }
-      }
-    } else if (t < a.k + a.n_swa) {
-      // SWA row; in prefill row j of query qi is row qi + j of the array, and
-      // rows before swa_first_row lie before a Bounded Replay start
-      if ((int64_t)qi + (t - a.k) >= (int64_t)a.swa_first_row) {
-        valid = 2;
-        src = (int64_t)qi * a.swa_q_stride + (int64_t)(t - a.k) * kHeadDim;
-      }
-    }
-    row_valid[tid] = valid;
-    row_src[tid] = src;
-  }
   __syncthreads();
-
-  // ---- gather: all loads first. Pass ps covers rows 64ps .. 64ps+63: warp w
-  // rows 64ps + 4w .. +3, 8 lanes per row; lane `sub` holds channels
-  // 32sub .. 32sub+31 of the low half and of the high half of the row ----
-  constexpr int kPasses = (kMaxRows + 63) / 64;
-  const int grp = lane >> 3, sub = lane & 7;
-  uint4 raw[kPasses][4];
-#pragma unroll
-  for (int ps = 0; ps < kPasses; ++ps) {
-    const int r = ps * 64 + warp * 4 + grp;
-    const int kind = r < rows ? row_valid[r] : 0;
-    const int64_t src = r < rows ? row_src[r] : 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw[ps][i] = make_uint4(0u, 0u, 0u, 0u);
-    if (kind == 1) {
-      const uint8_t* d = a.kv_data + src * kKvBytes + sub * 16;
-      raw[ps][0] = *reinterpret_cast<const uint4*>(d);
-      raw[ps][1] = *reinterpret_cast<const uint4*>(d + 128);
-      const uint8_t* sc = a.kv_scale + src * kKvScales + sub * 2;
-      raw[ps][2].x = (uint32_t)*reinterpret_cast<const uint16_t*>(sc) |
-                     ((uint32_t)*reinterpret_cast<const uint16_t*>(sc + 16) << 16);
-    } else if (kind == 2) {
-      const uint8_t* e = a.swa + src + sub * 32;
-      raw[ps][0] = *reinterpret_cast<const uint4*>(e);
-      raw[ps][1] = *reinterpret_cast<const uint4*>(e + 16);
-      raw[ps][2] = *reinterpret_cast<const uint4*>(e + 256);
-      raw[ps][3] = *reinterpret_cast<const uint4*>(e + 272);
-    }
+  if (tid == 0) {
+    // Q of this query: 8 TMA boxes of [64 h][64 c] bf16, 128-byte swizzle
+    tc::mbar_arrive_expect_tx(q_full, 8 * kQBlk);
+    for (int b = 0; b < 8; ++b) tc::tma_load_2d(sQ + b * kQBlk, &tmap_q, b * 64, qi * kHeads, q_full);
   }
-  // dequantise one half (channels 256h .. 256h+255) of every row into R
-  auto dequant_half = [&](const int half) {
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) {
-      const int r = ps * 64 + warp * 4 + grp;
-      if (r >= rows) continue;
-      const int kind = row_valid[r];
-      uint32_t o[16];
-      if (kind == 1) {
-        const uint4 d = raw[ps][half];
-        const uint32_t scb = (raw[ps][2].x >> (16 * half)) & 0xFFFFu;
-        const uint32_t sa = lut_e4m3[scb & 0xFFu], sb = lut_e4m3[scb >> 8];
-        const uint32_t sa2 = sa | (sa << 16), sb2 = sb | (sb << 16);
-        const uint32_t w[4] = {d.x, d.y, d.z, d.w};  // w[i]: channels 8i .. 8i+7 of the lane's 32
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t v01, v23;
-            e2m1x4_to_bf16((w[i] >> (16 * hh)) & 0xFFFFu, v01, v23);
-            const uint32_t s2 = i < 2 ? sa2 : sb2;   // channels 0..15: scale a, 16..31: scale b
-            o[4 * i + 2 * hh] = mul_bf16x2(v01, s2);
-            o[4 * i + 2 * hh + 1] = mul_bf16x2(v23, s2);
-          }
-        }
-      } else if (kind == 2) {
-        const uint4 x = raw[ps][2 * half], y = raw[ps][2 * half + 1];
-        const uint32_t w[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t pair = w[e >> 1] >> (16 * (e & 1));
-          o[e] = (uint32_t)lut_e4m3[pair & 0xFFu] | ((uint32_t)lut_e4m3[(pair >> 8) & 0xFFu] << 16);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) o[e] = 0u;   // invalid rows are zero: P = 0 must not meet NaN
-      }
-      uint8_t* region = sR + (half * 4 + (sub >> 1)) * kBlkR;
-      const uint32_t c0 = (uint32_t)(sub & 1) * 4;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(region + tc::sw128_offset((uint32_t)r, c0 + j)) =
-            make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-    }
-  };
-  // S^T (+)= R[:, 128q .. +127] . Q[:, 128q .. +127]^T for every tile of 128 rows
-  auto issue_s = [&](const uint32_t tmem, const int q) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, 64, 0, 0);
-    const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQP) + (uint32_t)((q % 3) * kQQuarterBytes);
-    for (int t = 0; t < n_tiles; ++t)
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t blk = (uint32_t)(q * 2) + ((uint32_t)kk >> 2), off = ((uint32_t)kk & 3u) * 32u;
-        const uint64_t ad = tc::smem_desc(r_addr + blk * kBlkR + (uint32_t)t * (128u * 128u) + off, 0, 1024,
-                                          tc::kSwizzle128B);
-        const uint64_t bd = tc::smem_desc(q_addr + ((uint32_t)kk >> 2) * (kHeads * 128) + off, 0, 1024,
-                                          tc::kSwizzle128B);
-        tc::mma_bf16(tmem + kColS + 64u * (uint32_t)t, ad, bd, idesc, (q | kk) ? 1u : 0u);
-      }
-  };
-
-  dequant_half(0);
-  tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  bool lead_ok = true;   // meaningful in thread 0
-  if (tid == 0) {
-    lead_ok = tc::mbar_wait_bounded(&q_full[0], 0, s_abort, &g_attn_error);
-    if (lead_ok) {
-      issue_s(tmem, 0);
-      tc::mma_commit(bar_s0);
-      lead_ok = tc::mbar_wait_bounded(&q_full[1], 0, s_abort, &g_attn_error);
-      if (lead_ok) issue_s(tmem, 1);
+
+  // ---- Q to fp16 with a power-of-two scale per head: thread (h, block b)
+  // owns the 64 channels of head h in block b (one 128-byte row) ----
+  {
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(q_full, 0, s_abort, &g_attn_error));
+    const int h = tid >> 3, b = tid & 7;
+    uint4* row = reinterpret_cast<uint4*>(sQ + b * kQBlk + h * 128);
+    uint4 v[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) v[c] = ok ? row[c] : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t amax = 0;   // bf16 bits of |q| compare as unsigned integers
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
     }
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    // largest |q| has exponent e (bf16 exponent field e + 127); 2^(14 - e) puts
+    // it in [2^14, 2^15). Clamped so that 2^k and 2^-k stay normal fp32.
+    int k = 0;
+    if (amax != 0u) {
+      const int e = (int)((amax >> 7) & 0xFFu) - 127;
+      k = min(max(14 - e, -100), 100);
+    }
+    const float up = __int_as_float((127 + k) << 23);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        o[i] = f32x2_to_f16x2(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
+      row[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (b == 0) q_mul[h] = a.sm_scale * __int_as_float((127 - k) << 23) * 1.4426950408889634f;
   }
-  dequant_half(1);
-  if (tid == 0 && lead_ok) {
-    // slot 0 takes quarter 3 once quarter 0's MMAs have read it
-    lead_ok = tc::mbar_wait_bounded(bar_s0, 0, s_abort, &g_attn_error);
-    if (lead_ok) load_q_quarter(3);
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  if (tid == 0 && lead_ok) {
-    lead_ok = tc::mbar_wait_bounded(&q_full[2], 0, s_abort, &g_attn_error);
-    if (lead_ok) {
-      issue_s(tmem, 2);
-      lead_ok = tc::mbar_wait_bounded(&q_full[0], 1, s_abort, &g_attn_error);
-      if (lead_ok) {
-        issue_s(tmem, 3);
-        tc::mma_commit(bar_s1);
+
+  const int n_swt = a.n_swt, n_sel = a.n_sel;
+  uint32_t tiles_done = 0;   // parity source of bar_s / bar_pv
+  float* part_o_q = a.part_o + (int64_t)lq * a.n_part * kHeads * kHeadDim;
+  float* part_ml_q = a.part_ml + (int64_t)lq * a.n_part * kHeads * 2;
+
+  // One tile: rows [128 tile, 128 tile + 128) of the SWA window (swa) or of the
+  // selected list, giving partial `part`.
+  auto run_tile = [&](const bool swa, const int tile, const int part) {
+    // ---- row list ----
+    if (tid < kRows) {
+      int valid = 0;
+      int64_t src = 0;
+      const int t = tile * kRows + tid;
+      if (swa) {
+        // in prefill, row t of query qi is row qi + t of the array, and rows
+        // before swa_first_row lie before a Bounded Replay start
+        if (t < a.n_swa && (int64_t)qi + t >= (int64_t)a.swa_first_row) {
+          valid = 2;
+          src = (int64_t)qi * a.swa_q_stride + (int64_t)t * kHeadDim;
+        }
+      } else if (t < a.k) {
+        // n_visible may come from the kernel before this one (a KV append):
+        // read after pdl_wait(), like the indices
+        const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
+        const int32_t p = a.idx[(int64_t)seq * a.k + t];
+        if (p >= 0) {
+          if (p < nv) {
+            valid = 1;
+            src = (int64_t)seq * a.kv_seq_stride + p;
+          } else {
+            record_error(&g_attn_error, CSA2_ERR_DEVICE);
+          }
+        }
+      }
+      row_valid[tid] = valid;
+      row_src[tid] = src;
+    }
+    __syncthreads();
+    // ---- gather: thread (row r, quarter sub) loads channels 128 sub .. +127 ----
+    const int r = tid >> 2, sub = tid & 3;
+    const int kind = row_valid[r];
+    const int64_t src = row_src[r];
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) raw[i] = make_uint4(0u, 0u, 0u, 0u);
+    uint2 scl = make_uint2(0u, 0u);
+    if (kind == 1) {
+      const uint4* d = reinterpret_cast<const uint4*>(a.kv_data + src * kKvBytes + sub * 64);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) raw[i] = d[i];
+      scl = *reinterpret_cast<const uint2*>(a.kv_scale + src * kKvScales + sub * 8);
+    } else if (kind == 2) {
+      const uint4* e = reinterpret_cast<const uint4*>(a.swa + src + sub * 128);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) raw[i] = e[i];
+    }
+    // ---- dequantise into R: chunk m (channels 128 sub + 8m .. +7) goes to
+    // block 2 sub + m / 8, 16-byte column m % 8 of row r ----
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      uint32_t o0 = 0u, o1 = 0u, o2 = 0u, o3 = 0u;
+      if (kind == 1) {
+        const uint4 d = raw[m >> 2];
+        const uint32_t w = (m & 3) == 0 ? d.x : (m & 3) == 1 ? d.y : (m & 3) == 2 ? d.z : d.w;
+        const uint32_t sb = ((m >> 1) < 4 ? scl.x >> (8 * (m >> 1)) : scl.y >> (8 * ((m >> 1) - 4))) & 0xFFu;
+        const uint32_t s1 = e4m3x2_to_f16x2(sb);          // low half: the scale
+        const uint32_t s2 = __byte_perm(s1, 0u, 0x1010u);  // the scale in both halves
+        e2m1x4_to_f16(w & 0xFFFFu, o0, o1);
+        e2m1x4_to_f16(w >> 16, o2, o3);
+        o0 = mul_f16x2(o0, s2);
+        o1 = mul_f16x2(o1, s2);
+        o2 = mul_f16x2(o2, s2);
+        o3 = mul_f16x2(o3, s2);
+      } else if (kind == 2) {
+        const uint4 e = raw[m >> 1];
+        const uint32_t w0 = (m & 1) ? e.z : e.x, w1 = (m & 1) ? e.w : e.y;
+        o0 = e4m3x2_to_f16x2(w0 & 0xFFFFu);
+        o1 = e4m3x2_to_f16x2(w0 >> 16);
+        o2 = e4m3x2_to_f16x2(w1 & 0xFFFFu);
+        o3 = e4m3x2_to_f16x2(w1 >> 16);
+      }
+      // invalid rows are zero: P = 0 must not meet NaN
+      *reinterpret_cast<uint4*>(sR + (2 * sub + (m >> 3)) * kBlkR + tc::sw128_offset((uint32_t)r, (uint32_t)(m & 7))) =
+          make_uint4(o0, o1, o2, o3);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t par = tiles_done & 1u;
+    // ---- S^T = R Q^T ----
+    if (tid == 0 && !*s_abort) {
+      constexpr uint32_t idesc = idesc_f16(128, 64, 0, 0);
+      const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQ);
+      for (int b = 0; b < 8; ++b)
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)b * kBlkR + (uint32_t)kk * 32u, 0, 1024,
+                                            tc::kSwizzle128B);
+          const uint64_t bd = tc::smem_desc(q_addr + (uint32_t)b * kQBlk + (uint32_t)kk * 32u, 0, 1024,
+                                            tc::kSwizzle128B);
+          tc::mma_bf16(tmem + kColS, ad, bd, idesc, (b | kk) ? 1u : 0u);
+        }
+      tc::mma_commit(bar_s);
+    }
+    __syncwarp();
+    const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_bounded(bar_s, par, s_abort, &g_attn_error));
+    tc::tc_fence_after();
+    // ---- softmax: warp w reads the 32 rows of lane quadrant w % 4 and the 16
+    // heads 16 (w / 4) ..; the four quadrant warps of a head group meet at
+    // named barrier 1 + w / 4 ----
+    const int rq = warp & 3, hg = warp >> 2, h0 = hg * 16;
+    const int row = rq * 32 + lane;
+    const bool rv = s_ok && row_valid[row] != 0;
+    float p[16];
+    {
+      uint32_t sr[16];
+      if (s_ok) {
+        tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(rq * 32) << 16) + kColS + (uint32_t)h0, sr);
+        tc::tmem_ld_wait();
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) p[j] = rv ? __uint_as_float(sr[j]) * q_mul[h0 + j] : -INFINITY;
+    }
+    {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = p[j];
+      const float m = warp_transpose_reduce16<true>(v, lane);
+      if (lane < 16) red_m[rq][h0 + lane] = m;
+    }
+    named_barrier(1 + hg, 128);
+    float M[16];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      float4 m4 = *reinterpret_cast<const float4*>(&red_m[0][h0 + 4 * j4]);
+#pragma unroll
+      for (int q = 1; q < 4; ++q) {
+        const float4 o = *reinterpret_cast<const float4*>(&red_m[q][h0 + 4 * j4]);
+        m4.x = fmaxf(m4.x, o.x);
+        m4.y = fmaxf(m4.y, o.y);
+        m4.z = fmaxf(m4.z, o.z);
+        m4.w = fmaxf(m4.w, o.w);
+      }
+      M[4 * j4] = m4.x;
+      M[4 * j4 + 1] = m4.y;
+      M[4 * j4 + 2] = m4.z;
+      M[4 * j4 + 3] = m4.w;
+    }
+    // P = 2^(s - M), fp16, stored K-major for the PV product: row h of the
+    // 64-row block row / 64, element row % 64
+    {
+      uint8_t* blkp = sP + (row >> 6) * kPBlk;
+      const uint32_t chunk = (uint32_t)(row & 63) >> 3, within = ((uint32_t)row & 7u) * 2u;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        p[j] = (p[j] == -INFINITY) ? 0.0f : exp2f(p[j] - M[j]);
+        const __half hv = __float2half_rn(p[j]);
+        *reinterpret_cast<__half*>(blkp + tc::sw128_offset((uint32_t)(h0 + j), chunk) + within) = hv;
       }
     }
-  }
-  if (tid == 0 && !lead_ok) *s_abort = 1;
-  __syncwarp();
-  // warp-uniform outcomes: the tcgen05.ld below needs the whole warp
-  const bool s_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_s1, 0, s_abort, &g_attn_error));
-  tc::tc_fence_after();
-
-  // ---- softmax over the chunk's rows. Warp w reads TMEM lanes 32(w%4) .. (rows
-  // 32(w%4) + lane of tile 0, and rows 128 + lane of tile 1 for w%4 == 0) and
-  // heads 16(w/4) .. +15 ----
-  constexpr int kHpw = 16;  // heads per warp
-  const int rq = warp & 3, hb = (warp >> 2) * kHpw;
-  const int row0 = rq * 32 + lane, row1 = 128 + lane;
-  const bool two = n_tiles > 1 && rq == 0;  // warp-uniform
-  const bool rv0 = s_ok && row0 < rows && row_valid[row0] != 0;
-  const bool rv1 = s_ok && two && row1 < rows && row_valid[row1] != 0;
-  float p0[kHpw], p1[kHpw];
-  auto load_scores = [&]() {
-    uint32_t r0[kHpw], r1[kHpw];
-    if (s_ok) {
-      tc::tmem_ld_32x32b_x16(tmem + ((uint32_t)(rq * 32) << 16) + kColS + hb, r0);
-      if (two) tc::tmem_ld_32x32b_x16(tmem + kColS + 64u + hb, r1);
-      tc::tmem_ld_wait();
+    {
+      const float l = warp_transpose_reduce16<false>(p, lane);
+      if (lane < 16) red_l[rq][h0 + lane] = l;
     }
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) {
-      p0[j] = rv0 ? __uint_as_float(r0[j]) * a.sm_scale : -INFINITY;
-      p1[j] = rv1 ? __uint_as_float(r1[j]) * a.sm_scale : -INFINITY;
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    // ---- O^T = R^T P^T : 4 x (M = 128 channels), N = 64, K = 128 rows ----
+    if (tid == 0 && s_ok) {
+      constexpr uint32_t idesc = idesc_f16(128, 64, 1, 0);  // A (channels x rows) is MN-major
+      const uint32_t r_addr = tc::smem_u32(sR), p_addr = tc::smem_u32(sP);
+      for (int mb = 0; mb < 4; ++mb)
+        for (int kk = 0; kk < kRows / 16; ++kk) {
+          // A: channels 128 mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
+          //    rows 16 kk .. +15 (8-row groups: SBO apart)
+          const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)(2 * mb) * kBlkR + (uint32_t)kk * 16u * 128u, kBlkR,
+                                            1024, tc::kSwizzle128B);
+          // B: the 64 P rows (heads), rows t = 16 kk .. +15 inside the 64-row block kk / 4
+          const uint64_t bd = tc::smem_desc(p_addr + (uint32_t)(kk >> 2) * kPBlk + ((uint32_t)kk & 3u) * 32u, 0,
+                                            1024, tc::kSwizzle128B);
+          tc::mma_bf16(tmem + kColO + 64u * (uint32_t)mb, ad, bd, idesc, kk ? 1u : 0u);
+        }
+      tc::mma_commit(bar_pv);
     }
-  };
-  load_scores();
-  // per-head max over the warp's rows lands in lane (head - hb) mod 16
-  {
-    float v[kHpw];
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) v[j] = fmaxf(p0[j], p1[j]);
-    const float m = warp_transpose_reduce<true, kHpw>(v, lane);
-    if (lane < kHpw) red[rq][hb + lane] = m;
-  }
-  __syncthreads();
-  if (tid < kHeads) m_s[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
-  __syncthreads();
-  // P = exp(S - m) from a second read of S; P_hi = bf16(P), P_lo = bf16(P - P_hi),
-  // stored K-major for the PV MMA as B-operand rows n = h (hi) and 64 + h (lo):
-  // per 64 rows t a block of [128 n][128 B]
-  // the scores are still in p0 / p1 (the reduction worked on a copy);
-  // exp(s - m) = 2^(s log2 e - m log2 e); only the warps of lane quadrant 0
-  // hold rows of the second tile
-  constexpr float kLog2e = 1.4426950408889634f;
-#pragma unroll
-  for (int j = 0; j < kHpw; ++j) {
-    const float ml = m_s[hb + j] * kLog2e;
-    p0[j] = (p0[j] == -INFINITY) ? 0.0f : exp2f(fmaf(p0[j], kLog2e, -ml));
-  }
-  if (two) {
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) {
-      const float ml = m_s[hb + j] * kLog2e;
-      p1[j] = (p1[j] == -INFINITY) ? 0.0f : exp2f(fmaf(p1[j], kLog2e, -ml));
+    // (m, l) of the tile, log2 domain; l = 0 marks a partial with no rows
+    if (tid < kHeads) {
+      const int h = tid;
+      const float m = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
+      const float l = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
+      *reinterpret_cast<float2*>(part_ml_q + ((int64_t)part * kHeads + h) * 2) = make_float2(m, l);
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) p1[j] = 0.0f;
-  }
-  auto store_p = [&](const int t, const float (&pv)[kHpw]) {
-    uint8_t* blkp = sQP + (t >> 6) * kPBlk;
-    const uint32_t chunk = (uint32_t)(t & 63) >> 3, within = ((uint32_t)t & 7u) * 2u;
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) {
-      const uint32_t h = (uint32_t)(hb + j);
-      const __nv_bfloat16 hi = __float2bfloat16_rn(pv[j]);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(pv[j] - __bfloat162float(hi));
-      *reinterpret_cast<__nv_bfloat16*>(blkp + tc::sw128_offset(h, chunk) + within) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(blkp + tc::sw128_offset(h + kHeads, chunk) + within) = lo;
-    }
-  };
-  if (row0 < rows) store_p(row0, p0);
-  if (two && row1 < rows) store_p(row1, p1);
-  __syncthreads();  // red[] reads for m_s are done before it is reused for the sums
-  {
-    float v[kHpw];
-#pragma unroll
-    for (int j = 0; j < kHpw; ++j) v[j] = p0[j] + p1[j];
-    const float l = warp_transpose_reduce<false, kHpw>(v, lane);
-    if (lane < kHpw) red[rq][hb + lane] = l;
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  if (tid < kHeads) l_s[tid] = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
-
-  // ---- O^T = R^T . [P_hi; P_lo]^T : 4 x (M = 128 channels), N = 128, K = rows ----
-  if (tid == 0 && s_ok) {
-    constexpr uint32_t idesc = tc::idesc_bf16(128, 128, 1, 0);  // A (channels x rows) is MN-major
-    const uint32_t r_addr = tc::smem_u32(sR), p_addr = tc::smem_u32(sQP);
-    const int ksteps = rows / 16;
-    for (int mb = 0; mb < 4; ++mb) {
-      for (int kk = 0; kk < ksteps; ++kk) {
-        // A: channels 128mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
-        //    rows 16kk .. +15 (8-row groups: SBO apart)
-        const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)(2 * mb) * kBlkR + (uint32_t)kk * 16u * 128u, kBlkR,
-                                          1024, tc::kSwizzle128B);
-        // B: 128 P rows (hi, lo), rows t = 16kk .. +15 inside the 64-row block kk/4
-        const uint64_t bd = tc::smem_desc(p_addr + (uint32_t)(kk >> 2) * kPBlk + ((uint32_t)kk & 3u) * 32u, 0, 1024,
-                                          tc::kSwizzle128B);
-        tc::mma_bf16(tmem + kColO + 128u * (uint32_t)mb, ad, bd, idesc, kk ? 1u : 0u);
-      }
-    }
-    tc::mma_commit(bar_pv);
-  }
-  __syncwarp();
-  const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, 0, s_abort, &g_attn_error));
-  tc::tc_fence_after();
-
-  // warp w reads the O^T lanes of quadrant w%4 in channel block mb = w/4
-  const int mb = warp >> 2;
-  const int c_own = mb * 128 + rq * 32 + lane;
-  const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 128u * (uint32_t)mb;
-  if (a.fused) {
-    // ---- merge inside the cluster of this query's chunks (rank = split) ----
-    // each chunk stores its unnormalised O as [h][c] fp32 in its own shared
-    // memory; after one cluster barrier every CTA reads all chunks' (m, l),
-    // forms the weights exp(m_j - M) / L, and rank r sums heads
-    // [64r/n, 64(r+1)/n) over the chunks in fixed order, writing the output.
-    namespace cg = cooperative_groups;
-    cg::cluster_group cl = cg::this_cluster();
-    const int nsp = a.n_split;
-    const int rank = (int)cl.block_rank();
-    __shared__ float w_s[kMaxClusterChunks][kHeads];   // m_j, then the weights
-    __shared__ float f_l[kMaxClusterChunks][kHeads];   // l_j, then l_j exp(m_j - M)
-    __shared__ float e_s[kMaxClusterChunks][kHeads];   // exp(m_j - M)
-    __shared__ float M_s[kHeads];
-    float* o_s = reinterpret_cast<float*>(sR);  // 128 KiB of the R tile, free after the PV product
+    __syncwarp();
+    const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, par, s_abort, &g_attn_error));
+    tc::tc_fence_after();
+    // ---- partial O to the workspace: warp w reads channel lanes of quadrant
+    // w % 4 in block w / 4, all 64 heads; [h][c] fp32 ----
+    const int mb = warp >> 2;
+    const int c_own = mb * 128 + rq * 32 + lane;
+    const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)mb;
+    float* po = part_o_q + (int64_t)part * kHeads * kHeadDim + c_own;
 #pragma unroll
     for (int hh = 0; hh < kHeads; hh += 32) {
-      uint32_t rh[32], rl[32];
+      uint32_t ov[32];
       if (ok) {
-        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, rh);
-        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)(kHeads + hh), rl);
+        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
         tc::tmem_ld_wait();
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        o_s[(hh + j) * kHeadDim + c_own] = ok ? __uint_as_float(rh[j]) + __uint_as_float(rl[j]) : 0.0f;
+      for (int j = 0; j < 32; ++j) po[(hh + j) * kHeadDim] = ok ? __uint_as_float(ov[j]) : 0.0f;
     }
-    if (tid < kHeads && !ok) l_s[tid] = 0.0f;
-    cl.sync();
-    // rank r sums heads [64r/n, 64(r+1)/n): items i = tid + kThreads u are
-    // float4 columns of that slice; the remote loads of the first two items
-    // go out before the weights are formed
-    const int h0 = kHeads * rank / nsp, h1 = kHeads * (rank + 1) / nsp;
-    const int n_items = (h1 - h0) * (kHeadDim / 4);
-    float4 v[2][kMaxClusterChunks];
-    auto load_items = [&](const int i0) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kThreads;
-        const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
-#pragma unroll
-        for (int j = 0; j < kMaxClusterChunks; ++j)
-          if (j < nsp && i < n_items)
-            v[u][j] = *reinterpret_cast<const float4*>(cl.map_shared_rank(o_s, j) + h * kHeadDim + c4);
-      }
-    };
-    load_items(tid);
-    // (m, l) of every chunk, one remote load each; e_j = l_j exp(m_j - M)
-    if (tid < nsp * kHeads) {
-      const int j = tid / kHeads, h = tid % kHeads;
-      const float lj = *cl.map_shared_rank(&l_s[h], j);
-      w_s[j][h] = lj > 0.0f ? *cl.map_shared_rank(&m_s[h], j) : -INFINITY;
-      f_l[j][h] = lj;
-    }
+    ++tiles_done;
+    // the next tile rewrites the row list, R, P and the tensor memory only
+    // after every thread is past this tile's reads of them
+    tc::tc_fence_before();
     __syncthreads();
-    // thread (j, h): M = max_j m_j, e_j = exp(m_j - M), then L = sum_j l_j e_j in
-    // fixed order and the weight e_j / L (m_s and l_s stay as they are: the
-    // other CTAs of the cluster may still be reading them)
-    if (tid < nsp * kHeads) {
-      const int j = tid / kHeads, h = tid % kHeads;
-      float M = -INFINITY;
-      for (int jj = 0; jj < nsp; ++jj) M = fmaxf(M, w_s[jj][h]);
-      const float e = f_l[j][h] > 0.0f ? expf(w_s[j][h] - M) : 0.0f;
-      e_s[j][h] = e;
-      f_l[j][h] *= e;  // l_j e_j, read by every j below
-      if (j == 0) M_s[h] = M;
+    tc::tc_fence_after();
+  };
+
+  for (int j = rank; j < n_swt; j += C) run_tile(true, j, j);
+  pdl_wait();
+  for (int i = rank; i < n_sel; i += C) run_tile(false, i, n_swt + i);
+
+  // ---- merge: rank r sums heads [64r/C, 64(r+1)/C) over all partials ----
+  cluster_sync_release_acquire();
+  const int n_part = a.n_part;
+  const int hb0 = kHeads * rank / C, hb1 = kHeads * (rank + 1) / C;
+  const int nh = hb1 - hb0;
+  float* wts = reinterpret_cast<float*>(sR);   // [n_part][nh] weights (R is free now)
+  float* lse_s = wts + kMaxPartials * kHeads;  // [nh]
+  if (tid < nh) {
+    const int h = hb0 + tid;
+    float M = -INFINITY;
+    for (int j = 0; j < n_part; ++j) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml_q + ((int64_t)j * kHeads + h) * 2));
+      if (ml.y > 0.0f) M = fmaxf(M, ml.x);
     }
-    __syncthreads();
-    if (tid < nsp * kHeads) {
-      const int j = tid / kHeads, h = tid % kHeads;
-      float Lsum = 0.0f;
-      for (int jj = 0; jj < nsp; ++jj) Lsum += f_l[jj][h];   // fixed order
-      w_s[j][h] = Lsum > 0.0f ? e_s[j][h] / Lsum : 0.0f;
-      if (j == 0 && rank == 0 && a.lse) a.lse[(int64_t)qi * kHeads + h] = Lsum > 0.0f ? M_s[h] + logf(Lsum) : -INFINITY;
+    float Lsum = 0.0f;
+    for (int j = 0; j < n_part; ++j) {   // fixed order
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml_q + ((int64_t)j * kHeads + h) * 2));
+      const float e = ml.y > 0.0f ? exp2f(ml.x - M) : 0.0f;
+      wts[j * nh + tid] = e;
+      Lsum += ml.y * e;
     }
-    __syncthreads();
-    for (int i0 = tid; i0 < n_items; i0 += 2 * kThreads) {
-      if (i0 != tid) load_items(i0);
+    const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+    for (int j = 0; j < n_part; ++j) wts[j * nh + tid] *= inv;
+    lse_s[tid] = Lsum > 0.0f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
+  }
+  __syncthreads();
+  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
+  const int n_items = nh * (kHeadDim / 4);
+  constexpr int kBatch = 6;   // partials loaded together
+  for (int it = tid; it < n_items; it += kThreads) {
+    const int hl = it / (kHeadDim / 4), c4 = (it % (kHeadDim / 4)) * 4;
+    const float* src = part_o_q + (int64_t)(hb0 + hl) * kHeadDim + c4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < n_part; j0 += kBatch) {
+      float4 v[kBatch];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kThreads;
-        if (i >= n_items) break;
-        const int h = h0 + i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < kBatch; ++u)
+        if (j0 + u < n_part)
+          v[u] = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)(j0 + u) * kHeads * kHeadDim));
 #pragma unroll
-        for (int j = 0; j < kMaxClusterChunks; ++j) {   // fixed rank order
-          if (j >= nsp) break;
-          const float f = w_s[j][h];
-          acc.x = fmaf(v[u][j].x, f, acc.x);
-          acc.y = fmaf(v[u][j].y, f, acc.y);
-          acc.z = fmaf(v[u][j].z, f, acc.z);
-          acc.w = fmaf(v[u][j].w, f, acc.w);
-        }
-        const int64_t o = ((int64_t)qi * kHeads + h) * kHeadDim + c4;
-        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
-        const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(a.out + o) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+      for (int u = 0; u < kBatch; ++u) {   // fixed partial order
+        if (j0 + u >= n_part) break;
+        const float f = wts[(j0 + u) * nh + hl];
+        acc.x = fmaf(v[u].x, f, acc.x);
+        acc.y = fmaf(v[u].y, f, acc.y);
+        acc.z = fmaf(v[u].z, f, acc.z);
+        acc.w = fmaf(v[u].w, f, acc.w);
       }
     }
-    cl.sync();  // the other ranks have finished reading this CTA's shared memory
-  } else {
-    // ---- partial O = O_hi + O_lo (unnormalised, fp32) and (max, sum) to the workspace ----
-    float* po = a.part_o + ((int64_t)lq * a.n_split + split) * kHeads * kHeadDim;
-    if (ok) {
-#pragma unroll
-      for (int hh = 0; hh < kHeads; hh += 32) {
-        uint32_t rh[32], rl[32];
-        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, rh);
-        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)(kHeads + hh), rl);
-        tc::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          po[(hh + j) * kHeadDim + c_own] = __uint_as_float(rh[j]) + __uint_as_float(rl[j]);
-      }
-    }
-    if (tid < kHeads) {
-      float* ml = a.part_ml + (((int64_t)lq * a.n_split + split) * kHeads + tid) * 2;
-      ml[0] = m_s[tid];
-      ml[1] = ok ? l_s[tid] : 0.0f;
-    }
+    const int64_t o = ((int64_t)qi * kHeads + hb0 + hl) * kHeadDim + c4;
+    if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(a.out + o) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
   }
   tc::tc_fence_before();
   __syncthreads();
