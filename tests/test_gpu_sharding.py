@@ -11,6 +11,11 @@ import oracle
 from fp4_kv_cache_02_gb300.sharding import Csa2Ops, ShardPlan, sequential_decode_step
 
 from helpers import ATTN_ROW_TOL, DecodeCase, attn_row_error, check_topk, dev
+
+# sharded and unsharded steps split the same softmax into different partials;
+# each rounds its P to fp16 (relative 2^-11) against its own maximum, so the
+# two outputs may differ by two such roundings of the largest term
+SHARD_ROW_TOL = 2 * 2.0 ** -11
 from oracle_ops import shard_inputs
 
 pytestmark = pytest.mark.gpu
@@ -166,7 +171,7 @@ def test_sharded_decode_step_equals_unsharded_and_oracle(csa2, world):
     _sync_ok(csa2)
     assert torch.equal(idx, ref_idx)                 # same scores, same deterministic selection
     assert torch.equal(out, out32.to(torch.bfloat16))
-    assert attn_row_error(out32.cpu().numpy(), ref32.cpu().numpy()) <= 1e-4
+    assert attn_row_error(out32.cpu().numpy(), ref32.cpu().numpy()) <= SHARD_ROW_TOL
     gi, o32 = idx.cpu().numpy(), out32.cpu().numpy()
     for b in range(case.B):
         check_topk(case.oracle_scores(b), gi[b], k)
@@ -186,7 +191,7 @@ def test_sharded_decode_step_with_pool_equals_unsharded(csa2):
     _sync_ok(csa2)
     assert torch.equal(idx_full, ref_full)
     assert torch.equal(idx, ref_idx)
-    assert attn_row_error(out32.cpu().numpy(), ref32.cpu().numpy()) <= 1e-4
+    assert attn_row_error(out32.cpu().numpy(), ref32.cpu().numpy()) <= SHARD_ROW_TOL
     gi, o32 = idx.cpu().numpy(), out32.cpu().numpy()
     for b in range(case.B):
         ref, _ = case.oracle_attention(b, 0, gi[b])
