@@ -38,8 +38,7 @@ struct AttnArgs {
   float sm_scale;
   int32_t q0;               // first query of this launch
   int32_t n_sel, n_swt, n_part;  // tiles of selected rows, SWA tiles, partials (= tiles) per query
-  float* part_o;            // [n_q][n_part][64][512] unnormalised partial outputs
-  float* part_ml;           // [n_q][n_part][64][2] (max, sum), log2 domain
+  float* part_o;            // [n_q][n_part][16][64][32]: unnormalised partial outputs, 32-channel blocks
   uint16_t* out;            // [n_q][64][512] bf16
   float* out_f32;           // nullable
   float* lse;               // nullable
@@ -82,15 +81,15 @@ static int attn_kernel_attr() {
   return csa2_smem_optin((const void*)attn_tc::attn_tc_kernel, attn_tc::kSmemBytes, optin);
 }
 
-// Whether a cluster of `size` CTAs of the kernel can be resident, cached per
-// device.
-static bool attn_cluster_fits(int size) {
+// How many clusters of `size` CTAs of the kernel can be resident at once (0:
+// none), cached per device.
+static int attn_max_clusters(int size) {
   constexpr int kMaxDevices = 64;
-  static int cache[kMaxDevices][attn_tc::kMaxCluster + 1];  // 0 unknown, 1 fits, 2 does not
+  static int cache[kMaxDevices][attn_tc::kMaxCluster + 1];  // count + 1; 0 unknown
   static std::mutex mu;
   int dev = 0;
-  if (size < 1 || size > attn_tc::kMaxCluster) return false;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (size < 1 || size > attn_tc::kMaxCluster) return 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!cache[dev][size]) {
     int n = 0;
@@ -111,9 +110,9 @@ static bool attn_cluster_fits(int size) {
         n = 0;
       }
     }
-    cache[dev][size] = n > 0 ? 1 : 2;
+    cache[dev][size] = n + 1;
   }
-  return cache[dev][size] == 1;
+  return cache[dev][size] - 1;
 }
 
 struct AttnPlan {
@@ -121,16 +120,24 @@ struct AttnPlan {
   int cluster;               // CTAs per query
 };
 
-// Tiles of 128 rows; one cluster of up to 8 CTAs per query (one selected tile
-// a CTA at k = 512), smaller when the device cannot hold a cluster that size.
-static AttnPlan attn_plan(int32_t k, int32_t n_swa, bool query_device) {
+// Tiles of 128 rows. One CTA per tile (a cluster of n_part CTAs per query)
+// when those clusters all fit on the device at once: every CTA then walks one
+// tile, the SWA tiles early. Otherwise clusters of min(n_sel, 8) CTAs (one
+// selected tile each at k = 512) with the SWA tiles spread over them, smaller
+// when the device cannot hold a cluster that size. n_q: queries of one launch.
+static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_device) {
   AttnPlan p;
   p.n_sel = (k + attn_tc::kRows - 1) / attn_tc::kRows;
   p.n_swt = (n_swa + attn_tc::kRows - 1) / attn_tc::kRows;
   p.n_part = p.n_sel + p.n_swt;
   int c = p.n_sel < 1 ? 1 : p.n_sel > attn_tc::kMaxCluster ? attn_tc::kMaxCluster : p.n_sel;
-  if (query_device)
-    while (c > 1 && !attn_cluster_fits(c)) c >>= 1;
+  if (query_device) {
+    if (p.n_part > c && p.n_part <= attn_tc::kMaxCluster && attn_max_clusters(p.n_part) >= n_q) {
+      c = p.n_part;
+    } else {
+      while (c > 1 && attn_max_clusters(c) < 1) c >>= 1;
+    }
+  }
   p.cluster = c;
   return p;
 }
@@ -148,9 +155,9 @@ extern "C" size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k, 
   if (n_queries <= 0 || k < 0 || n_swa < 0) return 0;
   // partials are indexed by query within one launch of at most kQueriesPerLaunch
   const int32_t nq = attn_queries_per_launch(n_queries);
-  const AttnPlan plan = attn_plan(k, n_swa, false);
+  const AttnPlan plan = attn_plan(nq, k, n_swa, false);
   if (plan.n_part == 0) return 256;
-  return attn_part_o_bytes(nq, plan.n_part) + (size_t)nq * plan.n_part * kHeads * 2 * 4;
+  return attn_part_o_bytes(nq, plan.n_part);
 }
 
 extern "C" int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k, int32_t n_swa) {
@@ -161,7 +168,7 @@ extern "C" int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k, in
 static int launch_attn(AttnArgs a, const void* q_bf16, int32_t n_q, uint16_t* out, float* out_f32, float* lse,
                        void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (attn_kernel_attr() != CSA2_OK) return CSA2_ERR_CUDA;
-  const AttnPlan plan = attn_plan(a.k, a.n_swa, true);
+  const AttnPlan plan = attn_plan(attn_queries_per_launch(n_q), a.k, a.n_swa, true);
   if (plan.n_part > attn_tc::kMaxPartials) return CSA2_ERR_UNSUPPORTED_SHAPE;
   a.n_sel = plan.n_sel;
   a.n_swt = plan.n_swt;
@@ -172,7 +179,6 @@ static int launch_attn(AttnArgs a, const void* q_bf16, int32_t n_q, uint16_t* ou
   const size_t need = csa2_sparse_attn_workspace_size(n_q, a.k, a.n_swa);
   if (!ws || ws_bytes < need || !csa2_aligned(ws, 256)) return CSA2_ERR_WORKSPACE;
   a.part_o = (float*)ws;
-  a.part_ml = (float*)((char*)ws + attn_part_o_bytes(attn_queries_per_launch(n_q), plan.n_part));
   // Q rows of all queries as a 2-D bf16 tensor [n_q * 64][512], loaded in
   // [64 heads][64 channels] boxes with the 128-byte swizzle the MMA reads.
   auto encode = tensor_map_encoder();
@@ -208,7 +214,7 @@ extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
   if (B < 0 || L < 1 || k < 0 || n_swa < 0 || cap < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
   if (k > CSA2_MAX_TOPK || n_swa > 512) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 8) || !csa2_aligned(out_bf16, 8) ||
+  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 16) || !csa2_aligned(out_bf16, 8) ||
       (swa && !csa2_aligned(swa, 16)) || (out_f32 && !csa2_aligned(out_f32, 16)))
     return CSA2_ERR_ALIGNMENT;
   if (B == 0) return CSA2_OK;
@@ -237,7 +243,7 @@ extern "C" int csa2_sparse_attn_prefill_replay(const void* q_bf16, int32_t T, co
   if (T < 0 || k < 0 || n_swa < 0 || n_entries < 0 || replay_row < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
   if (k > CSA2_MAX_TOPK || n_swa > 512) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 8) || !csa2_aligned(out_bf16, 8) ||
+  if (!csa2_aligned(q_bf16, 16) || !csa2_aligned(kv_data, 16) || !csa2_aligned(kv_scale, 16) || !csa2_aligned(out_bf16, 8) ||
       (swa && !csa2_aligned(swa, 16)) || (out_f32 && !csa2_aligned(out_f32, 16)))
     return CSA2_ERR_ALIGNMENT;
   if (T == 0) return CSA2_OK;

@@ -10,9 +10,11 @@
 // tiles of selected entries. A thread-block cluster of C CTAs serves one
 // query; CTA r takes the tiles whose index is r modulo C, and each tile gives
 // one partial softmax (m, l, O) over its rows:
-//   1. the rows are loaded (all loads issued at once) and dequantised into
-//      shared memory as fp16 R[t][c] in 128-byte-swizzled blocks of 64
-//      channels. fp16 holds every row value exactly: an E2M1 x E4M3 product
+//   1. the rows are copied into a staging area by the bulk-copy engine (the
+//      SWA rows of a tile in one copy, a selected latent as 256 B of codes +
+//      32 B of scales: plain loads are bounded by the few misses an SM keeps
+//      in flight) and dequantised into shared memory as fp16 R[t][c] in
+//      128-byte-swizzled blocks of 64 channels. fp16 holds every row value exactly: an E2M1 x E4M3 product
 //      has at most 6 significant bits and lies in [2^-10, 2688]; an E4M3 SWA
 //      value is a subset of fp16;
 //   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (kind::f16, M = 128 rows,
@@ -26,13 +28,14 @@
 //      and stored as the K-major B operand;
 //   4. O^T[c][h] = sum_t R[t][c] P[h][t] on the tensor cores (M = 128
 //      channels x 4 blocks, N = 64, K = 128), the R tile read as an MN-major
-//      operand; the unnormalised O and (m, l) go to the workspace.
+//      operand; the unnormalised O is staged in shared memory and sent to the
+//      workspace by one bulk copy, (m, l) by plain stores.
 // The SWA tiles depend on nothing the kernel before this one writes, so they
 // run before the programmatic-launch wait; only the selected tiles follow it.
-// Merge: after one cluster barrier (release / acquire) CTA r reads the
-// partials of heads [64r/C, 64(r+1)/C) from the workspace (L2), weighs them
-// by 2^(m_j - M) / L in fixed partial order (deterministic) and writes the
-// output and the log-sum-exp.
+// Merge: after one cluster barrier (release / acquire) CTA r bulk-copies the
+// slices of heads [64r/C, 64(r+1)/C) of every partial from the workspace
+// (L2), weighs them by 2^(m_j - M) / L in fixed partial order
+// (deterministic) and writes the output and the log-sum-exp.
 #pragma once
 
 #include "tc_common.cuh"
@@ -50,6 +53,7 @@ constexpr int kOffR = 0;                        // 8 blocks = 128 KiB
 constexpr int kOffQ = kOffR + 8 * kBlkR;        // 8 blocks = 64 KiB
 constexpr int kOffP = kOffQ + 8 * kQBlk;        // 2 blocks = 16 KiB
 constexpr int kOffMisc = kOffP + 2 * kPBlk;
+constexpr int kOffStage = kOffR + 4 * kBlkR;    // a tile's raw rows, in R's upper half (64 KiB)
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                   // S^T: 64 columns (heads), lanes = rows
@@ -57,7 +61,11 @@ constexpr uint32_t kColO = 64;                  // O^T: 4 blocks x 64 columns (h
 constexpr int kMaxPartials = 36;                // 32 tiles of selected rows (k <= 4096) + 4 SWA tiles (<= 512 rows)
 
 static_assert(kSmemBytes <= 232448 - 4096, "shared memory budget (static arrays included)");
-static_assert(kMaxPartials * kHeads * 3 * 4 <= 8 * kBlkR, "merge scratch fits the R region");
+static_assert(kRows * kHeadDim <= 4 * kBlkR && kRows * (kKvBytes + kKvScales) <= 4 * kBlkR, "staging fits");
+// merge: (max, sum) and weights of every partial of the CTA's heads live in
+// the P region (at most 36 partials x 16 heads with 4 or more CTAs, 5 x 64
+// with one CTA, 6 x 32 with two, 7 x 22 with three)
+static_assert(36 * 16 * 12 <= 2 * kPBlk && 7 * 22 * 12 <= 2 * kPBlk, "merge scratch fits the P region");
 
 // kind::f16 with fp16 A/B, fp32 accumulate; a_mn / b_mn select MN-major operands.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
@@ -123,6 +131,18 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// (max, sum) pair into the shared memory of CTA `rank` of the cluster.
+__device__ __forceinline__ void st_cluster_f32x2(const void* local_addr, uint32_t rank, float x, float y) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(tc::smem_u32(local_addr)), "r"(rank));
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(x), "f"(y) : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_release_acquire() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -140,16 +160,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sR = sm + kOffR;
   uint8_t* sQ = sm + kOffQ;
   uint8_t* sP = sm + kOffP;
+  uint8_t* sStage = sm + kOffStage;
   uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kOffMisc);  // S^T complete
   uint64_t* bar_pv = bar_s + 1;                                  // O^T complete
   uint64_t* q_full = bar_s + 2;                                  // Q landed
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 24);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 28);
+  uint64_t* bar_g = bar_s + 3;                                   // a tile's rows landed (128 arrivals)
+  uint64_t* bar_m = bar_s + 4;                                   // merge slices landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc + 40);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 44);
   __shared__ __align__(16) float red_m[4][kHeads];
   __shared__ __align__(16) float red_l[4][kHeads];
   __shared__ float q_mul[kHeads];        // sm_scale * 2^-k_h * log2(e)
   __shared__ int row_valid[kRows];       // 0 none, 1 selected latent, 2 SWA row
-  __shared__ int64_t row_src[kRows];     // entry index in the plane, or SWA byte offset
+  // (max, sum) of every partial for the heads this CTA merges, written by the
+  // CTAs of the cluster through distributed shared memory: [part][head - hb0]
+  __shared__ float2 ml_in[kMaxPartials * 16];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = (int)gridDim.x;
@@ -162,10 +187,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_pv, 1);
     tc::mbar_init(q_full, 1);
+    tc::mbar_init(bar_g, kRows);
+    tc::mbar_init(bar_m, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
+  // every CTA of the cluster has started before any writes into another's
+  // shared memory (the wait follows the Q conversion)
+  cluster_arrive_relaxed();
   __syncthreads();
   if (tid == 0) {
     // Q of this query: 8 TMA boxes of [64 h][64 c] bf16, 128-byte swizzle
@@ -177,19 +207,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  // ---- Q to fp16 with a power-of-two scale per head: thread (h, block b)
-  // owns the 64 channels of head h in block b (one 128-byte row) ----
+  // ---- Q to fp16 with a power-of-two scale per head: thread (h, j) owns the
+  // 16-byte column j of head h's row in each of the 8 blocks (bank-conflict
+  // free: the 8 threads of a head cover the row's 8 columns) ----
   {
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(q_full, 0, s_abort, &g_attn_error));
-    const int h = tid >> 3, b = tid & 7;
-    uint4* row = reinterpret_cast<uint4*>(sQ + b * kQBlk + h * 128);
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_spin_bounded(q_full, 0, s_abort, &g_attn_error));
+    const int h = tid >> 3, j = tid & 7;
+    const uint32_t col = (uint32_t)((j ^ (h & 7)) << 4);
     uint4 v[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) v[c] = ok ? row[c] : make_uint4(0u, 0u, 0u, 0u);
+    for (int b = 0; b < 8; ++b)
+      v[b] = ok ? *reinterpret_cast<const uint4*>(sQ + b * kQBlk + h * 128 + col) : make_uint4(0u, 0u, 0u, 0u);
     uint32_t amax = 0;   // bf16 bits of |q| compare as unsigned integers
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
     }
@@ -205,26 +237,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float up = __int_as_float((127 + k) << 23);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t w[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
       uint32_t o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         o[i] = f32x2_to_f16x2(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
-      row[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(sQ + b * kQBlk + h * 128 + col) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    if (b == 0) q_mul[h] = a.sm_scale * __int_as_float((127 - k) << 23) * 1.4426950408889634f;
+    if (j == 0) q_mul[h] = a.sm_scale * __int_as_float((127 - k) << 23) * 1.4426950408889634f;
   }
 
-  const int n_swt = a.n_swt, n_sel = a.n_sel;
-  uint32_t tiles_done = 0;   // parity source of bar_s / bar_pv
-  float* part_o_q = a.part_o + (int64_t)lq * a.n_part * kHeads * kHeadDim;
-  float* part_ml_q = a.part_ml + (int64_t)lq * a.n_part * kHeads * 2;
+  cluster_wait();   // the peers have started: their shared memory may be written
+  const int n_swt = a.n_swt, n_part = a.n_part;
+  uint32_t tiles_done = 0;   // parity source of bar_g / bar_s / bar_pv
+  float* part_o_q = a.part_o + (int64_t)lq * n_part * kHeads * kHeadDim;
 
   // One tile: rows [128 tile, 128 tile + 128) of the SWA window (swa) or of the
   // selected list, giving partial `part`.
-  auto run_tile = [&](const bool swa, const int tile, const int part) {
-    // ---- row list ----
+  auto run_tile = [&](const bool swa, const int tile, const int part, const bool more_tiles) {
+    const uint32_t par = tiles_done & 1u;
+    // ---- row list; thread r < 128 starts the bulk copies of row r into the
+    // staging area (selected rows: 256 B of codes + 32 B of scales); the SWA
+    // rows of the tile are one contiguous copy ----
     if (tid < kRows) {
       int valid = 0;
       int64_t src = 0;
@@ -232,80 +267,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (swa) {
         // in prefill, row t of query qi is row qi + t of the array, and rows
         // before swa_first_row lie before a Bounded Replay start
-        if (t < a.n_swa && (int64_t)qi + t >= (int64_t)a.swa_first_row) {
-          valid = 2;
-          src = (int64_t)qi * a.swa_q_stride + (int64_t)t * kHeadDim;
+        if (t < a.n_swa && (int64_t)qi + t >= (int64_t)a.swa_first_row) valid = 2;
+        if (tid == 0) {
+          const int n_rows = min(kRows, a.n_swa - tile * kRows);
+          const uint32_t bytes = (uint32_t)n_rows * kHeadDim;
+          tc::mbar_arrive_expect_tx(bar_g, bytes);
+          tc::bulk_load(sStage, a.swa + (int64_t)qi * a.swa_q_stride + (int64_t)tile * kRows * kHeadDim, bytes, bar_g);
+        } else {
+          tc::mbar_arrive(bar_g);
         }
-      } else if (t < a.k) {
-        // n_visible may come from the kernel before this one (a KV append):
-        // read after pdl_wait(), like the indices
-        const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
-        const int32_t p = a.idx[(int64_t)seq * a.k + t];
-        if (p >= 0) {
-          if (p < nv) {
-            valid = 1;
-            src = (int64_t)seq * a.kv_seq_stride + p;
-          } else {
-            record_error(&g_attn_error, CSA2_ERR_DEVICE);
+      } else {
+        if (t < a.k) {
+          // n_visible may come from the kernel before this one (a KV append):
+          // read after pdl_wait(), like the indices
+          const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
+          const int32_t p = a.idx[(int64_t)seq * a.k + t];
+          if (p >= 0) {
+            if (p < nv) {
+              valid = 1;
+              src = (int64_t)seq * a.kv_seq_stride + p;
+            } else {
+              record_error(&g_attn_error, CSA2_ERR_DEVICE);
+            }
           }
+        }
+        if (valid) {
+          tc::mbar_arrive_expect_tx(bar_g, kKvBytes + kKvScales);
+          tc::bulk_load(sStage + tid * kKvBytes, a.kv_data + src * kKvBytes, kKvBytes, bar_g);
+          tc::bulk_load(sStage + kRows * kKvBytes + tid * kKvScales, a.kv_scale + src * kKvScales, kKvScales, bar_g);
+        } else {
+          tc::mbar_arrive(bar_g);
         }
       }
       row_valid[tid] = valid;
-      row_src[tid] = src;
     }
     __syncthreads();
-    // ---- gather: thread (row r, quarter sub) loads channels 128 sub .. +127 ----
-    const int r = tid >> 2, sub = tid & 3;
-    const int kind = row_valid[r];
-    const int64_t src = row_src[r];
-    uint4 raw[8];
+    const bool g_ok = __all_sync(0xffffffffu, tc::mbar_wait_spin_bounded(bar_g, par, s_abort, &g_attn_error));
+    // ---- dequantise into R (fp16, SW128 blocks of 64 channels). The staged
+    // bytes sit in R's upper half: read them all, then write R ----
+    if (swa) {
+      // warp w: rows 8w .. 8w+7; lane l: channels 16l .. 16l+15 of the row
+      uint4 raw[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) raw[i] = make_uint4(0u, 0u, 0u, 0u);
-    uint2 scl = make_uint2(0u, 0u);
-    if (kind == 1) {
-      const uint4* d = reinterpret_cast<const uint4*>(a.kv_data + src * kKvBytes + sub * 64);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) raw[i] = d[i];
-      scl = *reinterpret_cast<const uint2*>(a.kv_scale + src * kKvScales + sub * 8);
-    } else if (kind == 2) {
-      const uint4* e = reinterpret_cast<const uint4*>(a.swa + src + sub * 128);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) raw[i] = e[i];
-    }
-    // ---- dequantise into R: chunk m (channels 128 sub + 8m .. +7) goes to
-    // block 2 sub + m / 8, 16-byte column m % 8 of row r ----
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      uint32_t o0 = 0u, o1 = 0u, o2 = 0u, o3 = 0u;
-      if (kind == 1) {
-        const uint4 d = raw[m >> 2];
-        const uint32_t w = (m & 3) == 0 ? d.x : (m & 3) == 1 ? d.y : (m & 3) == 2 ? d.z : d.w;
-        const uint32_t sb = ((m >> 1) < 4 ? scl.x >> (8 * (m >> 1)) : scl.y >> (8 * ((m >> 1) - 4))) & 0xFFu;
-        const uint32_t s1 = e4m3x2_to_f16x2(sb);          // low half: the scale
-        const uint32_t s2 = __byte_perm(s1, 0u, 0x1010u);  // the scale in both halves
-        e2m1x4_to_f16(w & 0xFFFFu, o0, o1);
-        e2m1x4_to_f16(w >> 16, o2, o3);
-        o0 = mul_f16x2(o0, s2);
-        o1 = mul_f16x2(o1, s2);
-        o2 = mul_f16x2(o2, s2);
-        o3 = mul_f16x2(o3, s2);
-      } else if (kind == 2) {
-        const uint4 e = raw[m >> 1];
-        const uint32_t w0 = (m & 1) ? e.z : e.x, w1 = (m & 1) ? e.w : e.y;
-        o0 = e4m3x2_to_f16x2(w0 & 0xFFFFu);
-        o1 = e4m3x2_to_f16x2(w0 >> 16);
-        o2 = e4m3x2_to_f16x2(w1 & 0xFFFFu);
-        o3 = e4m3x2_to_f16x2(w1 >> 16);
+      for (int i = 0; i < 8; ++i) {
+        const int r = warp * 8 + i;
+        raw[i] = (g_ok && row_valid[r]) ? *reinterpret_cast<const uint4*>(sStage + r * kHeadDim + lane * 16)
+                                        : make_uint4(0u, 0u, 0u, 0u);
       }
-      // invalid rows are zero: P = 0 must not meet NaN
-      *reinterpret_cast<uint4*>(sR + (2 * sub + (m >> 3)) * kBlkR + tc::sw128_offset((uint32_t)r, (uint32_t)(m & 7))) =
-          make_uint4(o0, o1, o2, o3);
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = warp * 8 + i;
+        uint8_t* blk = sR + (lane >> 2) * kBlkR;
+        const uint32_t c0 = (uint32_t)(lane & 3) * 2u;
+        const uint4 e = raw[i];
+        // zero bytes decode to +0: invalid rows stay zero (P = 0 must not meet NaN)
+        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0)) =
+            make_uint4(e4m3x2_to_f16x2(e.x & 0xFFFFu), e4m3x2_to_f16x2(e.x >> 16), e4m3x2_to_f16x2(e.y & 0xFFFFu),
+                       e4m3x2_to_f16x2(e.y >> 16));
+        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + 1u)) =
+            make_uint4(e4m3x2_to_f16x2(e.z & 0xFFFFu), e4m3x2_to_f16x2(e.z >> 16), e4m3x2_to_f16x2(e.w & 0xFFFFu),
+                       e4m3x2_to_f16x2(e.w >> 16));
+      }
+    } else {
+      // warp w: rows 8w .. 8w+7, two per step; lane l: row 8w + 2i + l / 16,
+      // channels 32 (l % 16) .. +31 (16 bytes of codes, 2 scale bytes)
+      uint4 raw[4];
+      uint32_t scl[4];
+      const int c16 = lane & 15;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = warp * 8 + 2 * i + (lane >> 4);
+        const bool v = g_ok && row_valid[r];
+        raw[i] = v ? *reinterpret_cast<const uint4*>(sStage + r * kKvBytes + c16 * 16) : make_uint4(0u, 0u, 0u, 0u);
+        scl[i] = v ? (uint32_t)*reinterpret_cast<const uint16_t*>(sStage + kRows * kKvBytes + r * kKvScales + c16 * 2)
+                   : 0u;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = warp * 8 + 2 * i + (lane >> 4);
+        uint8_t* blk = sR + (c16 >> 1) * kBlkR;
+        const uint32_t c0 = (uint32_t)(c16 & 1) * 4u;
+        const uint32_t sc2 = e4m3x2_to_f16x2(scl[i]);       // scales of channels +0..15 (low) and +16..31 (high)
+        const uint32_t sa = __byte_perm(sc2, 0u, 0x1010u);  // low scale in both halves
+        const uint32_t sb = __byte_perm(sc2, 0u, 0x3232u);  // high scale in both halves
+        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};  // w[k]: channels 8k .. 8k+7
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+          const uint32_t s2 = kq < 2 ? sa : sb;
+          uint32_t o0, o1, o2, o3;
+          e2m1x4_to_f16(w[kq] & 0xFFFFu, o0, o1);
+          e2m1x4_to_f16(w[kq] >> 16, o2, o3);
+          // zero codes with a zero scale give +0: invalid rows stay zero
+          *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + (uint32_t)kq)) =
+              make_uint4(mul_f16x2(o0, s2), mul_f16x2(o1, s2), mul_f16x2(o2, s2), mul_f16x2(o3, s2));
+        }
+      }
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    const uint32_t par = tiles_done & 1u;
     // ---- S^T = R Q^T ----
     if (tid == 0 && !*s_abort) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 0, 0);
@@ -321,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(bar_s);
     }
     __syncwarp();
-    const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_bounded(bar_s, par, s_abort, &g_attn_error));
+    const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_spin_bounded(bar_s, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
     // ---- softmax: warp w reads the 32 rows of lane quadrant w % 4 and the 16
     // heads 16 (w / 4) ..; the four quadrant warps of a head group meet at
@@ -401,61 +464,98 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       tc::mma_commit(bar_pv);
     }
-    // (m, l) of the tile, log2 domain; l = 0 marks a partial with no rows
+    // (m, l) of the tile, log2 domain (l = 0 marks a partial with no rows),
+    // into the shared memory of the CTA that merges head h
     if (tid < kHeads) {
       const int h = tid;
       const float m = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
       const float l = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
-      *reinterpret_cast<float2*>(part_ml_q + ((int64_t)part * kHeads + h) * 2) = make_float2(m, l);
+      int r = (h * C) / kHeads;   // owner: the rank r with 64r/C <= h < 64(r+1)/C
+      while (kHeads * (r + 1) / C <= h) ++r;
+      while (kHeads * r / C > h) --r;
+      const int o0 = kHeads * r / C, onh = kHeads * (r + 1) / C - o0;
+      st_cluster_f32x2(&ml_in[part * onh + (h - o0)], (uint32_t)r, m, l);
     }
     __syncwarp();
-    const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, par, s_abort, &g_attn_error));
+    const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_spin_bounded(bar_pv, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
-    // ---- partial O to the workspace: warp w reads channel lanes of quadrant
-    // w % 4 in block w / 4, all 64 heads; [h][c] fp32 ----
-    const int mb = warp >> 2;
-    const int c_own = mb * 128 + rq * 32 + lane;
-    const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)mb;
-    float* po = part_o_q + (int64_t)part * kHeads * kHeadDim + c_own;
+    // ---- partial O: warp w reads the 32 channel lanes 32 cb .. of quadrant
+    // w % 4 in block w / 4 (cb = 4 (w / 4) + w % 4), all 64 heads, into R as
+    // [h][32] fp32 and sends those 8 KiB to the workspace with one bulk copy;
+    // a partial is laid out [cb][h][32] ----
+    {
+      const int cb = (warp >> 2) * 4 + rq;
+      const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
+      float* so = reinterpret_cast<float*>(sR) + cb * (kHeads * 32);
 #pragma unroll
-    for (int hh = 0; hh < kHeads; hh += 32) {
-      uint32_t ov[32];
-      if (ok) {
-        tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
-        tc::tmem_ld_wait();
+      for (int hh = 0; hh < kHeads; hh += 32) {
+        uint32_t ov[32];
+        if (ok) {
+          tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
+          tc::tmem_ld_wait();
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) so[(hh + j) * 32 + lane] = ok ? __uint_as_float(ov[j]) : 0.0f;
       }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) po[(hh + j) * kHeadDim] = ok ? __uint_as_float(ov[j]) : 0.0f;
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc::bulk_store(part_o_q + ((int64_t)part * 16 + cb) * (kHeads * 32), so, kHeads * 32 * 4);
+        tc::bulk_commit();
+        if (more_tiles) tc::bulk_wait_read_all();   // R is rewritten by the next tile
+      }
     }
+    tc::tc_fence_before();
     ++tiles_done;
     // the next tile rewrites the row list, R, P and the tensor memory only
     // after every thread is past this tile's reads of them
-    tc::tc_fence_before();
     __syncthreads();
-    tc::tc_fence_after();
   };
 
-  for (int j = rank; j < n_swt; j += C) run_tile(true, j, j);
+  // tile j of the list [SWA tiles, selected tiles] belongs to CTA j mod C; the
+  // SWA tiles come first, before the wait for the indices
+  for (int j = rank; j < n_part; j += C) {
+    if (j >= n_swt) break;
+    run_tile(true, j, j, j + C < n_part);
+  }
   pdl_wait();
-  for (int i = rank; i < n_sel; i += C) run_tile(false, i, n_swt + i);
+  for (int j = rank; j < n_part; j += C)
+    if (j >= n_swt) run_tile(false, j - n_swt, j, j + C < n_part);
 
   // ---- merge: rank r sums heads [64r/C, 64(r+1)/C) over all partials ----
+  if (lane == 0) {
+    tc::bulk_wait_all();       // this warp's partial slices are in global memory
+    tc::fence_proxy_async_all();
+  }
+  __syncwarp();
   cluster_sync_release_acquire();
-  const int n_part = a.n_part;
   const int hb0 = kHeads * rank / C, hb1 = kHeads * (rank + 1) / C;
   const int nh = hb1 - hb0;
-  float* wts = reinterpret_cast<float*>(sR);   // [n_part][nh] weights (R is free now)
-  float* lse_s = wts + kMaxPartials * kHeads;  // [nh]
-  if (tid < nh) {
-    const int h = hb0 + tid;
-    float M = -INFINITY;
-    for (int j = 0; j < n_part; ++j) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml_q + ((int64_t)j * kHeads + h) * 2));
-      if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  // slices of the partials (heads hb0 .. hb1-1 of each 32-channel block) by
+  // bulk copies into R and Q, which are free now; a slot is [cb][nh][32]
+  const uint32_t piece = (uint32_t)nh * 32 * 4;
+  const uint32_t slot_bytes = 16 * piece;
+  const int per_batch = (int)((uint32_t)(kOffP - kOffR) / (slot_bytes ? slot_bytes : 1u));
+  auto issue_batch = [&](const int j0, const int nb) {
+    // thread t < 16 nb copies piece cb = t % 16 of partial j0 + t / 16
+    if (tid == 0) tc::mbar_arrive_expect_tx(bar_m, (uint32_t)nb * slot_bytes);
+    __syncwarp();
+    if (tid < 16 * nb) {
+      const int u = tid >> 4, cb = tid & 15;
+      tc::bulk_load(sR + (size_t)u * slot_bytes + (size_t)cb * piece,
+                    part_o_q + (((int64_t)(j0 + u) * 16 + cb) * kHeads + hb0) * 32, piece, bar_m);
     }
+  };
+  if (n_part > 0) issue_batch(0, min(per_batch, n_part));
+  float* wts = reinterpret_cast<float*>(sP);   // [n_part][nh] weights
+  __shared__ float lse_s[kHeads];
+  if (tid < nh) {
+    float M = -INFINITY;
+    for (int j = 0; j < n_part; ++j)
+      if (ml_in[j * nh + tid].y > 0.0f) M = fmaxf(M, ml_in[j * nh + tid].x);
     float Lsum = 0.0f;
     for (int j = 0; j < n_part; ++j) {   // fixed order
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(part_ml_q + ((int64_t)j * kHeads + h) * 2));
+      const float2 ml = ml_in[j * nh + tid];
       const float e = ml.y > 0.0f ? exp2f(ml.x - M) : 0.0f;
       wts[j * nh + tid] = e;
       Lsum += ml.y * e;
@@ -464,33 +564,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_part; ++j) wts[j * nh + tid] *= inv;
     lse_s[tid] = Lsum > 0.0f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
   }
-  __syncthreads();
-  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
+  __syncthreads();   // the weights are visible
   const int n_items = nh * (kHeadDim / 4);
-  constexpr int kBatch = 6;   // partials loaded together
-  for (int it = tid; it < n_items; it += kThreads) {
-    const int hl = it / (kHeadDim / 4), c4 = (it % (kHeadDim / 4)) * 4;
-    const float* src = part_o_q + (int64_t)(hb0 + hl) * kHeadDim + c4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < n_part; j0 += kBatch) {
-      float4 v[kBatch];
+  constexpr int kMaxItems = kHeads * (kHeadDim / 4) / kThreads;   // 16 (one CTA taking all heads)
+  float4 acc[kMaxItems];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (j0 + u < n_part)
-          v[u] = __ldcg(reinterpret_cast<const float4*>(src + (int64_t)(j0 + u) * kHeads * kHeadDim));
+  for (int u = 0; u < kMaxItems; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint32_t mpar = 0;
+  for (int j0 = 0; j0 < n_part; j0 += per_batch) {
+    const int nb = min(per_batch, n_part - j0);
+    const bool m_ok = tc::mbar_wait_spin_bounded(bar_m, mpar, s_abort, &g_attn_error);
+    mpar ^= 1u;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {   // fixed partial order
-        if (j0 + u >= n_part) break;
-        const float f = wts[(j0 + u) * nh + hl];
-        acc.x = fmaf(v[u].x, f, acc.x);
-        acc.y = fmaf(v[u].y, f, acc.y);
-        acc.z = fmaf(v[u].z, f, acc.z);
-        acc.w = fmaf(v[u].w, f, acc.w);
+    for (int u = 0; u < kMaxItems; ++u) {
+      const int it = tid + u * kThreads;
+      if (it >= n_items) break;
+      // item: head hb0 + hl, channels 4 (it % 128) .. : block cb, float4 c4 of it
+      const int hl = it >> 7, cb = (it >> 3) & 15, c4 = it & 7;
+      const int off = (cb * nh + hl) * 32 + 4 * c4;
+      for (int jj = 0; jj < nb; ++jj) {   // fixed partial order
+        const float4 v = m_ok ? *reinterpret_cast<const float4*>(sR + (size_t)jj * slot_bytes + (size_t)off * 4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float f = wts[(j0 + jj) * nh + hl];
+        acc[u].x = fmaf(v.x, f, acc[u].x);
+        acc[u].y = fmaf(v.y, f, acc[u].y);
+        acc[u].z = fmaf(v.z, f, acc[u].z);
+        acc[u].w = fmaf(v.w, f, acc[u].w);
       }
     }
-    const int64_t o = ((int64_t)qi * kHeads + hb0 + hl) * kHeadDim + c4;
-    if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc;
-    const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x, acc.y), b1 = __floats2bfloat162_rn(acc.z, acc.w);
+    __syncthreads();   // the next batch overwrites the slots
+    if (j0 + per_batch < n_part) issue_batch(j0 + per_batch, min(per_batch, n_part - j0 - per_batch));
+  }
+  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
+#pragma unroll
+  for (int u = 0; u < kMaxItems; ++u) {
+    const int it = tid + u * kThreads;
+    if (it >= n_items) break;
+    const int hl = it >> 7, c = (it & 127) * 4;
+    const int64_t o = ((int64_t)qi * kHeads + hb0 + hl) * kHeadDim + c;
+    if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc[u];
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+    const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
     *reinterpret_cast<uint2*>(a.out + o) =
         make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
   }

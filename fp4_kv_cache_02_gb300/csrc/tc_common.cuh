@@ -74,6 +74,30 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait_bounded, but polls without suspending for the first
+// `spin_ns`: for waits on a short critical path, where every waiting warp
+// has nothing else to do and a suspended warp would resume late.
+__device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                       int* err_word, uint64_t spin_ns = 20000ull) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < spin_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort) return false;
+  }
+  return mbar_wait_bounded(bar, parity, abort, err_word);
+}
+
 // ---- TMA ------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                             int32_t c2, uint64_t* bar) {
@@ -97,6 +121,21 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
                "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// Bulk copy shared -> global (16-byte aligned addresses, size a multiple of
+// 16), tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(smem_src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until this thread's committed bulk stores have read their shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Waits until this thread's committed bulk stores have completed (written global memory).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders generic-proxy and async-proxy (bulk copy, TMA) accesses of all state spaces.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // 16- and 4-byte asynchronous global -> shared copies; src_bytes = 0 fills the
 // destination with zeros and reads nothing.
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
