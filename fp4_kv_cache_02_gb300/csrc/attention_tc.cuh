@@ -14,9 +14,9 @@
 //      SWA rows of a tile in one copy, a selected latent as 256 B of codes +
 //      32 B of scales: plain loads are bounded by the few misses an SM keeps
 //      in flight) and dequantised into shared memory as fp16 R[t][c] in
-//      128-byte-swizzled blocks of 64 channels. fp16 holds every row value exactly: an E2M1 x E4M3 product
-//      has at most 6 significant bits and lies in [2^-10, 2688]; an E4M3 SWA
-//      value is a subset of fp16;
+//      128-byte-swizzled blocks of 64 channels. fp16 holds every row value
+//      exactly: an E2M1 x E4M3 product has at most 6 significant bits and
+//      lies in [2^-10, 2688]; an E4M3 SWA value is a subset of fp16;
 //   2. S^T[t][h] = R[t] . Q[h] on the tensor cores (kind::f16, M = 128 rows,
 //      N = 64 heads, K = 512). Q was converted once per CTA from bf16 to fp16
 //      with a power-of-two scale per head (2^k_h puts the head's largest
@@ -93,18 +93,14 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   return r;
 }
 
-// Four E2M1 codes (the 16-bit x: channel i in bits 4i..4i+3) to four exact
-// fp16 values in two fp16x2 words. The fp16 of every E2M1 magnitude (0, 0.5,
-// 1, 1.5, 2, 3, 4, 6) has a zero low byte; its high byte comes from an
-// 8-entry byte table picked by prmt, the sign from a sign-replicating prmt.
-__device__ __forceinline__ void e2m1x4_to_f16(uint32_t x, uint32_t& v01, uint32_t& v23) {
-  const uint32_t mag = __byte_perm(0x3E3C3800u, 0x46444240u, x & 0x7777u);
-  // msb of bytes: x << 4 holds the signs of codes 0 and 2, x those of 1 and 3
-  uint32_t smask;
-  asm("prmt.b32 %0, %1, %2, 0x9D8C;" : "=r"(smask) : "r"(x), "r"(x << 4));
-  const uint32_t hi4 = mag | (smask & 0x80808080u);
-  v01 = __byte_perm(hi4, 0u, 0x1404u);
-  v23 = __byte_perm(hi4, 0u, 0x3424u);
+// Eight E2M1 codes (the 32-bit w: channel i in bits 4i..4i+3) to eight exact
+// fp16 values in four fp16x2 words (o0: channels 0, 1; ...; o3: 6, 7).
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(w));
 }
 
 // Transpose-reduce across a warp: lane L holds v[0..16) (one value per head);
@@ -125,6 +121,13 @@ __device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lan
   }
   const float o = __shfl_xor_sync(0xffffffffu, v[0], 16);
   return kMax ? fmaxf(v[0], o) : v[0] + o;
+}
+
+// 2^x (ex2.approx: relative error below 2^-22; +inf/-inf/NaN pass through).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 16-byte column j of head h's row in each of the 8 blocks (bank-conflict
   // free: the 8 threads of a head cover the row's 8 columns) ----
   {
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_spin_bounded(q_full, 0, s_abort, &g_attn_error));
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(q_full, 0, s_abort, &g_attn_error));
     const int h = tid >> 3, j = tid & 7;
     const uint32_t col = (uint32_t)((j ^ (h & 7)) << 4);
     uint4 v[8];
@@ -302,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_valid[tid] = valid;
     }
     __syncthreads();
-    const bool g_ok = __all_sync(0xffffffffu, tc::mbar_wait_spin_bounded(bar_g, par, s_abort, &g_attn_error));
+    const bool g_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_g, par, s_abort, &g_attn_error));
     // ---- dequantise into R (fp16, SW128 blocks of 64 channels). The staged
     // bytes sit in R's upper half: read them all, then write R ----
     if (swa) {
@@ -320,14 +323,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = warp * 8 + i;
         uint8_t* blk = sR + (lane >> 2) * kBlkR;
         const uint32_t c0 = (uint32_t)(lane & 3) * 2u;
+        // lanes of odd blocks write their second chunk first, so that the
+        // lanes of one store cover eight different bank groups
+        const uint32_t sw = (uint32_t)(lane >> 2) & 1u;
         const uint4 e = raw[i];
+        const uint32_t a0 = sw ? e.z : e.x, a1 = sw ? e.w : e.y, b0 = sw ? e.x : e.z, b1 = sw ? e.y : e.w;
         // zero bytes decode to +0: invalid rows stay zero (P = 0 must not meet NaN)
-        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0)) =
-            make_uint4(e4m3x2_to_f16x2(e.x & 0xFFFFu), e4m3x2_to_f16x2(e.x >> 16), e4m3x2_to_f16x2(e.y & 0xFFFFu),
-                       e4m3x2_to_f16x2(e.y >> 16));
-        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + 1u)) =
-            make_uint4(e4m3x2_to_f16x2(e.z & 0xFFFFu), e4m3x2_to_f16x2(e.z >> 16), e4m3x2_to_f16x2(e.w & 0xFFFFu),
-                       e4m3x2_to_f16x2(e.w >> 16));
+        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + sw)) =
+            make_uint4(e4m3x2_to_f16x2(a0 & 0xFFFFu), e4m3x2_to_f16x2(a0 >> 16), e4m3x2_to_f16x2(a1 & 0xFFFFu),
+                       e4m3x2_to_f16x2(a1 >> 16));
+        *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + (sw ^ 1u))) =
+            make_uint4(e4m3x2_to_f16x2(b0 & 0xFFFFu), e4m3x2_to_f16x2(b0 >> 16), e4m3x2_to_f16x2(b1 & 0xFFFFu),
+                       e4m3x2_to_f16x2(b1 >> 16));
       }
     } else {
       // warp w: rows 8w .. 8w+7, two per step; lane l: row 8w + 2i + l / 16,
@@ -352,15 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sc2 = e4m3x2_to_f16x2(scl[i]);       // scales of channels +0..15 (low) and +16..31 (high)
         const uint32_t sa = __byte_perm(sc2, 0u, 0x1010u);  // low scale in both halves
         const uint32_t sb = __byte_perm(sc2, 0u, 0x3232u);  // high scale in both halves
-        const uint32_t w[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};  // w[k]: channels 8k .. 8k+7
+        // word k of the 16 bytes: channels 8k .. 8k+7; step kq writes word
+        // (kq + c16 / 2) % 4, so that the 16 lanes of a row cover eight bank
+        // groups
+        const int rot = (c16 >> 1) & 3;
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
-          const uint32_t s2 = kq < 2 ? sa : sb;
+          const int k = (kq + rot) & 3;
+          const uint32_t w = k == 0 ? raw[i].x : k == 1 ? raw[i].y : k == 2 ? raw[i].z : raw[i].w;
+          const uint32_t s2 = k < 2 ? sa : sb;
           uint32_t o0, o1, o2, o3;
-          e2m1x4_to_f16(w[kq] & 0xFFFFu, o0, o1);
-          e2m1x4_to_f16(w[kq] >> 16, o2, o3);
+          e2m1x8_to_f16(w, o0, o1, o2, o3);
           // zero codes with a zero scale give +0: invalid rows stay zero
-          *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + (uint32_t)kq)) =
+          *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + (uint32_t)k)) =
               make_uint4(mul_f16x2(o0, s2), mul_f16x2(o1, s2), mul_f16x2(o2, s2), mul_f16x2(o3, s2));
         }
       }
@@ -372,19 +383,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- S^T = R Q^T ----
     if (tid == 0 && !*s_abort) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 0, 0);
-      const uint32_t r_addr = tc::smem_u32(sR), q_addr = tc::smem_u32(sQ);
-      for (int b = 0; b < 8; ++b)
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)b * kBlkR + (uint32_t)kk * 32u, 0, 1024,
-                                            tc::kSwizzle128B);
-          const uint64_t bd = tc::smem_desc(q_addr + (uint32_t)b * kQBlk + (uint32_t)kk * 32u, 0, 1024,
-                                            tc::kSwizzle128B);
-          tc::mma_bf16(tmem + kColS, ad, bd, idesc, (b | kk) ? 1u : 0u);
-        }
+      // descriptors advance by constant steps (address fields count 16 bytes)
+      const uint64_t ad0 = tc::smem_desc(tc::smem_u32(sR), 0, 1024, tc::kSwizzle128B);
+      const uint64_t bd0 = tc::smem_desc(tc::smem_u32(sQ), 0, 1024, tc::kSwizzle128B);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {   // block b = i / 4 (64 channels), K step kk = i % 4 (16 channels)
+        const uint64_t ko = (uint64_t)((i & 3) * 2);
+        tc::mma_bf16(tmem + kColS, ad0 + (uint64_t)((i >> 2) * (kBlkR >> 4)) + ko,
+                     bd0 + (uint64_t)((i >> 2) * (kQBlk >> 4)) + ko, idesc, i ? 1u : 0u);
+      }
       tc::mma_commit(bar_s);
     }
     __syncwarp();
-    const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_spin_bounded(bar_s, par, s_abort, &g_attn_error));
+    const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_bounded(bar_s, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
     // ---- softmax: warp w reads the 32 rows of lane quadrant w % 4 and the 16
     // heads 16 (w / 4) ..; the four quadrant warps of a head group meet at
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t chunk = (uint32_t)(row & 63) >> 3, within = ((uint32_t)row & 7u) * 2u;
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        p[j] = (p[j] == -INFINITY) ? 0.0f : exp2f(p[j] - M[j]);
+        p[j] = (p[j] == -INFINITY) ? 0.0f : fast_exp2(p[j] - M[j]);
         const __half hv = __float2half_rn(p[j]);
         *reinterpret_cast<__half*>(blkp + tc::sw128_offset((uint32_t)(h0 + j), chunk) + within) = hv;
       }
@@ -450,18 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- O^T = R^T P^T : 4 x (M = 128 channels), N = 64, K = 128 rows ----
     if (tid == 0 && s_ok) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 1, 0);  // A (channels x rows) is MN-major
-      const uint32_t r_addr = tc::smem_u32(sR), p_addr = tc::smem_u32(sP);
-      for (int mb = 0; mb < 4; ++mb)
-        for (int kk = 0; kk < kRows / 16; ++kk) {
-          // A: channels 128 mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
-          //    rows 16 kk .. +15 (8-row groups: SBO apart)
-          const uint64_t ad = tc::smem_desc(r_addr + (uint32_t)(2 * mb) * kBlkR + (uint32_t)kk * 16u * 128u, kBlkR,
-                                            1024, tc::kSwizzle128B);
-          // B: the 64 P rows (heads), rows t = 16 kk .. +15 inside the 64-row block kk / 4
-          const uint64_t bd = tc::smem_desc(p_addr + (uint32_t)(kk >> 2) * kPBlk + ((uint32_t)kk & 3u) * 32u, 0,
-                                            1024, tc::kSwizzle128B);
-          tc::mma_bf16(tmem + kColO + 64u * (uint32_t)mb, ad, bd, idesc, kk ? 1u : 0u);
-        }
+      // A: channels 128 mb .. +127 (64-channel blocks 2mb, 2mb+1: LBO apart),
+      //    rows 16 kk .. +15 (8-row groups: SBO apart);
+      // B: the 64 P rows (heads), rows t = 16 kk .. +15 inside the 64-row block kk / 4
+      const uint64_t ad0 = tc::smem_desc(tc::smem_u32(sR), kBlkR, 1024, tc::kSwizzle128B);
+      const uint64_t bd0 = tc::smem_desc(tc::smem_u32(sP), 0, 1024, tc::kSwizzle128B);
+#pragma unroll
+      for (int i = 0; i < 4 * (kRows / 16); ++i) {   // channel block mb = i / 8, K step kk = i % 8
+        const int mb = i >> 3, kk = i & 7;
+        tc::mma_bf16(tmem + kColO + 64u * (uint32_t)mb,
+                     ad0 + (uint64_t)((2 * mb * kBlkR + kk * 16 * 128) >> 4),
+                     bd0 + (uint64_t)(((kk >> 2) * kPBlk + (kk & 3) * 32) >> 4), idesc, kk ? 1u : 0u);
+      }
       tc::mma_commit(bar_pv);
     }
     // (m, l) of the tile, log2 domain (l = 0 marks a partial with no rows),
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       st_cluster_f32x2(&ml_in[part * onh + (h - o0)], (uint32_t)r, m, l);
     }
     __syncwarp();
-    const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_spin_bounded(bar_pv, par, s_abort, &g_attn_error));
+    const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
     // ---- partial O: warp w reads the 32 channel lanes 32 cb .. of quadrant
     // w % 4 in block w / 4 (cb = 4 (w / 4) + w % 4), all 64 heads, into R as
@@ -514,13 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // tile j of the list [SWA tiles, selected tiles] belongs to CTA j mod C; the
   // SWA tiles come first, before the wait for the indices
+  bool waited = false;
+#pragma unroll 1
   for (int j = rank; j < n_part; j += C) {
-    if (j >= n_swt) break;
-    run_tile(true, j, j, j + C < n_part);
+    const bool swa = j < n_swt;
+    if (!swa && !waited) {
+      pdl_wait();
+      waited = true;
+    }
+    run_tile(swa, swa ? j : j - n_swt, j, j + C < n_part);
   }
-  pdl_wait();
-  for (int j = rank; j < n_part; j += C)
-    if (j >= n_swt) run_tile(false, j - n_swt, j, j + C < n_part);
+  if (!waited) pdl_wait();
 
   // ---- merge: rank r sums heads [64r/C, 64(r+1)/C) over all partials ----
   if (lane == 0) {
@@ -531,22 +546,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_release_acquire();
   const int hb0 = kHeads * rank / C, hb1 = kHeads * (rank + 1) / C;
   const int nh = hb1 - hb0;
-  // slices of the partials (heads hb0 .. hb1-1 of each 32-channel block) by
-  // bulk copies into R and Q, which are free now; a slot is [cb][nh][32]
-  const uint32_t piece = (uint32_t)nh * 32 * 4;
-  const uint32_t slot_bytes = 16 * piece;
-  const int per_batch = (int)((uint32_t)(kOffP - kOffR) / (slot_bytes ? slot_bytes : 1u));
-  auto issue_batch = [&](const int j0, const int nb) {
-    // thread t < 16 nb copies piece cb = t % 16 of partial j0 + t / 16
-    if (tid == 0) tc::mbar_arrive_expect_tx(bar_m, (uint32_t)nb * slot_bytes);
+  // groups of up to 16 heads (one group when C >= 4): the group's slices of
+  // the partials come by bulk copies into R and Q (free now), a slot per
+  // partial laid out [cb][gh][32]; each thread sums 4 float4 items in fixed
+  // partial order. The first batch is requested before the weights are formed.
+  auto issue_batch = [&](const int g0, const int gh, const int j0, const int nb) {
+    const uint32_t piece = (uint32_t)gh * 32 * 4;
+    if (tid == 0) tc::mbar_arrive_expect_tx(bar_m, (uint32_t)nb * 16 * piece);
     __syncwarp();
-    if (tid < 16 * nb) {
+    if (tid < 16 * nb) {   // thread t copies piece cb = t % 16 of partial j0 + t / 16
       const int u = tid >> 4, cb = tid & 15;
-      tc::bulk_load(sR + (size_t)u * slot_bytes + (size_t)cb * piece,
-                    part_o_q + (((int64_t)(j0 + u) * 16 + cb) * kHeads + hb0) * 32, piece, bar_m);
+      tc::bulk_load(sR + (size_t)u * 16 * piece + (size_t)cb * piece,
+                    part_o_q + (((int64_t)(j0 + u) * 16 + cb) * kHeads + hb0 + g0) * 32, piece, bar_m);
     }
   };
-  if (n_part > 0) issue_batch(0, min(per_batch, n_part));
+  auto batch_size = [&](const int gh) { return (int)((uint32_t)(kOffP - kOffR) / ((uint32_t)gh * 32 * 4 * 16)); };
+  if (nh > 0 && n_part > 0) issue_batch(0, min(16, nh), 0, min(batch_size(min(16, nh)), n_part));
   float* wts = reinterpret_cast<float*>(sP);   // [n_part][nh] weights
   __shared__ float lse_s[kHeads];
   if (tid < nh) {
@@ -556,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float Lsum = 0.0f;
     for (int j = 0; j < n_part; ++j) {   // fixed order
       const float2 ml = ml_in[j * nh + tid];
-      const float e = ml.y > 0.0f ? exp2f(ml.x - M) : 0.0f;
+      const float e = ml.y > 0.0f ? fast_exp2(ml.x - M) : 0.0f;
       wts[j * nh + tid] = e;
       Lsum += ml.y * e;
     }
@@ -564,49 +579,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_part; ++j) wts[j * nh + tid] *= inv;
     lse_s[tid] = Lsum > 0.0f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
   }
-  __syncthreads();   // the weights are visible
-  const int n_items = nh * (kHeadDim / 4);
-  constexpr int kMaxItems = kHeads * (kHeadDim / 4) / kThreads;   // 16 (one CTA taking all heads)
-  float4 acc[kMaxItems];
-#pragma unroll
-  for (int u = 0; u < kMaxItems; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
   uint32_t mpar = 0;
-  for (int j0 = 0; j0 < n_part; j0 += per_batch) {
-    const int nb = min(per_batch, n_part - j0);
-    const bool m_ok = tc::mbar_wait_spin_bounded(bar_m, mpar, s_abort, &g_attn_error);
-    mpar ^= 1u;
+#pragma unroll 1
+  for (int g0 = 0; g0 < nh; g0 += 16) {
+    const int gh = min(16, nh - g0);
+    const uint32_t slot_bytes = (uint32_t)gh * 32 * 4 * 16;
+    const int per_batch = batch_size(gh);
+    float4 acc[4];
 #pragma unroll
-    for (int u = 0; u < kMaxItems; ++u) {
-      const int it = tid + u * kThreads;
-      if (it >= n_items) break;
-      // item: head hb0 + hl, channels 4 (it % 128) .. : block cb, float4 c4 of it
-      const int hl = it >> 7, cb = (it >> 3) & 15, c4 = it & 7;
-      const int off = (cb * nh + hl) * 32 + 4 * c4;
-      for (int jj = 0; jj < nb; ++jj) {   // fixed partial order
-        const float4 v = m_ok ? *reinterpret_cast<const float4*>(sR + (size_t)jj * slot_bytes + (size_t)off * 4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float f = wts[(j0 + jj) * nh + hl];
-        acc[u].x = fmaf(v.x, f, acc[u].x);
-        acc[u].y = fmaf(v.y, f, acc[u].y);
-        acc[u].z = fmaf(v.z, f, acc[u].z);
-        acc[u].w = fmaf(v.w, f, acc[u].w);
+    for (int u = 0; u < 4; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int j0 = 0; j0 < n_part; j0 += per_batch) {
+      const int nb = min(per_batch, n_part - j0);
+      __syncthreads();   // the slots are free; the weights are visible
+      if (g0 > 0 || j0 > 0) issue_batch(g0, gh, j0, nb);
+      const bool m_ok = tc::mbar_wait_bounded(bar_m, mpar, s_abort, &g_attn_error);
+      mpar ^= 1u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = tid + u * kThreads;   // item: head g0 + it / 128, channels 4 (it % 128) ..
+        if (it >= gh * (kHeadDim / 4)) break;
+        const int hl = it >> 7, cb = (it >> 3) & 15, c4 = it & 7;
+        const int off = ((cb * gh + hl) * 32 + 4 * c4) * 4;
+#pragma unroll 1
+        for (int jj = 0; jj < nb; ++jj) {   // fixed partial order
+          const float4 v = m_ok ? *reinterpret_cast<const float4*>(sR + (size_t)jj * slot_bytes + off)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float f = wts[(j0 + jj) * nh + g0 + hl];
+          acc[u].x = fmaf(v.x, f, acc[u].x);
+          acc[u].y = fmaf(v.y, f, acc[u].y);
+          acc[u].z = fmaf(v.z, f, acc[u].z);
+          acc[u].w = fmaf(v.w, f, acc[u].w);
+        }
       }
     }
-    __syncthreads();   // the next batch overwrites the slots
-    if (j0 + per_batch < n_part) issue_batch(j0 + per_batch, min(per_batch, n_part - j0 - per_batch));
-  }
-  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
 #pragma unroll
-  for (int u = 0; u < kMaxItems; ++u) {
-    const int it = tid + u * kThreads;
-    if (it >= n_items) break;
-    const int hl = it >> 7, c = (it & 127) * 4;
-    const int64_t o = ((int64_t)qi * kHeads + hb0 + hl) * kHeadDim + c;
-    if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc[u];
-    const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
-    const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
-    *reinterpret_cast<uint2*>(a.out + o) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+    for (int u = 0; u < 4; ++u) {
+      const int it = tid + u * kThreads;
+      if (it >= gh * (kHeadDim / 4)) break;
+      const int hl = it >> 7, c = (it & 127) * 4;
+      const int64_t o = ((int64_t)qi * kHeads + hb0 + g0 + hl) * kHeadDim + c;
+      if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc[u];
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
+      const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
+      *reinterpret_cast<uint2*>(a.out + o) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+    }
   }
   tc::tc_fence_before();
   __syncthreads();

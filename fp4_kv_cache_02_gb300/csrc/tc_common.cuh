@@ -74,30 +74,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// As mbar_wait_bounded, but polls without suspending for the first
-// `spin_ns`: for waits on a short critical path, where every waiting warp
-// has nothing else to do and a suspended warp would resume late.
-__device__ __forceinline__ bool mbar_wait_spin_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                       int* err_word, uint64_t spin_ns = 20000ull) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (globaltimer_ns() - t0 < spin_ns) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if (*abort) return false;
-  }
-  return mbar_wait_bounded(bar, parity, abort, err_word);
-}
-
 // ---- TMA ------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                                             int32_t c2, uint64_t* bar) {
