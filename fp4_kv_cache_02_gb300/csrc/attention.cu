@@ -121,10 +121,13 @@ struct AttnPlan {
 };
 
 // Tiles of 128 rows. One CTA per tile (a cluster of n_part CTAs per query)
-// when those clusters all fit on the device at once: every CTA then walks one
-// tile, the SWA tiles early. Otherwise clusters of min(n_sel, 8) CTAs (one
-// selected tile each at k = 512) with the SWA tiles spread over them, smaller
-// when the device cannot hold a cluster that size. n_q: queries of one launch.
+// when those clusters all fit on the device at once (every CTA then walks one
+// tile, the SWA tiles early), or when there are so many queries that the
+// launch runs in many waves anyway (balanced CTAs waste the least). In
+// between, clusters of min(n_sel, 8) CTAs (one selected tile each at k = 512)
+// with the SWA tiles spread over them: one wave with some CTAs walking two
+// tiles beats two waves. Smaller clusters when the device cannot hold a
+// cluster that size. n_q: queries of one launch.
 static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_device) {
   AttnPlan p;
   p.n_sel = (k + attn_tc::kRows - 1) / attn_tc::kRows;
@@ -132,7 +135,8 @@ static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_devi
   p.n_part = p.n_sel + p.n_swt;
   int c = p.n_sel < 1 ? 1 : p.n_sel > attn_tc::kMaxCluster ? attn_tc::kMaxCluster : p.n_sel;
   if (query_device) {
-    if (p.n_part > c && p.n_part <= attn_tc::kMaxCluster && attn_max_clusters(p.n_part) >= n_q) {
+    const int fit = p.n_part > c && p.n_part <= attn_tc::kMaxCluster ? attn_max_clusters(p.n_part) : 0;
+    if (fit > 0 && (fit >= n_q || n_q >= 4 * fit)) {
       c = p.n_part;
     } else {
       while (c > 1 && attn_max_clusters(c) < 1) c >>= 1;
