@@ -218,6 +218,21 @@ def compress_kv(C, Z, bias, m):
     return out
 
 
+def bf16_rne(x):
+    """Round float64 values to the nearest bfloat16 value (8 significant bits,
+    ties to even), returned as float64. Reading 13 of the compressor: the
+    merged entry is rounded to bf16, the type of every latent the cache packs."""
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)                  # x = m 2^e, 0.5 <= |m| < 1 (m = 0 for x = 0)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)   # np.rint: round half to even
+
+
+def compress_kv_bf16(C, Z, bias, m):
+    """The compressor's entries as the cache stores them: compress_kv rounded
+    to bf16 (reading 13), then packed like any latent by pack_kv_fp4."""
+    return bf16_rne(compress_kv(C, Z, bias, m))
+
+
 def compressed_visible(pos, m):
     """Complete compressed entries visible to a query at token position pos:
     entry j covers tokens jm .. jm+m-1 and is visible once its last token is at

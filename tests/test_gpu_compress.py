@@ -1,8 +1,9 @@
 """GPU parity of the encoder Full-layer pieces: the softmax-weighted sequence
-compressor (bf16 entry within one bf16 rounding of the oracle's fp64 value,
-packed bytes bit-exact with the oracle's packing of the kernel's own bf16
-entry) and the prefill indexer scan over compressed entries (causal count of
-complete entries)."""
+compressor (bf16 entry within one bf16 rounding of the oracle's fp64 value;
+packed bytes bit-exact with the oracle's packing of its own bf16-rounded
+entry wherever the fp32 arithmetic cannot flip a bf16 rounding) and the
+prefill indexer scan over compressed entries (causal count of complete
+entries)."""
 
 import numpy as np
 import pytest
@@ -44,9 +45,24 @@ def test_compressor_matches_oracle(csa2, m, n):
     step = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
     cmax = np.abs(C.astype(np.float64)).reshape(n_out, m, 512).max(axis=1)
     assert np.all(np.abs(got - ref) <= step + 2.0 ** -20 * cmax + 1e-30)
-    # the packed entry is the oracle's packing of the kernel's own bf16 entry
+    # end to end: the packed bytes equal the oracle's packing of its own
+    # entry rounded to bf16, for every 16-channel block (one E4M3 scale, 8
+    # code bytes) whose fp64 values all lie farther than the kernel's fp32
+    # error from a bf16 rounding midpoint; a block with a value that close
+    # may round either way in fp32 and is checked against the oracle's
+    # packing of the kernel's own bf16 entry instead
+    gd, gs = kvd[:n_out].cpu().numpy(), kvs[:n_out].cpu().numpy()
+    rd, rs = oracle.pack_kv_fp4(oracle.compress_kv_bf16(C, Z, bias, m).astype(np.float32))
+    tol = 2.0 ** -20 * cmax + 4 * 2.0 ** -24 * np.abs(ref)
+    mid = np.floor(ref / step) * step + step / 2          # the bf16 midpoint inside ref's step
+    near = (np.abs(ref - mid) <= tol).reshape(n_out, 32, 16).any(axis=2)   # [entry][block]
+    same_d = (gd.reshape(n_out, 32, 8) == rd.reshape(n_out, 32, 8)).all(axis=2)
+    same_s = gs == rs
+    assert np.all(same_d[~near]) and np.all(same_s[~near])
+    print(f"m={m}: {int(near.sum())} of {near.size} blocks within the fp32 error of a bf16 midpoint")
     d, s = oracle.pack_kv_fp4(got)
-    assert np.array_equal(kvd[:n_out].cpu().numpy(), d) and np.array_equal(kvs[:n_out].cpu().numpy(), s)
+    kd, ks = d.reshape(n_out, 32, 8), s.reshape(n_out, 32)
+    assert np.array_equal(gd.reshape(n_out, 32, 8)[near], kd[near]) and np.array_equal(gs[near], ks[near])
     assert torch.all(kvd[n_out:] == 0xAB) and torch.all(kvs[n_out:] == 0xAB)
 
 

@@ -67,3 +67,26 @@ def test_compressed_visible_counts_complete_entries():
     assert [oracle.compressed_visible(p, 1) for p in range(5)] == [1, 2, 3, 4, 5]
     assert [oracle.compressed_visible(p, 2) for p in range(6)] == [0, 1, 1, 2, 2, 3]
     assert [oracle.compressed_visible(p, 4) for p in range(9)] == [0, 0, 0, 1, 1, 1, 1, 2, 2]
+
+
+def test_bf16_rounding_matches_the_library_cast():
+    # float32 inputs are exact in float64: the oracle's rounding must equal
+    # torch's round-to-nearest-even float32 -> bfloat16 cast, ties included
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(13)
+    x = (rng.standard_normal(200000) * np.exp2(rng.integers(-30, 30, 200000))).astype(np.float32)
+    bits = x.view(np.uint32)
+    ties = ((bits & ~np.uint32(0xFFFF)) | np.uint32(0x8000)).view(np.float32)   # exactly half a bf16 step
+    for v in (x, ties, np.array([0.0, -0.0, 1.0, -1.0, 3.0, 255.0, 257.0, 65280.0], np.float32)):
+        ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+        assert np.array_equal(oracle.bf16_rne(v.astype(np.float64)), ref)
+
+
+def test_bf16_rounding_of_values_between_float32_neighbours():
+    # a float64 just above a bf16 midpoint rounds up even where float32 would
+    # first round it onto the midpoint (no double rounding)
+    mid = 1.0 + 2.0 ** -8                           # halfway between bf16 1 and 1 + 2^-7
+    assert oracle.bf16_rne(mid) == 1.0              # tie to even
+    assert oracle.bf16_rne(mid + 2.0 ** -40) == 1.0 + 2.0 ** -7
+    assert oracle.bf16_rne(mid - 2.0 ** -40) == 1.0
+    assert oracle.bf16_rne(-(mid + 2.0 ** -40)) == -(1.0 + 2.0 ** -7)
