@@ -296,10 +296,10 @@ def measure_decode(csa2, ctx, wid, B, steps, warmup, use_graph=True, with_e2e=Tr
     if reindex:
         stages.append(("reindex_topk", st_reindex))
     stages.append(("sparse_attn", st_attn))
-    # our kernels per step: counter clear + scan (q quantisation, each CTA's running Top-K and, with the
-    # pool, block maxima) + candidate merge 3; pool: clear, histogram, select, finalize, expand 5;
-    # reindex: clear, scan, merge 3; attention: as the library plans it for B * L query-layers
-    n_launches = 3 + (5 + 3 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
+    # our kernels per step: workspace clear + scan (q quantisation, fused histogram and, with the pool,
+    # block maxima) + select + finalize 4; pool: clear, histogram, select, finalize, expand 5; reindex:
+    # clear, scan, select, finalize 4; attention: as the library plans it for B * L query-layers
+    n_launches = 4 + (5 + 4 if reindex else 0) + csa2.lib().csa2_sparse_attn_kernel_launches(B * L, K, W)
 
     def step(ev=None):
         for j, (_, fn) in enumerate(stages):

@@ -7,12 +7,8 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
                                uint32_t* hist, float* bmax, int early_reads, const void* q_bf16,
-                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done, uint2* cand,
-                               int32_t* cand_n, int32_t cand_k, cudaStream_t stream);
-int csa2_scan_chunks(int32_t B, int64_t n_pos);
-int csa2_launch_cand_merge(const uint2* cand, const int32_t* cand_n, int32_t B, int32_t n_chunks, int32_t k,
-                           int32_t* idx, cudaStream_t stream);
-int csa2_zero_words(void* p, size_t bytes, cudaStream_t stream);
+                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done,
+                               cudaStream_t stream);
 int csa2_topk_prepare(int32_t B, int64_t n, int32_t k, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream, uint32_t** hist, int32_t** scan_ctr, int32_t* scan_ctr_stride);
 int csa2_topk_from_hist(const float* scores, int32_t B, int64_t n, const int32_t* n_valid, const int32_t* positions,
@@ -80,8 +76,7 @@ extern "C" int csa2_index_score(const uint8_t* q_data, const uint8_t* q_e8m0, co
   if (positions == nullptr && n_pos > cap) return CSA2_ERR_INVALID_ARG;
   if (positions && !csa2_aligned(positions, 4)) return CSA2_ERR_ALIGNMENT;
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                    nullptr, nullptr, 0, nullptr, nullptr, 0, nullptr, nullptr, nullptr, 0,
-                                    (cudaStream_t)stream);
+                                    nullptr, nullptr, 0, nullptr, nullptr, 0, nullptr, (cudaStream_t)stream);
 }
 
 extern "C" int csa2_index_score_claimed(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
@@ -94,52 +89,24 @@ extern "C" int csa2_index_score_claimed(const uint8_t* q_data, const uint8_t* q_
   if (!csa2_aligned(tile_counters, 8)) return CSA2_ERR_ALIGNMENT;
   // sequence b's counter and finished-CTA count: tile_counters[2b], [2b + 1]
   return csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, nullptr, n_pos, scores,
-                                    nullptr, nullptr, 0, nullptr, tile_counters, 2, tile_counters + 1, nullptr,
-                                    nullptr, 0, (cudaStream_t)stream);
+                                    nullptr, nullptr, 0, nullptr, tile_counters, 2, tile_counters + 1,
+                                    (cudaStream_t)stream);
 }
 
 static inline size_t al256(size_t x) { return (x + 255) / 256 * 256; }
 
-// The fused path (Top-k inside the scan) serves k up to this; larger k take
-// the histogram path (scan with histogram -> select -> finalize).
-static constexpr int32_t kFusedTopkMaxK = 1024;
-
-static bool fused_topk(int32_t B, int64_t n_pos, int32_t k) {
-  return k <= kFusedTopkMaxK && csa2_scan_chunks(B, n_pos) <= 1024;
-}
-
-// Fused-path layout after the block maxima: candidates [B][chunks][k] (key,
-// position), their counts [B][chunks], the scan's tile counters [B][2] (zeroed
-// each call), then the pool's scratch.
-struct FusedWs {
-  size_t cand, cand_n, ctr, rest;
-};
-static FusedWs fused_ws_layout(int32_t B, int64_t n_pos, int32_t k) {
-  const size_t chunks = (size_t)csa2_scan_chunks(B, n_pos);
-  FusedWs w;
-  w.cand = 0;
-  w.cand_n = al256(w.cand + (size_t)B * chunks * (size_t)k * 8);
-  w.ctr = al256(w.cand_n + (size_t)B * chunks * 4);
-  w.rest = al256(w.ctr + (size_t)B * 8);
-  return w;
-}
-
-// Bytes of the leading scores (histogram path) or block maxima (pool).
-static size_t index_topk_head_bytes(int32_t B, int64_t n_pos, int32_t pool_blocks, bool fused) {
-  size_t head = fused ? 0 : al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
-  if (pool_blocks > 0) head += al256((size_t)B * (size_t)((n_pos + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK + 1) * 4);
-  return head;
-}
-
 extern "C" size_t csa2_index_topk_workspace_size(int32_t B, int64_t n_pos, int32_t k, int32_t pool_blocks) {
   if (B <= 0 || n_pos < 0 || k <= 0) return 0;
-  const size_t pool = pool_blocks > 0 ? csa2_block_pool_workspace_size(B, n_pos, CSA2_POOL_BLOCK, pool_blocks) : 0;
-  if (fused_topk(B, n_pos, k))
-    return index_topk_head_bytes(B, n_pos, pool_blocks, true) + fused_ws_layout(B, n_pos, k).rest + pool;
-  // histogram path: the pool's Top-K reuses the Full Top-K's scratch after it
+  size_t scores = al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
   size_t t = csa2_topk_workspace_size(B, n_pos, k);
-  if (pool > t) t = pool;
-  return index_topk_head_bytes(B, n_pos, pool_blocks, false) + t;
+  if (pool_blocks > 0) {
+    // block maxima (written by the scan) get their own slice; the pool's
+    // Top-K reuses the Full Top-K's scratch after it
+    scores += al256((size_t)B * (size_t)((n_pos + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK + 1) * 4);
+    size_t p = csa2_block_pool_workspace_size(B, n_pos, CSA2_POOL_BLOCK, pool_blocks);
+    if (p > t) t = p;
+  }
+  return scores + t;
 }
 
 static int index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const void* q_bf16, const float* w, int32_t B,
@@ -160,36 +127,15 @@ static int index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const void* 
   if (!workspace || workspace_bytes < need || !csa2_aligned(workspace, 256)) return CSA2_ERR_WORKSPACE;
   if (B == 0) return CSA2_OK;
   cudaStream_t s = (cudaStream_t)stream;
-  const bool fused = fused_topk(B, n_pos, k);
-  char* base = (char*)workspace;
-  float* scores = fused ? nullptr : (float*)base;
-  size_t off = fused ? 0 : al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
+  float* scores = (float*)workspace;
+  size_t off = al256((size_t)B * (size_t)(n_pos > 0 ? n_pos : 1) * 4);
   float* bmax = nullptr;
   if (pool_blocks > 0) {
-    bmax = (float*)(base + off);
+    bmax = (float*)((char*)workspace + off);
     off += al256((size_t)B * (size_t)((n_pos + CSA2_POOL_BLOCK - 1) / CSA2_POOL_BLOCK + 1) * 4);
   }
-  char* rest = base + off;
+  char* rest = (char*)workspace + off;
   size_t rest_bytes = workspace_bytes - off;
-  if (fused) {
-    // the scan keeps each CTA's Top-k (its candidates); one CTA per row merges
-    const FusedWs fw = fused_ws_layout(B, n_pos, k);
-    uint2* cand = (uint2*)(rest + fw.cand);
-    int32_t* cand_n = (int32_t*)(rest + fw.cand_n);
-    int32_t* ctr = (int32_t*)(rest + fw.ctr);
-    rc = csa2_zero_words(ctr, al256((size_t)B * 8), s);
-    if (rc) return rc;
-    rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos,
-                                    nullptr, nullptr, bmax, 1, q_bf16, ctr, 2, nullptr, cand, cand_n, k,
-                                    s);  // just after the counter clear
-    if (rc) return rc;
-    rc = csa2_launch_cand_merge(cand, cand_n, B, csa2_scan_chunks(B, n_pos), k, idx, s);
-    if (rc) return rc;
-    if (pool_blocks > 0)
-      rc = csa2_launch_pool_from_bmax(bmax, B, n_pos, n_visible, CSA2_POOL_BLOCK, pool_blocks, pool,
-                                      rest + fw.rest, rest_bytes - fw.rest, s);
-    return rc;
-  }
   // the scan's epilogue builds the Top-K histogram (and the pool's block maxima)
   uint32_t* hist = nullptr;
   int32_t* scan_ctr = nullptr;
@@ -197,7 +143,7 @@ static int index_topk(const uint8_t* q_data, const uint8_t* q_e8m0, const void* 
   rc = csa2_topk_prepare(B, n_pos, k, rest, rest_bytes, s, &hist, &scan_ctr, &scan_ctr_stride);
   if (rc) return rc;
   rc = csa2_launch_index_score_tc(q_data, q_e8m0, w, B, ik_data, ik_scale, cap, n_visible, positions, n_pos, scores,
-                                  hist, bmax, 1, q_bf16, scan_ctr, scan_ctr_stride, nullptr, nullptr, nullptr, 0,
+                                  hist, bmax, 1, q_bf16, scan_ctr, scan_ctr_stride, nullptr,
                                   s);  // just after the workspace clear
   if (rc) return rc;
   rc = csa2_topk_from_hist(scores, B, n_pos, positions ? nullptr : n_visible, positions, k, idx, rest, s);

@@ -64,25 +64,12 @@ static int device_sm_count() {
 // (gathered row by row). early_reads: the kernel just before in the stream
 // writes nothing the scan reads (it only clears the Top-K workspace), so the
 // scan's loads may start before that kernel ends.
-// CTAs per sequence of the decode scan: one wave of 3 CTAs per SM, each on a
-// run of tiles of one sequence (fewer when the sequence has fewer tiles).
-int csa2_scan_chunks(int32_t B, int64_t n_pos) {
-  const int64_t tiles = (n_pos + scan_tc::kTileRows - 1) / scan_tc::kTileRows;
-  if (B <= 0 || tiles <= 0) return 1;
-  const int64_t target = 3LL * device_sm_count();
-  int64_t chunks = target / B;
-  if (chunks < 1) chunks = 1;
-  if (chunks > tiles) chunks = tiles;
-  const int64_t per = (tiles + chunks - 1) / chunks;
-  return (int)((tiles + per - 1) / per);
-}
-
 int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, const float* w, int32_t B,
                                const uint8_t* ik_data, const uint8_t* ik_scale, int64_t cap,
                                const int32_t* n_visible, const int32_t* positions, int64_t n_pos, float* scores,
                                uint32_t* hist, float* bmax, int early_reads, const void* q_bf16,
-                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done, uint2* cand,
-                               int32_t* cand_n, int32_t cand_k, cudaStream_t stream) {
+                               int32_t* tile_ctr, int32_t tile_ctr_stride, int32_t* tile_done,
+                               cudaStream_t stream) {
   if (n_pos == 0 || B == 0) return CSA2_OK;
   if (q_bf16 ? !csa2_aligned(q_bf16, 16) : (!csa2_aligned(q_data, 16) || !csa2_aligned(q_e8m0, 4)))
     return CSA2_ERR_ALIGNMENT;
@@ -99,9 +86,12 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
     return CSA2_ERR_CUDA;
   // one wave of 3 CTAs per SM, each on a contiguous run of tiles of one sequence
   const int64_t tiles = (n_pos + scan_tc::kTileRows - 1) / scan_tc::kTileRows;
-  const int64_t chunks = csa2_scan_chunks(B, n_pos);
+  const int64_t target = 3LL * device_sm_count();
+  int64_t chunks = target / B;
+  if (chunks < 1) chunks = 1;
+  if (chunks > tiles) chunks = tiles;
   const int64_t per = (tiles + chunks - 1) / chunks;
-  if (cand && (cand_k < 1 || cand_k > scan_tc::kMaxCandK || hist)) return CSA2_ERR_UNSUPPORTED_SHAPE;
+  chunks = (tiles + per - 1) / per;
   static Csa2PerDeviceOnce optin;
   if (csa2_smem_optin((const void*)scan_tc::index_score_tc_kernel, scan_tc::kSmemBytes, optin) != CSA2_OK)
     return CSA2_ERR_CUDA;
@@ -110,7 +100,7 @@ int csa2_launch_index_score_tc(const uint8_t* q_data, const uint8_t* q_e8m0, con
   scan_tc::Params prm{ik_data, positions, q_data, q_e8m0, w, ik_scale, cap, n_visible, n_pos, scores, (int32_t)per,
                       hist, positions ? nullptr : bmax, early_reads, (const uint16_t*)q_bf16,
                       positions ? nullptr : tile_ctr, tile_ctr_stride, scan_tc::kStages, 2,
-                      positions ? nullptr : tile_done, cand, cand_n, cand_k};
+                      positions ? nullptr : tile_done};
   CSA2_LAUNCH_PDL(scan_tc::index_score_tc_kernel, dim3((unsigned)B, (unsigned)chunks), dim3(scan_tc::kThreads),
                   (size_t)scan_tc::kSmemBytes, stream, map, prm);
   return CSA2_OK;

@@ -26,7 +26,6 @@
 #include <cudaTypedefs.h>
 
 #include "codec_blocks.cuh"
-#include "cta_select.cuh"
 #include "tc_common.cuh"
 
 namespace csa2 {
@@ -53,22 +52,11 @@ constexpr int kOffSfb = kOffQ + kIdxHeads * kIkBytes; // 2048 bytes of q
 constexpr int kOffBars = kOffSfb + 512;
 constexpr int kNumBars = 2 * kStages + 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kOffHist = kOffMisc + 16;               // Top-K histogram of this CTA's scores, or
-                                                      // its running Top-K (candidate buffer and select scratch)
+constexpr int kOffHist = kOffMisc + 16;               // Top-K histogram of this CTA's scores
 constexpr int kRing = 16;                             // tile index of each tile in flight (claimed mode)
 constexpr int kOffRing = kOffHist + kTopkHistBins * 4;
 constexpr int kSmemBytes = kOffRing + kRing * 4 + 1024;  // + alignment slack
 static_assert(kOffQ % 1024 == 0, "q operand must be 1024-byte aligned");
-// running Top-K inside the histogram's 16 KiB: candidates, a 256-bin digit
-// histogram, select scratch, the count and the acceptance key
-constexpr int kCandCap = 1856;
-constexpr int kOffCand = kOffHist;
-constexpr int kOffCandHist = kOffCand + kCandCap * 8;
-constexpr int kOffCandScr = kOffCandHist + ctasel::kBins * 4;
-constexpr int kOffCandN = kOffCandScr + 40 * 4;
-constexpr int kMaxCandK = 1024;   // k of the running Top-K; a tile adds at most 128 candidates
-static_assert(kOffCandN + 8 <= kOffHist + kTopkHistBins * 4, "running Top-K fits the histogram's space");
-static_assert(kMaxCandK + 2 * kTileRows <= kCandCap && kCandCap <= 16 * 128, "candidate buffer sizes");
 
 struct Params {
   const uint8_t* ik_data;  // read directly (cp.async) in the positions mode
@@ -103,14 +91,6 @@ struct Params {
   // optional, beside tile_ctr (same stride): CTAs of the sequence that have
   // finished; the last one puts both words back to zero for the next launch
   int32_t* tile_done;
-  // optional, instead of the histogram: the exact Top-`cand_k` (key, position)
-  // of the scores this CTA produced, by (score desc, position asc), written
-  // to cand[(b * gridDim.y + chunk) * cand_k ..] with its count in
-  // cand_n[b * gridDim.y + chunk]. Every other entry of the CTA is beaten by
-  // cand_k of these, so the row's Top-K is among the CTAs' candidates.
-  uint2* cand;
-  int32_t* cand_n;
-  int32_t cand_k;
 };
 
 __global__ void __launch_bounds__(kThreads, 3)
@@ -134,14 +114,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
   uint32_t* s_hist = reinterpret_cast<uint32_t*>(sm + kOffHist);
-  uint2* s_cand = reinterpret_cast<uint2*>(sm + kOffCand);
-  uint32_t* s_chist = reinterpret_cast<uint32_t*>(sm + kOffCandHist);
-  uint32_t* s_cscr = reinterpret_cast<uint32_t*>(sm + kOffCandScr);
-  volatile uint32_t* s_ncand = reinterpret_cast<volatile uint32_t*>(sm + kOffCandN);
-  volatile uint32_t* s_thr = s_ncand + 1;   // candidates need a key at or above it
   volatile int32_t* s_ring = reinterpret_cast<volatile int32_t*>(sm + kOffRing);
   const bool with_hist = p.hist != nullptr;
-  const bool with_cand = p.cand != nullptr;
   const bool pos_mode = p.positions != nullptr;
   // claimed mode: tiles come from the sequence's counter, their indices pass
   // from the producer to the MMA warp and the epilogue through s_ring; a tile
@@ -180,8 +154,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       tc::mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
     }
     *s_abort = 0;
-    *s_ncand = 0u;
-    *s_thr = 0u;
     tc::fence_mbar_init();
   }
   if (threadIdx.x < 128 && p.q_bf16) {
@@ -379,30 +351,14 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int h = 0; h < kIdxHeads; ++h) wr[h] = p.w[(int64_t)b * kIdxHeads + h];
     const int row = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float* out = p.scores ? p.scores + (int64_t)b * p.n_pos : nullptr;
-    const ctasel::Group eg{1, 128};   // the four epilogue warps
+    float* out = p.scores + (int64_t)b * p.n_pos;
     for (int i = 0; claimed || i < n_tiles; ++i) {
       const int a = i & 1;
       const uint32_t aph = (uint32_t)(i >> 1) & 1u;
-      // outcome uniform over the four warps (tcgen05.ld below needs whole
-      // warps, and the running Top-K's barriers need all four); the barrier
-      // also orders the previous tile's candidate writes before the check below
-      const bool got = tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error);
-      if (!ctasel::group_all(eg, got)) break;
+      // warp-uniform outcome: tcgen05.ld below needs the whole warp
+      if (!__all_sync(0xffffffffu, tc::mbar_wait_bounded(&acc_full[a], aph, s_abort, &g_index_error))) break;
       const int64_t tile = claimed ? (int64_t)s_ring[i % kRing] : t_begin + i;
       if (tile < 0) break;
-      if (with_cand) {
-        const int nc = (int)*s_ncand;
-        if (nc > kCandCap - kTileRows) {   // room for one more tile's candidates
-          uint32_t kth;
-          const int kept = ctasel::select_topk_inplace(s_cand, nc, p.cand_k, eg, s_chist, s_cscr, &kth);
-          if (threadIdx.x == 0) {
-            *s_ncand = (uint32_t)kept;
-            *s_thr = kth;
-          }
-          eg.sync();
-        }
-      }
       tc::tc_fence_after();
       uint32_t r[32];
       tc::tmem_ld_32x32b_x32(tmem + lane_base + acc_col(a), r);
@@ -415,13 +371,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       for (int h = 0; h < kIdxHeads; ++h) sc = fmaf(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), sc);
       const int64_t li = tile * kTileRows + row;  // list index
       bool valid = li < nv;
-      int64_t posv = li;
       if (pos_mode) {
         const int32_t pp = li < p.n_pos ? p.positions[(int64_t)b * p.n_pos + li] : -1;
         valid = pp >= 0 && pp < nv_pos;
-        posv = pp;
       }
-      if (out && li < p.n_pos) out[li] = valid ? sc : -INFINITY;
+      if (li < p.n_pos) out[li] = valid ? sc : -INFINITY;
       if (p.bmax) {
         // maximum over the block of 8 consecutive entries (8 consecutive lanes);
         // entries past n_visible and NaN scores take no part
@@ -433,20 +387,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       if (with_hist && valid && score_is_candidate(sc))
         atomicAdd(&s_hist[score_key(sc) >> (32 - kTopkHistBits)], 1u);
-      if (with_cand && valid && score_is_candidate(sc)) {
-        const uint32_t key = score_key(sc);
-        if (key >= *s_thr) s_cand[atomicAdd((uint32_t*)s_ncand, 1u)] = make_uint2(key, (uint32_t)posv);
-      }
-    }
-    if (with_cand) {
-      // this CTA's exact Top-k, to the global candidate slice
-      eg.sync();
-      const int nc = (int)*s_ncand;
-      uint32_t kth;
-      const int kept = ctasel::select_topk_inplace(s_cand, nc, p.cand_k, eg, s_chist, s_cscr, &kth);
-      const int64_t slot = (int64_t)b * n_chunks + chunk;
-      for (int j = threadIdx.x; j < kept; j += 128) p.cand[slot * p.cand_k + j] = s_cand[j];
-      if (threadIdx.x == 0) p.cand_n[slot] = kept;
     }
     // tiles past the visible entries: this CTA's range, or in claimed mode
     // every n_chunks-th tile from t_vis + chunk
@@ -456,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int64_t t = fill_lo; t < fill_hi; t += fill_step) {
       const int64_t lo = t * kTileRows;
       const int64_t hi = lo + kTileRows < p.n_pos ? lo + kTileRows : p.n_pos;
-      if (out)
-        for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
+      for (int64_t pos = lo + threadIdx.x; pos < hi; pos += 128) out[pos] = -INFINITY;
       if (p.bmax) {
         float* bm = p.bmax + (int64_t)b * ((p.n_pos + 7) / 8);
         for (int64_t j = lo / 8 + threadIdx.x; j < (hi + 7) / 8; j += 128) bm[j] = -INFINITY;

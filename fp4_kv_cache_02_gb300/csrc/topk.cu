@@ -887,76 +887,6 @@ __global__ void __launch_bounds__(kFinThreads, 1) topk_finalize_kernel(int64_t n
   for (uint32_t i = threadIdx.x; i < (uint32_t)k; i += kFinThreads) dst[i] = i < nout ? out[i] : -1;
 }
 
-// ---- Top-K of the decode scan's candidates ------------------------------------
-// The decode scan leaves, per (row, CTA), that CTA's exact Top-k (key,
-// position) pairs: every entry of the row outside them is beaten by k entries
-// of its own CTA, so the row's Top-k is among the candidates. One CTA per row
-// selects it exactly: the k-th largest key by radix passes over the
-// candidates (empty slots read as key 0, below every candidate), the ties at
-// that key cut by smaller position, then the winners' positions in ascending
-// order.
-constexpr int kMaxMergeChunks = 1024;
-
-__global__ void __launch_bounds__(kFinThreads, 1)
-    topk_cand_merge_kernel(const uint2* __restrict__ cand, const int32_t* __restrict__ cand_n, int32_t n_chunks,
-                           int32_t k, int32_t n2, int32_t* __restrict__ idx) {
-  pdl_begin();
-  extern __shared__ uint32_t msm[];
-  uint32_t* cnt = msm;                                        // [kMaxMergeChunks]
-  uint32_t* hist = cnt + kMaxMergeChunks;                     // [kRadixBins]
-  uint32_t* scratch = hist + kRadixBins;                      // [kFinThreads + 8]
-  int32_t* win = reinterpret_cast<int32_t*>(scratch + kFinThreads + 8);  // [n2]
-  __shared__ uint32_t s_nwin;
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const uint2* cb = cand + (size_t)b * n_chunks * k;
-  uint32_t local = 0;
-  for (int c = tid; c < n_chunks; c += blockDim.x) {
-    const int32_t v = cand_n[(size_t)b * n_chunks + c];
-    cnt[c] = (uint32_t)(v < 0 ? 0 : v > k ? k : v);
-    local += cnt[c];
-  }
-  if (tid == 0) s_nwin = 0u;
-  uint32_t total;
-  (void)block_exclusive_scan(local, &total, scratch);   // also a barrier: cnt is complete
-  const int slots = n_chunks * k;
-  auto real = [&](int i) -> bool { const int c = i / k; return i - c * k < (int)cnt[c]; };
-  auto key_at = [&](int i) -> uint32_t { return real(i) ? cb[i].x : 0u; };
-  bool all = total <= (uint32_t)k;
-  uint32_t T = 0u, pcut = 0u;
-  bool cut = false;
-  if (!all) {
-    uint32_t need_ties;
-    T = radix_select_desc(slots, (uint32_t)k, 0, 0u, key_at, hist, scratch, &need_ties);
-    uint32_t t = 0;
-    for (int i = tid; i < slots; i += blockDim.x) t += real(i) && cb[i].x == T;
-    uint32_t ties;
-    (void)block_exclusive_scan(t, &ties, scratch);
-    if (ties > need_ties) {
-      // the need_ties smallest positions among the ties: the largest ~position
-      auto tie_at = [&](int i) -> uint32_t { return real(i) && cb[i].x == T ? ~cb[i].y : 0u; };
-      uint32_t r2;
-      pcut = radix_select_desc(slots, need_ties, 0, 0u, tie_at, hist, scratch, &r2);
-      cut = true;
-    }
-  }
-  for (int i = tid; i < slots; i += blockDim.x) {
-    if (!real(i)) continue;
-    const uint2 e = cb[i];
-    const bool w = all || e.x > T || (e.x == T && (!cut || ~e.y >= pcut));
-    if (w) {
-      const uint32_t slot = atomicAdd(&s_nwin, 1u);
-      if (slot < (uint32_t)k) win[slot] = (int32_t)e.y;
-    }
-  }
-  __syncthreads();
-  const uint32_t nw = min(s_nwin, (uint32_t)k);
-  for (int i = (int)nw + tid; i < n2; i += blockDim.x) win[i] = 0x7FFFFFFF;
-  __syncthreads();
-  block_sort_asc(win, n2);
-  int32_t* dst = idx + (size_t)b * k;
-  for (int i = tid; i < k; i += blockDim.x) dst[i] = i < (int)nw ? win[i] : -1;
-}
-
 // Clears the leading `words` 16-byte words of a workspace (the histograms and
 // counters) as a kernel, so the clear joins the chain of dependent launches.
 __global__ void zero_kernel(uint4* __restrict__ p, int64_t words) {
@@ -1085,30 +1015,6 @@ int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n
   CSA2_LAUNCH_PDL(topk_hist_kernel, grid, dim3(kSelThreads), 0, stream, scores, n, n_valid, positions, chunk, k, ws);
   CSA2_CHECK_LAUNCH();
   return csa2_topk_from_hist(scores, B, n, n_valid, positions, k, idx, workspace, stream);
-}
-
-// Row Top-k from the decode scan's per-CTA candidates (cand [B][n_chunks][k],
-// counts cand_n [B][n_chunks]); idx [B][k] ascending, -1 padded.
-int csa2_launch_cand_merge(const uint2* cand, const int32_t* cand_n, int32_t B, int32_t n_chunks, int32_t k,
-                           int32_t* idx, cudaStream_t stream) {
-  if (B == 0) return CSA2_OK;
-  if (n_chunks < 1 || n_chunks > kMaxMergeChunks || k < 1 || k > 4096) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  int n2 = kFinThreads;
-  while (n2 < k) n2 <<= 1;
-  const size_t smem = (size_t)(kMaxMergeChunks + kRadixBins + kFinThreads + 8 + n2) * 4;
-  CSA2_LAUNCH_PDL(topk_cand_merge_kernel, dim3((unsigned)B), dim3(kFinThreads), smem, stream, cand, cand_n, n_chunks,
-                  k, n2, idx);
-  return CSA2_OK;
-}
-
-// Zeroes `bytes` (a multiple of 16) at a 16-byte aligned `p`, as a kernel in
-// the chain of dependent launches.
-int csa2_zero_words(void* p, size_t bytes, cudaStream_t stream) {
-  const int64_t words = (int64_t)(bytes / 16);
-  if (words <= 0) return CSA2_OK;
-  CSA2_LAUNCH_PDL(zero_kernel, dim3((unsigned)((words + 255) / 256 < 304 ? (words + 255) / 256 : 304)), dim3(256), 0,
-                  stream, (uint4*)p, words);
-  return CSA2_OK;
 }
 
 extern "C" int csa2_topk(const float* scores, int32_t B, int64_t n, const int32_t* n_valid,

@@ -306,8 +306,8 @@ def test_index_score_block_scales_land_on_their_own_rows_and_blocks(csa2):
 
 @pytest.mark.parametrize("mode", ["dense", "pool", "positions"])
 def test_index_topk_from_bf16_q_equals_quantise_then_index(csa2, mode):
-    """The scan that quantises q itself must give the indices and pool of
-    csa2_quant_mxfp4 followed by csa2_index_topk."""
+    """The scan that quantises q itself must give the bytes, scores, indices and
+    pool of csa2_quant_mxfp4 followed by csa2_index_topk."""
     case = DecodeCase(workload=88, Ns=[20000, 7000, 130], reindex=(mode == "pool"), planted_blocks=4 if mode == "pool" else 0)
     g = case.to_device()
     B, cap, k = case.B, case.cap, 512
@@ -339,7 +339,9 @@ def test_index_topk_from_bf16_q_equals_quantise_then_index(csa2, mode):
                                  **kw)
         torch.cuda.synchronize()
         assert csa2.csa2_get_last_error() == 0
-        outs.append((idx.clone(), None if pool is None else pool.clone()))
+        scores = ws[:B * n_pos * 4].view(torch.float32).view(B, n_pos).clone()
+        outs.append((idx.clone(), None if pool is None else pool.clone(), scores))
     assert torch.equal(outs[0][0], outs[1][0])
     if mode == "pool":
         assert torch.equal(outs[0][1], outs[1][1])
+    assert torch.equal(outs[0][2], outs[1][2])
