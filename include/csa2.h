@@ -463,8 +463,7 @@ size_t csa2_sparse_attn_workspace_size(int32_t n_queries, int32_t k,
                                        int32_t n_swa);
 
 /** Kernel launches one attention call makes for n_queries on the current
- *  device (the chunks of a query merge in a cluster or in a second kernel,
- *  whichever the launch plan finds faster); 0 for invalid sizes. */
+ *  device (one per batch of up to 256 queries); 0 for invalid sizes. */
 int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k,
                                      int32_t n_swa);
 
@@ -484,8 +483,16 @@ int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k,
  *   out [B][L][64][512] bf16; out_f32 (nullable) the same before the bf16
  *   rounding; lse (nullable) [B][L][64] natural-log sum of exp(S), -inf for
  *   a query with no rows (its output is 0).
- *   k + n_swa <= 5120. q, swa and out_f32 16-byte aligned, out 8-byte
- *   aligned, the planes as in the conventions above.
+ *   k <= CSA2_MAX_TOPK, n_swa <= 512. q, swa and out_f32 16-byte aligned,
+ *   out 8-byte aligned, the planes 16-byte aligned as in the conventions above.
+ *   q and the swa rows are read before this call waits for the kernel just
+ *   before it on the stream (the indices and n_visible are read after): they
+ *   must not be written by that kernel when it is one of this library's
+ *   attention or merge kernels (which let their successor start early); the
+ *   packers and anything launched without programmatic dependence are safe.
+ *   Precision: rows and q enter the tensor cores as fp16 (exact: the row
+ *   values have at most 6 significant bits, q is scaled by a power of two per
+ *   head), P as fp16 (relative rounding 2^-11), fp32 accumulation.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, ALIGNMENT, WORKSPACE, CUDA.
  */
 int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
