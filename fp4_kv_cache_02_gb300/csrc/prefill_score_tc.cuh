@@ -14,14 +14,18 @@
 // B operand) in shared memory and streams a chunk of 128-entry key tiles (the
 // A operand) through a TMA pipeline. Per key tile the MMA warp issues eight
 // 128 x 128 x 128 block-scaled MXF4 products, one per group of four queries,
-// into three TMEM accumulators in rotation. Sixteen epilogue warps in two
-// sets take alternate groups: warp w of a set reads TMEM lanes 32(w % 4)..
-// (32 keys) and the 2 x 32 head columns of two queries of the group, frees the
-// accumulator, applies ReLU (half of the heads by max, half as
-// x + |x| = 2 ReLU(x), to share the ALU and FMA pipes), weights the heads with
-// packed f32x2 FMAs and stores 32 consecutive scores of each
-// query. The epilogue, not the tensor pipe, bounds this kernel: about two
-// instructions per (entry, head) value against 128 MACs of tensor work.
+// into three TMEM accumulators in rotation. Sixteen epilogue warps in four
+// sets take the groups in turn: warp w of a set reads TMEM lanes 32(w % 4)..
+// (32 keys) and the 4 x 32 head columns of the group, two queries at a time,
+// frees the accumulator after the second load, applies ReLU (half of the
+// heads by max, half as x + |x| = 2 ReLU(x), to share the ALU and FMA pipes),
+// weights the heads with packed f32x2 FMAs and stores 32 consecutive scores of
+// each query. The epilogue's issue rate, not the tensor pipe, bounds this
+// kernel: about three instructions per (entry, head) value against 128 MACs
+// of tensor work, so the per-group costs (barrier wait, loads, release, mask
+// and address arithmetic) are taken once per four queries, and the causal
+// mask and bounds only on tiles that some query of the block does not see
+// whole.
 #pragma once
 
 #include <cuda.h>
@@ -42,8 +46,8 @@ constexpr int kTileBytes = kTileRows * kIkBytes;  // 8192
 constexpr int kSfBytes = kTileRows * kIkScales;   // 512
 constexpr int kQRows = kQBlock * kIdxHeads;       // 1024
 constexpr int kAcc = 3;                           // TMEM accumulators in rotation
-constexpr int kSets = 2;                          // epilogue warp sets, taking alternate groups
-constexpr int kSetWarps = 8;                      // warps of a set: 4 lane quadrants x 2 query pairs
+constexpr int kSets = 4;                          // epilogue warp sets, taking groups in rotation
+constexpr int kSetWarps = 4;                      // warps of a set: one per lane quadrant
 constexpr int kEpiWarps = kSets * kSetWarps;      // 16
 constexpr int kProducerWarp = kEpiWarps;          // 16
 constexpr int kMmaWarp = kEpiWarps + 1;           // 17
@@ -60,10 +64,12 @@ constexpr int kOffSfT = kOffA + kStages * kTileBytes;        // key scales, tran
 constexpr int kOffSfb = kOffSfT + kStages * kSfBytes;     // 8 groups x 512 B, transposed for tcgen05.cp
 constexpr int kOffW = kOffSfb + kGroups * 512;            // [32 queries][32 heads] fp32
 constexpr int kOffBars = kOffW + kQBlock * kIdxHeads * 4;
-constexpr int kNumBars = 2 * kStages + 2 * kAcc;
+constexpr int kNumBars = 2 * kStages + kSets + kAcc;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + alignment slack
 static_assert(kOffA % 1024 == 0 && kOffSfb % 16 == 0, "operand alignment");
+static_assert(kGroups % kSets == 0, "a tile's groups divide evenly over the epilogue sets");
+static_assert(kSets >= kAcc, "a set barrier runs at most one phase ahead of its set");
 
 struct Params {
   const uint8_t* q_e8m0;   // [T][32][4]
@@ -79,6 +85,11 @@ struct Params {
 __device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
   unsigned long long r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ unsigned long long pack_u32x2(uint32_t lo, uint32_t hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
   return r;
 }
 __device__ __forceinline__ float sum_f32x2(unsigned long long v) {
@@ -105,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sW = reinterpret_cast<float*>(sm + kOffW);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kOffBars);
   uint64_t* empty = full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  uint64_t* acc_empty = acc_full + kAcc;
+  uint64_t* acc_full = empty + kStages;   // per epilogue set: its next group is in TMEM
+  uint64_t* acc_empty = acc_full + kSets; // per accumulator: drained into registers
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(sm + kOffMisc + 4);
   uint64_t* qbar = reinterpret_cast<uint64_t*>(sm + kOffMisc + 8);
@@ -131,9 +142,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < kAcc; ++a) {
-      tc::mbar_init(&acc_full[a], 1);
       tc::mbar_init(&acc_empty[a], kSetWarps);  // one arrival per warp of the set
     }
+    // a set's groups are committed in its own order, at most one ahead of the
+    // set (the MMA after that needs an accumulator the set still holds), so
+    // one parity bit per set barrier tells its phases apart; a barrier shared by
+    // the sets would not
+    for (int k = 0; k < kSets; ++k) tc::mbar_init(&acc_full[k], 1);
     tc::mbar_init(qbar, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
@@ -225,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t sf_desc0 = tc::smem_desc(tc::smem_u32(sSfT), 0, 128, tc::kSwizzleNone);
       int a = 0;              // accumulator of the next group
       uint32_t uses = 0;      // bit a: parity of the uses of accumulator a so far
-      int last_a = -1;
+      int last_f = -1;        // set barrier of the last commit, and its parity
       uint32_t last_par = 0;
       for (int i = 0; ok && i < n_mma_tiles; ++i) {
         const int s = i % kStages;
@@ -246,65 +261,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sfb = tmem + kSfbCol + 4u * g;
           tc::mma_mxf4(d, ad, bd, idesc0, sfa, sfb, 0);
           tc::mma_mxf4(d, ad + 2, bd + 2, idesc1, sfa, sfb, 1);  // second K half: +32 bytes
-          tc::mma_commit(&acc_full[a]);
-          last_a = a;
-          last_par = par;
+          tc::mma_commit(&acc_full[g % kSets]);
+          last_f = g % kSets;
+          last_par = (uint32_t)(i * (kGroups / kSets) + g / kSets) & 1u;
           uses ^= 1u << a;
           a = a == kAcc - 1 ? 0 : a + 1;
         }
         if (ok) tc::mma_commit(&empty[s]);
       }
-      if (*s_abort && last_a >= 0)  // MMAs must finish before tensor memory is freed
-        tc::mbar_wait_bounded(&acc_full[last_a], last_par, s_abort, &g_index_error, 100000000ull);
+      if (*s_abort && last_f >= 0)  // MMAs must finish before tensor memory is freed
+        tc::mbar_wait_bounded(&acc_full[last_f], last_par, s_abort, &g_index_error, 100000000ull);
     }
     __syncwarp();
   } else {
-    // ---- epilogue: set k (8 warps) drains groups u = k, k + 2, ...; warp w of
-    // a set reads TMEM lanes 32(w % 4).. (32 keys) and the 2 x 32 head columns
-    // of queries 2(w / 4), 2(w / 4) + 1 of the group, frees the accumulator,
-    // then does the math ----
-    const int set = warp / kSetWarps, ws = warp % kSetWarps;
-    const int quad = ws & 3, pair = ws >> 2;
-    const uint32_t lane_off = ((uint32_t)(quad * 32) << 16) + 64u * (uint32_t)pair;
-    const int n_groups = n_mma_tiles * kGroups;
-    for (int u = set; u < n_groups; u += kSets) {
-      const int i = u / kGroups, g = u % kGroups;
-      const int a = u % kAcc;
-      const int64_t j = (c0 + i) * kTileRows + quad * 32 + lane;  // this thread's entry
-      const int64_t jm_last = j * p.m + (p.m - 1);                 // its last token
-      // warp-uniform outcome: tcgen05.ld below needs the whole warp
-      if (!__all_sync(0xffffffffu,
-                      tc::mbar_wait_bounded(&acc_full[a], (uint32_t)(u / kAcc) & 1u, s_abort, &g_index_error)))
-        break;
-      tc::tc_fence_after();
-      uint32_t r[2][32];
-      tc::tmem_ld_32x32b_x32(tmem + acc_col(a) + lane_off, r[0]);
-      tc::tmem_ld_32x32b_x32(tmem + acc_col(a) + lane_off + 32u, r[1]);
-      tc::tmem_ld_wait();
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
-      const int qi = g * kGroupQ + 2 * pair;  // first of the two queries within the block
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const ulonglong2* wq = reinterpret_cast<const ulonglong2*>(sW + (qi + k) * kIdxHeads);
-        // heads 4m, 4m+1: ReLU by max (ALU pipe); heads 4m+2, 4m+3: x + |x| =
-        // 2 ReLU(x) (FMA pipe), halved at the end (exact); four independent
-        // f32x2 accumulators
-        unsigned long long am0 = 0ull, aa0 = 0ull, am1 = 0ull, aa1 = 0ull;
-#pragma unroll
-        for (int h = 0; h < kIdxHeads; h += 8) {
-          const ulonglong2 wa = wq[h >> 2], wb = wq[(h >> 2) + 1];
-          const float* x = reinterpret_cast<const float*>(r[k]) + h;
-          fma_f32x2(am0, pack_f32x2(fmaxf(x[0], 0.0f), fmaxf(x[1], 0.0f)), wa.x);
-          fma_f32x2(aa0, pack_f32x2(x[2] + fabsf(x[2]), x[3] + fabsf(x[3])), wa.y);
-          fma_f32x2(am1, pack_f32x2(fmaxf(x[4], 0.0f), fmaxf(x[5], 0.0f)), wb.x);
-          fma_f32x2(aa1, pack_f32x2(x[6] + fabsf(x[6]), x[7] + fabsf(x[7])), wb.y);
+    // ---- epilogue: set k (4 warps) drains groups g = k, k + 4 of every tile;
+    // warp w of a set reads TMEM lanes 32(w % 4).. (32 keys) ----
+    const int set = warp / kSetWarps, quad = warp % kSetWarps;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int64_t N = p.n_entries;
+    const bool all_q = t0 + kQBlock <= p.T;  // no query of the block past T
+    bool live = true;
+    for (int i = 0; live && i < n_mma_tiles; ++i) {
+      // per tile: this thread's entry, its last token, and whether every query
+      // of the block sees the whole tile (then no mask and no bounds per store)
+      const int64_t jt = (c0 + i) * kTileRows;
+      const int64_t j = jt + quad * 32 + lane;
+      const int64_t jm_last = j * p.m + (p.m - 1);
+      const bool whole = all_q && jt + kTileRows <= N && (jt + kTileRows) * p.m - 1 <= p.p0 + t0;
+      float* dst = p.scores + ((int64_t)t0 + kGroupQ * set) * N + j;
+#pragma unroll 1
+      for (int g = set; g < kGroups; g += kSets, dst += kSets * kGroupQ * N) {
+        const int a = (i * kGroups + g) % kAcc;  // the MMA fills accumulators in rotation
+        // warp-uniform outcome: tcgen05.ld below needs the whole warp
+        const uint32_t par = (uint32_t)(i * (kGroups / kSets) + g / kSets) & 1u;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait_bounded(&acc_full[set], par, s_abort, &g_index_error))) {
+          live = false;
+          break;
         }
-        const float e = sum_f32x2(am0) + sum_f32x2(am1) + 0.5f * (sum_f32x2(aa0) + sum_f32x2(aa1));
-        const int t = t0 + qi + k;
-        // entry j (tokens jm .. jm+m-1) is complete at the query's position p0 + t
-        if (t < p.T && j < p.n_entries) p.scores[(int64_t)t * p.n_entries + j] = jm_last <= p.p0 + t ? e : -INFINITY;
+        tc::tc_fence_after();
+        float e[kGroupQ];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          // queries 2 half, 2 half + 1 of the group: 2 x 32 head columns
+          uint32_t r[2][32];
+          tc::tmem_ld_32x32b_x32(tmem + acc_col(a) + lane_off + 64u * half, r[0]);
+          tc::tmem_ld_32x32b_x32(tmem + acc_col(a) + lane_off + 64u * half + 32u, r[1]);
+          tc::tmem_ld_wait();
+          if (half == 1) {  // the accumulator is free once its last columns are in registers
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            uint32_t* x = r[k];
+            // ReLU in place, so that head pairs stay in the register pairs the
+            // tensor-memory load wrote (packed FMAs take them as they are):
+            // heads 4m, 4m+1 by max (ALU pipe), heads 4m+2, 4m+3 as x + |x| =
+            // 2 ReLU(x) (FMA pipe), halved at the end (exact)
+#pragma unroll
+            for (int h = 0; h < kIdxHeads; h += 4) {
+              x[h] = __float_as_uint(fmaxf(__uint_as_float(x[h]), 0.0f));
+              x[h + 1] = __float_as_uint(fmaxf(__uint_as_float(x[h + 1]), 0.0f));
+              x[h + 2] = __float_as_uint(__uint_as_float(x[h + 2]) + fabsf(__uint_as_float(x[h + 2])));
+              x[h + 3] = __float_as_uint(__uint_as_float(x[h + 3]) + fabsf(__uint_as_float(x[h + 3])));
+            }
+            const ulonglong2* wq = reinterpret_cast<const ulonglong2*>(sW + (g * kGroupQ + 2 * half + k) * kIdxHeads);
+            unsigned long long am0 = 0ull, aa0 = 0ull, am1 = 0ull, aa1 = 0ull;
+#pragma unroll
+            for (int h = 0; h < kIdxHeads; h += 8) {
+              const ulonglong2 wa = wq[h >> 2], wb = wq[(h >> 2) + 1];
+              fma_f32x2(am0, pack_u32x2(x[h], x[h + 1]), wa.x);
+              fma_f32x2(aa0, pack_u32x2(x[h + 2], x[h + 3]), wa.y);
+              fma_f32x2(am1, pack_u32x2(x[h + 4], x[h + 5]), wb.x);
+              fma_f32x2(aa1, pack_u32x2(x[h + 6], x[h + 7]), wb.y);
+            }
+            e[2 * half + k] = sum_f32x2(am0) + sum_f32x2(am1) + 0.5f * (sum_f32x2(aa0) + sum_f32x2(aa1));
+          }
+        }
+        if (whole) {
+          float* d = dst;
+#pragma unroll
+          for (int k = 0; k < kGroupQ; ++k, d += N) *d = e[k];
+        } else {
+          // entry j (tokens jm .. jm+m-1) is complete at the query's position p0 + t
+#pragma unroll
+          for (int k = 0; k < kGroupQ; ++k) {
+            const int t = t0 + g * kGroupQ + k;
+            if (t < p.T && j < N) dst[k * N] = jm_last <= p.p0 + t ? e[k] : -INFINITY;
+          }
+        }
       }
     }
     // tiles of the chunk past every query of the block
