@@ -378,9 +378,21 @@ def measure_decode(csa2, ctx, wid, B, steps, warmup, use_graph=True, with_e2e=Tr
                                                               stream=stream), steps)
     del scores
 
+    # (3b) Reuse layers: the attention alone, per layer (the step's call) and
+    # fused (each selected tile gathered once per pair of layers), on the
+    # step's indices, L2 flushed before each
+    attn_alone = None
+    if L >= 2:
+        attn_alone = {
+            "per_layer_ms": ctx.timed(st_attn, steps),
+            "fused_reuse_ms": ctx.timed(lambda: csa2.csa2_sparse_attn_reuse(
+                io["Q"], inp["kv_data"], inp["kv_scale"], inp["n_visible"], io["idx"], io["swa"], io["out"], aws),
+                steps)}
+        assert csa2.csa2_get_last_error() == 0
+
     res = {"wl": wl, "B": B, "N": N, "L": L, "K": K, "W": W, "reindex": reindex, "ms": ms_max,
            "eager_ms": eager_ms, "stage_ms": stage_ms, "scan_ms": scan_ms, "n_launches": n_launches,
-           "graph": graph is not None, "clocks": clk.summary()}
+           "graph": graph is not None, "clocks": clk.summary(), "attn_alone": attn_alone}
     if not with_e2e:
         return res
 
@@ -508,6 +520,14 @@ def decode_summary(res, world, hbm_peak, peak_kind):
         "gpu_launches_per_step": res["n_launches"],
         "clocks": res["clocks"],
     }
+    if res.get("attn_alone"):
+        # the Reuse layers' attention timed alone: the step's per-layer call and
+        # the fused call (bit-identical outputs), with the selected rows' bytes
+        # read once per sequence for the fused one
+        aa = res["attn_alone"]
+        out["reuse_attention"] = {
+            "per_layer_ms": round(aa["per_layer_ms"], 5), "fused_reuse_ms": round(aa["fused_reuse_ms"], 5),
+            "note": "csa2_sparse_attn_decode vs csa2_sparse_attn_reuse on the step's indices, eager, L2 flushed"}
     if "e2e_ms" in res:
         out["e2e"] = {"value": round(world * B / (res["e2e_ms"] * 1e-3), 1), "unit": "queries/s",
                       "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],

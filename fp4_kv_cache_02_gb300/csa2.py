@@ -87,6 +87,8 @@ def _load():
         "csa2_sparse_attn_kernel_launches": (ctypes.c_int, [i32, i32, i32]),
         "csa2_sparse_attn_decode": (ctypes.c_int, [vp, i32, i32, vp, vp, i64, vp, vp, i32, vp, i32, f32,
                                                    vp, vp, vp, vp, sz, vp]),
+        "csa2_sparse_attn_reuse": (ctypes.c_int, [vp, i32, i32, vp, vp, i64, vp, vp, i32, vp, i32, f32,
+                                                  vp, vp, vp, vp, sz, vp]),
         "csa2_sparse_attn_prefill": (ctypes.c_int, [vp, i32, vp, vp, i64, vp, i32, vp, i32, f32, vp, vp,
                                                     vp, vp, sz, vp]),
         "csa2_sparse_attn_prefill_replay": (ctypes.c_int, [vp, i32, vp, vp, i64, vp, i32, vp, i32, i32, f32, vp,
@@ -385,6 +387,23 @@ def csa2_sparse_attn_decode(q, kv_data, kv_scale, n_visible, idx, swa, out, work
     k = idx.shape[1]
     n_swa = swa.shape[2] if swa is not None else 0
     _call("csa2_sparse_attn_decode", _p(q), B, L, _p(kv_data), _p(kv_scale), cap, _p(n_visible), _p(idx), k,
+          _p(swa), n_swa, float(sm_scale), _p(out), _p(out_f32), _p(lse), _p(workspace), workspace.numel(),
+          _s(stream))
+
+
+def csa2_sparse_attn_reuse(q, kv_data, kv_scale, n_visible, idx, swa, out, workspace, out_f32=None, lse=None,
+                           sm_scale=1.0, stream=None):
+    """As csa2_sparse_attn_decode, with each selected tile gathered once for a
+    pair of the L Reuse layers (bit-identical results)."""
+    _req(q, torch.bfloat16, "q"); _req(kv_data, torch.uint8, "kv_data"); _req(kv_scale, torch.uint8, "kv_scale")
+    _req(n_visible, torch.int32, "n_visible"); _req(idx, torch.int32, "idx"); _req(out, torch.bfloat16, "out")
+    _req(workspace, torch.uint8, "workspace"); _req(swa, torch.uint8, "swa", allow_none=True)
+    _req(out_f32, torch.float32, "out_f32", allow_none=True); _req(lse, torch.float32, "lse", allow_none=True)
+    B, L = q.shape[0], q.shape[1]
+    cap = kv_data.shape[1]
+    k = idx.shape[1]
+    n_swa = swa.shape[2] if swa is not None else 0
+    _call("csa2_sparse_attn_reuse", _p(q), B, L, _p(kv_data), _p(kv_scale), cap, _p(n_visible), _p(idx), k,
           _p(swa), n_swa, float(sm_scale), _p(out), _p(out_f32), _p(lse), _p(workspace), workspace.numel(),
           _s(stream))
 

@@ -31,14 +31,15 @@ struct AttnArgs {
   const int32_t* idx;       // [n_seq][k]
   int32_t k;
   int32_t L;                // queries per sequence (layers sharing the Top-K)
+  int32_t lgrp;             // Reuse mode: layers attended per gather of a selected tile (divides L)
   const uint8_t* swa;       // SWA bytes
   int64_t swa_q_stride;     // bytes between consecutive queries' windows
   int32_t n_swa;
   int32_t swa_first_row;    // prefill: SWA rows before this row of the array are masked (Bounded Replay)
   float sm_scale;
-  int32_t q0;               // first query of this launch
-  int32_t n_sel, n_swt, n_part;  // tiles of selected rows, SWA tiles, partials (= tiles) per query
-  float* part_o;            // [n_q][n_part][16][64][32]: unnormalised partial outputs, 32-channel blocks
+  int32_t q0;               // first unit of this launch: query, or sequence in Reuse mode
+  int32_t n_sel, n_swt, n_part;  // tiles of selected rows, SWA tiles, partials per query
+  float* part_o;            // [units][L or 1][n_part][16][64][32]: unnormalised partial outputs, 32-channel blocks
   uint16_t* out;            // [n_q][64][512] bf16
   float* out_f32;           // nullable
   float* lse;               // nullable
@@ -75,23 +76,26 @@ int csa2_read_and_clear_attn_error(cudaStream_t s) {
   return v;
 }
 
-// Opts the kernel into its dynamic shared memory, once per device.
+// Opts the kernels into their dynamic shared memory, once per device.
 static int attn_kernel_attr() {
-  static Csa2PerDeviceOnce optin;
-  return csa2_smem_optin((const void*)attn_tc::attn_tc_kernel, attn_tc::kSmemBytes, optin);
+  static Csa2PerDeviceOnce optin, optin_reuse;
+  if (csa2_smem_optin((const void*)attn_tc::attn_tc_kernel<false>, attn_tc::kSmemBytes, optin) != CSA2_OK)
+    return CSA2_ERR_CUDA;
+  return csa2_smem_optin((const void*)attn_tc::attn_tc_kernel<true>, attn_tc::kSmemBytes, optin_reuse);
 }
 
-// How many clusters of `size` CTAs of the kernel can be resident at once (0:
-// none), cached per device.
-static int attn_max_clusters(int size) {
+// How many clusters of `size` CTAs of the kernel (Reuse mode or not) can be
+// resident at once (0: none), cached per device.
+static int attn_max_clusters(int size, bool reuse = false) {
   constexpr int kMaxDevices = 64;
-  static int cache[kMaxDevices][attn_tc::kMaxCluster + 1];  // count + 1; 0 unknown
+  static int cache[kMaxDevices][2][attn_tc::kMaxCluster + 1];  // count + 1; 0 unknown
   static std::mutex mu;
   int dev = 0;
   if (size < 1 || size > attn_tc::kMaxCluster) return 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev][size]) {
+  int& slot = cache[dev][reuse ? 1 : 0][size];
+  if (!slot) {
     int n = 0;
     if (attn_kernel_attr() == CSA2_OK) {
       cudaLaunchConfig_t cfg = {};
@@ -105,14 +109,15 @@ static int attn_max_clusters(int size) {
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&n, (void*)attn_tc::attn_tc_kernel, &cfg) != cudaSuccess) {
+      const void* kern = reuse ? (const void*)attn_tc::attn_tc_kernel<true> : (const void*)attn_tc::attn_tc_kernel<false>;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
         (void)cudaGetLastError();
         n = 0;
       }
     }
-    cache[dev][size] = n + 1;
+    slot = n + 1;
   }
-  return cache[dev][size] - 1;
+  return slot - 1;
 }
 
 struct AttnPlan {
@@ -146,6 +151,24 @@ static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_devi
   return p;
 }
 
+// Reuse mode: a cluster per sequence whose CTAs take the L x n_swt SWA tiles
+// and the selected tiles, each selected tile gathered once per group of lgrp
+// layers (lgrp = 2 for even L: measured faster than one gather for all L
+// layers, whose passes then run back to back on one CTA). Possible when one
+// cluster holds the merge of the L x 64 (layer, head) rows: at most 64 rows a
+// CTA (C >= L) and the (max, sum) exchange within its shared-memory table.
+static bool attn_reuse_plan(int L, AttnPlan& p, int& lgrp) {
+  lgrp = L % 2 == 0 ? 2 : L;
+  const int items = L * p.n_swt + p.n_sel * (L / lgrp);
+  const int c = items < attn_tc::kMaxCluster ? items : attn_tc::kMaxCluster;
+  if (c < L) return false;
+  const int nh = (kHeads * L + c - 1) / c;
+  if (p.n_part * nh > attn_tc::kMaxPartials * 16) return false;
+  if (attn_max_clusters(c, true) < 1) return false;
+  p.cluster = c;
+  return true;
+}
+
 static inline int attn_queries_per_launch(int32_t n_queries) {
   return n_queries < kQueriesPerLaunch ? n_queries : kQueriesPerLaunch;
 }
@@ -170,9 +193,9 @@ extern "C" int csa2_sparse_attn_kernel_launches(int32_t n_queries, int32_t k, in
 }
 
 static int launch_attn(AttnArgs a, const void* q_bf16, int32_t n_q, uint16_t* out, float* out_f32, float* lse,
-                       void* ws, size_t ws_bytes, cudaStream_t stream) {
+                       void* ws, size_t ws_bytes, cudaStream_t stream, bool reuse = false) {
   if (attn_kernel_attr() != CSA2_OK) return CSA2_ERR_CUDA;
-  const AttnPlan plan = attn_plan(attn_queries_per_launch(n_q), a.k, a.n_swa, true);
+  AttnPlan plan = attn_plan(attn_queries_per_launch(n_q), a.k, a.n_swa, true);
   if (plan.n_part > attn_tc::kMaxPartials) return CSA2_ERR_UNSUPPORTED_SHAPE;
   a.n_sel = plan.n_sel;
   a.n_swt = plan.n_swt;
@@ -196,10 +219,28 @@ static int launch_attn(AttnArgs a, const void* q_bf16, int32_t n_q, uint16_t* ou
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return CSA2_ERR_CUDA;
+  int lgrp = 1;
+  if (reuse && a.L >= 2) {
+    if (!attn_reuse_plan(a.L, plan, lgrp)) return CSA2_ERR_UNSUPPORTED_SHAPE;
+    a.lgrp = lgrp;
+    // units are sequences: at most kQueriesPerLaunch queries (B x L) a launch
+    const int32_t n_seq = n_q / a.L, per = kQueriesPerLaunch / a.L;
+    for (int32_t s0 = 0; s0 < n_seq; s0 += per) {
+      const int32_t ns = n_seq - s0 < per ? n_seq - s0 : per;
+      a.q0 = s0;
+      if (csa2_launch_pdl_cluster(attn_tc::attn_tc_kernel<true>, dim3((unsigned)plan.cluster, (unsigned)ns),
+                                  dim3(attn_tc::kThreads), (size_t)attn_tc::kSmemBytes, stream,
+                                  (unsigned)plan.cluster, qmap, a) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return CSA2_ERR_CUDA;
+      }
+    }
+    return CSA2_OK;
+  }
   for (int32_t q0 = 0; q0 < n_q; q0 += kQueriesPerLaunch) {
     const int32_t nq = n_q - q0 < kQueriesPerLaunch ? n_q - q0 : kQueriesPerLaunch;
     a.q0 = q0;
-    if (csa2_launch_pdl_cluster(attn_tc::attn_tc_kernel, dim3((unsigned)plan.cluster, (unsigned)nq),
+    if (csa2_launch_pdl_cluster(attn_tc::attn_tc_kernel<false>, dim3((unsigned)plan.cluster, (unsigned)nq),
                                 dim3(attn_tc::kThreads), (size_t)attn_tc::kSmemBytes, stream,
                                 (unsigned)plan.cluster, qmap, a) != cudaSuccess) {
       (void)cudaGetLastError();
@@ -209,11 +250,11 @@ static int launch_attn(AttnArgs a, const void* q_bf16, int32_t n_q, uint16_t* ou
   return CSA2_OK;
 }
 
-extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L, const uint8_t* kv_data,
-                                       const uint8_t* kv_scale, int64_t cap, const int32_t* n_visible,
-                                       const int32_t* idx, int32_t k, const uint8_t* swa, int32_t n_swa,
-                                       float sm_scale, void* out_bf16, float* out_f32, float* lse, void* workspace,
-                                       size_t workspace_bytes, csa2_stream_t stream) {
+static int sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L, const uint8_t* kv_data,
+                              const uint8_t* kv_scale, int64_t cap, const int32_t* n_visible, const int32_t* idx,
+                              int32_t k, const uint8_t* swa, int32_t n_swa, float sm_scale, void* out_bf16,
+                              float* out_f32, float* lse, void* workspace, size_t workspace_bytes,
+                              csa2_stream_t stream, bool reuse) {
   if (!q_bf16 || !kv_data || !kv_scale || !n_visible || !idx || !out_bf16) return CSA2_ERR_INVALID_ARG;
   if (B < 0 || L < 1 || k < 0 || n_swa < 0 || cap < 0) return CSA2_ERR_INVALID_ARG;
   if (n_swa > 0 && !swa) return CSA2_ERR_INVALID_ARG;
@@ -230,12 +271,32 @@ extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
   a.idx = idx;
   a.k = k;
   a.L = L;
+  a.lgrp = 1;
   a.swa = swa;
   a.swa_q_stride = (int64_t)n_swa * kHeadDim;
   a.n_swa = n_swa;
   a.swa_first_row = INT32_MIN;  // decode windows are never truncated
   a.sm_scale = sm_scale;
-  return launch_attn(a, q_bf16, B * L, (uint16_t*)out_bf16, out_f32, lse, workspace, workspace_bytes, (cudaStream_t)stream);
+  return launch_attn(a, q_bf16, B * L, (uint16_t*)out_bf16, out_f32, lse, workspace, workspace_bytes,
+                     (cudaStream_t)stream, reuse);
+}
+
+extern "C" int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L, const uint8_t* kv_data,
+                                       const uint8_t* kv_scale, int64_t cap, const int32_t* n_visible,
+                                       const int32_t* idx, int32_t k, const uint8_t* swa, int32_t n_swa,
+                                       float sm_scale, void* out_bf16, float* out_f32, float* lse, void* workspace,
+                                       size_t workspace_bytes, csa2_stream_t stream) {
+  return sparse_attn_decode(q_bf16, B, L, kv_data, kv_scale, cap, n_visible, idx, k, swa, n_swa, sm_scale, out_bf16,
+                            out_f32, lse, workspace, workspace_bytes, stream, false);
+}
+
+extern "C" int csa2_sparse_attn_reuse(const void* q_bf16, int32_t B, int32_t L, const uint8_t* kv_data,
+                                      const uint8_t* kv_scale, int64_t cap, const int32_t* n_visible,
+                                      const int32_t* idx, int32_t k, const uint8_t* swa, int32_t n_swa,
+                                      float sm_scale, void* out_bf16, float* out_f32, float* lse, void* workspace,
+                                      size_t workspace_bytes, csa2_stream_t stream) {
+  return sparse_attn_decode(q_bf16, B, L, kv_data, kv_scale, cap, n_visible, idx, k, swa, n_swa, sm_scale, out_bf16,
+                            out_f32, lse, workspace, workspace_bytes, stream, true);
 }
 
 extern "C" int csa2_sparse_attn_prefill_replay(const void* q_bf16, int32_t T, const uint8_t* kv_data,
@@ -260,6 +321,7 @@ extern "C" int csa2_sparse_attn_prefill_replay(const void* q_bf16, int32_t T, co
   a.idx = idx;
   a.k = k;
   a.L = 1;
+  a.lgrp = 1;
   a.swa = swa;
   a.swa_q_stride = kHeadDim;  // query t uses rows t .. t + n_swa - 1
   a.n_swa = n_swa;

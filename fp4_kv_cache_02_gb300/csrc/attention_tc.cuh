@@ -151,7 +151,17 @@ __device__ __forceinline__ void cluster_sync_release_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// grid (C, queries of the launch), clusters of C CTAs along x
+// grid (C, units of the launch), clusters of C CTAs along x. A unit is one
+// query (kReuse false) or one sequence with its L Reuse layers (kReuse true).
+//
+// Reuse mode ("DeepSeek-V4.1-Flash" section 2.3.1: the Reuse layers attend
+// to the Full layer's selection with their own Q and SWA rows): a cluster
+// serves a sequence. Its work items are the L x n_swt SWA tiles (one layer
+// each) and the n_sel tiles of selected rows, each gathered and dequantised
+// once and then attended by the L layers back to back while the next layer's
+// Q is being loaded. Partials are written to the workspace by plain stores,
+// and the cluster merges the L x 64 (layer, head) rows.
+template <bool kReuse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
   // barriers, tensor memory, Q and the SWA tiles need nothing from the
@@ -175,16 +185,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float red_l[4][kHeads];
   __shared__ float q_mul[kHeads];        // sm_scale * 2^-k_h * log2(e)
   __shared__ int row_valid[kRows];       // 0 none, 1 selected latent, 2 SWA row
-  // (max, sum) of every partial for the heads this CTA merges, written by the
-  // CTAs of the cluster through distributed shared memory: [part][head - hb0]
+  // (max, sum) of every partial for the (layer,) head rows this CTA merges,
+  // written by the CTAs of the cluster through distributed shared memory:
+  // [part][row - hb0]
   __shared__ float2 ml_in[kMaxPartials * 16];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = (int)gridDim.x;
   const int rank = (int)blockIdx.x;
-  const int lq = blockIdx.y;
-  const int qi = a.q0 + lq;
-  const int seq = qi / a.L;
+  const int unit = a.q0 + (int)blockIdx.y;   // query, or sequence in Reuse mode
+  const int L = kReuse ? a.L : 1;
+  const int seq = kReuse ? unit : unit / a.L;
+  const int HR = kHeads * L;                 // (layer, head) rows of the unit
+  const int n_swt = a.n_swt, n_sel = a.n_sel, n_part = a.n_part;
+  // Reuse mode: a selected tile is one item per group of lgrp layers (gathered
+  // once per group); SWA tiles are one item per layer
+  const int lgrp = kReuse ? a.lgrp : 1;
+  const int n_grp = L / lgrp;
+  const int n_items = L * n_swt + n_sel * n_grp;   // SWA tiles (per layer), then (selected tile, group)
+  // partial rows of the unit in the workspace: [layer][n_part][16][64][32]
+  float* part_o_u = a.part_o + (int64_t)blockIdx.y * L * n_part * kHeads * kHeadDim;
 
   if (tid == 0) {
     tc::mbar_init(bar_s, 1);
@@ -197,13 +217,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0) tc::tmem_alloc(s_tmem, kTmemCols);
   // every CTA of the cluster has started before any writes into another's
-  // shared memory (the wait follows the Q conversion)
+  // shared memory (the wait follows the first Q conversion)
   cluster_arrive_relaxed();
   __syncthreads();
-  if (tid == 0) {
-    // Q of this query: 8 TMA boxes of [64 h][64 c] bf16, 128-byte swizzle
-    tc::mbar_arrive_expect_tx(q_full, 8 * kQBlk);
-    for (int b = 0; b < 8; ++b) tc::tma_load_2d(sQ + b * kQBlk, &tmap_q, b * 64, qi * kHeads, q_full);
+
+  // the layer of each attention pass of this CTA, in order: an SWA item is one
+  // pass of its layer, a selected item one pass per layer
+  auto item_layer0 = [&](const int j) {
+    if (!kReuse) return 0;
+    return j < L * n_swt ? j / n_swt : ((j - L * n_swt) % n_grp) * lgrp;
+  };
+  // Q of query (seq, layer) into sQ: 8 TMA boxes of [64 h][64 c] bf16, 128-byte swizzle
+  auto issue_q = [&](const int layer) {
+    if (tid == 0) {
+      const int qrow = (kReuse ? seq * L + layer : unit) * kHeads;
+      tc::mbar_arrive_expect_tx(q_full, 8 * kQBlk);
+      for (int b = 0; b < 8; ++b) tc::tma_load_2d(sQ + b * kQBlk, &tmap_q, b * 64, qrow, q_full);
+    }
+  };
+  uint32_t q_loads = 0;   // parity source of q_full
+  int q_layer = -1;       // layer whose Q sQ holds (or is loading)
+  if (rank < n_items) {
+    q_layer = item_layer0(rank);
+    issue_q(q_layer);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -213,8 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- Q to fp16 with a power-of-two scale per head: thread (h, j) owns the
   // 16-byte column j of head h's row in each of the 8 blocks (bank-conflict
   // free: the 8 threads of a head cover the row's 8 columns) ----
-  {
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(q_full, 0, s_abort, &g_attn_error));
+  auto convert_q = [&]() {
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(q_full, q_loads & 1u, s_abort, &g_attn_error));
+    ++q_loads;
     const int h = tid >> 3, j = tid & 7;
     const uint32_t col = (uint32_t)((j ^ (h & 7)) << 4);
     uint4 v[8];
@@ -249,20 +286,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4*>(sQ + b * kQBlk + h * 128 + col) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     if (j == 0) q_mul[h] = a.sm_scale * __int_as_float((127 - k) << 23) * 1.4426950408889634f;
+    // the converted Q is read by the MMA (async proxy) after the next barrier
+    tc::fence_proxy_async_smem();
+  };
+  bool q_ready = false;   // sQ holds the converted Q of q_layer
+  if (rank < n_items) {
+    convert_q();
+    q_ready = true;
   }
 
   cluster_wait();   // the peers have started: their shared memory may be written
-  const int n_swt = a.n_swt, n_part = a.n_part;
-  uint32_t tiles_done = 0;   // parity source of bar_g / bar_s / bar_pv
-  float* part_o_q = a.part_o + (int64_t)lq * n_part * kHeads * kHeadDim;
+  uint32_t items_done = 0;   // parity source of bar_g
+  uint32_t passes_done = 0;  // parity source of bar_s / bar_pv
 
-  // One tile: rows [128 tile, 128 tile + 128) of the SWA window (swa) or of the
-  // selected list, giving partial `part`.
-  auto run_tile = [&](const bool swa, const int tile, const int part, const bool more_tiles) {
-    const uint32_t par = tiles_done & 1u;
-    // ---- row list; thread r < 128 starts the bulk copies of row r into the
-    // staging area (selected rows: 256 B of codes + 32 B of scales); the SWA
-    // rows of the tile are one contiguous copy ----
+  // ---- one tile's rows: rows [128 tile, 128 tile + 128) of the SWA window of
+  // query qi_swa (swa) or of the sequence's selected list, gathered by the
+  // bulk-copy engine and dequantised into R ----
+  auto gather_dequant = [&](const bool swa, const int tile, const int qi_swa) {
+    const uint32_t par = items_done & 1u;
+    // thread r < 128 starts the bulk copies of row r into the staging area
+    // (selected rows: 256 B of codes + 32 B of scales); the SWA rows of the
+    // tile are one contiguous copy
     if (tid < kRows) {
       int valid = 0;
       int64_t src = 0;
@@ -270,12 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (swa) {
         // in prefill, row t of query qi is row qi + t of the array, and rows
         // before swa_first_row lie before a Bounded Replay start
-        if (t < a.n_swa && (int64_t)qi + t >= (int64_t)a.swa_first_row) valid = 2;
+        if (t < a.n_swa && (int64_t)qi_swa + t >= (int64_t)a.swa_first_row) valid = 2;
         if (tid == 0) {
           const int n_rows = min(kRows, a.n_swa - tile * kRows);
           const uint32_t bytes = (uint32_t)n_rows * kHeadDim;
           tc::mbar_arrive_expect_tx(bar_g, bytes);
-          tc::bulk_load(sStage, a.swa + (int64_t)qi * a.swa_q_stride + (int64_t)tile * kRows * kHeadDim, bytes, bar_g);
+          tc::bulk_load(sStage, a.swa + (int64_t)qi_swa * a.swa_q_stride + (int64_t)tile * kRows * kHeadDim, bytes,
+                        bar_g);
         } else {
           tc::mbar_arrive(bar_g);
         }
@@ -306,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const bool g_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_g, par, s_abort, &g_attn_error));
+    ++items_done;
     // ---- dequantise into R (fp16, SW128 blocks of 64 channels). The staged
     // bytes sit in R's upper half: read them all, then write R ----
     if (swa) {
@@ -380,6 +426,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    return g_ok;
+  };
+
+  // ---- one attention pass over the rows in R with the converted Q of layer
+  // `layer` in sQ, giving partial `part` of that layer's query. next_layer >= 0:
+  // the layer of the CTA's next pass, whose Q is loaded into sQ as soon as
+  // this pass's S^T is complete. more_rows: R is rewritten after this pass ----
+  auto attend = [&](const int layer, const int part, const int next_layer, const bool more_rows) {
+    const uint32_t par = passes_done & 1u;
     // ---- S^T = R Q^T ----
     if (tid == 0 && !*s_abort) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 0, 0);
@@ -397,6 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     const bool s_ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait_bounded(bar_s, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
+    // sQ is free once S^T is complete: start the next layer's Q
+    if (kReuse && next_layer >= 0 && next_layer != q_layer) {
+      issue_q(next_layer);
+      q_layer = next_layer;
+      q_ready = false;
+    }
     // ---- softmax: warp w reads the 32 rows of lane quadrant w % 4 and the 16
     // heads 16 (w / 4) ..; the four quadrant warps of a head group meet at
     // named barrier 1 + w / 4 ----
@@ -475,95 +536,139 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::mma_commit(bar_pv);
     }
-    // (m, l) of the tile, log2 domain (l = 0 marks a partial with no rows),
-    // into the shared memory of the CTA that merges head h
+    // (m, l) of the pass, log2 domain (l = 0 marks a partial with no rows),
+    // into the shared memory of the CTA that merges (layer, head) row hr
     if (tid < kHeads) {
-      const int h = tid;
+      const int h = tid, hr = layer * kHeads + h;
       const float m = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
       const float l = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
-      int r = (h * C) / kHeads;   // owner: the rank r with 64r/C <= h < 64(r+1)/C
-      while (kHeads * (r + 1) / C <= h) ++r;
-      while (kHeads * r / C > h) --r;
-      const int o0 = kHeads * r / C, onh = kHeads * (r + 1) / C - o0;
-      st_cluster_f32x2(&ml_in[part * onh + (h - o0)], (uint32_t)r, m, l);
+      int r = (hr * C) / HR;   // owner: the rank r with HR r / C <= hr < HR (r + 1) / C
+      while (HR * (r + 1) / C <= hr) ++r;
+      while (HR * r / C > hr) --r;
+      const int o0 = HR * r / C, onh = HR * (r + 1) / C - o0;
+      st_cluster_f32x2(&ml_in[part * onh + (hr - o0)], (uint32_t)r, m, l);
     }
     __syncwarp();
     const bool ok = __all_sync(0xffffffffu, s_ok && tc::mbar_wait_bounded(bar_pv, par, s_abort, &g_attn_error));
     tc::tc_fence_after();
     // ---- partial O: warp w reads the 32 channel lanes 32 cb .. of quadrant
-    // w % 4 in block w / 4 (cb = 4 (w / 4) + w % 4), all 64 heads, into R as
-    // [h][32] fp32 and sends those 8 KiB to the workspace with one bulk copy;
-    // a partial is laid out [cb][h][32] ----
+    // w % 4 in block w / 4 (cb = 4 (w / 4) + w % 4), all 64 heads; a partial is
+    // laid out [cb][h][32] ----
     {
       const int cb = (warp >> 2) * 4 + rq;
       const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
-      float* so = reinterpret_cast<float*>(sR) + cb * (kHeads * 32);
+      float* dst = part_o_u + (((int64_t)layer * n_part + part) * 16 + cb) * (kHeads * 32);
+      if (kReuse) {
+        // R stays for the next layer: plain stores, 128 contiguous bytes per
+        // warp and head
 #pragma unroll
-      for (int hh = 0; hh < kHeads; hh += 32) {
-        uint32_t ov[32];
-        if (ok) {
-          tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
-          tc::tmem_ld_wait();
+        for (int hh = 0; hh < kHeads; hh += 32) {
+          uint32_t ov[32];
+          if (ok) {
+            tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
+            tc::tmem_ld_wait();
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[(hh + j) * 32 + lane] = ok ? __uint_as_float(ov[j]) : 0.0f;
         }
+      } else {
+        // staged in R as [h][32] fp32, then 8 KiB to the workspace by one bulk copy
+        float* so = reinterpret_cast<float*>(sR) + cb * (kHeads * 32);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) so[(hh + j) * 32 + lane] = ok ? __uint_as_float(ov[j]) : 0.0f;
-      }
-      tc::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tc::bulk_store(part_o_q + ((int64_t)part * 16 + cb) * (kHeads * 32), so, kHeads * 32 * 4);
-        tc::bulk_commit();
-        if (more_tiles) tc::bulk_wait_read_all();   // R is rewritten by the next tile
+        for (int hh = 0; hh < kHeads; hh += 32) {
+          uint32_t ov[32];
+          if (ok) {
+            tc::tmem_ld_32x32b_x32(o_base + (uint32_t)hh, ov);
+            tc::tmem_ld_wait();
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) so[(hh + j) * 32 + lane] = ok ? __uint_as_float(ov[j]) : 0.0f;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::bulk_store(dst, so, kHeads * 32 * 4);
+          tc::bulk_commit();
+          if (more_rows) tc::bulk_wait_read_all();   // R is rewritten by the next tile
+        }
       }
     }
     tc::tc_fence_before();
-    ++tiles_done;
-    // the next tile rewrites the row list, R, P and the tensor memory only
-    // after every thread is past this tile's reads of them
+    ++passes_done;
+    // the next pass rewrites S, P, O (and maybe R) only after every thread is
+    // past this pass's reads of them
     __syncthreads();
   };
 
-  // tile j of the list [SWA tiles, selected tiles] belongs to CTA j mod C; the
+  // items j of the list [SWA tiles, selected tiles] belong to CTA j mod C; the
   // SWA tiles come first, before the wait for the indices
   bool waited = false;
 #pragma unroll 1
-  for (int j = rank; j < n_part; j += C) {
-    const bool swa = j < n_swt;
+  for (int j = rank; j < n_items; j += C) {
+    const bool swa = j < L * n_swt;
     if (!swa && !waited) {
       pdl_wait();
       waited = true;
     }
-    run_tile(swa, swa ? j : j - n_swt, j, j + C < n_part);
+    const int jn = j + C;   // the CTA's next item
+    const int l0 = item_layer0(j);
+    const int swa_tile = swa ? j - l0 * n_swt : 0;
+    const int sel_tile = swa ? 0 : (j - L * n_swt) / n_grp;
+    const bool rows_ok = gather_dequant(swa, swa ? swa_tile : sel_tile, kReuse ? seq * L + l0 : unit);
+    (void)rows_ok;
+    const int n_layers = swa ? 1 : lgrp;
+    for (int li = 0; li < n_layers; ++li) {
+      const int layer = l0 + li;
+      if (!q_ready || q_layer != layer) {   // its load was started by the previous pass (or now)
+        if (q_layer != layer) {
+          issue_q(layer);
+          q_layer = layer;
+        }
+        convert_q();
+        q_ready = true;
+        __syncthreads();
+      }
+      const int next_layer = li + 1 < n_layers ? layer + 1 : (jn < n_items ? item_layer0(jn) : -1);
+      attend(layer, swa ? swa_tile : n_swt + sel_tile, next_layer, jn < n_items);
+    }
   }
   if (!waited) pdl_wait();
 
-  // ---- merge: rank r sums heads [64r/C, 64(r+1)/C) over all partials ----
-  if (lane == 0) {
+  // ---- merge: rank r sums rows [HR r/C, HR (r+1)/C) over all partials ----
+  if (kReuse) {
+    // this CTA's partial stores are visible to the cluster after the barrier;
+    // the merge reads them with bulk copies (async proxy)
+    tc::fence_proxy_async_all();
+  } else if (lane == 0) {
     tc::bulk_wait_all();       // this warp's partial slices are in global memory
     tc::fence_proxy_async_all();
   }
   __syncwarp();
   cluster_sync_release_acquire();
-  const int hb0 = kHeads * rank / C, hb1 = kHeads * (rank + 1) / C;
+  if (kReuse) tc::fence_proxy_async_all();
+  const int hb0 = HR * rank / C, hb1 = HR * (rank + 1) / C;
   const int nh = hb1 - hb0;
-  // groups of up to 16 heads (one group when C >= 4): the group's slices of
-  // the partials come by bulk copies into R and Q (free now), a slot per
-  // partial laid out [cb][gh][32]; each thread sums 4 float4 items in fixed
-  // partial order. The first batch is requested before the weights are formed.
+  // groups of up to 16 rows of one layer: the group's slices of the partials
+  // come by bulk copies into R and Q (free now), a slot per partial laid out
+  // [cb][gh][32]; each thread sums 4 float4 items in fixed partial order. The
+  // first batch is requested before the weights are formed.
+  auto group_size = [&](const int g0) { return min(min(16, nh - g0), kHeads - (hb0 + g0) % kHeads); };
   auto issue_batch = [&](const int g0, const int gh, const int j0, const int nb) {
     const uint32_t piece = (uint32_t)gh * 32 * 4;
+    const int layer = (hb0 + g0) / kHeads, h0 = (hb0 + g0) % kHeads;
     if (tid == 0) tc::mbar_arrive_expect_tx(bar_m, (uint32_t)nb * 16 * piece);
     __syncwarp();
     if (tid < 16 * nb) {   // thread t copies piece cb = t % 16 of partial j0 + t / 16
       const int u = tid >> 4, cb = tid & 15;
       tc::bulk_load(sR + (size_t)u * 16 * piece + (size_t)cb * piece,
-                    part_o_q + (((int64_t)(j0 + u) * 16 + cb) * kHeads + hb0 + g0) * 32, piece, bar_m);
+                    part_o_u + ((((int64_t)layer * n_part + j0 + u) * 16 + cb) * kHeads + h0) * 32, piece, bar_m);
     }
   };
   auto batch_size = [&](const int gh) { return (int)((uint32_t)(kOffP - kOffR) / ((uint32_t)gh * 32 * 4 * 16)); };
-  if (nh > 0 && n_part > 0) issue_batch(0, min(16, nh), 0, min(batch_size(min(16, nh)), n_part));
+  if (nh > 0 && n_part > 0) issue_batch(0, group_size(0), 0, min(batch_size(group_size(0)), n_part));
   float* wts = reinterpret_cast<float*>(sP);   // [n_part][nh] weights
   __shared__ float lse_s[kHeads];
+  // lse_s, wts: this CTA's rows (nh <= 64 when the plan allows this launch)
   if (tid < nh) {
     float M = -INFINITY;
     for (int j = 0; j < n_part; ++j)
@@ -579,11 +684,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_part; ++j) wts[j * nh + tid] *= inv;
     lse_s[tid] = Lsum > 0.0f ? (M + log2f(Lsum)) * 0.6931471805599453f : -INFINITY;
   }
-  if (a.lse && tid < nh) a.lse[(int64_t)qi * kHeads + hb0 + tid] = lse_s[tid];
+  // output row of (layer, head) row hr
+  auto out_row = [&](const int hr) {
+    return ((int64_t)(kReuse ? seq * L + hr / kHeads : unit) * kHeads + hr % kHeads);
+  };
+  if (a.lse && tid < nh) a.lse[out_row(hb0 + tid)] = lse_s[tid];
   uint32_t mpar = 0;
 #pragma unroll 1
-  for (int g0 = 0; g0 < nh; g0 += 16) {
-    const int gh = min(16, nh - g0);
+  for (int g0 = 0; g0 < nh;) {
+    const int gh = group_size(g0);
     const uint32_t slot_bytes = (uint32_t)gh * 32 * 4 * 16;
     const int per_batch = batch_size(gh);
     float4 acc[4];
@@ -598,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mpar ^= 1u;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int it = tid + u * kThreads;   // item: head g0 + it / 128, channels 4 (it % 128) ..
+        const int it = tid + u * kThreads;   // item: row g0 + it / 128, channels 4 (it % 128) ..
         if (it >= gh * (kHeadDim / 4)) break;
         const int hl = it >> 7, cb = (it >> 3) & 15, c4 = it & 7;
         const int off = ((cb * gh + hl) * 32 + 4 * c4) * 4;
@@ -619,13 +728,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int it = tid + u * kThreads;
       if (it >= gh * (kHeadDim / 4)) break;
       const int hl = it >> 7, c = (it & 127) * 4;
-      const int64_t o = ((int64_t)qi * kHeads + hb0 + g0 + hl) * kHeadDim + c;
+      const int64_t o = out_row(hb0 + g0 + hl) * kHeadDim + c;
       if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + o) = acc[u];
       const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[u].x, acc[u].y);
       const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[u].z, acc[u].w);
       *reinterpret_cast<uint2*>(a.out + o) =
           make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
     }
+    g0 += gh;
   }
   tc::tc_fence_before();
   __syncthreads();

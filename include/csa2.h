@@ -504,6 +504,35 @@ int csa2_sparse_attn_decode(const void* q_bf16, int32_t B, int32_t L,
                             size_t workspace_bytes, csa2_stream_t stream);
 
 /**
+ * Fused Reuse-layer decode attention (report section 2.3.1: the Reuse layers
+ * of a sequence attend to the selection of its Full layer, each with its own
+ * query and SWA KV; notes section 4.2: they share that selection): the same
+ * arguments, results and limits as csa2_sparse_attn_decode, computed with one
+ * cluster of CTAs per sequence in which every 128-row tile of selected
+ * entries is gathered and dequantised once per pair of layers (once for all
+ * L when L is odd) instead of once per layer. The partials of one layer are
+ * the same as csa2_sparse_attn_decode's and are merged in the same order, so
+ * the outputs are bit-identical to that call's.
+ * When to use it: the per-layer call spreads the layers over more CTAs and
+ * is faster at small batches; this call does less gather and dequantisation
+ * work and is faster once the per-layer call fills the device several times
+ * over (measured on GB300 at k = 512, 128 SWA rows: L = 2, B = 64: 81 vs
+ * 91 us; L = 4 only at parity from B = 64).
+ * Errors: those of csa2_sparse_attn_decode, and UNSUPPORTED_SHAPE when one
+ * cluster (at most 8 CTAs) cannot hold the merge of the L x 64 (layer, head)
+ * rows: L > 8, or k and n_swa so large that the tiles' (max, sum) pairs do
+ * not fit its table ((ceil(k/128) + ceil(n_swa/128)) * ceil(64 L / C) > 576
+ * for the cluster size C = min(8, the sequence's work items)).
+ */
+int csa2_sparse_attn_reuse(const void* q_bf16, int32_t B, int32_t L,
+                           const uint8_t* kv_data, const uint8_t* kv_scale,
+                           int64_t cap, const int32_t* n_visible,
+                           const int32_t* idx, int32_t k, const uint8_t* swa,
+                           int32_t n_swa, float sm_scale, void* out_bf16,
+                           float* out_f32, float* lse, void* workspace,
+                           size_t workspace_bytes, csa2_stream_t stream);
+
+/**
  * Sparse prefill attention: T queries of one sequence, each with its own
  * Top-K and its own causal SWA window.
  *   q [T][64][512] bf16; kv planes of the sequence with n_entries entries;

@@ -50,6 +50,59 @@ def test_decode_attention_matches_oracle(csa2):
             assert attn_row_error(out.float().cpu().numpy()[b, l], ref) <= ATTN_ROW_TOL + 2.0 ** -8
 
 
+def _run_reuse(csa2, g, idx, k, n_swa, B, L):
+    out = torch.empty(B, L, 64, 512, dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty(B, L, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, L, 64, dtype=torch.float32, device="cuda")
+    ws = csa2.attn_workspace(B * L, k, n_swa)
+    csa2.csa2_sparse_attn_reuse(g["Q"], g["kv_data"], g["kv_scale"], g["n_visible"], idx,
+                                g["swa"] if n_swa else None, out, ws, out_f32=out32, lse=lse)
+    torch.cuda.synchronize()
+    assert csa2.csa2_get_last_error() == 0
+    return out, out32, lse
+
+
+@pytest.mark.parametrize("L,k,n_swa", [(3, 1024, 128), (4, 512, 128), (4, 512, 40), (2, 300, 256)])
+def test_reuse_attention_matches_oracle_and_per_layer_call(csa2, L, k, n_swa):
+    """The fused Reuse-layer call (each selected tile gathered once per pair of
+    layers) against the oracle, and bit for bit against the per-layer call:
+    same partials, same merge order. k = 1024 at L = 3 gives CTAs with two
+    items and merge slices that cross a layer boundary; n_swa = 40 a partial
+    SWA tile; k = 300 a ragged selected tile with two SWA tiles per layer."""
+    case = DecodeCase(workload=93, Ns=[5000, 1500], L=L, n_swa=n_swa)
+    g = case.to_device()
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.permutation(n)[:k] for n in case.Ns]).astype(np.int32)
+    idx[1, 7:31] = -1
+    out, out32, lse = _run_reuse(csa2, g, dev(idx), k, n_swa, case.B, case.L)
+    o32, l32 = out32.cpu().numpy(), lse.cpu().numpy()
+    assert torch.equal(out, out32.to(torch.bfloat16))
+    for b in range(case.B):
+        for l in range(case.L):
+            ref, ref_lse = case.oracle_attention(b, l, idx[b])
+            assert attn_row_error(o32[b, l], ref) <= ATTN_ROW_TOL
+            np.testing.assert_allclose(l32[b, l], ref_lse, rtol=1e-5, atol=1e-5)
+    pout, pout32, plse = _run_decode(csa2, g, dev(idx), k, n_swa, case.B, case.L)
+    assert torch.equal(out32, pout32) and torch.equal(lse, plse) and torch.equal(out, pout)
+
+
+def test_reuse_attention_limits(csa2):
+    """L = 1 is the per-layer call; a cluster of 8 CTAs cannot merge 9 layers."""
+    case = DecodeCase(workload=92, Ns=[700], L=1)
+    g = case.to_device()
+    idx = dev(np.arange(64, dtype=np.int32)[None, :] * 5)
+    out, out32, lse = _run_reuse(csa2, g, idx, 64, 128, 1, 1)
+    pout, pout32, plse = _run_decode(csa2, g, idx, 64, 128, 1, 1)
+    assert torch.equal(out32, pout32) and torch.equal(lse, plse)
+    q9 = torch.zeros(1, 9, 64, 512, dtype=torch.bfloat16, device="cuda")
+    swa9 = torch.zeros(1, 9, 128, 512, dtype=torch.uint8, device="cuda")
+    out9 = torch.empty(1, 9, 64, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(csa2.Csa2Error) as e:
+        csa2.csa2_sparse_attn_reuse(q9, g["kv_data"], g["kv_scale"], g["n_visible"], idx, swa9, out9,
+                                    csa2.attn_workspace(9, 64, 128))
+    assert e.value.status == -2
+
+
 def test_decode_attention_special_cases(csa2):
     case = DecodeCase(workload=95, Ns=[300], n_swa=0)
     g = case.to_device()
