@@ -556,7 +556,7 @@ def run_gpu(args):
 
     # ---- the fused KV append, for its roofline and its decode latency ----
     app = measure_append(csa2, torch, B, device, args.steps, ctx.flush_l2, ctx.stream)
-    pre = measure_prefill(csa2, ctx, max(3, min(args.steps, 10))) if args.prefill else None
+    pre = measure_prefill(csa2, ctx, max(3, min(args.steps, 10)), *args.prefill_shape) if args.prefill else None
     torch.cuda.empty_cache()
 
     # ---- the other workloads, each its own decode step (or prefill pipeline) ----
@@ -672,7 +672,9 @@ def run_gpu(args):
             "peak_kind": f"{bf16_kind} bf16",
             "note": "as prefill_attention with the Bounded-Replay cut at swa row 64 (FLOPs counted over 640 rows)"}
         workloads["3"] = {
-            "workload": WORKLOADS[3].name, "queries": pre["T"], "visible_entries_max": pre["N"],
+            "workload": (WORKLOADS[3].name if (pre["T"], pre["N"] - pre["T"]) == (PREFILL_T, PREFILL_P0)
+                         else f"prefill_t{pre['T']}_after_{pre['N'] - pre['T']}"),
+            "queries": pre["T"], "visible_entries_max": pre["N"],
             "queries_per_s": round(pre["T"] / (pre["pipeline_ms"] * 1e-3), 1),
             "ms_per_step": round(pre["pipeline_ms"], 4),
             "stages_ms": {k_: round(v, 4) for k_, v in pre["stages_ms"].items()},
@@ -697,7 +699,7 @@ APPEND_BYTES_PER_ENTRY = 512 * 2 + 128 * 2 + KV_BYTES_PER_ENTRY + IK_BYTES_PER_E
 PREFILL_T, PREFILL_P0, PREFILL_REPLAY_ROW = 4096, 126976, 64
 
 
-def measure_prefill(csa2, ctx, steps):
+def measure_prefill(csa2, ctx, steps, T=None, p0=None):
     """The prefill workload (4,096 queries at positions 126,976 .. 131,071 of
     one sequence) as a pipeline, eager, with an event between stages: indexer
     q -> MXFP4, the causal indexer scan (4,096 MAC per query-entry pair, FP4
@@ -708,7 +710,9 @@ def measure_prefill(csa2, ctx, steps):
     compressed entries, and the compressor."""
     torch, device, stream = ctx.torch, ctx.device, ctx.stream
     from fp4_kv_cache_02_gb300.inputs import device_normal, device_uniform
-    T, p0, W, K = PREFILL_T, PREFILL_P0, 128, 512
+    T = PREFILL_T if T is None else T
+    p0 = PREFILL_P0 if p0 is None else p0
+    W, K = 128, 512
     N = p0 + T
     q_bf = device_normal((T, 32, 128), 71, device)
     q_data = torch.empty(T, 32, 64, dtype=torch.uint8, device=device)
@@ -764,8 +768,9 @@ def measure_prefill(csa2, ctx, steps):
     ctx.timed(cscan, 2)
     cscan_ms = ctx.timed(cscan, steps)
     del scores
-    # the compressor: 262,144 tokens of C and Z (bf16) into 131,072 packed entries
-    n_tok = 2 * 131072
+    # the compressor: 2 N tokens of C and Z (bf16) into the N packed entries of
+    # the planes above (262,144 tokens into 131,072 entries at the default shape)
+    n_tok = 2 * N
     C = device_normal((n_tok, 512), 78, device)
     Z = device_normal((n_tok, 512), 79, device)
     bias = device_normal((m, 512), 80, device).float().contiguous()
@@ -923,6 +928,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches instead of a CUDA graph of the step")
+    ap.add_argument("--prefill-shape", default=f"{PREFILL_T},{PREFILL_P0}",
+                    help="T,P0 of the prefill workload: T queries at positions P0 .. P0+T-1 (profiling a smaller case)")
     ap.add_argument("--no-prefill", dest="prefill", action="store_false",
                     help="skip the prefill scan and attention timings reported beside the decode step")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -933,6 +940,7 @@ def main(argv=None):
                     help="comma-separated workloads also measured into the line's `workloads` object ('' for none)")
     args = ap.parse_args(argv)
     args.workloads = [int(x) for x in args.workloads.split(",") if x.strip()]
+    args.prefill_shape = tuple(int(x) for x in args.prefill_shape.split(","))
     if 3 not in args.workloads:
         args.prefill = False
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps

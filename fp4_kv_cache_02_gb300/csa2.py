@@ -211,6 +211,10 @@ def csa2_compress_kv(c, z, bias, m, kv_data, kv_scale, out=None, stream=None):
     _req(kv_data, torch.uint8, "kv_data"); _req(kv_scale, torch.uint8, "kv_scale")
     _req(out, torch.bfloat16, "out", allow_none=True)
     n_tokens = c.numel() // 512
+    n_out = n_tokens // int(m) if int(m) > 0 else 0
+    if (z.numel() != c.numel() or bias.numel() < int(m) * 512 or kv_data.numel() < n_out * 256
+            or kv_scale.numel() < n_out * 32 or (out is not None and out.numel() < n_out * 512)):
+        raise ValueError("csa2_compress_kv: z must match c, bias holds m x 512, and the outputs hold n_tokens / m entries")
     _call("csa2_compress_kv", _p(c), _p(z), _p(bias), n_tokens, int(m), _p(kv_data), _p(kv_scale), _p(out),
           _s(stream))
 
