@@ -151,8 +151,14 @@ __device__ __forceinline__ void cluster_sync_release_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Modes: the tiles of a query spread over a cluster and merged through the
+// workspace (latency: every tile in parallel), one sequence's Reuse layers in
+// a cluster, or a query's tiles in sequence on one CTA (throughput).
+enum : int { kModeCluster = 0, kModeReuse = 1, kModeSeq = 2 };
+
 // grid (C, units of the launch), clusters of C CTAs along x. A unit is one
-// query (kReuse false) or one sequence with its L Reuse layers (kReuse true).
+// query (kModeCluster, kModeSeq) or one sequence with its L Reuse layers
+// (kModeReuse).
 //
 // Reuse mode ("DeepSeek-V4.1-Flash" section 2.3.1: the Reuse layers attend
 // to the Full layer's selection with their own Q and SWA rows): a cluster
@@ -161,9 +167,18 @@ __device__ __forceinline__ void cluster_sync_release_acquire() {
 // once and then attended by the L layers back to back while the next layer's
 // Q is being loaded. Partials are written to the workspace by plain stores,
 // and the cluster merges the L x 64 (layer, head) rows.
-template <bool kReuse>
+//
+// Sequential mode (C = 1, for launches that fill the device several times
+// over): the CTA walks its query's tiles in turn with an online softmax: the
+// running (max, sum) of each head lives in shared memory, O^T stays in tensor
+// memory and is rescaled by 2^(m_old - m_new) before each tile's PV product
+// accumulates onto it, and the CTA writes the normalised output itself, with
+// no partials and no merge.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, AttnArgs a) {
+  constexpr bool kReuse = kMode == kModeReuse;
+  constexpr bool kSeq = kMode == kModeSeq;
   // barriers, tensor memory, Q and the SWA tiles need nothing from the
   // preceding kernel; its outputs (the indices) are read after pdl_wait()
   pdl_launch_dependents();
@@ -189,6 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // written by the CTAs of the cluster through distributed shared memory:
   // [part][row - hb0]
   __shared__ float2 ml_in[kMaxPartials * 16];
+  // sequential mode: running max (log2 domain) and sum of each head, and the
+  // factor this tile rescales O by
+  __shared__ float m_run[kHeads], l_run[kHeads], alpha_s[kHeads];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int C = (int)gridDim.x;
@@ -206,6 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // partial rows of the unit in the workspace: [layer][n_part][16][64][32]
   float* part_o_u = a.part_o + (int64_t)blockIdx.y * L * n_part * kHeads * kHeadDim;
 
+  if (kSeq && tid < kHeads) {
+    m_run[tid] = -INFINITY;
+    l_run[tid] = 0.0f;
+  }
   if (tid == 0) {
     tc::mbar_init(bar_s, 1);
     tc::mbar_init(bar_pv, 1);
@@ -499,6 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       M[4 * j4 + 2] = m4.z;
       M[4 * j4 + 3] = m4.w;
     }
+    if (kSeq) {   // P relative to the running max over this and the earlier tiles
+#pragma unroll
+      for (int j = 0; j < 16; ++j) M[j] = fmaxf(M[j], m_run[h0 + j]);
+    }
     // P = 2^(s - M), fp16, stored K-major for the PV product: row h of the
     // 64-row block row / 64, element row % 64
     {
@@ -519,6 +545,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    if (kSeq) {
+      // running (max, sum) of each head; O^T of the earlier tiles rescaled to
+      // the new max before this tile's PV accumulates onto it
+      if (tid < kHeads) {
+        const int h = tid;
+        const float mt = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
+        const float mo = m_run[h], mn = fmaxf(mo, mt);
+        const float alpha = mo == -INFINITY ? 0.0f : fast_exp2(mo - mn);
+        const float lt = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
+        l_run[h] = l_run[h] * alpha + lt;
+        m_run[h] = mn;
+        alpha_s[h] = alpha;
+      }
+      if (passes_done > 0) {
+        __syncthreads();
+        const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
+#pragma unroll 1
+        for (int hh = 0; hh < kHeads; hh += 16) {
+          uint32_t ov[16];
+          tc::tmem_ld_32x32b_x16(o_base + (uint32_t)hh, ov);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha_s[hh + j]);
+          tc::tmem_st_32x32b_x16(o_base + (uint32_t)hh, ov);
+        }
+        tc::tmem_st_wait();
+        tc::tc_fence_before();
+        __syncthreads();
+        tc::tc_fence_after();
+      }
+    }
     // ---- O^T = R^T P^T : 4 x (M = 128 channels), N = 64, K = 128 rows ----
     if (tid == 0 && s_ok) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 1, 0);  // A (channels x rows) is MN-major
@@ -532,13 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mb = i >> 3, kk = i & 7;
         tc::mma_bf16(tmem + kColO + 64u * (uint32_t)mb,
                      ad0 + (uint64_t)((2 * mb * kBlkR + kk * 16 * 128) >> 4),
-                     bd0 + (uint64_t)(((kk >> 2) * kPBlk + (kk & 3) * 32) >> 4), idesc, kk ? 1u : 0u);
+                     bd0 + (uint64_t)(((kk >> 2) * kPBlk + (kk & 3) * 32) >> 4), idesc,
+                     (kk || (kSeq && passes_done > 0)) ? 1u : 0u);
       }
       tc::mma_commit(bar_pv);
     }
     // (m, l) of the pass, log2 domain (l = 0 marks a partial with no rows),
     // into the shared memory of the CTA that merges (layer, head) row hr
-    if (tid < kHeads) {
+    if (!kSeq && tid < kHeads) {
       const int h = tid, hr = layer * kHeads + h;
       const float m = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
       const float l = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
@@ -554,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- partial O: warp w reads the 32 channel lanes 32 cb .. of quadrant
     // w % 4 in block w / 4 (cb = 4 (w / 4) + w % 4), all 64 heads; a partial is
     // laid out [cb][h][32] ----
-    {
+    if (!kSeq) {
       const int cb = (warp >> 2) * 4 + rq;
       const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
       float* dst = part_o_u + (((int64_t)layer * n_part + part) * 16 + cb) * (kHeads * 32);
@@ -633,6 +691,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (!waited) pdl_wait();
+
+  if (kSeq) {
+    // ---- output: O^T / l per head from tensor memory; warp w: channels
+    // 128 (w / 4) + 32 (w % 4) + lane, all 64 heads ----
+    const int rq = warp & 3;
+    const int c = 128 * (warp >> 2) + 32 * rq + lane;
+    if (tid < kHeads) {
+      const float l = l_run[tid];
+      alpha_s[tid] = l > 0.0f ? 1.0f / l : 0.0f;
+      if (a.lse) a.lse[(int64_t)unit * kHeads + tid] = l > 0.0f ? (m_run[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
+    float* of = a.out_f32 ? a.out_f32 + (int64_t)unit * kHeads * kHeadDim + c : nullptr;
+    uint16_t* ob = a.out + (int64_t)unit * kHeads * kHeadDim + c;
+#pragma unroll 1
+    for (int hh = 0; hh < kHeads; hh += 16) {
+      uint32_t ov[16];
+      if (passes_done > 0) {
+        tc::tmem_ld_32x32b_x16(o_base + (uint32_t)hh, ov);
+        tc::tmem_ld_wait();
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float v = passes_done > 0 ? __uint_as_float(ov[j]) * alpha_s[hh + j] : 0.0f;
+        if (of) of[(hh + j) * kHeadDim] = v;
+        ob[(hh + j) * kHeadDim] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc::tc_fence_after();
+      tc::tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
 
   // ---- merge: rank r sums rows [HR r/C, HR (r+1)/C) over all partials ----
   if (kReuse) {

@@ -103,6 +103,36 @@ def test_reuse_attention_limits(csa2):
     assert e.value.status == -2
 
 
+def test_many_queries_walk_their_tiles_on_one_cta(csa2):
+    """A launch of many query-layers (here 160 x 1, above four waves of
+    5-CTA clusters) runs one CTA per query with an online softmax in tensor
+    memory: sampled queries against the oracle, including sequences with
+    fewer visible entries than k (-1 entries) and one whose rows are all
+    skipped (only its SWA rows remain); then, with no SWA rows, a query with
+    no rows at all gives 0 and lse -inf."""
+    B = 160
+    Ns = [700 + 37 * (b % 9) for b in range(B)]
+    case = DecodeCase(workload=91, Ns=Ns, L=1)
+    g = case.to_device()
+    rng = np.random.default_rng(4)
+    k = 512
+    idx = np.stack([rng.permutation(n)[:k] for n in Ns]).astype(np.int32)
+    idx[5, 100:400] = -1
+    idx[17, :] = -1
+    out, out32, lse = _run_decode(csa2, g, dev(idx), k, 128, B, 1)
+    o32, l32 = out32.cpu().numpy(), lse.cpu().numpy()
+    assert torch.equal(out, out32.to(torch.bfloat16))
+    for b in (0, 5, 17, 63, 100, 159):
+        ref, ref_lse = case.oracle_attention(b, 0, idx[b])
+        assert attn_row_error(o32[b, 0], ref) <= ATTN_ROW_TOL
+        np.testing.assert_allclose(l32[b, 0], ref_lse, rtol=1e-5, atol=1e-5)
+    again, _, _ = _run_decode(csa2, g, dev(idx), k, 128, B, 1)
+    assert torch.equal(out, again)
+    out0, out0_32, lse0 = _run_decode(csa2, g, dev(idx), k, 0, B, 1)
+    assert torch.all(out0_32[17] == 0) and torch.all(lse0[17] == -float("inf"))
+    assert np.isfinite(lse0.cpu().numpy()[3]).all()
+
+
 def test_decode_attention_special_cases(csa2):
     case = DecodeCase(workload=95, Ns=[300], n_swa=0)
     g = case.to_device()
