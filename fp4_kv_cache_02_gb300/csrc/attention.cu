@@ -132,14 +132,16 @@ struct AttnPlan {
 
 // Tiles of 128 rows. One CTA per tile (a cluster of n_part CTAs per query)
 // when those clusters all fit on the device at once: every CTA then walks one
-// tile, the SWA tiles early. When there are so many queries that such a launch
-// would run in four or more waves, one CTA per query walks the query's tiles
-// in turn with an online softmax (no partials, no merge: measured faster for
-// 4,096 prefill queries and for 32 x 4 query-layers). In between, clusters of
-// min(n_sel, 8) CTAs (one selected tile each at k = 512) with the SWA tiles
-// spread over them: one wave with some CTAs walking two tiles beats two waves.
-// Smaller clusters when the device cannot hold a cluster that size. n_q:
-// queries of one launch.
+// tile, the SWA tiles early. Else clusters of min(n_sel, 8) CTAs (one selected
+// tile each at k = 512) with the SWA tiles spread over them, when they all fit
+// at once: one wave with some CTAs walking two tiles beats two waves. Past one
+// wave of those, one CTA per query walks the query's tiles in turn with an
+// online softmax (no partials, no merge), as it does whenever the plan comes
+// down to one CTA per query. Measured (k = 512, 128 SWA rows,
+// L2 flushed): 32 queries 33 us in clusters of 4 against 52 one CTA each; 48
+// and 64 queries 60 us in two waves of clusters against 52; 96 queries 89
+// against 54; 4,096 prefill queries 2.91 ms in clusters of 5 against 1.38 ms.
+// n_q: queries of one launch.
 static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_device) {
   AttnPlan p;
   p.n_sel = (k + attn_tc::kRows - 1) / attn_tc::kRows;
@@ -151,11 +153,13 @@ static AttnPlan attn_plan(int32_t n_q, int32_t k, int32_t n_swa, bool query_devi
     const int fit = p.n_part > c && p.n_part <= attn_tc::kMaxCluster ? attn_max_clusters(p.n_part) : 0;
     if (fit > 0 && fit >= n_q) {
       c = p.n_part;
-    } else if (fit > 0 && n_q >= 4 * fit) {
-      c = 1;
-      p.seq = true;
     } else {
       while (c > 1 && attn_max_clusters(c) < 1) c >>= 1;
+      // a cluster of one would only add the merge to the sequential walk
+      if (c == 1 || attn_max_clusters(c) < n_q) {
+        c = 1;
+        p.seq = true;
+      }
     }
   }
   p.cluster = c;
