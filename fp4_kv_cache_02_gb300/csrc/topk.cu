@@ -70,9 +70,22 @@ struct TopkWs {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline void topk_regions(int64_t n, int64_t* region, int32_t* n_regions) {
+// Regions of m tiles of kSelTile scores. m = 1 (the most parallel select) until
+// the launch holds more than kSelTilesPerLaunch tiles (rows x tiles a row):
+// then each CTA walks up to 8 tiles, so that the per-CTA work (the row's
+// histogram read, the threshold search, the second-level flush) is paid once
+// per several tiles (4,096 prefill rows of 131,072 scores: 4 regions a row).
+constexpr int64_t kSelTilesPerLaunch = 8192;
+__host__ __device__ inline void topk_regions(int32_t B, int64_t n, int64_t* region, int32_t* n_regions) {
   const int64_t tiles = n > 0 ? (n + kSelTile - 1) / kSelTile : 1;
-  const int64_t m = (tiles + kMaxRegions - 1) / kMaxRegions;
+  int64_t m = (tiles + kMaxRegions - 1) / kMaxRegions;
+  const int64_t all = (int64_t)(B > 0 ? B : 1) * tiles;
+  if (all > kSelTilesPerLaunch) {
+    int64_t mt = (all + kSelTilesPerLaunch - 1) / kSelTilesPerLaunch;
+    mt = mt > 8 ? 8 : mt;
+    mt = mt > tiles ? tiles : mt;
+    m = m > mt ? m : mt;
+  }
   *region = m * kSelTile;
   *n_regions = (int32_t)((tiles + m - 1) / m);
 }
@@ -81,7 +94,7 @@ __host__ __device__ inline size_t topk_ws_layout(int32_t B, int64_t n, int32_t k
   (void)k;
   int64_t region;
   int32_t nr;
-  topk_regions(n, &region, &nr);
+  topk_regions(B, n, &region, &nr);
   size_t off = 0;
   size_t hist = off;   off = align_up(off + (size_t)B * kHistBins * 4, 256);
   size_t hist2 = off;  off = align_up(off + (size_t)B * kHist2Bins * 4, 256);
@@ -107,17 +120,6 @@ __host__ __device__ inline size_t topk_ws_zero_bytes(int32_t B) {
                   256);
 }
 
-__device__ __forceinline__ bool load_candidate(const float* __restrict__ scores, const int32_t* __restrict__ positions,
-                                               int64_t row_off, int64_t i, int64_t nv, uint32_t* key, int32_t* pos) {
-  if (i >= nv) return false;
-  float s = scores[row_off + i];
-  int32_t p = positions ? positions[row_off + i] : (int32_t)i;
-  if (p < 0 || !score_is_candidate(s)) return false;
-  *key = score_key(s);
-  *pos = p;
-  return true;
-}
-
 __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
                                   uint32_t* scratch);
 
@@ -133,18 +135,22 @@ __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
   const int64_t row_off = (int64_t)b * n;
   int64_t nv = n_valid ? min((int64_t)n_valid[b], n) : n;
   int64_t lo = (int64_t)blockIdx.x * chunk, hi = min(lo + chunk, nv);
+  const bool has_pos = positions != nullptr;
   for (int64_t sub = lo; sub < hi; sub += (int64_t)kSelThreads * 16) {
-    uint32_t key[16];
-    uint32_t ok = 0;
+    // all loads of the sub-chunk in flight first: predicated, nothing reads
+    // them before the last one is issued
+    float sv[16];
+    int32_t pv[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {  // all loads of the sub-chunk in flight first
+    for (int e = 0; e < 16; ++e) {
       const int64_t i = sub + (int64_t)e * kSelThreads + threadIdx.x;
-      int32_t p;
-      ok |= (uint32_t)(i < hi && load_candidate(scores, positions, row_off, i, nv, &key[e], &p)) << e;
+      const bool in = i < hi;
+      sv[e] = in ? scores[row_off + i] : __uint_as_float(0x7fc00000u);
+      pv[e] = in && has_pos ? positions[row_off + i] : 0;
     }
 #pragma unroll
     for (int e = 0; e < 16; ++e)
-      if (ok & (1u << e)) atomicAdd(&sh[key[e] >> (32 - kHistBits)], 1u);
+      if (pv[e] >= 0 && score_is_candidate(sv[e])) atomicAdd(&sh[score_key(sv[e]) >> (32 - kHistBits)], 1u);
   }
   __syncthreads();
   uint32_t* gh = ws.hist + (size_t)b * kHistBins;
