@@ -324,7 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- one tile's rows: rows [128 tile, 128 tile + 128) of the SWA window of
   // query qi_swa (swa) or of the sequence's selected list, gathered by the
   // bulk-copy engine and dequantised into R ----
-  auto gather_dequant = [&](const bool swa, const int tile, const int qi_swa) {
+  // thread r < 128: the index of row r of the CTA's next selected tile, loaded
+  // while the current tile is attended (pf_tile: that tile, -1 none); the
+  // sequence's visible count, read once
+  int32_t pf_idx = -1;
+  int pf_tile = -1;
+  int64_t nv_seq = -1;
+  auto gather_dequant = [&](const bool swa, const int tile, const int qi_swa, const int next_sel_tile) {
     const uint32_t par = items_done & 1u;
     // thread r < 128 starts the bulk copies of row r into the staging area
     // (selected rows: 256 B of codes + 32 B of scales); the SWA rows of the
@@ -350,10 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t < a.k) {
           // n_visible may come from the kernel before this one (a KV append):
           // read after pdl_wait(), like the indices
-          const int64_t nv = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
-          const int32_t p = a.idx[(int64_t)seq * a.k + t];
+          if (nv_seq < 0) nv_seq = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
+          const int32_t p = pf_tile == tile ? pf_idx : a.idx[(int64_t)seq * a.k + t];
           if (p >= 0) {
-            if (p < nv) {
+            if (p < nv_seq) {
               valid = 1;
               src = (int64_t)seq * a.kv_seq_stride + p;
             } else {
@@ -367,6 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::bulk_load(sStage + kRows * kKvBytes + tid * kKvScales, a.kv_scale + src * kKvScales, kKvScales, bar_g);
         } else {
           tc::mbar_arrive(bar_g);
+        }
+        // the next selected tile's index for this row, in flight through this tile
+        if (next_sel_tile >= 0) {
+          const int tn = next_sel_tile * kRows + tid;
+          pf_idx = tn < a.k ? a.idx[(int64_t)seq * a.k + tn] : -1;
+          pf_tile = next_sel_tile;
         }
       }
       row_valid[tid] = valid;
@@ -672,7 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int l0 = item_layer0(j);
     const int swa_tile = swa ? j - l0 * n_swt : 0;
     const int sel_tile = swa ? 0 : (j - L * n_swt) / n_grp;
-    const bool rows_ok = gather_dequant(swa, swa ? swa_tile : sel_tile, kReuse ? seq * L + l0 : unit);
+    const int next_sel = jn < n_items && jn >= L * n_swt ? (jn - L * n_swt) / n_grp : -1;
+    const bool rows_ok =
+        gather_dequant(swa, swa ? swa_tile : sel_tile, kReuse ? seq * L + l0 : unit, swa ? -1 : next_sel);
     (void)rows_ok;
     const int n_layers = swa ? 1 : lgrp;
     for (int li = 0; li < n_layers; ++li) {
