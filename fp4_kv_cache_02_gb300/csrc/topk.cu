@@ -603,6 +603,159 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
   }
 }
 
+// ---- passes 1 + 2 in one, for batches of many long dense rows -------------
+// One CTA per row reads the row once, a tile of kSelTile scores at a time (the
+// next tile's loads in flight while the current one is processed). Each tile
+// goes into the shared-memory histogram, and its keys at or above the running
+// threshold bin are appended, in position order, to their region's slice. The
+// running bin is the threshold bin of the histogram so far, recomputed after
+// each of the first four tiles and then after every fourth: it only rises as
+// keys arrive and never passes the row's final threshold bin t, so the slices
+// hold every key of bin t and above (and some below it). At the end the exact
+// t is found, each slice is compacted in place to its keys in bin t or above,
+// and the keys in bin t are counted in the second-level histogram: the
+// workspace then holds what the histogram and select kernels leave for the
+// finalize. Scores move as raw 32-bit words and are keyed with integer
+// operations only, so no NaN passes through a float register.
+constexpr uint32_t kCandKeyLo = 0x00800000u;  // score_key(-inf) + 1
+constexpr uint32_t kCandKeyHi = 0xff800000u;  // score_key(+inf)
+constexpr uint32_t kNotCandidateBits = 0xffffffffu;  // a negative NaN: key 0
+// score_key() of the fp32 score whose bit pattern is b, in integer operations
+__device__ __forceinline__ uint32_t key_of_bits(uint32_t b) {
+  return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kSelThreads, 4) topk_collect_kernel(const float* __restrict__ scores, int64_t n,
+                                                                      const int32_t* __restrict__ n_valid, int32_t k,
+                                                                      TopkWs ws) {
+  pdl_begin();
+  __shared__ uint32_t sh[kHistBins];
+  __shared__ uint32_t h2[kHist2Bins];
+  __shared__ uint32_t scratch[kSelThreads + 2];
+  __shared__ uint32_t s_scan[33];
+  const int b = blockIdx.x;
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0u;
+  for (int i = threadIdx.x; i < kHist2Bins; i += kSelThreads) h2[i] = 0u;
+  __syncthreads();
+  const int64_t row_off = (int64_t)b * n;
+  const int64_t nv = n_valid ? max((int64_t)0, min((int64_t)n_valid[b], n)) : n;
+  const uint32_t* wrow = reinterpret_cast<const uint32_t*>(scores + row_off);
+  const bool vec = (((uintptr_t)wrow) & 15) == 0;
+  uint2* cand = ws.cand + row_off;
+  uint32_t* rcount = ws.rcount + (size_t)b * ws.n_regions;
+  int t_run = -1;        // threshold bin of the histogram so far (-1: fewer than k keys)
+  uint32_t written = 0;  // superset entries of the current region
+  int reg = 0;           // current region
+  uint32_t nx[kPerThread];
+  auto load_tile = [&](int64_t i0) {
+    if (vec && i0 + kPerThread <= nv) {
+      const uint4* sp = reinterpret_cast<const uint4*>(wrow + i0);
+#pragma unroll
+      for (int q = 0; q < kPerThread / 4; ++q) {
+        const uint4 v = __ldcs(sp + q);
+        nx[4 * q] = v.x; nx[4 * q + 1] = v.y; nx[4 * q + 2] = v.z; nx[4 * q + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < kPerThread; ++e) nx[e] = i0 + e < nv ? wrow[i0 + e] : kNotCandidateBits;
+    }
+  };
+  if (nv > 0) load_tile((int64_t)threadIdx.x * kPerThread);
+  int j = 0;
+  for (int64_t lo = 0; lo < nv; lo += kSelTile, ++j) {
+    const int r = (int)(lo / ws.region);
+    if (r != reg) {      // the earlier region's superset is complete
+      if (threadIdx.x == 0) rcount[reg] = written;
+      reg = r;
+      written = 0;
+    }
+    uint32_t cur[kPerThread];
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) cur[e] = nx[e];
+    const int64_t p0 = lo + (int64_t)threadIdx.x * kPerThread;
+    if (lo + kSelTile < nv) load_tile(p0 + kSelTile);
+    // a key is a candidate when it lies in [key(-inf) + 1, key(+inf)] (NaNs of
+    // either sign, and the words loaded past n_valid, fall outside); it is
+    // flagged when it is also at or above the running bin
+    const uint32_t lo_flag = t_run > 0 ? max((uint32_t)t_run << (32 - kHistBits), kCandKeyLo) : kCandKeyLo;
+    uint32_t flag = 0;
+#pragma unroll
+    for (int e = 0; e < kPerThread; ++e) {
+      const uint32_t key = key_of_bits(cur[e]);
+      if (key - kCandKeyLo <= kCandKeyHi - kCandKeyLo) atomicAdd(&sh[key >> (32 - kHistBits)], 1u);
+      flag |= (uint32_t)(key - lo_flag <= kCandKeyHi - lo_flag) << e;
+    }
+    uint32_t total;
+    const uint32_t ex = block_exclusive_scan((uint32_t)__popc(flag), &total, s_scan);
+    if (flag) {
+      int64_t o = (int64_t)r * ws.region + written + ex;
+#pragma unroll
+      for (int e = 0; e < kPerThread; ++e)
+        if ((flag >> e) & 1u) cand[o++] = make_uint2(key_of_bits(cur[e]), (uint32_t)(p0 + e));
+    }
+    written += total;
+    if (j < 4 || (j & 3) == 3) {
+      uint32_t above;
+      t_run = find_threshold_bin(sh, kHistBins, (uint32_t)k, &above, scratch);  // (its barriers publish sh)
+    }
+  }
+  if (threadIdx.x == 0) {
+    rcount[reg] = written;
+    for (int r = reg + 1; r < ws.n_regions; ++r) rcount[r] = 0u;  // past n_valid
+  }
+  // the exact threshold bin of the row and the counts the finalize reads
+  // (the last tile's scan published the histogram)
+  uint32_t above;
+  const int t = find_threshold_bin(sh, kHistBins, (uint32_t)k, &above, scratch);
+  if (threadIdx.x == 0) {
+    ws.cnt[b].t = t;
+    ws.cnt[b].above = above;
+    ws.cnt[b].pad[0] = t >= 0 ? sh[t] : 0u;
+  }
+  // compaction of every region's slice to its keys in bin t or above, in
+  // order, in place: a chunk is read into registers before the scan's barrier
+  // and written after it, and the writes never pass the chunk's reads. The
+  // slices and their counts were written by this CTA before a barrier, so they
+  // are read with plain loads (an L2-only load may not see them yet).
+  bool any_t = false;
+  for (int r = 0; r <= reg; ++r) {
+    const uint32_t m = rcount[r];
+    uint2* sl = cand + (int64_t)r * ws.region;
+    uint32_t kept = 0;
+    for (uint32_t base = 0; base < m; base += (uint32_t)kSelThreads * 4) {
+      uint2 c[4];
+      uint32_t f = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t g = base + threadIdx.x * 4 + e;
+        if (g < m) {
+          c[e] = sl[g];
+          const int digit = (int)(c[e].x >> (32 - kHistBits));
+          f |= (uint32_t)(digit >= t) << e;
+          if (digit == t) {
+            atomicAdd(&h2[(c[e].x >> kHist2Shift) & (kHist2Bins - 1)], 1u);
+            any_t = true;
+          }
+        }
+      }
+      uint32_t tot;
+      const uint32_t ex = block_exclusive_scan((uint32_t)__popc(f), &tot, s_scan);
+      uint32_t o = kept + ex;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((f >> e) & 1u) sl[o++] = c[e];
+      kept += tot;
+      __syncthreads();   // this chunk's writes land before the next chunk is read
+    }
+    if (threadIdx.x == 0) rcount[r] = kept;
+  }
+  if (__syncthreads_or(any_t)) {
+    uint32_t* gh2 = ws.hist2 + (size_t)b * kHist2Bins;
+    for (int i = threadIdx.x; i < kHist2Bins; i += kSelThreads)
+      if (h2[i]) gh2[i] = h2[i];
+  }
+}
+
 // Appends every entry [0, count) of `ld` to out (through the s_nout ticket).
 template <typename LoadFn>
 __device__ void take_all(uint32_t count, LoadFn ld, int32_t k, int32_t* out, uint32_t& s_nout) {
@@ -1016,6 +1169,16 @@ int csa2_launch_topk(const float* scores, int32_t B, int64_t n, const int32_t* n
   TopkWs ws;
   topk_ws_layout(B, n, k, &ws, (char*)workspace);
   int64_t chunk = topk_chunk(B, n);
+  if (!positions && chunk >= n && n > 0) {
+    // a CTA per whole row: histogram and candidates in one pass over the scores
+    CSA2_LAUNCH_PDL(topk_collect_kernel, dim3((unsigned)B), dim3(kSelThreads), 0, stream, scores, n, n_valid, k, ws);
+    CSA2_CHECK_LAUNCH();
+    int rc = topk_finalize_attr();
+    if (rc) return rc;
+    CSA2_LAUNCH_PDL(topk_finalize_kernel, dim3((unsigned)B), dim3(kFinThreads), kFinSmem, stream, n, k, ws, idx, 1);
+    CSA2_CHECK_LAUNCH();
+    return CSA2_OK;
+  }
   int64_t chunks = n > 0 ? (n + chunk - 1) / chunk : 1;
   dim3 grid((unsigned)chunks, (unsigned)B);
   CSA2_LAUNCH_PDL(topk_hist_kernel, grid, dim3(kSelThreads), 0, stream, scores, n, n_valid, positions, chunk, k, ws);

@@ -83,6 +83,32 @@ def test_topk_exact_on_identical_scores(csa2, n, k, levels):
         assert np.all(got[b, len(expect):] == -1)
 
 
+@pytest.mark.parametrize("B,n,levels", [(640, 9000, 0), (700, 60000, 0), (612, 20000, 7), (610, 4096, 0)])
+def test_topk_many_rows_one_cta_each(csa2, B, n, levels):
+    """Batches of at least 608 rows take one CTA per row (histogram and
+    candidates in one pass); ragged n_valid (0, below k, a tile and one more,
+    full), planted ties, -inf and NaN must still give the oracle's set."""
+    rng = np.random.default_rng(B + n + levels)
+    k = 512
+    if levels:
+        s = rng.integers(0, levels, (B, n)).astype(np.float32)
+    else:
+        s = rng.standard_normal((B, n)).astype(np.float32)
+        s[rng.integers(0, B, 50), rng.integers(0, n, 50)] = 4.25  # ties at the top
+    s[0, :64] = -np.inf
+    s[1, ::13] = np.nan
+    nvalid = rng.integers(1, n + 1, B).astype(np.int32)
+    nvalid[:6] = [0, 1, k - 1, 4097 if n > 4097 else n, n, n - 1]
+    idx = torch.empty(B, k, dtype=torch.int32, device="cuda")
+    csa2.csa2_topk(dev(s), k, idx, csa2.topk_workspace(B, n, k), n_valid=dev(nvalid))
+    got = idx.cpu().numpy()
+    for b in range(B):
+        ref, _ = oracle.topk(s[b, :nvalid[b]], k)
+        expect = sorted(int(p) for p in ref if p >= 0)
+        assert list(got[b, :len(expect)]) == expect, b
+        assert np.all(got[b, len(expect):] == -1), b
+
+
 def test_topk_one_million_row(csa2):
     rng = np.random.default_rng(9)
     n, k = 1 << 20, 512
