@@ -660,7 +660,8 @@ def run_gpu(args):
             "bound": "hbm", "achieved": round(cmp_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(cmp_gbs / hbm_peak, 4), "ms": round(pre["cmp_ms"], 4),
             "algorithmic_bytes_per_launch": pre["cmp_bytes"], "entries_per_launch": pre["cmp_entries"],
-            "note": "262,144 tokens of C and Z (bf16) in, 131,072 packed 288-byte entries out"}
+            "note": f"{2 * pre['cmp_entries']:,} tokens of C and Z (bf16) in, {pre['cmp_entries']:,} packed "
+                    "288-byte entries out"}
         line["kernel_rooflines"]["prefill_attention"] = {
             "bound": "tensor", "achieved": round(at_tf, 1), "peak": round(bf16_peak, 1), "unit": "TFLOP/s",
             "frac": round(at_tf / bf16_peak, 4), "ms": round(pre["attn_ms"], 4),

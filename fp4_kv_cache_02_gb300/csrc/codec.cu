@@ -121,56 +121,77 @@ __global__ void unpack_fp8_kernel(const uint8_t* __restrict__ in, int64_t n, uin
   out[i] = *reinterpret_cast<uint16_t*>(&b);
 }
 
-// ---- fused append: one warp per new entry (b, t) ----------------------------
-// Lane l encodes main-KV block l (channels 16l .. 16l+15); lanes 0..3 also
-// encode indexer-key block l (channels 32l .. 32l+31). The entry goes to
-// position n_visible[b] + t. A sequence whose T entries do not fit below the
-// capacity (or whose count is negative) gets none of them, keeps its count
-// and records a device error.
+// ---- fused append: one warp per kPerWarp new entries (b, t) ------------------
+// The warp issues all its entries' loads before encoding any (two entries a
+// warp for bulk appends; one for small batches, where the grid is the limit).
+// Lane l encodes
+// main-KV block l (channels 16l .. 16l+15) and indexer-key channels 4l .. 4l+3:
+// the eight lanes of an MXFP4 block (32 channels) share its amax through
+// shuffles. An entry goes to position n_visible[b] + t. A sequence whose T
+// entries do not fit below the capacity (or whose count is negative) gets
+// none of them, keeps its count and records a device error.
 constexpr int kAppendWarps = 8;
+constexpr int64_t kAppendPairsFrom = 16384;  // entries from which a warp takes two
 
+template <int kPerWarp>
 __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
     const uint16_t* __restrict__ kv, const uint16_t* __restrict__ ik, int32_t B, int32_t T,
     uint8_t* __restrict__ kv_data, uint8_t* __restrict__ kv_scale, uint8_t* __restrict__ ik_data,
     uint8_t* __restrict__ ik_scale, int64_t cap, const int32_t* __restrict__ n_visible,
     int32_t* __restrict__ n_visible_out) {
+  static_assert(kIdxDim == 32 * 4 && kHeadDim == 32 * 16, "a lane holds 16 latent and 4 key channels");
   pdl_begin();
   const int lane = threadIdx.x & 31;
-  const int64_t e = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
-  if (e >= (int64_t)B * T) return;
-  const int b = (int)(e / T), t = (int)(e % T);
-  const int64_t nv = n_visible[b];
-  const bool fits = nv >= 0 && nv + T <= cap;
-  if (n_visible_out && t == 0 && lane == 0) n_visible_out[b] = (int32_t)(fits ? nv + T : nv);
-  if (!fits) {
-    if (lane == 0 && t == 0) record_error(&g_codec_error, CSA2_ERR_DEVICE);
-    return;
-  }
-  const int64_t p = nv + t;
-  const int64_t row = (int64_t)b * cap + p;
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(kv + e * kHeadDim + lane * 16);
-    const uint4 v0 = src[0], v1 = src[1];
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint2 d;
-    uint8_t sc;
-    encode_kv_fp4_block(w, d, sc);
-    *reinterpret_cast<uint2*>(kv_data + row * kKvBytes + lane * 8) = d;
-    kv_scale[row * kKvScales + lane] = sc;
-  }
-  if (lane < kIdxDim / 32) {
-    const uint4* src = reinterpret_cast<const uint4*>(ik + e * kIdxDim + lane * 32);
-    uint32_t w[16];
+  const int64_t entries = (int64_t)B * T;
+  const int64_t e0 = ((int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5)) * kPerWarp;
+  if (e0 >= entries) return;
+  uint4 kv_lo[kPerWarp], kv_hi[kPerWarp];
+  uint2 ikw[kPerWarp];
+  int64_t nvs[kPerWarp];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 v = src[i];
-      w[4 * i + 0] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+  for (int j = 0; j < kPerWarp; ++j) {
+    const int64_t e = e0 + j;
+    if (e < entries) {
+      const uint4* src = reinterpret_cast<const uint4*>(kv + e * kHeadDim + lane * 16);
+      kv_lo[j] = src[0];
+      kv_hi[j] = src[1];
+      ikw[j] = reinterpret_cast<const uint2*>(ik + e * kIdxDim)[lane];
+      nvs[j] = n_visible[e / T];
     }
-    uint4 d;
-    uint8_t sc;
-    encode_mxfp4_block(w, d, sc);
-    *reinterpret_cast<uint4*>(ik_data + row * (kIdxDim / 2) + lane * 16) = d;
-    ik_scale[row * (kIdxDim / 32) + lane] = sc;
+  }
+#pragma unroll
+  for (int j = 0; j < kPerWarp; ++j) {
+    const int64_t e = e0 + j;
+    if (e >= entries) break;
+    const int b = (int)(e / T), t = (int)(e % T);
+    const int64_t nv = nvs[j];
+    const bool fits = nv >= 0 && nv + T <= cap;
+    if (n_visible_out && t == 0 && lane == 0) n_visible_out[b] = (int32_t)(fits ? nv + T : nv);
+    if (!fits) {
+      if (lane == 0 && t == 0) record_error(&g_codec_error, CSA2_ERR_DEVICE);
+      continue;
+    }
+    const int64_t row = (int64_t)b * cap + nv + t;
+    {
+      const uint32_t w[8] = {kv_lo[j].x, kv_lo[j].y, kv_lo[j].z, kv_lo[j].w,
+                             kv_hi[j].x, kv_hi[j].y, kv_hi[j].z, kv_hi[j].w};
+      uint2 d;
+      uint8_t sc;
+      encode_kv_fp4_block(w, d, sc);
+      *reinterpret_cast<uint2*>(kv_data + row * kKvBytes + lane * 8) = d;
+      kv_scale[row * kKvScales + lane] = sc;
+    }
+    {
+      uint32_t amax_bits = max(max(ikw[j].x & 0x7FFFu, (ikw[j].x >> 16) & 0x7FFFu),
+                               max(ikw[j].y & 0x7FFFu, (ikw[j].y >> 16) & 0x7FFFu));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, o));
+      float inv;
+      const int X = mxfp4_exponent(amax_bits, inv);
+      *reinterpret_cast<uint16_t*>(ik_data + row * (kIdxDim / 2) + lane * 2) =
+          (uint16_t)encode_e2m1x4(ikw[j].x, ikw[j].y, inv);
+      if ((lane & 7) == 0) ik_scale[row * (kIdxDim / 32) + lane / 8] = (uint8_t)(X + 127);
+    }
   }
 }
 
@@ -179,42 +200,93 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
 // softmax over the block's tokens of Z[row][c] + bias[a][c], and the entry is
 // the weighted sum of C[row][c]; it is rounded to bf16 and packed like the
 // latent of csa2_kv_append. Lane l owns channels 16l .. 16l+15 (one E4M3 block).
+// kM > 0 fixes m at compile time: every load of the entry (Z, C and the bias
+// rows) is issued before the arithmetic. kM = 0 walks a runtime m. Both do the
+// same operations in the same order, so they give the same bits.
+template <int kM>
 __global__ void __launch_bounds__(kAppendWarps * 32) compress_kv_kernel(
     const uint16_t* __restrict__ C, const uint16_t* __restrict__ Z, const float* __restrict__ bias, int64_t n_out,
-    int32_t m, uint8_t* __restrict__ kv_data, uint8_t* __restrict__ kv_scale, uint16_t* __restrict__ out_bf16) {
+    int32_t m_rt, uint8_t* __restrict__ kv_data, uint8_t* __restrict__ kv_scale, uint16_t* __restrict__ out_bf16) {
   pdl_begin();
+  const int m = kM > 0 ? kM : m_rt;
   const int lane = threadIdx.x & 31;
   const int64_t e = (int64_t)blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
   if (e >= n_out) return;
   const int c0 = lane * 16;
-  auto load16 = [&](const uint16_t* base, int64_t row, float (&v)[16]) {
+  auto load_words = [&](const uint16_t* base, int64_t row, uint32_t (&w)[8]) {
     const uint4* src = reinterpret_cast<const uint4*>(base + row * kHeadDim + c0);
     const uint4 a = src[0], b = src[1];
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  };
+  auto load_bias = [&](int a, float (&v)[16]) {
+    const float4* src = reinterpret_cast<const float4*>(bias + (int64_t)a * kHeadDim + c0);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    for (int q = 0; q < 4; ++q) {
+      const float4 x = src[q];
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
   };
-  float mx[16], den[16], num[16], z[16], c[16];
+  auto lo = [](uint32_t w) { return bf16_bits_to_f32(w & 0xFFFFu); };
+  auto hi = [](uint32_t w) { return bf16_bits_to_f32(w >> 16); };
+  float mx[16], den[16], num[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) mx[i] = -INFINITY;
-  for (int a = 0; a < m; ++a) {
-    load16(Z, e * m + a, z);
+  if constexpr (kM > 0) {
+    uint32_t zw[kM][8], cw[kM][8];
+    float bv[kM][16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) mx[i] = fmaxf(mx[i], z[i] + bias[a * kHeadDim + c0 + i]);
-  }
+    for (int a = 0; a < kM; ++a) {
+      load_words(Z, e * kM + a, zw[a]);
+      load_words(C, e * kM + a, cw[a]);
+      load_bias(a, bv[a]);
+    }
 #pragma unroll
-  for (int i = 0; i < 16; ++i) den[i] = num[i] = 0.0f;
-  for (int a = 0; a < m; ++a) {
-    load16(Z, e * m + a, z);
-    load16(C, e * m + a, c);
+    for (int a = 0; a < kM; ++a)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float wgt = expf(z[i] + bias[a * kHeadDim + c0 + i] - mx[i]);
-      den[i] += wgt;
-      num[i] = fmaf(wgt, c[i], num[i]);
+      for (int i = 0; i < 8; ++i) {
+        mx[2 * i] = fmaxf(mx[2 * i], lo(zw[a][i]) + bv[a][2 * i]);
+        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], hi(zw[a][i]) + bv[a][2 * i + 1]);
+      }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) den[i] = num[i] = 0.0f;
+#pragma unroll
+    for (int a = 0; a < kM; ++a)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float w0 = expf(lo(zw[a][i]) + bv[a][2 * i] - mx[2 * i]);
+        const float w1 = expf(hi(zw[a][i]) + bv[a][2 * i + 1] - mx[2 * i + 1]);
+        den[2 * i] += w0;
+        den[2 * i + 1] += w1;
+        num[2 * i] = fmaf(w0, lo(cw[a][i]), num[2 * i]);
+        num[2 * i + 1] = fmaf(w1, hi(cw[a][i]), num[2 * i + 1]);
+      }
+  } else {
+    uint32_t zw[8], cw[8];
+    float bv[16];
+    for (int a = 0; a < m; ++a) {
+      load_words(Z, e * m + a, zw);
+      load_bias(a, bv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx[2 * i] = fmaxf(mx[2 * i], lo(zw[i]) + bv[2 * i]);
+        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], hi(zw[i]) + bv[2 * i + 1]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) den[i] = num[i] = 0.0f;
+    for (int a = 0; a < m; ++a) {
+      load_words(Z, e * m + a, zw);
+      load_words(C, e * m + a, cw);
+      load_bias(a, bv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float w0 = expf(lo(zw[i]) + bv[2 * i] - mx[2 * i]);
+        const float w1 = expf(hi(zw[i]) + bv[2 * i + 1] - mx[2 * i + 1]);
+        den[2 * i] += w0;
+        den[2 * i + 1] += w1;
+        num[2 * i] = fmaf(w0, lo(cw[i]), num[2 * i]);
+        num[2 * i + 1] = fmaf(w1, hi(cw[i]), num[2 * i + 1]);
+      }
     }
   }
   uint32_t w[8];
@@ -343,9 +415,15 @@ extern "C" int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t 
   cudaStream_t s = (cudaStream_t)stream;
   const bool in_place = n_visible_out == n_visible;
   const int64_t entries = (int64_t)B * T;
-  CSA2_LAUNCH_PDL(kv_append_kernel, grid_for(entries, kAppendWarps), dim3(kAppendWarps * 32), 0, s,
-                  (const uint16_t*)kv_bf16, (const uint16_t*)ik_bf16, B, T, kv_data, kv_scale, ik_data, ik_scale, cap,
-                  n_visible, in_place ? (int32_t*)nullptr : n_visible_out);
+  int32_t* nv_out = in_place ? (int32_t*)nullptr : n_visible_out;
+  if (entries >= kAppendPairsFrom)
+    CSA2_LAUNCH_PDL(kv_append_kernel<2>, grid_for((entries + 1) / 2, kAppendWarps), dim3(kAppendWarps * 32), 0, s,
+                    (const uint16_t*)kv_bf16, (const uint16_t*)ik_bf16, B, T, kv_data, kv_scale, ik_data, ik_scale,
+                    cap, n_visible, nv_out);
+  else
+    CSA2_LAUNCH_PDL(kv_append_kernel<1>, grid_for(entries, kAppendWarps), dim3(kAppendWarps * 32), 0, s,
+                    (const uint16_t*)kv_bf16, (const uint16_t*)ik_bf16, B, T, kv_data, kv_scale, ik_data, ik_scale,
+                    cap, n_visible, nv_out);
   if (in_place)
     CSA2_LAUNCH_PDL(advance_visible_kernel, grid_for(B, 256), dim3(256), 0, s, n_visible_out, B, T, cap);
   return CSA2_OK;
@@ -356,13 +434,22 @@ extern "C" int csa2_compress_kv(const void* c_bf16, const void* z_bf16, const fl
                                 csa2_stream_t stream) {
   if (!c_bf16 || !z_bf16 || !bias || !kv_data || !kv_scale || n_tokens < 0 || m < 1) return CSA2_ERR_INVALID_ARG;
   if (n_tokens % m) return CSA2_ERR_UNSUPPORTED_SHAPE;
-  if (!csa2_aligned(c_bf16, 16) || !csa2_aligned(z_bf16, 16) || !csa2_aligned(kv_data, 8) ||
-      (out_bf16 && !csa2_aligned(out_bf16, 16)))
+  if (!csa2_aligned(c_bf16, 16) || !csa2_aligned(z_bf16, 16) || !csa2_aligned(bias, 16) ||
+      !csa2_aligned(kv_data, 8) || (out_bf16 && !csa2_aligned(out_bf16, 16)))
     return CSA2_ERR_ALIGNMENT;
   const int64_t n_out = n_tokens / m;
   if (n_out == 0) return CSA2_OK;
-  CSA2_LAUNCH_PDL(compress_kv_kernel, grid_for(n_out, kAppendWarps), dim3(kAppendWarps * 32), 0,
-                  (cudaStream_t)stream, (const uint16_t*)c_bf16, (const uint16_t*)z_bf16, bias, n_out, m, kv_data,
-                  kv_scale, (uint16_t*)out_bf16);
+  const dim3 grid(grid_for(n_out, kAppendWarps)), block(kAppendWarps * 32);
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint16_t *cp = (const uint16_t*)c_bf16, *zp = (const uint16_t*)z_bf16;
+  if (m == 1)
+    CSA2_LAUNCH_PDL(compress_kv_kernel<1>, grid, block, 0, s, cp, zp, bias, n_out, m, kv_data, kv_scale,
+                    (uint16_t*)out_bf16);
+  else if (m == 2)
+    CSA2_LAUNCH_PDL(compress_kv_kernel<2>, grid, block, 0, s, cp, zp, bias, n_out, m, kv_data, kv_scale,
+                    (uint16_t*)out_bf16);
+  else
+    CSA2_LAUNCH_PDL(compress_kv_kernel<0>, grid, block, 0, s, cp, zp, bias, n_out, m, kv_data, kv_scale,
+                    (uint16_t*)out_bf16);
   return CSA2_OK;
 }

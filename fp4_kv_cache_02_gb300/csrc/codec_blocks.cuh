@@ -15,6 +15,30 @@ namespace csa2 {
 // E8M0 code. The shared exponent is floor(log2(amax)) - 2 (the largest E2M1
 // magnitude is 6 = 1.5 * 2^2), clamped to the E8M0 range; values are scaled
 // by its power of two and rounded to nearest-even E2M1, saturating.
+// The shared exponent X of an MXFP4 block, from the largest magnitude bit
+// pattern (sign cleared) among its bf16 values, and the scaling 2^-X as fp32.
+__device__ __forceinline__ int mxfp4_exponent(uint32_t amax_bits, float& inv) {
+  // floor(log2(amax)) is the unbiased exponent field for a normal amax;
+  // subnormal or zero amax clamps to -127.
+  const int exp_field = (int)(amax_bits >> 7);  // bf16 exponent field
+  int X = exp_field == 0 ? -127 : (exp_field - 127) - 2;
+  X = X < -127 ? -127 : (X > 127 ? 127 : X);
+  // 2^-X as fp32 (X = 127 gives the subnormal 2^-127)
+  inv = X == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - X) << 23);
+  return X;
+}
+
+// Four consecutive values of an MXFP4 block (two words of bf16 pairs), scaled
+// by 2^-X and rounded to nearest-even E2M1, saturating: two bytes, element 0 in
+// the low nibble.
+__device__ __forceinline__ uint32_t encode_e2m1x4(uint32_t pair0, uint32_t pair1, float inv) {
+  const float a0 = bf16_bits_to_f32(pair0 & 0xFFFFu) * inv;
+  const float a1 = bf16_bits_to_f32(pair0 >> 16) * inv;
+  const float a2 = bf16_bits_to_f32(pair1 & 0xFFFFu) * inv;
+  const float a3 = bf16_bits_to_f32(pair1 >> 16) * inv;
+  return cvt_e2m1x2(a0, a1) | (cvt_e2m1x2(a2, a3) << 8);
+}
+
 __device__ __forceinline__ void encode_mxfp4_block(const uint32_t (&w)[16], uint4& data, uint8_t& e8m0) {
   uint32_t amax_bits = 0;
 #pragma unroll
@@ -22,28 +46,12 @@ __device__ __forceinline__ void encode_mxfp4_block(const uint32_t (&w)[16], uint
     amax_bits = max(amax_bits, (w[i] & 0x7FFFu));
     amax_bits = max(amax_bits, ((w[i] >> 16) & 0x7FFFu));
   }
-  // floor(log2(amax)) is the unbiased exponent field for a normal amax;
-  // subnormal or zero amax clamps to -127.
-  const int exp_field = (int)(amax_bits >> 7);  // bf16 exponent field
-  int X = exp_field == 0 ? -127 : (exp_field - 127) - 2;
-  X = X < -127 ? -127 : (X > 127 ? 127 : X);
-  // 2^-X as fp32 (X = 127 gives the subnormal 2^-127)
-  const float inv = X == 127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(127 - X) << 23);
+  float inv;
+  const int X = mxfp4_exponent(amax_bits, inv);
   uint32_t out[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint32_t pair0 = w[4 * i + 2 * j], pair1 = w[4 * i + 2 * j + 1];
-      const float a0 = bf16_bits_to_f32(pair0 & 0xFFFFu) * inv;
-      const float a1 = bf16_bits_to_f32(pair0 >> 16) * inv;
-      const float a2 = bf16_bits_to_f32(pair1 & 0xFFFFu) * inv;
-      const float a3 = bf16_bits_to_f32(pair1 >> 16) * inv;
-      word |= (cvt_e2m1x2(a0, a1) | (cvt_e2m1x2(a2, a3) << 8)) << (16 * j);
-    }
-    out[i] = word;
-  }
+  for (int i = 0; i < 4; ++i)
+    out[i] = encode_e2m1x4(w[4 * i], w[4 * i + 1], inv) | (encode_e2m1x4(w[4 * i + 2], w[4 * i + 3], inv) << 16);
   data = make_uint4(out[0], out[1], out[2], out[3]);
   e8m0 = (uint8_t)(X + 127);
 }

@@ -168,7 +168,7 @@ int csa2_kv_append(const void* kv_bf16, const void* ik_bf16, int32_t B,
  * rounded to bf16 and packed as the main-KV latent (E2M1 + E4M3/16, the bytes
  * csa2_pack_kv_fp4 writes for that bf16 row).
  *   c_bf16, z_bf16 [n_tokens][512] bf16 (16-byte aligned), bias [m][512]
- *   fp32; n_tokens a multiple of m. Entries 0 .. n_tokens/m - 1 of kv_data
+ *   fp32 (16-byte aligned); n_tokens a multiple of m. Entries 0 .. n_tokens/m - 1 of kv_data
  *   [..][256] (8-byte aligned) and kv_scale [..][32] are written (offset the
  *   plane pointers to append); out_bf16 [n_tokens/m][512] (nullable, 16-byte
  *   aligned) receives the bf16 entries.

@@ -62,6 +62,23 @@ def test_append_is_bit_exact_with_the_oracle(csa2, T, mode):
         assert np.array_equal(got_nv, ref_nv)
 
 
+@pytest.mark.parametrize("mode", ["separate", "inplace"])
+def test_bulk_append_takes_two_entries_a_warp(csa2, mode):
+    """16,389 entries (an odd count, above the bulk threshold): warps encode
+    two entries each, the last one alone; sequence 2 does not fit."""
+    rng = np.random.default_rng(75)
+    B, T, cap = 3, 5463, 6000
+    kv, ik = _rows(rng, (B, T, 512)), _rows(rng, (B, T, 128))
+    nv = np.array([0, 537, 600], np.int32)
+    got, got_nv, status = _append(csa2, kv, ik, _planes(B, cap, 0x3C), nv, mode)
+    ref = _planes(B, cap, 0x3C)
+    ref_nv = oracle.kv_append(kv, ik, *ref, nv)
+    assert status == -7                               # sequence 2 is dropped and reported
+    assert np.array_equal(got_nv, ref_nv)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
+
+
 def test_append_that_does_not_fit_is_dropped_and_reported(csa2):
     rng = np.random.default_rng(80)
     B, cap, T = 3, 128, 6
