@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
   uint4 kv_lo[kPerWarp], kv_hi[kPerWarp];
   uint2 ikw[kPerWarp];
   int64_t nvs[kPerWarp];
+  int bs[kPerWarp], ts[kPerWarp];
 #pragma unroll
   for (int j = 0; j < kPerWarp; ++j) {
     const int64_t e = e0 + j;
@@ -156,14 +157,17 @@ __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(
       kv_lo[j] = src[0];
       kv_hi[j] = src[1];
       ikw[j] = reinterpret_cast<const uint2*>(ik + e * kIdxDim)[lane];
-      nvs[j] = n_visible[e / T];
+      // (a 32-bit division whenever the entry index fits)
+      bs[j] = e <= 0x7FFFFFFF ? (int)((uint32_t)e / (uint32_t)T) : (int)(e / T);
+      ts[j] = (int)(e - (int64_t)bs[j] * T);
+      nvs[j] = n_visible[bs[j]];
     }
   }
 #pragma unroll
   for (int j = 0; j < kPerWarp; ++j) {
     const int64_t e = e0 + j;
     if (e >= entries) break;
-    const int b = (int)(e / T), t = (int)(e % T);
+    const int b = bs[j], t = ts[j];
     const int64_t nv = nvs[j];
     const bool fits = nv >= 0 && nv + T <= cap;
     if (n_visible_out && t == 0 && lane == 0) n_visible_out[b] = (int32_t)(fits ? nv + T : nv);

@@ -161,16 +161,17 @@ __global__ void __launch_bounds__(kSelThreads) topk_hist_kernel(
 // Block-wide search, from the top bin down, for the first bin at which the
 // running count reaches `need`. Returns the bin (-1 if the total is below
 // `need`) and the count strictly above it. `h` has `nbins` entries in shared
-// memory, nbins a multiple of blockDim.x (a multiple of 32); `scratch` holds
-// blockDim.x + 2 words. Thread j owns bins [nbins-(j+1)*per, nbins-j*per); a
-// warp-shuffle scan over the threads finds the owner of the crossing.
+// memory; nbins and blockDim.x are powers of two, nbins >= blockDim.x >= 32;
+// `scratch` holds blockDim.x + 2 words. Thread j owns bins
+// [nbins-(j+1)*per, nbins-j*per); a warp-shuffle scan over the threads finds
+// the owner of the crossing.
 __device__ int find_threshold_bin(const uint32_t* h, int nbins, uint32_t need, uint32_t* above_out,
                                   uint32_t* scratch) {
   const int per = nbins / blockDim.x;
   const int j = threadIdx.x, lane = j & 31, warp = j >> 5, nwarps = blockDim.x >> 5;
   const int top = nbins - j * per;
   uint32_t local = 0;
-  for (int i = 0; i < per; ++i) local += h[top - 1 - ((i + j) % per)];  // rotated: no bank conflicts
+  for (int i = 0; i < per; ++i) local += h[top - 1 - ((i + j) & (per - 1))];  // rotated: no bank conflicts
   uint32_t incl = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -415,6 +416,31 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   return r;
 }
 
+// Block-wide exclusive scan with one barrier: each warp publishes its total in
+// `buf` (one word per warp), and every thread sums the totals of the warps
+// before its own. Consecutive calls must alternate between two buffers: a
+// buffer is written again only after every thread has passed the barrier of
+// the call in between, so after it has been read.
+__device__ __forceinline__ uint32_t block_exclusive_scan_1bar(uint32_t v, uint32_t* total, uint32_t* buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) buf[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    const uint32_t x = buf[w];
+    before += w < warp ? x : 0u;
+    tot += x;
+  }
+  *total = tot;
+  return before + incl - v;
+}
+
 // ---- pass 2: every key in bin t or above, written per region in order ------
 // Loads the kPerThread consecutive scores [i0, i0 + kPerThread) of a row (16-byte
 // vectors when the row allows) and returns the mask of candidates.
@@ -609,7 +635,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_select_kernel(
 // goes into the shared-memory histogram, and its keys at or above the running
 // threshold bin are appended, in position order, to their region's slice. The
 // running bin is the threshold bin of the histogram so far, recomputed after
-// each of the first four tiles and then after every fourth: it only rises as
+// each of the first four tiles and then after every eighth: it only rises as
 // keys arrive and never passes the row's final threshold bin t, so the slices
 // hold every key of bin t and above (and some below it). At the end the exact
 // t is found, each slice is compacted in place to its keys in bin t or above,
@@ -632,6 +658,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_collect_kernel(const floa
   __shared__ uint32_t sh[kHistBins];
   __shared__ uint32_t h2[kHist2Bins];
   __shared__ uint32_t scratch[kSelThreads + 2];
+  __shared__ uint32_t s_wsum[2][kSelThreads / 32];  // the tile loop's scans, alternating
   __shared__ uint32_t s_scan[33];
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0u;
@@ -662,11 +689,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_collect_kernel(const floa
   };
   if (nv > 0) load_tile((int64_t)threadIdx.x * kPerThread);
   int j = 0;
+  int64_t reg_lo = 0;    // first score of the current region (regions are whole tiles)
   for (int64_t lo = 0; lo < nv; lo += kSelTile, ++j) {
-    const int r = (int)(lo / ws.region);
-    if (r != reg) {      // the earlier region's superset is complete
+    if (lo >= reg_lo + ws.region) {  // the earlier region's superset is complete
       if (threadIdx.x == 0) rcount[reg] = written;
-      reg = r;
+      ++reg;
+      reg_lo += ws.region;
       written = 0;
     }
     uint32_t cur[kPerThread];
@@ -686,15 +714,15 @@ __global__ void __launch_bounds__(kSelThreads, 4) topk_collect_kernel(const floa
       flag |= (uint32_t)(key - lo_flag <= kCandKeyHi - lo_flag) << e;
     }
     uint32_t total;
-    const uint32_t ex = block_exclusive_scan((uint32_t)__popc(flag), &total, s_scan);
+    const uint32_t ex = block_exclusive_scan_1bar((uint32_t)__popc(flag), &total, s_wsum[j & 1]);
     if (flag) {
-      int64_t o = (int64_t)r * ws.region + written + ex;
+      int64_t o = reg_lo + written + ex;
 #pragma unroll
       for (int e = 0; e < kPerThread; ++e)
         if ((flag >> e) & 1u) cand[o++] = make_uint2(key_of_bits(cur[e]), (uint32_t)(p0 + e));
     }
     written += total;
-    if (j < 4 || (j & 3) == 3) {
+    if (j < 4 || (j & 7) == 7) {
       uint32_t above;
       t_run = find_threshold_bin(sh, kHistBins, (uint32_t)k, &above, scratch);  // (its barriers publish sh)
     }
