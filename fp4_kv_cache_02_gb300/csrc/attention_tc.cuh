@@ -130,6 +130,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
+// Sequential mode: the reference max a head's P is taken against (log2
+// domain). It stays at the running value `ref` until a tile's max `mt` passes
+// it by more than kSeqMaxSlack, so that most tiles leave O^T as it is: P is
+// then at most 2^kSeqMaxSlack, far inside fp16, and the output O / l and the
+// log-sum-exp are the same quantities whatever reference is used.
+constexpr float kSeqMaxSlack = 8.0f;
+__device__ __forceinline__ float seq_ref_max(float ref, float mt) {
+  return mt > ref + kSeqMaxSlack ? mt : ref;
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -533,9 +543,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       M[4 * j4 + 2] = m4.z;
       M[4 * j4 + 3] = m4.w;
     }
-    if (kSeq) {   // P relative to the running max over this and the earlier tiles
+    if (kSeq) {   // P relative to the head's reference max (seq_ref_max)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) M[j] = fmaxf(M[j], m_run[h0 + j]);
+      for (int j = 0; j < 16; ++j) M[j] = seq_ref_max(m_run[h0 + j], M[j]);
     }
     // P = 2^(s - M), fp16, stored K-major for the PV product: row h of the
     // 64-row block row / 64, element row % 64
@@ -560,18 +570,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kSeq) {
       // running (max, sum) of each head; O^T of the earlier tiles rescaled to
       // the new max before this tile's PV accumulates onto it
+      bool moved = false;
       if (tid < kHeads) {
         const int h = tid;
         const float mt = fmaxf(fmaxf(red_m[0][h], red_m[1][h]), fmaxf(red_m[2][h], red_m[3][h]));
-        const float mo = m_run[h], mn = fmaxf(mo, mt);
-        const float alpha = mo == -INFINITY ? 0.0f : fast_exp2(mo - mn);
+        const float mo = m_run[h], mn = seq_ref_max(mo, mt);
+        moved = mn != mo;
+        const float alpha = !moved ? 1.0f : mo == -INFINITY ? 0.0f : fast_exp2(mo - mn);
         const float lt = s_ok ? red_l[0][h] + red_l[1][h] + red_l[2][h] + red_l[3][h] : 0.0f;
         l_run[h] = l_run[h] * alpha + lt;
         m_run[h] = mn;
         alpha_s[h] = alpha;
       }
-      if (passes_done > 0) {
-        __syncthreads();
+      // O^T of the earlier tiles is rescaled only when some head's reference
+      // max moved (the barrier also publishes alpha_s)
+      if (__syncthreads_or(moved) && passes_done > 0) {
         const uint32_t o_base = tmem + ((uint32_t)(rq * 32) << 16) + kColO + 64u * (uint32_t)(warp >> 2);
 #pragma unroll 1
         for (int hh = 0; hh < kHeads; hh += 16) {
