@@ -53,15 +53,16 @@ constexpr int kOffR = 0;                        // 8 blocks = 128 KiB
 constexpr int kOffQ = kOffR + 8 * kBlkR;        // 8 blocks = 64 KiB
 constexpr int kOffP = kOffQ + 8 * kQBlk;        // 2 blocks = 16 KiB
 constexpr int kOffMisc = kOffP + 2 * kPBlk;
-constexpr int kOffStage = kOffR + 4 * kBlkR;    // a tile's raw rows, in R's upper half (64 KiB)
+constexpr int kOffStage = kOffR + 4 * kBlkR;    // an SWA tile's raw rows, in R's upper half (64 KiB)
 constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;                   // S^T: 64 columns (heads), lanes = rows
 constexpr uint32_t kColO = 64;                  // O^T: 4 blocks x 64 columns (heads), lanes = channels
 constexpr int kMaxPartials = 36;                // 32 tiles of selected rows (k <= 4096) + 4 SWA tiles (<= 512 rows)
 
-static_assert(kSmemBytes <= 232448 - 4096, "shared memory budget (static arrays included)");
-static_assert(kRows * kHeadDim <= 4 * kBlkR && kRows * (kKvBytes + kKvScales) <= 4 * kBlkR, "staging fits");
+// the kernel's static arrays take under 10 KiB (8.5 KiB at most over the modes)
+static_assert(kSmemBytes <= 232448 - 10240, "shared memory budget (static arrays included)");
+static_assert(kRows * kHeadDim <= 4 * kBlkR, "the SWA staging fits in R's upper half");
 // merge: (max, sum) and weights of every partial of the CTA's heads live in
 // the P region (at most 36 partials x 16 heads with 4 or more CTAs, 5 x 64
 // with one CTA, 6 x 32 with two, 7 x 22 with three)
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(16) float red_l[4][kHeads];
   __shared__ float q_mul[kHeads];        // sm_scale * 2^-k_h * log2(e)
   __shared__ int row_valid[kRows];       // 0 none, 1 selected latent, 2 SWA row
+  __shared__ int64_t row_src[kRows];     // a selected tile's cache row per tile row (-1: none)
   // (max, sum) of every partial for the (layer,) head rows this CTA merges,
   // written by the CTAs of the cluster through distributed shared memory:
   // [part][row - hb0]
@@ -342,9 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int64_t nv_seq = -1;
   auto gather_dequant = [&](const bool swa, const int tile, const int qi_swa, const int next_sel_tile) {
     const uint32_t par = items_done & 1u;
-    // thread r < 128 starts the bulk copies of row r into the staging area
-    // (selected rows: 256 B of codes + 32 B of scales); the SWA rows of the
-    // tile are one contiguous copy
+    // SWA tiles: one contiguous bulk copy of the tile's rows into the staging
+    // area. Selected tiles: thread r < 128 resolves row r to its cache row,
+    // and the dequantising threads load the codes and scales straight from
+    // global memory (no staging copy, no wait on the copy engine)
     if (tid < kRows) {
       int valid = 0;
       int64_t src = 0;
@@ -377,13 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (valid) {
-          tc::mbar_arrive_expect_tx(bar_g, kKvBytes + kKvScales);
-          tc::bulk_load(sStage + tid * kKvBytes, a.kv_data + src * kKvBytes, kKvBytes, bar_g);
-          tc::bulk_load(sStage + kRows * kKvBytes + tid * kKvScales, a.kv_scale + src * kKvScales, kKvScales, bar_g);
-        } else {
-          tc::mbar_arrive(bar_g);
-        }
+        row_src[tid] = valid ? src : -1;
         // the next selected tile's index for this row, in flight through this tile
         if (next_sel_tile >= 0) {
           const int tn = next_sel_tile * kRows + tid;
@@ -394,10 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_valid[tid] = valid;
     }
     __syncthreads();
-    const bool g_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_g, par, s_abort, &g_attn_error));
-    ++items_done;
+    bool g_ok = true;
+    if (swa) {
+      g_ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(bar_g, par, s_abort, &g_attn_error));
+      ++items_done;
+    }
     // ---- dequantise into R (fp16, SW128 blocks of 64 channels). The staged
-    // bytes sit in R's upper half: read them all, then write R ----
+    // SWA bytes sit in R's upper half: read them all, then write R ----
     if (swa) {
       // warp w: rows 8w .. 8w+7; lane l: channels 16l .. 16l+15 of the row
       uint4 raw[8];
@@ -434,13 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c16 = lane & 15;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int r = warp * 8 + 2 * i + (lane >> 4);
-        const bool v = g_ok && row_valid[r];
-        raw[i] = v ? *reinterpret_cast<const uint4*>(sStage + r * kKvBytes + c16 * 16) : make_uint4(0u, 0u, 0u, 0u);
-        scl[i] = v ? (uint32_t)*reinterpret_cast<const uint16_t*>(sStage + kRows * kKvBytes + r * kKvScales + c16 * 2)
-                   : 0u;
+        const int64_t src = row_src[warp * 8 + 2 * i + (lane >> 4)];
+        raw[i] = src >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.kv_data + src * kKvBytes) + c16)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        scl[i] = src >= 0 ? (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(a.kv_scale + src * kKvScales) + c16)
+                          : 0u;
       }
-      __syncthreads();
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = warp * 8 + 2 * i + (lane >> 4);
