@@ -141,6 +141,11 @@ __device__ __forceinline__ float seq_ref_max(float ref, float mt) {
   return mt > ref + kSeqMaxSlack ? mt : ref;
 }
 
+// A hint: the cache line holding p is fetched into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -463,6 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(blk + tc::sw128_offset((uint32_t)r, c0 + (uint32_t)k)) =
               make_uint4(mul_f16x2(o0, s2), mul_f16x2(o1, s2), mul_f16x2(o2, s2), mul_f16x2(o3, s2));
         }
+      }
+      // the next selected tile's row for this thread (its index arrived during
+      // this tile) is brought into L2 while this tile is attended
+      if (tid < kRows && next_sel_tile >= 0 && pf_tile == next_sel_tile && pf_idx >= 0 && pf_idx < nv_seq) {
+        const int64_t nsrc = (int64_t)seq * a.kv_seq_stride + pf_idx;
+        prefetch_l2(a.kv_data + nsrc * kKvBytes);
+        prefetch_l2(a.kv_data + nsrc * kKvBytes + 128);
+        prefetch_l2(a.kv_scale + nsrc * kKvScales);
       }
     }
     tc::fence_proxy_async_smem();
