@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t pf_idx = -1;
   int pf_tile = -1;
   int64_t nv_seq = -1;
+  bool pf_rows = false;   // pf_idx's row is still to be prefetched into L2
   auto gather_dequant = [&](const bool swa, const int tile, const int qi_swa, const int next_sel_tile) {
     const uint32_t par = items_done & 1u;
     // SWA tiles: one contiguous bulk copy of the tile's rows into the staging
@@ -613,6 +614,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
       }
     }
+    if (pf_rows) {   // (only threads below 128 set it)
+      if (pf_idx >= 0 && pf_idx < nv_seq) {
+        const int64_t nsrc = (int64_t)seq * a.kv_seq_stride + pf_idx;
+        prefetch_l2(a.kv_data + nsrc * kKvBytes);
+        prefetch_l2(a.kv_data + nsrc * kKvBytes + 128);
+        prefetch_l2(a.kv_scale + nsrc * kKvScales);
+      }
+      pf_rows = false;
+    }
     // ---- O^T = R^T P^T : 4 x (M = 128 channels), N = 64, K = 128 rows ----
     if (tid == 0 && s_ok) {
       constexpr uint32_t idesc = idesc_f16(128, 64, 1, 0);  // A (channels x rows) is MN-major
@@ -713,6 +723,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool rows_ok =
         gather_dequant(swa, swa ? swa_tile : sel_tile, kReuse ? seq * L + l0 : unit, swa ? -1 : next_sel);
     (void)rows_ok;
+    if (!kSeq && swa && next_sel >= 0 && !waited) {
+      // the CTA's next item is a selected tile: wait for the indices now, so
+      // that this thread's index of it arrives (and its row is prefetched into
+      // L2, pf_rows) while the SWA tile is attended. (Not in the sequential
+      // mode: there the SWA pass of a launch's first CTAs overlaps the end of
+      // the launch before, which an earlier wait would give up.)
+      pdl_wait();
+      waited = true;
+      if (tid < kRows) {
+        if (nv_seq < 0) nv_seq = a.n_visible ? (int64_t)a.n_visible[seq] : a.nv_const;
+        const int tn = next_sel * kRows + tid;
+        pf_idx = tn < a.k ? a.idx[(int64_t)seq * a.k + tn] : -1;
+        pf_tile = next_sel;
+        pf_rows = true;
+      }
+    }
     const int n_layers = swa ? 1 : lgrp;
     for (int li = 0; li < n_layers; ++li) {
       const int layer = l0 + li;
