@@ -133,6 +133,36 @@ def test_many_queries_walk_their_tiles_on_one_cta(csa2):
     assert np.isfinite(lse0.cpu().numpy()[3]).all()
 
 
+def test_sequential_mode_rescales_when_a_head_max_jumps(csa2):
+    """In the one-CTA-per-query mode a head's P is taken against a reference
+    max that moves only when a tile's max passes it by more than 2^8; then O
+    is rescaled. Query 3 gets, for head 0, a whole selected tile of rows
+    scoring ~14.9 (log2; the other tiles stay near 3) and one later row
+    scoring ~24.9, so the reference moves twice, the second time with the
+    first tile still weighing ~11 % of the result. Sampled queries against
+    the oracle."""
+    B = 160
+    Ns = [700 + 37 * (b % 9) for b in range(B)]
+    case = DecodeCase(workload=91, Ns=Ns, L=1)
+    rng = np.random.default_rng(6)
+    k = 512
+    idx = np.stack([rng.permutation(n)[:k] for n in Ns]).astype(np.int32)
+    b = 3
+    sgn = np.where(case.Q[b, 0, 0] >= 0, 1.0, -1.0).astype(np.float32)
+    for rows, c in ((idx[b, 128:256], 6 * 0.09375), (idx[b, 400:401], 6 * 0.15625)):
+        d, sc = oracle.pack_kv_fp4(np.tile(c * sgn, (len(rows), 1)))
+        case.kv_data[b, rows], case.kv_scale[b, rows] = d, sc
+    g = case.to_device()
+    out, out32, lse = _run_decode(csa2, g, dev(idx), k, 128, B, 1)
+    o32, l32 = out32.cpu().numpy(), lse.cpu().numpy()
+    ref, ref_lse = case.oracle_attention(b, 0, idx[b])
+    assert ref_lse[0] * np.log2(np.e) > 20.0      # head 0 is dominated by the planted rows
+    for q in (b, 0, 159):
+        ref, ref_lse = case.oracle_attention(q, 0, idx[q])
+        assert attn_row_error(o32[q, 0], ref) <= ATTN_ROW_TOL
+        np.testing.assert_allclose(l32[q, 0], ref_lse, rtol=1e-5, atol=1e-5)
+
+
 def test_decode_attention_special_cases(csa2):
     case = DecodeCase(workload=95, Ns=[300], n_swa=0)
     g = case.to_device()
