@@ -10,10 +10,12 @@
 // tiles of selected entries. A thread-block cluster of C CTAs serves one
 // query; CTA r takes the tiles whose index is r modulo C, and each tile gives
 // one partial softmax (m, l, O) over its rows:
-//   1. the rows are copied into a staging area by the bulk-copy engine (the
-//      SWA rows of a tile in one copy, a selected latent as 256 B of codes +
-//      32 B of scales: plain loads are bounded by the few misses an SM keeps
-//      in flight) and dequantised into shared memory as fp16 R[t][c] in
+//   1. the SWA rows of a tile come by one bulk copy into a staging area; a
+//      selected latent (256 B of codes + 32 B of scales) is loaded straight
+//      into the threads that dequantise it, four rows a thread in flight
+//      (the copy engine spends ~7 ns a row, which a tile's 128 separate rows
+//      turn into the longest step), the next tile's rows prefetched into L2;
+//      the rows are dequantised into shared memory as fp16 R[t][c] in
 //      128-byte-swizzled blocks of 64 channels. fp16 holds every row value
 //      exactly: an E2M1 x E4M3 product has at most 6 significant bits and
 //      lies in [2^-10, 2688]; an E4M3 SWA value is a subset of fp16;
@@ -339,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t passes_done = 0;  // parity source of bar_s / bar_pv
 
   // ---- one tile's rows: rows [128 tile, 128 tile + 128) of the SWA window of
-  // query qi_swa (swa) or of the sequence's selected list, gathered by the
-  // bulk-copy engine and dequantised into R ----
+  // query qi_swa (swa: one bulk copy) or of the sequence's selected list
+  // (plain loads by the dequantising threads), dequantised into R ----
   // thread r < 128: the index of row r of the CTA's next selected tile, loaded
   // while the current tile is attended (pf_tile: that tile, -1 none); the
   // sequence's visible count, read once
